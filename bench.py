@@ -1,0 +1,436 @@
+"""Benchmark of the routed MoE SwiGLU FFN forward pass on GB300.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
+                  [--impl ours|reference]
+
+A step is one layer call (router, sort, both projections, combine) over one
+batch of T fresh seeded tokens.  The default workload is the Qwen-3-style
+decode layer (H=2048, I=768, E=128, top-8) at T=1.  Each rank (torchrun, one
+per GPU) runs its own replica over its own token stream: the calls are
+independent problems, so there is no data-path collective ("scaling": "weak").
+
+Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
+cudaDeviceSynchronize.  Between steps a 512 MB buffer is written to flush L2,
+and each step is bracketed by its own CUDA events on the launching stream, so
+the flush is not timed; value = tokens of all ranks / max over ranks of the
+summed step times.  A second pass over the same steps records per-kernel
+events (the library's stage events) for the roofline of the dominant kernel.
+e2e repeats the steps through the host-buffer entry point (pinned inputs
+copied in, output copied out, inside each step's events).
+
+--impl reference times the FP64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload (it is the slow baseline, not a target).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; decode HBM TB/s vs peak; T=2048 TFLOPS vs BF16 peak"
+DEFAULT_WORKLOAD = "decode_h2048_i768_e128_k8"
+FLUSH_BYTES = 512 << 20
+
+# Kernel sources whose change voids a stored ncu traffic figure.
+KERNEL_SOURCES = {
+    "decode_gate_up": ["decode.cu"],
+    "decode_down": ["decode.cu"],
+    "gemm_gate_up": ["grouped_gemm.cu"],
+    "gemm_down": ["grouped_gemm.cu"],
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--T", type=int, default=None)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained"), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def source_digest(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "mixture_experts_ffn_gate_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel, workload, T):
+    """DRAM bytes per launch from a committed ncu summary, or None if absent
+    or taken on a different version of the kernel's source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = table.get(f"{kernel}@{workload}/T{T}")
+    if not rec or rec.get("source_sha") != source_digest(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                rows.append(f)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit())}
+
+
+def algorithmic_bytes(wl, T, U):
+    """Per-call algorithmic HBM bytes: each touched expert's weights once
+    (U*6*H*I), x in (T*H*2), logits in (T*E*4), out written (T*H*4)."""
+    return U * 6 * wl.H * wl.I + T * wl.H * 2 + T * wl.E * 4 + T * wl.H * 4
+
+
+def kernel_bytes(kernel, wl, T, U, k):
+    """Algorithmic bytes of one launch of a kernel."""
+    H, I = wl.H, wl.I
+    if kernel == "decode_gate_up":
+        return U * 2 * I * H * 2 + T * H * 2 + T * k * I * 4
+    if kernel == "decode_down":
+        return U * H * I * 2 + T * k * I * 4 + T * H * 4 + T * k * 4
+    if kernel == "gemm_gate_up":
+        return U * 2 * I * H * 2 + T * k * H * 2 + 2 * T * k * I * 2
+    if kernel == "gemm_down":
+        return U * H * I * 2 + 2 * T * k * I * 2 + T * k * H * 4
+    return None
+
+
+def reference_arm(args, wl, T):
+    """The FP64 oracle on the host cores, on a bounded sample of the workload."""
+    import numpy as np
+
+    import oracle
+    from mixture_experts_ffn_gate_gb300 import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0))
+    # weights of the experts the sampled tokens select, drawn on the host
+    steps, warm = args.steps, args.warmup
+    per_token = 6.0 * wl.H * wl.I * wl.k  # flops per token
+    # cap the run at ~120 s of oracle time (measured rate ~1 GFLOP/s/thread)
+    budget_tokens = max(1, int(120e9 * min(cores, max(T, 1)) / per_token))
+    t_step = min(T, budget_tokens)
+    steps_run = max(1, min(steps, budget_tokens // max(t_step, 1)))
+    batches = [synth.make_tokens(wl, T, call=i) for i in range(warm + steps_run)]
+    need = set()
+    for x, L in batches:
+        idx, _ = oracle.route(L[:t_step].numpy(), wl.k)
+        need.update(np.unique(idx).tolist())
+    need = sorted(need)
+    emap = -np.ones(wl.E, np.int32)
+    emap[need] = np.arange(len(need), dtype=np.int32)
+    g, d = synth.make_weights(wl, device="cpu", experts=need)
+    wgu, wd = synth.bf16_bits(g), synth.bf16_bits(d)
+    del g, d
+    for x, L in batches[:warm]:
+        oracle.forward(synth.bf16_bits(x[:t_step]), L[:t_step].numpy(), wgu, wd, wl.k,
+                       expert_map=emap, nthreads=cores)
+    t0 = time.perf_counter()
+    for x, L in batches[warm:]:
+        oracle.forward(synth.bf16_bits(x[:t_step]), L[:t_step].numpy(), wgu, wd, wl.k,
+                       expert_map=emap, nthreads=cores)
+    dt = time.perf_counter() - t0
+    tokens = t_step * steps_run
+    value = tokens / dt
+    sample = (f"{steps_run} steps of {t_step} of the {T} tokens per step (fresh seeded tokens), "
+              f"weights of the {len(need)} experts they select drawn on the host")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": steps_run, "warmup": warm,
+            "ms_per_step": 1e3 * dt / steps_run, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, t_step),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, T, wgu_dev, wd_dev, token_batches):
+    """The oracle as it stands on the host cores, on a bounded sample of the
+    workload (~10-30 s of CPU work); returns the cpu_baseline object."""
+    import numpy as np
+
+    import oracle
+    from mixture_experts_ffn_gate_gb300 import synth
+    import torch
+
+    cores = len(os.sched_getaffinity(0))
+    per_token = 6.0 * wl.H * wl.I * wl.k
+    n_tok = max(1, min(int(15e9 * cores / per_token), 4096))
+    xs, Ls = [], []
+    got = 0
+    for x, L in token_batches:
+        take = min(x.shape[0], n_tok - got)
+        xs.append(x[:take].cpu())
+        Ls.append(L[:take].cpu())
+        got += take
+        if got >= n_tok:
+            break
+    x = torch.cat(xs)
+    L = torch.cat(Ls).numpy()
+    idx, _ = oracle.route(L, wl.k)
+    used = np.unique(idx)
+    emap = -np.ones(wl.E, np.int32)
+    emap[used] = np.arange(len(used), dtype=np.int32)
+    sel = torch.as_tensor(used, dtype=torch.long, device=wgu_dev.device)
+    wgu = synth.bf16_bits(wgu_dev.index_select(0, sel))
+    wd = synth.bf16_bits(wd_dev.index_select(0, sel))
+    xb = synth.bf16_bits(x)
+    t0 = time.perf_counter()
+    oracle.forward(xb, L, wgu, wd, wl.k, expert_map=emap, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": got / dt, "unit": "tokens/s", "cores": min(cores, got), "kind": "oracle",
+            "sample": f"{got} fresh seeded tokens of the workload in one oracle call "
+                      f"({len(used)} experts), {dt:.1f} s"}
+
+
+def main():
+    args = parse()
+    from mixture_experts_ffn_gate_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    T = args.T if args.T is not None else wl.T[0]
+    if args.impl == "reference":
+        reference_arm(args, wl, T)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    from mixture_experts_ffn_gate_gb300 import moe_ffn as m
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    __graft_entry__.build() if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    m.lib()
+
+    dev = torch.device("cuda", local)
+    K, W = args.steps, max(3, args.warmup)
+    wgu, wd = synth.make_weights(wl, device=dev)
+    bias = synth.make_bias(wl)
+    # rank r processes calls [r*(W+K), (r+1)*(W+K)) of the token stream
+    batches = [synth.make_tokens(wl, T, call=rank * (W + K) + i, device=dev, bias=bias)
+               for i in range(W + K)]
+    ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
+    out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(i, opts=None, idx=None):
+        x, L = batches[i]
+        m.moe_ffn_forward_ex(x, L, wgu, wd, wl.k, out=out, workspace=ws, topk_idx=idx,
+                             opts=opts, stream=stream)
+
+    probe = m.moe_ffn_opts()
+    call(0, probe)
+    path, n_stages = probe.path_taken, probe.n_stages
+    stage_names = [m.moe_ffn_stage_name(path, s) for s in range(n_stages)]
+
+    # unique experts touched per step (routing of each batch, untimed)
+    idx_buf = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
+    U = []
+    for i in range(W, W + K):
+        call(i, None, idx_buf)
+        U.append(int(torch.unique(idx_buf).numel()))
+    torch.cuda.synchronize()
+
+    for i in range(W):
+        flush.fill_(float(i))
+        call(i)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for j in range(K):
+            flush.fill_(float(j))
+            starts[j].record(stream)
+            call(W + j)
+            ends[j].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+        if world > 1:
+            dist.barrier()
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        total_ms = sum(step_ms)
+
+        # per-kernel pass over the same steps, stage events between kernels
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
+               for _ in range(K)]
+        arrs = []
+        for j in range(K):
+            for e in evs[j]:
+                e.record(stream)
+            arrs.append(m.stage_event_array(evs[j]))
+        torch.cuda.synchronize()
+        for j in range(K):
+            flush.fill_(float(j))
+            o = m.moe_ffn_opts()
+            o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
+            call(W + j, o)
+        torch.cuda.synchronize()
+        kern_ms = {name: [evs[j][s].elapsed_time(evs[j][s + 1]) for j in range(K)]
+                   for s, name in enumerate(stage_names)}
+
+        # e2e through the host-buffer entry point
+        e2e = None
+        if not args.no_e2e:
+            xh = [b[0].cpu().pin_memory() for b in batches]
+            lh = [b[1].cpu().pin_memory() for b in batches]
+            oh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
+            wsh = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev, host=True)
+            for i in range(W):
+                m.moe_ffn_forward_host(xh[i], lh[i], wgu, wd, wl.k, oh, wsh, stream=stream)
+            torch.cuda.synchronize()
+            e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+            e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+            for j in range(K):
+                flush.fill_(float(j))
+                e_starts[j].record(stream)
+                m.moe_ffn_forward_host(xh[W + j], lh[W + j], wgu, wd, wl.k, oh, wsh, stream=stream)
+                e_ends[j].record(stream)
+            torch.cuda.synchronize()
+            e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends))
+            e2e = {"ms": e2e_ms}
+
+    # max over ranks
+    t = torch.tensor([total_ms, e2e["ms"] if e2e else 0.0], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_max = float(t[0]), float(t[1])
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    tokens = T * K * world
+    value = tokens / (total_ms / 1e3)
+    mean_U = sum(U) / len(U)
+    call_bytes = sum(algorithmic_bytes(wl, T, u) for u in U) / K
+    flops = 6.0 * wl.H * wl.I * T * wl.k
+    # dominant kernel = largest share of the per-kernel pass
+    kern_avg = {n: sum(v) / len(v) for n, v in kern_ms.items()}
+    dom = max(kern_avg, key=kern_avg.get)
+    dom_bytes = sum(kernel_bytes(dom, wl, T, u, wl.k) for u in U) / K
+    achieved = dom_bytes / (kern_avg[dom] / 1e3) / 1e9
+    traffic = stored_traffic(dom, wl.name, T)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} HBM copy (burst)",
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "kernel_us": {n: round(1e3 * v, 3) for n, v in kern_avg.items()}}
+    whole_call_gbs = call_bytes / (total_ms / K / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "path": {1: "decode", 2: "grouped"}.get(path, path),
+                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MB write, not timed)",
+                   "timing": "CUDA events around each step on the launching stream, summed",
+                   "parallelism": f"replicas x{world} (independent token streams)"},
+        "roofline": roofline,
+        "call_hbm": {"achieved_gbs": whole_call_gbs, "frac_of_measured": whole_call_gbs / peaks["hbm_gbs"],
+                     "frac_of_8tbs_spec": whole_call_gbs / 8000.0, "bytes_per_call": call_bytes,
+                     "unique_experts_mean": mean_U},
+        "tensor": {"tflops": flops / (total_ms / K / 1e3) / 1e12,
+                   "frac_of_dense_bf16_peak": flops / (total_ms / K / 1e3) / 1e12 / peaks["bf16_tflops"]},
+        "gpu_launches": n_stages * K,
+        "stages": stage_names,
+        "wall_s": wall,
+    }
+    if e2e is not None:
+        line["e2e"] = {"value": tokens / (e2e_max / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": T * wl.H * 2 + T * wl.E * 4,
+                       "d2h_bytes_per_step": T * wl.H * 4}
+    line["clocks"] = clocks.summary()
+    if world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, T, wgu, wd, batches)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

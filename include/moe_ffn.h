@@ -1,0 +1,174 @@
+/*
+ * moe_ffn.h -- C ABI of libmoeffn.so: the forward pass of a routed
+ * Mixture-of-Experts SwiGLU FFN layer on one GB300 GPU (sm_103a).
+ *
+ * The layer, per token t with activation x[t] (H values) and router logits
+ * l[t] (E values):
+ *   1. select k experts: k times take the not-yet-chosen expert with the
+ *      largest logit, the smaller expert index winning ties (-0.0 == +0.0);
+ *      slot j is the j-th pick;
+ *   2. w[t][j] = softmax over the k chosen logits;
+ *   3. for each slot j, expert e: a = silu(W_gu[e][0:I] x) * (W_gu[e][I:2I] x),
+ *      y_j = W_down[e] a   (gate rows 0..I-1, up rows I..2I-1);
+ *   4. out[t] = sum over j ascending of w[t][j] * y_j.
+ * "Expert routing" and the per-output-dimension FP32 accumulation of the
+ * routed experts' contributions are named in the warp-decode article
+ * ("Cursor warp decode 공개 ... MoE 추론을 1.84x 가속", section 핵심 내용);
+ * keeping the intermediate activation unquantised with BF16 activations and
+ * FP32 accumulation is in its section 경쟁 구도 / 비교; a fixed floating-point
+ * accumulation order that makes outputs bit-identical regardless of hardware
+ * scheduling is in the Mixture-of-Kittens article (asapai.co.kr), section
+ * 결정론을 성능과 같은 급으로 올려놓은 선택.
+ *
+ * Conventions for every call below unless it says otherwise:
+ *   - Tensors are row-major and contiguous, in device memory owned by the
+ *     caller (e.g. a torch tensor's data_ptr()).  Base pointers must be
+ *     16-byte aligned.  BF16 is passed as void* (raw 16-bit patterns).
+ *   - x_bf16 [T,H]; router_logits_f32 [T,E]; w_gate_up_bf16 [E,2I,H];
+ *     w_down_bf16 [E,H,I]; out_f32 [T,H] (fully overwritten, must not alias
+ *     an input).
+ *   - Shape limits: T >= 0, 1 <= E <= 1024, 1 <= k <= min(E, 32),
+ *     H % 64 == 0, I % 64 == 0, H >= 64, I >= 64; T*k and every index must
+ *     fit in int32.  T == 0 returns MOE_OK and enqueues nothing.
+ *   - Argument checks are synchronous and happen before anything is
+ *     enqueued: a bad argument returns MOE_ERR_INVALID_ARG or
+ *     MOE_ERR_UNSUPPORTED_SHAPE and touches no memory.
+ *   - Calls are asynchronous on `stream`; results are valid once the stream
+ *     reaches the point of the call.  The library keeps no pointer after a
+ *     call returns; the caller keeps every buffer alive until the stream's
+ *     work is done.
+ *   - Launch failures are returned as MOE_ERR_CUDA (cudaPeekAtLastError);
+ *     faults during execution surface at the caller's next synchronisation.
+ *   - Results are deterministic: for the same inputs, path and device the
+ *     output bits do not change from run to run or with the launch knobs in
+ *     moe_ffn_opts.  The two paths (decode, grouped) are each deterministic
+ *     but are not bitwise equal to each other.
+ */
+#ifndef MOE_FFN_H
+#define MOE_FFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null pointer, negative size, k > E ... */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* valid but outside the shape limits      */
+    MOE_ERR_CUDA = 3,              /* a CUDA runtime call or launch failed    */
+    MOE_ERR_NO_MEMORY = 4,         /* stream-ordered workspace allocation failed */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 5,
+    MOE_ERR_TIMEOUT = 6            /* a device-side bounded wait gave up      */
+};
+
+/* Execution paths. */
+enum {
+    MOE_PATH_AUTO = 0,    /* decode for T <= decode_max_tokens, else grouped */
+    MOE_PATH_DECODE = 1,  /* warp per output scalar, weights streamed once   */
+    MOE_PATH_GROUPED = 2  /* counting sort + tcgen05 grouped GEMMs + combine */
+};
+
+#define MOE_MAX_STAGES 8
+
+/*
+ * Optional knobs and outputs of moe_ffn_forward_ex.  Zero-initialise and set
+ * what you need; zero means "library default" for every input field.
+ */
+typedef struct moe_ffn_opts {
+    /* inputs */
+    int32_t path;              /* MOE_PATH_* */
+    int32_t decode_max_tokens; /* AUTO threshold on T (default 64) */
+    int32_t gate_up_warps;     /* decode gate_up: warps per block, 1..16 (default 8) */
+    int32_t down_warps;        /* decode down: warps per block, 1..16 (default 8) */
+    int32_t gemm_ctas;         /* grouped GEMMs: persistent CTAs (default: one per SM) */
+    int32_t reserved_in[3];    /* must be zero */
+    /* nullable: MOE_MAX_STAGES + 1 created events.  When set, the call
+     * records stage_events[0] before its first kernel and stage_events[i+1]
+     * after kernel i, on `stream`, so the caller can time each kernel with
+     * cudaEventElapsedTime.  Recording events between kernels can change
+     * how they overlap, so time whole calls without it. */
+    cudaEvent_t *stage_events;
+    /* outputs */
+    int32_t n_stages;          /* kernels the call enqueued */
+    int32_t path_taken;        /* MOE_PATH_DECODE or MOE_PATH_GROUPED */
+    int32_t reserved_out[2];
+} moe_ffn_opts;
+
+/*
+ * The layer forward pass.  Uses a stream-ordered temporary workspace
+ * (cudaMallocAsync / cudaFreeAsync on `stream`), so it is safe on several
+ * streams at once.  Returns MOE_ERR_NO_MEMORY if that allocation fails.
+ */
+int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32,
+                    const void *w_gate_up_bf16, const void *w_down_bf16,
+                    int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                    float *out_f32, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace that moe_ffn_forward_ex needs for this shape on
+ * either path (the larger of the two), or 0 if the shape is invalid.
+ */
+size_t moe_ffn_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E,
+                               int64_t k);
+
+/*
+ * The forward pass with a caller-owned workspace (256-byte aligned, at least
+ * moe_ffn_workspace_bytes), optional routing outputs and options.  With a
+ * workspace the call allocates nothing and is reentrant; two calls that
+ * share a workspace must be ordered on one stream.
+ *   topk_idx_out  nullable int32 [T,k]: the chosen experts, slot order.
+ *   topk_w_out    nullable float [T,k]: their softmax weights.
+ *   opts          nullable; see moe_ffn_opts.
+ */
+int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32,
+                       const void *w_gate_up_bf16, const void *w_down_bf16,
+                       int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                       float *out_f32, void *workspace, size_t workspace_bytes,
+                       int32_t *topk_idx_out, float *topk_w_out,
+                       moe_ffn_opts *opts, cudaStream_t stream);
+
+/*
+ * End-to-end form for callers whose tokens live in host memory: x_host
+ * [T,H] bf16, logits_host [T,E] f32 and out_host [T,H] f32 are HOST buffers
+ * (page-locked for the copies to be asynchronous); the weights are device
+ * buffers as above.  The call enqueues host->device copies of the inputs,
+ * the forward pass and the device->host copy of the output on `stream`;
+ * out_host is valid after the stream is synchronised.  The workspace
+ * (device, at least moe_ffn_host_workspace_bytes) also holds the staged
+ * inputs and output.
+ */
+size_t moe_ffn_host_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E,
+                                    int64_t k);
+int moe_ffn_forward_host(const void *x_host, const float *logits_host,
+                         const void *w_gate_up_bf16, const void *w_down_bf16,
+                         int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                         float *out_host, void *workspace,
+                         size_t workspace_bytes, moe_ffn_opts *opts,
+                         cudaStream_t stream);
+
+/* Static text for a status code. */
+const char *moe_ffn_status_string(int status);
+
+/* Name of kernel `stage` (0-based) on `path`, or NULL past the last one. */
+const char *moe_ffn_stage_name(int path, int stage);
+
+/*
+ * Device fault word: bit flags that kernels set when a bounded device-side
+ * wait gives up (instead of hanging).  Reads the current device's word
+ * synchronously into *flags and, if clear != 0, resets it.  Returns MOE_OK,
+ * or MOE_ERR_CUDA if the read fails.  A non-zero word means some call since
+ * the last clear returned garbage in out_f32.
+ */
+int moe_ffn_device_faults(uint32_t *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H */

@@ -1,0 +1,88 @@
+// common.cuh -- small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Fault bits written to the device fault word when a bounded wait gives up.
+enum : uint32_t {
+    FAULT_GEMM_PRODUCER = 1u << 0,
+    FAULT_GEMM_MMA = 1u << 1,
+    FAULT_GEMM_EPILOGUE = 1u << 2,
+};
+
+// 16-byte streaming load that bypasses L1 allocation: expert weights are
+// read once per call.
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte read-only load through L1 (activations reused by a block's warps).
+__device__ __forceinline__ uint4 ld_nc16(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_nc_f4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// BF16 pair (low half = element 0) -> two floats, exactly.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Unpack 8 BF16 values held in a uint4.
+__device__ __forceinline__ void unpack8(const uint4 &v, float f[8])
+{
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// Warp sum with a fixed butterfly: every lane ends with the same bits, and
+// the association order depends only on the lane layout.
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// silu(g) * u in FP32 with the library expf.
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// A strict total order on FP32 router logits as an unsigned key: larger
+// float -> larger key; -0.0 and +0.0 map to the same key; every NaN maps to
+// a fixed key above +inf (NaN logits give a defined, meaningless routing
+// instead of broken indices).
+__device__ __forceinline__ uint32_t logit_key(float f)
+{
+    if (f == 0.0f) f = 0.0f;   // -0.0 -> +0.0
+    if (f != f) return 0xffffffffu;
+    uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+}  // namespace moe

@@ -1,0 +1,341 @@
+// moe_ffn_api.cu -- the C ABI: argument checks, workspace layout, path
+// choice and the launch sequence of each path.  Host code only.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "moe_ffn.h"
+
+namespace {
+
+using moe::ceil_div;
+using moe::round_up;
+
+constexpr int kDefaultDecodeMaxTokens = 64;
+constexpr int kDefaultWarps = 8;
+constexpr int kMaxDevices = 64;
+
+struct Shape {
+    int64_t T, H, I, E, k;
+};
+
+// Workspace regions, 256-byte aligned.  The routing/sort region is shared
+// by both paths; the rest is per path and the two overlap.
+struct Layout {
+    size_t idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, common_end;
+    size_t act;                          // decode: act f32 [T*k, I]
+    size_t xs, act_hi, act_lo, z;        // grouped
+    size_t decode_total, grouped_total, total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+Layout make_layout(const Shape &s)
+{
+    Layout L{};
+    const size_t n = (size_t)(s.T * s.k);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.idx = take(n * 4);
+    L.w = take(n * 4);
+    L.offs = take((size_t)(s.E + 1) * 4);
+    L.perm = take(n * 4);
+    L.pos = take(n * 4);
+    L.uexp = take((size_t)s.E * 4);
+    L.ucount = take(4);
+    L.chunks = take((size_t)(s.E + ceil_div((int64_t)n, moe::kGemmChunkMax) + 1) * 16);
+    L.nchunks = take(4);
+    L.common_end = o;
+    // decode path
+    L.act = take(n * (size_t)s.I * 4);
+    L.decode_total = o;
+    // grouped path
+    o = L.common_end;
+    L.xs = take(n * (size_t)s.H * 2);
+    L.act_hi = take(n * (size_t)s.I * 2);
+    L.act_lo = take(n * (size_t)s.I * 2);
+    L.z = take(n * (size_t)s.H * 4);
+    L.grouped_total = o;
+    L.total = L.decode_total > L.grouped_total ? L.decode_total : L.grouped_total;
+    return L;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+int check_shape(const Shape &s)
+{
+    if (s.T < 0 || s.H < 1 || s.I < 1 || s.E < 1 || s.k < 1 || s.k > s.E) return MOE_ERR_INVALID_ARG;
+    if (s.E > 1024 || s.k > 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (s.H % 64 || s.I % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (s.T * s.k > INT32_MAX / 2 || s.H > (1 << 24) || s.I > (1 << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+int check_args(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s,
+               const float *out)
+{
+    int st = check_shape(s);
+    if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    if (!x || !logits || !wgu || !wd || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(logits) || !aligned16(wgu) || !aligned16(wd) || !aligned16(out))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+int check_opts(const moe_ffn_opts *o)
+{
+    if (!o) return MOE_OK;
+    if (o->path < MOE_PATH_AUTO || o->path > MOE_PATH_GROUPED) return MOE_ERR_INVALID_ARG;
+    if (o->decode_max_tokens < 0) return MOE_ERR_INVALID_ARG;
+    if (o->gate_up_warps < 0 || o->gate_up_warps > 16) return MOE_ERR_INVALID_ARG;
+    if (o->down_warps < 0 || o->down_warps > 16) return MOE_ERR_INVALID_ARG;
+    if (o->gemm_ctas < 0) return MOE_ERR_INVALID_ARG;
+    for (int r : o->reserved_in)
+        if (r != 0) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+// Per-device one-time set-up: kernel attributes and the SM count.
+struct DeviceInfo {
+    bool ready = false;
+    int n_sm = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+int device_setup(DeviceInfo **info)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::routing_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::decode_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::gemm_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        d.ready = true;
+    }
+    *info = &d;
+    return MOE_OK;
+}
+
+const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
+const char *kGroupedStages[] = {"router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine"};
+
+// Records stage events around the launches of one call.
+struct Stages {
+    cudaEvent_t *ev;
+    cudaStream_t s;
+    int n = 0;
+    cudaError_t begin()
+    {
+        return ev ? cudaEventRecord(ev[0], s) : cudaSuccess;
+    }
+    cudaError_t done(cudaError_t launch)
+    {
+        if (launch != cudaSuccess) return launch;
+        ++n;
+        return ev ? cudaEventRecord(ev[n], s) : cudaSuccess;
+    }
+};
+
+#define MOE_TRY(expr)                                \
+    do {                                             \
+        cudaError_t e_ = (expr);                     \
+        if (e_ != cudaSuccess) return MOE_ERR_CUDA;  \
+    } while (0)
+
+int run_forward(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s, float *out,
+                char *ws, const Layout &L, int32_t *idx_out, float *w_out, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    int st = device_setup(&dev);
+    if (st != MOE_OK) return st;
+
+    const int T = (int)s.T, H = (int)s.H, I = (int)s.I, E = (int)s.E, k = (int)s.k;
+    const int n_assign = T * k;
+    int path = opts ? opts->path : MOE_PATH_AUTO;
+    if (path == MOE_PATH_AUTO) {
+        const int dmax = (opts && opts->decode_max_tokens) ? opts->decode_max_tokens : kDefaultDecodeMaxTokens;
+        path = (T <= dmax || !moe::gemm_supported(H, I)) ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
+    }
+    if (path == MOE_PATH_GROUPED && !moe::gemm_supported(H, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int gu_warps = (opts && opts->gate_up_warps) ? opts->gate_up_warps : kDefaultWarps;
+    const int dn_warps = (opts && opts->down_warps) ? opts->down_warps : kDefaultWarps;
+    const int gemm_ctas = (opts && opts->gemm_ctas) ? opts->gemm_ctas : dev->n_sm;
+
+    auto *idx = (int32_t *)(ws + L.idx);
+    auto *w = (float *)(ws + L.w);
+    auto *offs = (int32_t *)(ws + L.offs);
+    auto *perm = (int32_t *)(ws + L.perm);
+    auto *pos = (int32_t *)(ws + L.pos);
+    auto *uexp = (int32_t *)(ws + L.uexp);
+    auto *ucount = (int32_t *)(ws + L.ucount);
+    auto *chunks = (int4 *)(ws + L.chunks);
+    auto *nchunks = (int32_t *)(ws + L.nchunks);
+
+    Stages stg{opts ? opts->stage_events : nullptr, stream};
+    MOE_TRY(stg.begin());
+    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, idx_out, w_out, stream)));
+    if (path == MOE_PATH_DECODE) {
+        auto *act = (float *)(ws + L.act);
+        MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
+                                          nullptr, nullptr, stream)));
+        MOE_TRY(stg.done(moe::launch_decode_gate_up(x, wgu, uexp, ucount, offs, perm, T, H, I, E, k, gu_warps,
+                                                    act, stream)));
+        MOE_TRY(stg.done(moe::launch_decode_down(act, wd, w, uexp, ucount, offs, perm, T, H, I, k, dn_warps, out,
+                                                 stream)));
+    } else {
+        void *xs = ws + L.xs;
+        void *act_hi = ws + L.act_hi;
+        void *act_lo = ws + L.act_lo;
+        auto *z = (float *)(ws + L.z);
+        MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
+                                          chunks, nchunks, stream)));
+        MOE_TRY(stg.done(moe::launch_gather(x, perm, k, H, n_assign, xs, dev->n_sm, stream)));
+        MOE_TRY(stg.done(moe::launch_gemm_gate_up(xs, wgu, chunks, nchunks, n_assign, H, I, E, act_hi, act_lo,
+                                                  gemm_ctas, stream)));
+        MOE_TRY(stg.done(moe::launch_gemm_down(act_hi, act_lo, wd, chunks, nchunks, n_assign, H, I, E, z,
+                                               gemm_ctas, stream)));
+        MOE_TRY(stg.done(moe::launch_combine(z, w, pos, T, H, k, out, dev->n_sm, stream)));
+    }
+    if (opts) {
+        opts->n_stages = stg.n;
+        opts->path_taken = path;
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_ffn_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k)
+{
+    Shape s{T, H, I, E, k};
+    if (check_shape(s) != MOE_OK) return 0;
+    return make_layout(s).total;
+}
+
+int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+                       const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                       float *out_f32, void *workspace, size_t workspace_bytes, int32_t *topk_idx_out,
+                       float *topk_w_out, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    int st = check_args(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, s, out_f32);
+    if (st != MOE_OK) return st;
+    st = check_opts(opts);
+    if (st != MOE_OK) return st;
+    if (opts) {
+        opts->n_stages = 0;
+        opts->path_taken = 0;
+    }
+    if (T == 0) return MOE_OK;
+    if (!workspace || ((uintptr_t)workspace & 255)) return MOE_ERR_INVALID_ARG;
+    if ((topk_idx_out && !aligned16(topk_idx_out)) || (topk_w_out && !aligned16(topk_w_out)))
+        return MOE_ERR_INVALID_ARG;
+    const Layout L = make_layout(s);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return run_forward(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, s, out_f32, (char *)workspace, L,
+                       topk_idx_out, topk_w_out, opts, stream);
+}
+
+int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+                    const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float *out_f32,
+                    cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    int st = check_args(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, s, out_f32);
+    if (st != MOE_OK || T == 0) return st;
+    const size_t bytes = make_layout(s).total;
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_NO_MEMORY;
+    }
+    st = moe_ffn_forward_ex(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, T, H, I, E, k, out_f32, ws,
+                            bytes, nullptr, nullptr, nullptr, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && st == MOE_OK) st = MOE_ERR_CUDA;
+    return st;
+}
+
+size_t moe_ffn_host_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k)
+{
+    Shape s{T, H, I, E, k};
+    if (check_shape(s) != MOE_OK) return 0;
+    return align256((size_t)(T * H * 2)) + align256((size_t)(T * E * 4)) + align256((size_t)(T * H * 4)) +
+           make_layout(s).total;
+}
+
+int moe_ffn_forward_host(const void *x_host, const float *logits_host, const void *w_gate_up_bf16,
+                         const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                         float *out_host, void *workspace, size_t workspace_bytes, moe_ffn_opts *opts,
+                         cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    int st = check_shape(s);
+    if (st != MOE_OK) return st;
+    st = check_opts(opts);
+    if (st != MOE_OK) return st;
+    if (opts) {
+        opts->n_stages = 0;
+        opts->path_taken = 0;
+    }
+    if (T == 0) return MOE_OK;
+    if (!x_host || !logits_host || !out_host || !w_gate_up_bf16 || !w_down_bf16) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate_up_bf16) || !aligned16(w_down_bf16)) return MOE_ERR_INVALID_ARG;
+    if (!workspace || ((uintptr_t)workspace & 255)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < moe_ffn_host_workspace_bytes(T, H, I, E, k)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    char *p = (char *)workspace;
+    const size_t xb = (size_t)(T * H * 2), lb = (size_t)(T * E * 4), ob = (size_t)(T * H * 4);
+    void *x_dev = p;
+    auto *l_dev = (float *)(p + align256(xb));
+    auto *o_dev = (float *)(p + align256(xb) + align256(lb));
+    char *ws = p + align256(xb) + align256(lb) + align256(ob);
+    const Layout L = make_layout(s);
+    if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpyAsync(l_dev, logits_host, lb, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    st = run_forward(x_dev, l_dev, w_gate_up_bf16, w_down_bf16, s, o_dev, ws, L, nullptr, nullptr, opts, stream);
+    if (st != MOE_OK) return st;
+    if (cudaMemcpyAsync(out_host, o_dev, ob, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+const char *moe_ffn_status_string(int status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_NO_MEMORY: return "workspace allocation failed";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+const char *moe_ffn_stage_name(int path, int stage)
+{
+    if (stage < 0) return nullptr;
+    if (path == MOE_PATH_DECODE && stage < (int)(sizeof kDecodeStages / sizeof *kDecodeStages))
+        return kDecodeStages[stage];
+    if (path == MOE_PATH_GROUPED && stage < (int)(sizeof kGroupedStages / sizeof *kGroupedStages))
+        return kGroupedStages[stage];
+    return nullptr;
+}
+
+int moe_ffn_device_faults(uint32_t *flags, int clear)
+{
+    if (!flags) return MOE_ERR_INVALID_ARG;
+    return moe::read_fault_word(flags, clear != 0) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // extern "C"

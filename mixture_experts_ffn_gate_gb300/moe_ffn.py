@@ -1,0 +1,220 @@
+"""ctypes binding of libmoeffn.so (C ABI in include/moe_ffn.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions carry the C names and take torch tensors for device
+buffers; the stream defaults to torch's current stream.  There is no CPU
+fallback: if the library is not built, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_NO_MEMORY = 4
+MOE_ERR_WORKSPACE_TOO_SMALL = 5
+MOE_ERR_TIMEOUT = 6
+
+MOE_PATH_AUTO = 0
+MOE_PATH_DECODE = 1
+MOE_PATH_GROUPED = 2
+MOE_MAX_STAGES = 8
+
+EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",
+            "moe_ffn_host_workspace_bytes", "moe_ffn_forward_host", "moe_ffn_status_string",
+            "moe_ffn_stage_name", "moe_ffn_device_faults"]
+
+
+class moe_ffn_opts(ctypes.Structure):
+    """Mirror of ``struct moe_ffn_opts``."""
+    _fields_ = [("path", ctypes.c_int32), ("decode_max_tokens", ctypes.c_int32),
+                ("gate_up_warps", ctypes.c_int32), ("down_warps", ctypes.c_int32),
+                ("gemm_ctas", ctypes.c_int32), ("reserved_in", ctypes.c_int32 * 3),
+                ("stage_events", ctypes.c_void_p), ("n_stages", ctypes.c_int32),
+                ("path_taken", ctypes.c_int32), ("reserved_out", ctypes.c_int32 * 2)]
+
+
+class MoeFfnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {moe_ffn_status_string(status)} (status {status})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(
+                    f"{_build.LIB} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(_build.LIB)
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.moe_ffn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
+            L.moe_ffn_workspace_bytes.argtypes = [i64] * 5
+            L.moe_ffn_workspace_bytes.restype = ctypes.c_size_t
+            L.moe_ffn_forward_ex.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp,
+                                             ctypes.c_size_t, vp, vp,
+                                             ctypes.POINTER(moe_ffn_opts), vp]
+            L.moe_ffn_host_workspace_bytes.argtypes = [i64] * 5
+            L.moe_ffn_host_workspace_bytes.restype = ctypes.c_size_t
+            L.moe_ffn_forward_host.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp,
+                                               ctypes.c_size_t, ctypes.POINTER(moe_ffn_opts), vp]
+            L.moe_ffn_status_string.argtypes = [i32]
+            L.moe_ffn_status_string.restype = ctypes.c_char_p
+            L.moe_ffn_stage_name.argtypes = [i32, i32]
+            L.moe_ffn_stage_name.restype = ctypes.c_char_p
+            L.moe_ffn_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
+                      L.moe_ffn_device_faults):
+                f.restype = i32
+            _lib = L
+    return _lib
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(status, what):
+    if status != MOE_OK:
+        raise MoeFfnError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _shape(x, logits, w_gate_up, w_down):
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w_down.shape[2]
+    if logits.shape[0] != T or tuple(w_gate_up.shape) != (E, 2 * I, H) or tuple(w_down.shape) != (E, H, I):
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)} logits {tuple(logits.shape)} "
+                         f"w_gate_up {tuple(w_gate_up.shape)} w_down {tuple(w_down.shape)}")
+    return T, H, I, E
+
+
+def _dev(t, dtype, name):
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+
+
+def moe_ffn_status_string(status: int) -> str:
+    return lib().moe_ffn_status_string(int(status)).decode()
+
+
+def moe_ffn_stage_name(path: int, stage: int):
+    r = lib().moe_ffn_stage_name(int(path), int(stage))
+    return None if r is None else r.decode()
+
+
+def moe_ffn_workspace_bytes(T, H, I, E, k) -> int:
+    return int(lib().moe_ffn_workspace_bytes(T, H, I, E, k))
+
+
+def moe_ffn_host_workspace_bytes(T, H, I, E, k) -> int:
+    return int(lib().moe_ffn_host_workspace_bytes(T, H, I, E, k))
+
+
+def moe_ffn_device_faults(clear: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    _check(lib().moe_ffn_device_faults(ctypes.byref(v), int(clear)), "moe_ffn_device_faults")
+    return int(v.value)
+
+
+def moe_ffn_forward(x, logits, w_gate_up, w_down, k: int, out=None, stream=None):
+    """out[T,H] f32 = layer(x bf16 [T,H], logits f32 [T,E], weights).
+
+    Uses a stream-ordered temporary workspace inside the library.
+    """
+    T, H, I, E = _shape(x, logits, w_gate_up, w_down)
+    for t, d, n in ((x, torch.bfloat16, "x"), (logits, torch.float32, "logits"),
+                    (w_gate_up, torch.bfloat16, "w_gate_up"), (w_down, torch.bfloat16, "w_down")):
+        _dev(t, d, n)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(lib().moe_ffn_forward(_ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down),
+                                 T, H, I, E, k, _ptr(out), _stream(stream)), "moe_ffn_forward")
+    return out
+
+
+def new_workspace(T, H, I, E, k, device="cuda", host=False):
+    """A workspace tensor big enough for this shape (256-byte aligned)."""
+    n = (moe_ffn_host_workspace_bytes if host else moe_ffn_workspace_bytes)(T, H, I, E, k)
+    if n == 0:
+        raise MoeFfnError(MOE_ERR_UNSUPPORTED_SHAPE, "workspace size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_ffn_forward_ex(x, logits, w_gate_up, w_down, k: int, out=None, workspace=None,
+                       topk_idx=None, topk_w=None, opts: moe_ffn_opts | None = None,
+                       stream=None):
+    """The forward pass with a caller-owned workspace, optional routing
+    outputs (int32 / float32 [T,k]) and options.  Returns out."""
+    T, H, I, E = _shape(x, logits, w_gate_up, w_down)
+    for t, d, n in ((x, torch.bfloat16, "x"), (logits, torch.float32, "logits"),
+                    (w_gate_up, torch.bfloat16, "w_gate_up"), (w_down, torch.bfloat16, "w_down")):
+        _dev(t, d, n)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = new_workspace(T, H, I, E, k, device=x.device)
+    if topk_idx is not None:
+        _dev(topk_idx, torch.int32, "topk_idx")
+    if topk_w is not None:
+        _dev(topk_w, torch.float32, "topk_w")
+    _check(lib().moe_ffn_forward_ex(
+        _ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k, _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(topk_idx),
+        _ptr(topk_w), ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "moe_ffn_forward_ex")
+    return out
+
+
+def moe_ffn_forward_host(x_host, logits_host, w_gate_up, w_down, k: int, out_host,
+                         workspace, opts: moe_ffn_opts | None = None, stream=None):
+    """End-to-end call: x_host / logits_host / out_host are (pinned) CPU
+    tensors; copies in and out are enqueued with the forward pass."""
+    T, H = x_host.shape
+    E = logits_host.shape[1]
+    I = w_down.shape[2]
+    for t in (x_host, logits_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors")
+    _check(lib().moe_ffn_forward_host(
+        _ptr(x_host), _ptr(logits_host), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k,
+        _ptr(out_host), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(opts) if opts is not None else None, _stream(stream)),
+        "moe_ffn_forward_host")
+    return out_host
+
+
+def stage_event_array(events):
+    """A C array of cudaEvent_t for moe_ffn_opts.stage_events, from
+    MOE_MAX_STAGES + 1 torch.cuda.Event objects that have been recorded once
+    (torch creates the underlying event on first record)."""
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return arr

@@ -81,21 +81,23 @@ def _randn(shape, std, device, seed):
     return t
 
 
-def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None):
+def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=None):
     """Expert weights (w_gate_up [E,2I,H], w_down [E,H,I]) as BF16 on device.
 
     H, I, E default to the workload's; tests pass smaller ones to reuse the
-    recipe at other sizes.
+    recipe at other sizes.  ``experts`` (a list of expert ids) draws only
+    those blocks, in that order, with the same seeds as the full set.
     """
     H = H or wl.H
     I = I or wl.I
     E = E or wl.E
-    wgu = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=device)
-    wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=device)
-    for e in range(E):
-        wgu[e] = _randn((2 * I, H), 1.0 / math.sqrt(H), device,
+    ids = list(range(E)) if experts is None else list(experts)
+    wgu = torch.empty((len(ids), 2 * I, H), dtype=torch.bfloat16, device=device)
+    wd = torch.empty((len(ids), H, I), dtype=torch.bfloat16, device=device)
+    for j, e in enumerate(ids):
+        wgu[j] = _randn((2 * I, H), 1.0 / math.sqrt(H), device,
                         seed_for(wl.name, H, I, "w_gate_up", e)).to(torch.bfloat16)
-        wd[e] = _randn((H, I), 1.0 / math.sqrt(I), device,
+        wd[j] = _randn((H, I), 1.0 / math.sqrt(I), device,
                        seed_for(wl.name, H, I, "w_down", e)).to(torch.bfloat16)
     return wgu, wd
 

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle on the
+same seeded bytes, element by element, on sizes the oracle finishes in
+seconds (several tiles and a ragged tail), on edge cases, and on metamorphic
+properties that must hold bit-exactly."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_gate_gb300 import moe_ffn as m
+from mixture_experts_ffn_gate_gb300 import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+PATH_IDS = ["decode", "grouped"]
+
+
+@pytest.fixture(autouse=True)
+def _no_faults():
+    yield
+    assert m.moe_ffn_device_faults(clear=True) == 0, "a kernel's bounded wait gave up"
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+def test_tiny_workload(path):
+    wl = synth.WORKLOADS["tiny_t4_h256_i128_e8_k2"]
+    x, L, wgu, wd = gu.make_layer(wl, 4)
+    out, idx, w = gu.run_gpu(x, L, wgu, wd, wl.k, path)
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, wl.k), what=wl.name)
+
+
+# (T, H, I, E, k, bias_var): several tiles, ragged tails (H or I not a
+# multiple of 128/256), k = 1, k = E, a single expert, skewed routing.
+SHAPES = [
+    (1, 256, 128, 8, 2, 0.0),
+    (3, 320, 192, 5, 3, 0.0),
+    (37, 512, 192, 16, 4, 0.5),
+    (64, 384, 320, 12, 1, 0.0),
+    (9, 256, 128, 6, 6, 0.0),
+    (5, 128, 64, 1, 1, 0.0),
+    (130, 640, 256, 32, 8, 1.0),
+    (300, 256, 128, 4, 2, 4.0),   # heavy skew: > 256 tokens on one expert
+]
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "T%d_H%d_I%d_E%d_k%d" % s[:5])
+def test_shapes(path, shape):
+    T, H, I, E, k, bv = shape
+    wl = gu.custom(T, H, I, E, k, bv, name="shape_%d_%d_%d_%d_%d" % shape[:5])
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    out, idx, w = gu.run_gpu(x, L, wgu, wd, k, path)
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what=str(shape))
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+def test_exact_ties_and_signed_zero(path):
+    """Logits drawn from {-1, 0, 1} (and -0.0): ties everywhere; indices must
+    match the oracle's lower-index rule bit for bit."""
+    T, H, I, E, k = 40, 256, 128, 16, 5
+    wl = gu.custom(T, H, I, E, k, name="ties")
+    x, _, wgu, wd = gu.make_layer(wl, T)
+    g = torch.Generator().manual_seed(5)
+    L = (torch.randint(-1, 2, (T, E), generator=g).float())
+    L[L == 0] = -0.0 * torch.ones_like(L[L == 0])
+    L[::2, 3] = 0.0
+    L = L.cuda()
+    out, idx, w = gu.run_gpu(x, L, wgu, wd, k, path)
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what="ties")
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+def test_zero_input_gives_zero(path):
+    T, H, I, E, k = 7, 256, 128, 8, 2
+    wl = gu.custom(T, H, I, E, k, name="zero")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    out, _, _ = gu.run_gpu(torch.zeros_like(x), L, wgu, wd, k, path)
+    assert torch.all(out == 0)
+
+
+def test_zero_tokens():
+    wl = synth.WORKLOADS["tiny_t4_h256_i128_e8_k2"]
+    _, _, wgu, wd = gu.make_layer(wl, 4)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    L = torch.empty((0, 8), dtype=torch.float32, device="cuda")
+    out = m.moe_ffn_forward(x, L, wgu, wd, 2)
+    assert out.shape == (0, 256)
+    out = m.moe_ffn_forward_ex(x, L, wgu, wd, 2)
+    assert out.shape == (0, 256)
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+def test_metamorphic_bit_exact(path):
+    """Token permutation permutes rows; a token alone equals the same token
+    inside the batch; doubling W_down doubles the output -- all bit for bit."""
+    T, H, I, E, k = 24, 512, 256, 16, 4
+    wl = gu.custom(T, H, I, E, k, 0.5, name="meta")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    out, _, _ = gu.run_gpu(x, L, wgu, wd, k, path)
+    p = torch.randperm(T, generator=torch.Generator().manual_seed(3))
+    outp, _, _ = gu.run_gpu(x[p.cuda()].contiguous(), L[p.cuda()].contiguous(), wgu, wd, k, path)
+    assert torch.equal(outp, out[p])
+    for t in (0, 11, T - 1):
+        o1, _, _ = gu.run_gpu(x[t:t + 1].contiguous(), L[t:t + 1].contiguous(), wgu, wd, k, path)
+        assert torch.equal(o1[0], out[t]), t
+    out2, _, _ = gu.run_gpu(x, L, wgu, (wd.float() * 2).to(torch.bfloat16), k, path)
+    assert torch.equal(out2, out * 2)
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+def test_repeatable_100_runs(path):
+    T, H, I, E, k = 48, 512, 256, 32, 8
+    wl = gu.custom(T, H, I, E, k, 1.0, name="repeat")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    first, idx0, w0 = gu.run_gpu(x, L, wgu, wd, k, path)
+    ws = m.new_workspace(T, H, I, E, k)
+    o = m.moe_ffn_opts()
+    o.path = gu.PATHS[path]
+    outs = [m.moe_ffn_forward_ex(x, L, wgu, wd, k, workspace=ws, opts=o) for _ in range(100)]
+    torch.cuda.synchronize()
+    for r in outs:
+        assert torch.equal(r.cpu(), first)
+
+
+def test_decode_launch_config_sweep():
+    T, H, I, E, k = 20, 768, 320, 24, 6
+    wl = gu.custom(T, H, I, E, k, 0.5, name="sweep")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    ref, _, _ = gu.run_gpu(x, L, wgu, wd, k, "decode")
+    for gw in (1, 2, 4, 16):
+        for dw in (1, 3, 16):
+            out, _, _ = gu.run_gpu(x, L, wgu, wd, k, "decode", gate_up_warps=gw, down_warps=dw)
+            assert torch.equal(out, ref), (gw, dw)
+
+
+def test_grouped_launch_config_sweep():
+    T, H, I, E, k = 200, 512, 256, 12, 4
+    wl = gu.custom(T, H, I, E, k, 2.0, name="gsweep")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    ref, _, _ = gu.run_gpu(x, L, wgu, wd, k, "grouped")
+    for ctas in (1, 7, 64, 300):
+        out, _, _ = gu.run_gpu(x, L, wgu, wd, k, "grouped", gemm_ctas=ctas)
+        assert torch.equal(out, ref), ctas
+
+
+def test_auto_path_choice():
+    T, H, I, E, k = 80, 256, 128, 8, 2
+    wl = gu.custom(T, H, I, E, k, name="auto")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    for thr, want in ((0, m.MOE_PATH_GROUPED), (80, m.MOE_PATH_DECODE), (79, m.MOE_PATH_GROUPED)):
+        o = m.moe_ffn_opts()
+        o.decode_max_tokens = thr
+        m.moe_ffn_forward_ex(x, L, wgu, wd, k, opts=o)
+        assert o.path_taken == want, (thr, o.path_taken)
+        assert o.n_stages == (4 if want == m.MOE_PATH_DECODE else 6)
+
+
+def test_plain_forward_and_host_entry_match_ex():
+    T, H, I, E, k = 6, 512, 192, 16, 4
+    wl = gu.custom(T, H, I, E, k, name="entries")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    ref = m.moe_ffn_forward_ex(x, L, wgu, wd, k)
+    plain = m.moe_ffn_forward(x, L, wgu, wd, k)
+    xh = x.cpu().pin_memory()
+    lh = L.cpu().pin_memory()
+    oh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    ws = m.new_workspace(T, H, I, E, k, host=True)
+    m.moe_ffn_forward_host(xh, lh, wgu, wd, k, oh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(plain, ref) and torch.equal(oh, ref.cpu())
+
+
+def test_stage_events_time_each_kernel():
+    T, H, I, E, k = 4, 256, 128, 8, 2
+    wl = gu.custom(T, H, I, E, k, name="events")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
+    for e in evs:
+        e.record()
+    arr = m.stage_event_array(evs)
+    o = m.moe_ffn_opts()
+    o.stage_events = m.ctypes.cast(arr, m.ctypes.c_void_p)
+    m.moe_ffn_forward_ex(x, L, wgu, wd, k, opts=o)
+    torch.cuda.synchronize()
+    assert o.n_stages == 4
+    for i in range(o.n_stages):
+        assert evs[i].elapsed_time(evs[i + 1]) >= 0.0
+
+
+def test_errors_from_device_pointers():
+    """Bad shapes and a short workspace come back as status codes."""
+    T, H, I, E, k = 4, 256, 128, 8, 2
+    wl = gu.custom(T, H, I, E, k, name="errs")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    with pytest.raises(m.MoeFfnError) as ei:
+        m.moe_ffn_forward_ex(x, L, wgu, wd, 9)
+    assert ei.value.status in (m.MOE_ERR_INVALID_ARG, m.MOE_ERR_UNSUPPORTED_SHAPE)
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.MoeFfnError) as ei:
+        m.moe_ffn_forward_ex(x, L, wgu, wd, k, workspace=small)
+    assert ei.value.status == m.MOE_ERR_WORKSPACE_TOO_SMALL
