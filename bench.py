@@ -58,6 +58,7 @@ def parse():
     p.add_argument("--T", type=int, default=None)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--skip-baseline", action="store_true", help="omit the CPU oracle timing")
     return p.parse_args()
 
 
@@ -425,7 +426,7 @@ def main():
                        "h2d_bytes_per_step": T * wl.H * 2 + T * wl.E * 4,
                        "d2h_bytes_per_step": T * wl.H * 4}
     line["clocks"] = clocks.summary()
-    if world == 1:
+    if world == 1 and not args.skip_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T, wgu, wd, batches)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -1,10 +1,48 @@
-// grouped_gemm.cu -- the large-T path's grouped GEMMs (tcgen05, TMEM, TMA).
+// grouped_gemm.cu -- the large-T path's grouped GEMMs on the 5th-generation
+// tensor cores (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+//
+// Large batches are the regime where grouping tokens by expert pays (the
+// warp-decode article, section 배경 및 맥락, calls expert-grouped MoE efficient
+// for training and large batches, and section 경쟁 구도 / 비교 treats prefill
+// and decode as different problems).  After the counting sort, the tokens of
+// expert e are rows [offs[e], offs[e+1]) of the sorted order, cut into chunks
+// of at most kGemmChunkMax rows.
+//
+// Both GEMMs put the expert's weight rows on the MMA's M side (M = 128) and
+// the chunk's tokens on the N side (N = chunk rounded up to 16, <= 128), so
+// a skewed or tiny expert load never pads the weight tile:
+//   gate_up: D[128 x N] = W_gu[e][rows] . xs[chunk]^T, K = H.  The 128 rows of
+//            a tile are 4 groups of (16 gate rows i.., 16 up rows I+i..), so
+//            each epilogue warp holds gate and up of the same 16 neurons in
+//            its lanes 0-15 / 16-31 and pairs them with one shuffle.  The
+//            epilogue writes act = silu(g)*u as an unevaluated BF16 pair
+//            hi = bf16(act), lo = bf16(act - hi), keeping ~16 significant
+//            bits of the FP32 intermediate for the down GEMM (split-precision
+//            products as in Markidis et al. 2018, "NVIDIA Tensor Core
+//            Programmability, Performance & Precision").
+//   down:    D[128 x N] = W_down[e][h0:h0+128] . (act_hi + act_lo)[chunk]^T,
+//            K = I, two MMAs per K step into one accumulator; the epilogue
+//            writes z[sorted row, h] in FP32.
+// Every output element is one MMA chain over K in a fixed order, so results
+// do not depend on the grid size or on which CTA ran which tile.
+//
+// One persistent CTA per SM: warp 0 issues TMA loads into a ring of smem
+// stages, warp 1 issues tcgen05.mma into one of two TMEM accumulators,
+// warps 2-5 drain the other accumulator (tcgen05.ld) and store.  Every
+// mbarrier wait is bounded: on time-out the CTA raises a bit in the device
+// fault word, lets its copies and MMAs in flight finish (again bounded),
+// frees its TMEM and returns.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 
 __device__ uint32_t g_fault_word = 0;
+
+__device__ __forceinline__ void raise_fault(uint32_t bit) { atomicOr(&g_fault_word, bit); }
 
 cudaError_t read_fault_word(uint32_t *flags, bool clear)
 {
@@ -14,20 +52,347 @@ cudaError_t read_fault_word(uint32_t *flags, bool clear)
     return cudaMemcpyToSymbol(g_fault_word, &zero, sizeof(uint32_t));
 }
 
-cudaError_t gemm_init_device() { return cudaSuccess; }
+namespace {
 
-bool gemm_supported(int, int) { return false; }
+constexpr int BM = 128;                  // weight rows per tile (MMA M)
+constexpr int BK = 64;                   // K elements per stage: one 128-byte swizzle row
+constexpr int NMAX = kGemmChunkMax;      // tokens per chunk (MMA N <= NMAX)
+constexpr int ACC_COLS = 128;            // TMEM columns per accumulator (>= NMAX)
+constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulators
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain after an abort
 
-cudaError_t launch_gemm_gate_up(const void *, const void *, const int4 *, const int32_t *, int, int, int, int, void *,
-                                void *, int, cudaStream_t)
+static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulator");
+
+template <bool GATE_UP>
+struct Cfg {
+    static constexpr int STAGES = GATE_UP ? 6 : 4;
+    static constexpr int A_BYTES = BM * BK * 2;                           // 16 KB
+    static constexpr int B_TILE = NMAX * BK * 2;                          // 16 KB per operand
+    static constexpr int B_BYTES = B_TILE * (GATE_UP ? 1 : 2);            // x | act_hi + act_lo
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+};
+
+struct GemmArgs {
+    const int4 *chunks;   // {expert, first sorted row, rows, first chunk of expert}
+    const int32_t *nchunks;
+    const int32_t *offs;  // [E+1] sorted-row offsets per expert
+    int H, I;
+    int K;                // reduction length (H or I)
+    int m_tiles;          // weight tiles per expert
+    void *out0, *out1;    // act_hi, act_lo | z
+};
+
+struct Item {
+    int e, p0, n, m;
+};
+
+// Item i of the flat list: experts in order; within an expert, weight tile m
+// major and chunk minor, so the chunks that reuse one weight tile are
+// adjacent (they run at about the same time and share it through L2).
+__device__ __forceinline__ Item decode_item(int i, const GemmArgs &a)
 {
-    return cudaErrorNotSupported;
+    const int4 ch = __ldg(a.chunks + i / a.m_tiles);
+    const int e = ch.x, c0 = ch.w;
+    const int cnt = __ldg(a.offs + e + 1) - __ldg(a.offs + e);
+    const int nc = (cnt + NMAX - 1) / NMAX;
+    const int q = i - c0 * a.m_tiles;
+    const int m = q / nc, c = c0 + (q - m * nc);
+    const int4 cq = __ldg(a.chunks + c);
+    return {e, cq.y, cq.z, m};
 }
 
-cudaError_t launch_gemm_down(const void *, const void *, const void *, const int4 *, const int32_t *, int, int, int,
-                             int, float *, int, cudaStream_t)
+__device__ __forceinline__ int pad16(int n) { return (n + 15) & ~15; }
+
+template <bool GATE_UP>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
 {
-    return cudaErrorNotSupported;
+    using C = Cfg<GATE_UP>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + C::STAGES * C::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t *empty = full + C::STAGES;
+    uint64_t *tfull = empty + C::STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(full + s, 1);
+            ptx::mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull + b, 1);
+            ptx::mbar_init(tempty + b, 4);
+        }
+        ptx::mbar_init(drain, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB0);
+        if (!GATE_UP) ptx::prefetch_tensormap(&tmB1);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int total = __ldg(args.nchunks) * args.m_tiles;
+    const int KB = args.K / BK;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed[C::STAGES];
+            for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
+            for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
+                const Item it = decode_item(i, args);
+                const int nb = pad16(it.n) / 16;
+                const uint32_t bytes = C::A_BYTES + nb * 16 * BK * 2 * (GATE_UP ? 1 : 2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!ptx::mbar_wait_bounded(empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
+                        if (!*abort_flag) raise_fault(FAULT_GEMM_PRODUCER);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full + stage, bytes);
+                    ++armed[stage];
+                    const int k0 = kb * BK;
+                    uint8_t *a = sA + stage * C::A_BYTES;
+                    if (GATE_UP) {
+                        const int row0 = it.e * 2 * args.I + it.m * 64;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            ptx::tma_load_2d(a + g * 4096, &tmA, k0, row0 + 16 * g, full + stage);
+                            ptx::tma_load_2d(a + g * 4096 + 2048, &tmA, k0, row0 + args.I + 16 * g, full + stage);
+                        }
+                    } else {
+                        ptx::tma_load_2d(a, &tmA, k0, it.e * args.H + it.m * BM, full + stage);
+                    }
+                    uint8_t *b = sB + stage * C::B_BYTES;
+                    for (int j = 0; j < nb; ++j) {
+                        ptx::tma_load_2d(b + j * 2048, &tmB0, k0, it.p0 + 16 * j, full + stage);
+                        if (!GATE_UP)
+                            ptx::tma_load_2d(b + C::B_TILE + j * 2048, &tmB1, k0, it.p0 + 16 * j, full + stage);
+                    }
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            // let every armed copy land before the CTA can exit (the last
+            // armed phase of each stage completes after all earlier ones)
+            const volatile int keep_waiting = 0;
+            for (int s = 0; s < C::STAGES; ++s)
+                if (armed[s]) ptx::mbar_wait_bounded(full + s, (armed[s] - 1) & 1, &keep_waiting, kDrainLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int li = 0;
+            for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++li) {
+                const Item it = decode_item(i, args);
+                const uint32_t idesc = ptx::idesc_bf16_f32(BM, pad16(it.n));
+                const int acc = li & 1;
+                const uint32_t aph = (li >> 1) & 1;
+                if (!ptx::mbar_wait_bounded(tempty + acc, aph ^ 1, abort_flag, kWaitLimitNs)) {
+                    if (!*abort_flag) raise_fault(FAULT_GEMM_MMA);
+                    *abort_flag = 1;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem + acc * ACC_COLS;
+                bool ok = true;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!ptx::mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
+                        if (!*abort_flag) raise_fault(FAULT_GEMM_MMA);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = ptx::smem_u32(sA + stage * C::A_BYTES);
+                    const uint32_t b_addr = ptx::smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = ptx::sw128_desc(a_addr + k * 32);
+                        ptx::mma_bf16(d, ad, ptx::sw128_desc(b_addr + k * 32), idesc, (kb | k) != 0);
+                        if (!GATE_UP)
+                            ptx::mma_bf16(d, ad, ptx::sw128_desc(b_addr + C::B_TILE + k * 32), idesc, 1);
+                    }
+                    ptx::mma_commit(empty + stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull + acc);
+            }
+            // every MMA this thread issued has completed once drain fires
+            ptx::mma_commit(drain);
+            ptx::mbar_wait_bounded(drain, 0, abort_flag, kDrainLimitNs);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int li = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x, ++li) {
+            const Item it = decode_item(i, args);
+            const int acc = li & 1;
+            const uint32_t aph = (li >> 1) & 1;
+            if (!ptx::mbar_wait_bounded(tfull + acc, aph, abort_flag, kWaitLimitNs)) {
+                if (!*abort_flag) raise_fault(FAULT_GEMM_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * ACC_COLS;
+            for (int c0 = 0; c0 < it.n; c0 += 32) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tbase + c0, r);
+                ptx::tmem_wait_ld();
+                if (GATE_UP) {
+                    const int neuron = it.m * 64 + 16 * q + (lane & 15);
+                    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(lane < 16 ? args.out0 : args.out1);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float v = __uint_as_float(r[j]);
+                        const float o = __shfl_xor_sync(0xffffffffu, v, 16);
+                        const float a = lane < 16 ? swiglu(v, o) : swiglu(o, v);
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
+                        if (c0 + j < it.n)
+                            dst[(int64_t)(it.p0 + c0 + j) * args.I + neuron] = lane < 16 ? hi : lo;
+                    }
+                } else {
+                    const int h = it.m * BM + 32 * q + lane;
+                    float *z = reinterpret_cast<float *>(args.out0);
+                    if (h < args.H) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (c0 + j < it.n) z[(int64_t)(it.p0 + c0 + j) * args.H + h] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty + acc);
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder()
+{
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// A 2D BF16 tensor map over a row-major [rows, cols] matrix, box = 64 columns
+// (128 bytes, 128-byte swizzle) x box_rows rows.  Rows past the end read 0.
+cudaError_t make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {BK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int grid_for(int ctas, int n_assign, int m_tiles, int E)
+{
+    // an upper bound on the number of items: chunks <= E + n_assign / NMAX
+    const int64_t max_items = ((int64_t)E + n_assign / NMAX + 1) * m_tiles;
+    return (int)(ctas < max_items ? ctas : max_items);
+}
+
+}  // namespace
+
+cudaError_t gemm_init_device()
+{
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<true>::SMEM);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<false>::SMEM);
+}
+
+bool gemm_supported(int H, int I, int E)
+{
+    // TMA row coordinates are int32: the weight matrices' row counts must fit
+    return H % 64 == 0 && I % 64 == 0 && (int64_t)E * 2 * I < INT32_MAX && (int64_t)E * H < INT32_MAX &&
+           encoder() != nullptr;
+}
+
+cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chunks, const int32_t *nchunks,
+                                const int32_t *offs, int n_assign, int H, int I, int E, void *act_hi, void *act_lo,
+                                int ctas, cudaStream_t s)
+{
+    CUtensorMap tA, tB;
+    cudaError_t e = make_map(&tA, wgu, (uint64_t)E * 2 * I, H, 16);
+    if (e == cudaSuccess) e = make_map(&tB, xs, n_assign, H, 16);
+    if (e != cudaSuccess) return e;
+    GemmArgs a{chunks, nchunks, offs, H, I, H, I / 64, act_hi, act_lo};
+    grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<true>::SMEM, s>>>(tA, tB, tB,
+                                                                                                          a);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void *wd, const int4 *chunks,
+                             const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, float *z,
+                             int ctas, cudaStream_t s)
+{
+    CUtensorMap tA, tB0, tB1;
+    cudaError_t e = make_map(&tA, wd, (uint64_t)E * H, I, BM);
+    if (e == cudaSuccess) e = make_map(&tB0, act_hi, n_assign, I, 16);
+    if (e == cudaSuccess) e = make_map(&tB1, act_lo, n_assign, I, 16);
+    if (e != cudaSuccess) return e;
+    GemmArgs a{chunks, nchunks, offs, H, I, I, (H + BM - 1) / BM, z, nullptr};
+    grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(tA, tB0,
+                                                                                                            tB1, a);
+    return cudaPeekAtLastError();
 }
 
 }  // namespace moe

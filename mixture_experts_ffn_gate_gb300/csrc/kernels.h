@@ -7,7 +7,7 @@
 namespace moe {
 
 // Grouped path: at most this many assignments (token rows) per GEMM N-chunk.
-constexpr int kGemmChunkMax = 256;
+constexpr int kGemmChunkMax = 128;
 
 // routing.cu
 cudaError_t routing_init_device();
@@ -34,13 +34,13 @@ cudaError_t launch_decode_down(const float *act, const void *wd, const float *w,
 
 // grouped_gemm.cu
 cudaError_t gemm_init_device();
-bool gemm_supported(int H, int I);
+bool gemm_supported(int H, int I, int E);
 cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chunks, const int32_t *nchunks,
-                                int n_assign, int H, int I, int E, void *act_hi, void *act_lo, int ctas,
-                                cudaStream_t s);
+                                const int32_t *offs, int n_assign, int H, int I, int E, void *act_hi, void *act_lo,
+                                int ctas, cudaStream_t s);
 cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void *wd, const int4 *chunks,
-                             const int32_t *nchunks, int n_assign, int H, int I, int E, float *z, int ctas,
-                             cudaStream_t s);
+                             const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, float *z,
+                             int ctas, cudaStream_t s);
 cudaError_t read_fault_word(uint32_t *flags, bool clear);
 
 }  // namespace moe

@@ -163,9 +163,9 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
     int path = opts ? opts->path : MOE_PATH_AUTO;
     if (path == MOE_PATH_AUTO) {
         const int dmax = (opts && opts->decode_max_tokens) ? opts->decode_max_tokens : kDefaultDecodeMaxTokens;
-        path = (T <= dmax || !moe::gemm_supported(H, I)) ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
+        path = (T <= dmax || !moe::gemm_supported(H, I, E)) ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
     }
-    if (path == MOE_PATH_GROUPED && !moe::gemm_supported(H, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (path == MOE_PATH_GROUPED && !moe::gemm_supported(H, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
     const int gu_warps = (opts && opts->gate_up_warps) ? opts->gate_up_warps : kDefaultWarps;
     const int dn_warps = (opts && opts->down_warps) ? opts->down_warps : kDefaultWarps;
     const int gemm_ctas = (opts && opts->gemm_ctas) ? opts->gemm_ctas : dev->n_sm;
@@ -199,9 +199,9 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
         MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
                                           chunks, nchunks, stream)));
         MOE_TRY(stg.done(moe::launch_gather(x, perm, k, H, n_assign, xs, dev->n_sm, stream)));
-        MOE_TRY(stg.done(moe::launch_gemm_gate_up(xs, wgu, chunks, nchunks, n_assign, H, I, E, act_hi, act_lo,
-                                                  gemm_ctas, stream)));
-        MOE_TRY(stg.done(moe::launch_gemm_down(act_hi, act_lo, wd, chunks, nchunks, n_assign, H, I, E, z,
+        MOE_TRY(stg.done(moe::launch_gemm_gate_up(xs, wgu, chunks, nchunks, offs, n_assign, H, I, E, act_hi,
+                                                  act_lo, gemm_ctas, stream)));
+        MOE_TRY(stg.done(moe::launch_gemm_down(act_hi, act_lo, wd, chunks, nchunks, offs, n_assign, H, I, E, z,
                                                gemm_ctas, stream)));
         MOE_TRY(stg.done(moe::launch_combine(z, w, pos, T, H, k, out, dev->n_sm, stream)));
     }

@@ -137,13 +137,14 @@ __global__ void __launch_bounds__(SORT_THREADS) sort_kernel(const int32_t *__res
     const int slot = block_exclusive_scan(touched, scratch, &n_touched);
     if (touched) uexp[slot] = e;
     if (tid == 0) *ucount = n_touched;
-    // row chunks of at most chunk_max assignments per expert (grouped GEMMs)
+    // row chunks of at most chunk_max assignments per expert (grouped GEMMs):
+    // {expert, first sorted row, rows, index of the expert's first chunk}
     if (chunks) {
         const int nch = (e < E) ? (cnt + chunk_max - 1) / chunk_max : 0;
         int n_total;
         const int c0 = block_exclusive_scan(nch, scratch, &n_total);
         for (int c = 0; c < nch; ++c)
-            chunks[c0 + c] = make_int4(e, off + c * chunk_max, min(chunk_max, cnt - c * chunk_max), 0);
+            chunks[c0 + c] = make_int4(e, off + c * chunk_max, min(chunk_max, cnt - c * chunk_max), c0);
         if (tid == 0) *nchunks = n_total;
     }
     __syncthreads();
