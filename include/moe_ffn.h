@@ -152,6 +152,30 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host,
                          size_t workspace_bytes, moe_ffn_opts *opts,
                          cudaStream_t stream);
 
+/*
+ * No counterpart in the pages: an entry point for callers that cannot
+ * allocate device memory once they are running -- a serving loop whose
+ * latency budget cannot absorb an allocation that may synchronise the device
+ * or fail under memory pressure, or a plugin whose host engine owns all
+ * device memory through its own pool.  Same arguments, path choice and
+ * results as moe_ffn_forward, but the scratch lives in a fixed device array
+ * of MOE_FFN_NOALLOC_SCRATCH_BYTES inside the library (present in every GPU
+ * context that loads the library, until the process exits); the call
+ * allocates nothing.  Shapes whose workspace (moe_ffn_workspace_bytes)
+ * exceeds that size return MOE_ERR_WORKSPACE_TOO_SMALL before anything is
+ * enqueued.  The first call on each device looks up the array's device
+ * address (set-up, once per device, with that device current); make that
+ * first call before any stream capture.  All calls share the array: calls
+ * whose GPU work overlaps (other streams, unordered host threads) race and
+ * return wrong results, so order them on one stream.  Nothing in the array
+ * needs to start at zero; each call writes every byte it later reads.
+ */
+#define MOE_FFN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int moe_ffn_forward_noalloc(const void *x_bf16, const float *router_logits_f32,
+                            const void *w_gate_up_bf16, const void *w_down_bf16,
+                            int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                            float *out_f32, cudaStream_t stream);
+
 /* Static text for a status code. */
 const char *moe_ffn_status_string(int status);
 

@@ -30,7 +30,10 @@ MOE_MAX_STAGES = 8
 
 EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",
             "moe_ffn_host_workspace_bytes", "moe_ffn_forward_host", "moe_ffn_status_string",
-            "moe_ffn_stage_name", "moe_ffn_device_faults"]
+            "moe_ffn_stage_name", "moe_ffn_device_faults", "moe_ffn_forward_noalloc"]
+
+# Size of the library's fixed scratch array used by moe_ffn_forward_noalloc.
+MOE_FFN_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class moe_ffn_opts(ctypes.Structure):
@@ -82,8 +85,9 @@ def lib():
             L.moe_ffn_stage_name.argtypes = [i32, i32]
             L.moe_ffn_stage_name.restype = ctypes.c_char_p
             L.moe_ffn_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            L.moe_ffn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
             for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
-                      L.moe_ffn_device_faults):
+                      L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc):
                 f.restype = i32
             _lib = L
     return _lib
@@ -158,6 +162,25 @@ def moe_ffn_forward(x, logits, w_gate_up, w_down, k: int, out=None, stream=None)
     _dev(out, torch.float32, "out")
     _check(lib().moe_ffn_forward(_ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down),
                                  T, H, I, E, k, _ptr(out), _stream(stream)), "moe_ffn_forward")
+    return out
+
+
+def moe_ffn_forward_noalloc(x, logits, w_gate_up, w_down, k: int, out=None, stream=None):
+    """The forward pass for callers that cannot allocate device memory: the
+    library keeps its scratch in a fixed device array of
+    MOE_FFN_NOALLOC_SCRATCH_BYTES, shared by every call (order calls on one
+    stream).  ``out`` should be passed by such callers; when it is None this
+    wrapper allocates it with torch, for convenience only."""
+    T, H, I, E = _shape(x, logits, w_gate_up, w_down)
+    for t, d, n in ((x, torch.bfloat16, "x"), (logits, torch.float32, "logits"),
+                    (w_gate_up, torch.bfloat16, "w_gate_up"), (w_down, torch.bfloat16, "w_down")):
+        _dev(t, d, n)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    _check(lib().moe_ffn_forward_noalloc(_ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down),
+                                         T, H, I, E, k, _ptr(out), _stream(stream)),
+           "moe_ffn_forward_noalloc")
     return out
 
 
