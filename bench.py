@@ -56,6 +56,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--T", type=int, default=None)
+    p.add_argument("--E", type=int, default=None, help="fewer experts (profiling-size variant)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--skip-baseline", action="store_true", help="omit the CPU oracle timing")
@@ -259,6 +260,9 @@ def main():
     args = parse()
     from mixture_experts_ffn_gate_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
+    if args.E is not None:   # a smaller variant of the shape, for profiler captures
+        import dataclasses
+        wl = dataclasses.replace(wl, E=args.E, name=f"{wl.name}_e{args.E}")
     T = args.T if args.T is not None else wl.T[0]
     if args.impl == "reference":
         reference_arm(args, wl, T)
