@@ -42,8 +42,8 @@ FLUSH_BYTES = 512 << 20
 
 # Kernel sources whose change voids a stored ncu traffic figure.
 KERNEL_SOURCES = {
-    "decode_gate_up": ["decode.cu"],
-    "decode_down": ["decode.cu"],
+    "decode_gate_up": ["decode.cu", "decode1.cu"],
+    "decode_down": ["decode.cu", "decode1.cu"],
     "gemm_gate_up": ["grouped_gemm.cu"],
     "gemm_down": ["grouped_gemm.cu"],
 }

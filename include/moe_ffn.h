@@ -71,7 +71,10 @@ enum {
 enum {
     MOE_PATH_AUTO = 0,    /* decode for T <= decode_max_tokens, else grouped */
     MOE_PATH_DECODE = 1,  /* warp per output scalar, weights streamed once   */
-    MOE_PATH_GROUPED = 2  /* counting sort + tcgen05 grouped GEMMs + combine */
+    MOE_PATH_GROUPED = 2, /* counting sort + tcgen05 grouped GEMMs + combine */
+    MOE_PATH_DECODE_T1 = 3 /* reported only (path_taken): the decode path for
+                              T == 1, two kernels that route the token
+                              themselves; same results as MOE_PATH_DECODE */
 };
 
 #define MOE_MAX_STAGES 8
@@ -82,7 +85,7 @@ enum {
  */
 typedef struct moe_ffn_opts {
     /* inputs */
-    int32_t path;              /* MOE_PATH_* */
+    int32_t path;              /* MOE_PATH_AUTO, _DECODE or _GROUPED */
     int32_t decode_max_tokens; /* AUTO threshold on T (default 64) */
     int32_t gate_up_warps;     /* decode gate_up: warps per block, 1..16 (default 8) */
     int32_t down_warps;        /* decode down: warps per block, 1..16 (default 8) */
@@ -96,7 +99,7 @@ typedef struct moe_ffn_opts {
     cudaEvent_t *stage_events;
     /* outputs */
     int32_t n_stages;          /* kernels the call enqueued */
-    int32_t path_taken;        /* MOE_PATH_DECODE or MOE_PATH_GROUPED */
+    int32_t path_taken;        /* MOE_PATH_DECODE, _DECODE_T1 or _GROUPED */
     int32_t reserved_out[2];
 } moe_ffn_opts;
 

@@ -32,6 +32,16 @@ cudaError_t launch_decode_down(const float *act, const void *wd, const float *w,
                                const int32_t *ucount, const int32_t *offs, const int32_t *perm, int T, int H,
                                int I, int k, int warps, float *out, cudaStream_t s);
 
+// decode1.cu (single token)
+cudaError_t decode1_init_device();
+cudaError_t read_decode1_fault_word(uint32_t *flags, bool clear);
+bool decode1_supported(int H, int I, int E, int k, int n_sm);
+// gate_up then (programmatic dependent) down; gu = [k][2I] FP32 scratch.  If
+// `between` is set it is recorded on s between the two kernels.
+cudaError_t launch_decode1(const void *x, const float *logits, const void *wgu, const void *wd, int H, int I, int E,
+                           int k, int n_sm, float *gu, int32_t *idx_out, float *w_out, float *out, cudaStream_t s,
+                           cudaEvent_t between);
+
 // grouped_gemm.cu
 cudaError_t gemm_init_device();
 bool gemm_supported(int H, int I, int E);

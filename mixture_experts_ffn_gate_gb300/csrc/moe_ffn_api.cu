@@ -50,8 +50,9 @@ Layout make_layout(const Shape &s)
     L.chunks = take((size_t)(s.E + ceil_div((int64_t)n, moe::kGemmChunkMax) + 1) * 16);
     L.nchunks = take(4);
     L.common_end = o;
-    // decode path
-    L.act = take(n * (size_t)s.I * 4);
+    // decode path: act f32 [T*k, I]; the single-token kernels keep the gate
+    // and up dot products there instead, [k, 2I]
+    L.act = take(n * (size_t)s.I * 8);
     L.decode_total = o;
     // grouped path
     o = L.common_end;
@@ -118,6 +119,7 @@ int device_setup(DeviceInfo **info)
         if (cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::routing_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::decode_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::decode1_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::gemm_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         d.ready = true;
     }
@@ -126,6 +128,7 @@ int device_setup(DeviceInfo **info)
 }
 
 const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
+const char *kDecodeT1Stages[] = {"decode_gate_up", "decode_down"};
 const char *kGroupedStages[] = {"router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine"};
 
 // Records stage events around the launches of one call.
@@ -182,6 +185,20 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
+    if (path == MOE_PATH_DECODE && T == 1 && moe::decode1_supported(H, I, E, k, dev->n_sm)) {
+        // one token: two kernels that route it themselves, the second a
+        // programmatic dependent of the first
+        path = MOE_PATH_DECODE_T1;
+        MOE_TRY(moe::launch_decode1(x, logits, wgu, wd, H, I, E, k, dev->n_sm, (float *)(ws + L.act), idx_out,
+                                    w_out, out, stream, stg.ev ? stg.ev[1] : nullptr));
+        stg.n = 1;
+        MOE_TRY(stg.done(cudaSuccess));
+        if (opts) {
+            opts->n_stages = stg.n;
+            opts->path_taken = path;
+        }
+        return MOE_OK;
+    }
     MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, idx_out, w_out, stream)));
     if (path == MOE_PATH_DECODE) {
         auto *act = (float *)(ws + L.act);
@@ -327,6 +344,8 @@ const char *moe_ffn_stage_name(int path, int stage)
     if (stage < 0) return nullptr;
     if (path == MOE_PATH_DECODE && stage < (int)(sizeof kDecodeStages / sizeof *kDecodeStages))
         return kDecodeStages[stage];
+    if (path == MOE_PATH_DECODE_T1 && stage < (int)(sizeof kDecodeT1Stages / sizeof *kDecodeT1Stages))
+        return kDecodeT1Stages[stage];
     if (path == MOE_PATH_GROUPED && stage < (int)(sizeof kGroupedStages / sizeof *kGroupedStages))
         return kGroupedStages[stage];
     return nullptr;
@@ -335,7 +354,11 @@ const char *moe_ffn_stage_name(int path, int stage)
 int moe_ffn_device_faults(uint32_t *flags, int clear)
 {
     if (!flags) return MOE_ERR_INVALID_ARG;
-    return moe::read_fault_word(flags, clear != 0) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    uint32_t gemm = 0, decode = 0;
+    if (moe::read_fault_word(&gemm, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::read_decode1_fault_word(&decode, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
+    *flags = gemm | (decode << 8);  // bits 0-7: grouped GEMMs, 8-15: single-token decode
+    return MOE_OK;
 }
 
 }  // extern "C"

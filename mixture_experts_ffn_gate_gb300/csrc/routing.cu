@@ -10,6 +10,7 @@
 // depend on hardware scheduling.
 #include "common.cuh"
 #include "kernels.h"
+#include "route_block.cuh"
 
 namespace moe {
 
@@ -25,37 +26,15 @@ __global__ void __launch_bounds__(256) router_kernel(const float *__restrict__ l
 {
     extern __shared__ unsigned long long keys[];  // [E]
     __shared__ int sel[32];
+    __shared__ float wt[32];
     const int t = blockIdx.x;
-    const float *l = logits + (int64_t)t * E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        keys[e] = ((unsigned long long)logit_key(__ldg(l + e)) << 32) | (uint32_t)(0xffffffffu - (uint32_t)e);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const unsigned long long me = keys[e];
-        int r = 0;
-        for (int j = 0; j < E; ++j)
-            r += keys[j] > me;
-        if (r < k)
-            sel[r] = e;
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const float l0 = __ldg(l + sel[0]);
-        float ex = 0.0f;
-        int e = 0;
-        if (lane < k) {
-            e = sel[lane];
-            ex = expf(__ldg(l + e) - l0);
-        }
-        const float s = warp_sum(ex);
-        if (lane < k) {
-            const float wt = ex / s;
-            idx[(int64_t)t * k + lane] = e;
-            w[(int64_t)t * k + lane] = wt;
-            if (idx_copy) idx_copy[(int64_t)t * k + lane] = e;
-            if (w_copy) w_copy[(int64_t)t * k + lane] = wt;
-        }
+    route_token_block(logits + (int64_t)t * E, E, k, keys, sel, wt);
+    if (threadIdx.x < k) {
+        const int j = threadIdx.x;
+        idx[(int64_t)t * k + j] = sel[j];
+        w[(int64_t)t * k + j] = wt[j];
+        if (idx_copy) idx_copy[(int64_t)t * k + j] = sel[j];
+        if (w_copy) w_copy[(int64_t)t * k + j] = wt[j];
     }
 }
 
