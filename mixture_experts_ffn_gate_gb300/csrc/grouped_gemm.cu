@@ -57,7 +57,8 @@ namespace {
 constexpr int BM = 128;                  // weight rows per tile (MMA M)
 constexpr int BK = 64;                   // K elements per stage: one 128-byte swizzle row
 constexpr int NMAX = kGemmChunkMax;      // tokens per chunk (MMA N <= NMAX)
-constexpr int ACC_COLS = 128;            // TMEM columns per accumulator (>= NMAX)
+constexpr int ACC_COLS = 64;             // TMEM columns per accumulator (>= NMAX)
+constexpr int SMALL_ROWS = 16;           // B box for chunks of at most 16 rows
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulators
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
@@ -67,7 +68,7 @@ static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulato
 
 template <bool GATE_UP>
 struct Cfg {
-    static constexpr int STAGES = GATE_UP ? 6 : 4;
+    static constexpr int STAGES = GATE_UP ? 9 : 6;
     static constexpr int A_BYTES = BM * BK * 2;                           // 16 KB
     static constexpr int B_TILE = NMAX * BK * 2;                          // 16 KB per operand
     static constexpr int B_BYTES = B_TILE * (GATE_UP ? 1 : 2);            // x | act_hi + act_lo
@@ -109,9 +110,16 @@ __device__ __forceinline__ int pad16(int n) { return (n + 15) & ~15; }
 
 template <bool GATE_UP>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0s,
+                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1s,
                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
 {
+    // tmA: gate_up -- 5-D view of W_gu [E][2][I/16][16][H] (dims innermost
+    //      first: H, 16 rows, gate|up, row group, expert) whose {64,16,2,4,1}
+    //      box is one 128-row tile of 4 x (16 gate rows, 16 up rows);
+    //      down -- 2-D [E*H, I], box 64 x 128.
+    // tmB0/tmB1: the chunk's token rows (x, or act_hi/act_lo), box 64 x NMAX;
+    // tmB0s/tmB1s: the same with a 16-row box, for chunks of <= 16 rows.
     using C = Cfg<GATE_UP>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,7 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB0);
-        if (!GATE_UP) ptx::prefetch_tensormap(&tmB1);
+        ptx::prefetch_tensormap(&tmB0s);
+        if (!GATE_UP) {
+            ptx::prefetch_tensormap(&tmB1);
+            ptx::prefetch_tensormap(&tmB1s);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -163,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
                 const Item it = decode_item(i, args);
-                const int nb = pad16(it.n) / 16;
-                const uint32_t bytes = C::A_BYTES + nb * 16 * BK * 2 * (GATE_UP ? 1 : 2);
+                const bool small = it.n <= SMALL_ROWS;
+                const uint32_t bytes = C::A_BYTES + (small ? SMALL_ROWS : NMAX) * BK * 2 * (GATE_UP ? 1 : 2);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!ptx::mbar_wait_bounded(empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
                         if (!*abort_flag) raise_fault(FAULT_GEMM_PRODUCER);
@@ -175,22 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++armed[stage];
                     const int k0 = kb * BK;
                     uint8_t *a = sA + stage * C::A_BYTES;
-                    if (GATE_UP) {
-                        const int row0 = it.e * 2 * args.I + it.m * 64;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            ptx::tma_load_2d(a + g * 4096, &tmA, k0, row0 + 16 * g, full + stage);
-                            ptx::tma_load_2d(a + g * 4096 + 2048, &tmA, k0, row0 + args.I + 16 * g, full + stage);
-                        }
-                    } else {
+                    if (GATE_UP)
+                        ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4, it.e, full + stage);
+                    else
                         ptx::tma_load_2d(a, &tmA, k0, it.e * args.H + it.m * BM, full + stage);
-                    }
                     uint8_t *b = sB + stage * C::B_BYTES;
-                    for (int j = 0; j < nb; ++j) {
-                        ptx::tma_load_2d(b + j * 2048, &tmB0, k0, it.p0 + 16 * j, full + stage);
-                        if (!GATE_UP)
-                            ptx::tma_load_2d(b + C::B_TILE + j * 2048, &tmB1, k0, it.p0 + 16 * j, full + stage);
-                    }
+                    ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
+                    if (!GATE_UP) ptx::tma_load_2d(b + C::B_TILE, small ? &tmB1s : &tmB1, k0, it.p0, full + stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -341,6 +344,25 @@ cudaError_t make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// W_gate_up [E, 2I, H] viewed as [E][I/16][2][16][H] (dims innermost first:
+// H, 16 rows, gate|up, group of 16 neurons, expert).  A {64, 16, 2, 4, 1}
+// box at {k0, 0, 0, 4m, e} is neurons 64m..64m+63 of expert e laid out as
+// 4 x (16 gate rows, 16 up rows), 128-byte swizzled.
+cudaError_t make_gate_up_map(CUtensorMap *map, const void *base, int E, int I, int H)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t row = (cuuint64_t)H * 2;
+    const cuuint64_t dims[5] = {(cuuint64_t)H, 16, 2, (cuuint64_t)I / 16, (cuuint64_t)E};
+    const cuuint64_t strides[4] = {row, row * I, row * 16, row * 2 * I};
+    const cuuint32_t box[5] = {BK, 16, 2, 4, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int grid_for(int ctas, int n_assign, int m_tiles, int E)
 {
     // an upper bound on the number of items: chunks <= E + n_assign / NMAX
@@ -370,13 +392,14 @@ cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chu
                                 const int32_t *offs, int n_assign, int H, int I, int E, void *act_hi, void *act_lo,
                                 int ctas, cudaStream_t s)
 {
-    CUtensorMap tA, tB;
-    cudaError_t e = make_map(&tA, wgu, (uint64_t)E * 2 * I, H, 16);
-    if (e == cudaSuccess) e = make_map(&tB, xs, n_assign, H, 16);
+    CUtensorMap tA, tBs, tB;
+    cudaError_t e = make_gate_up_map(&tA, wgu, E, I, H);
+    if (e == cudaSuccess) e = make_map(&tBs, xs, n_assign, H, SMALL_ROWS);
+    if (e == cudaSuccess) e = make_map(&tB, xs, n_assign, H, NMAX);
     if (e != cudaSuccess) return e;
     GemmArgs a{chunks, nchunks, offs, H, I, H, I / 64, act_hi, act_lo};
-    grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<true>::SMEM, s>>>(tA, tB, tB,
-                                                                                                          a);
+    grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<true>::SMEM, s>>>(
+        tA, tBs, tB, tBs, tB, a);
     return cudaPeekAtLastError();
 }
 
@@ -384,14 +407,16 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
                              const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, float *z,
                              int ctas, cudaStream_t s)
 {
-    CUtensorMap tA, tB0, tB1;
+    CUtensorMap tA, tB0s, tB0, tB1s, tB1;
     cudaError_t e = make_map(&tA, wd, (uint64_t)E * H, I, BM);
-    if (e == cudaSuccess) e = make_map(&tB0, act_hi, n_assign, I, 16);
-    if (e == cudaSuccess) e = make_map(&tB1, act_lo, n_assign, I, 16);
+    if (e == cudaSuccess) e = make_map(&tB0s, act_hi, n_assign, I, SMALL_ROWS);
+    if (e == cudaSuccess) e = make_map(&tB0, act_hi, n_assign, I, NMAX);
+    if (e == cudaSuccess) e = make_map(&tB1s, act_lo, n_assign, I, SMALL_ROWS);
+    if (e == cudaSuccess) e = make_map(&tB1, act_lo, n_assign, I, NMAX);
     if (e != cudaSuccess) return e;
     GemmArgs a{chunks, nchunks, offs, H, I, I, (H + BM - 1) / BM, z, nullptr};
-    grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(tA, tB0,
-                                                                                                            tB1, a);
+    grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(
+        tA, tB0s, tB0, tB1s, tB1, a);
     return cudaPeekAtLastError();
 }
 

@@ -7,7 +7,7 @@
 namespace moe {
 
 // Grouped path: at most this many assignments (token rows) per GEMM N-chunk.
-constexpr int kGemmChunkMax = 128;
+constexpr int kGemmChunkMax = 64;
 
 // routing.cu
 cudaError_t routing_init_device();
