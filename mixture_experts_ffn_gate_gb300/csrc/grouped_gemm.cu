@@ -59,7 +59,8 @@ constexpr int BK = 64;                   // K elements per stage: one 128-byte s
 constexpr int NMAX = kGemmChunkMax;      // tokens per chunk (MMA N <= NMAX)
 constexpr int ACC_COLS = 64;             // TMEM columns per accumulator (>= NMAX)
 constexpr int SMALL_ROWS = 16;           // B box for chunks of at most 16 rows
-constexpr int TMEM_COLS = 2 * ACC_COLS;  // two accumulators
+constexpr int MT = 2;                    // weight tiles per item (share one token tile)
+constexpr int TMEM_COLS = 2 * MT * ACC_COLS;  // double-buffered, one accumulator per tile
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain after an abort
@@ -68,8 +69,9 @@ static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulato
 
 template <bool GATE_UP>
 struct Cfg {
-    static constexpr int STAGES = GATE_UP ? 9 : 6;
-    static constexpr int A_BYTES = BM * BK * 2;                           // 16 KB
+    static constexpr int STAGES = GATE_UP ? 5 : 4;
+    static constexpr int A_TILE = BM * BK * 2;                            // 16 KB per weight tile
+    static constexpr int A_BYTES = MT * A_TILE;
     static constexpr int B_TILE = NMAX * BK * 2;                          // 16 KB per operand
     static constexpr int B_BYTES = B_TILE * (GATE_UP ? 1 : 2);            // x | act_hi + act_lo
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -83,17 +85,19 @@ struct GemmArgs {
     const int32_t *offs;  // [E+1] sorted-row offsets per expert
     int H, I;
     int K;                // reduction length (H or I)
-    int m_tiles;          // weight tiles per expert
+    int m_tiles;          // groups of MT weight tiles per expert
+    int tiles;            // weight tiles per expert (the last group may have fewer)
+    int a_bytes;          // bytes of one weight box (MT tiles, fewer if the tensor is smaller)
     void *out0, *out1;    // act_hi, act_lo | z
 };
 
 struct Item {
-    int e, p0, n, m;
+    int e, p0, n, m;      // m: group of MT weight tiles, tiles MT*m ... MT*m+MT-1
 };
 
-// Item i of the flat list: experts in order; within an expert, weight tile m
-// major and chunk minor, so the chunks that reuse one weight tile are
-// adjacent (they run at about the same time and share it through L2).
+// Item i of the flat list: experts in order; within an expert, weight tile
+// group m major and chunk minor, so the chunks that reuse one weight tile
+// are adjacent (they run at about the same time and share it through L2).
 __device__ __forceinline__ Item decode_item(int i, const GemmArgs &a)
 {
     const int4 ch = __ldg(a.chunks + i / a.m_tiles);
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
                 const Item it = decode_item(i, args);
                 const bool small = it.n <= SMALL_ROWS;
-                const uint32_t bytes = C::A_BYTES + (small ? SMALL_ROWS : NMAX) * BK * 2 * (GATE_UP ? 1 : 2);
+                const uint32_t bytes = args.a_bytes + (small ? SMALL_ROWS : NMAX) * BK * 2 * (GATE_UP ? 1 : 2);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!ptx::mbar_wait_bounded(empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
                         if (!*abort_flag) raise_fault(FAULT_GEMM_PRODUCER);
@@ -187,10 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++armed[stage];
                     const int k0 = kb * BK;
                     uint8_t *a = sA + stage * C::A_BYTES;
+                    // MT tiles in one box; tiles past the expert's end read 0
+                    // (gate_up) or the next expert's rows (down), never stored
                     if (GATE_UP)
-                        ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4, it.e, full + stage);
+                        ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4 * MT, it.e, full + stage);
                     else
-                        ptx::tma_load_2d(a, &tmA, k0, it.e * args.H + it.m * BM, full + stage);
+                        ptx::tma_load_2d(a, &tmA, k0, it.e * args.H + it.m * BM * MT, full + stage);
                     uint8_t *b = sB + stage * C::B_BYTES;
                     ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
                     if (!GATE_UP) ptx::tma_load_2d(b + C::B_TILE, small ? &tmB1s : &tmB1, k0, it.p0, full + stage);
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d = tmem + acc * ACC_COLS;
+                const uint32_t d = tmem + acc * MT * ACC_COLS;
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!ptx::mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
@@ -237,10 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_addr = ptx::smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = ptx::sw128_desc(a_addr + k * 32);
-                        ptx::mma_bf16(d, ad, ptx::sw128_desc(b_addr + k * 32), idesc, (kb | k) != 0);
-                        if (!GATE_UP)
-                            ptx::mma_bf16(d, ad, ptx::sw128_desc(b_addr + C::B_TILE + k * 32), idesc, 1);
+                        const uint64_t bd = ptx::sw128_desc(b_addr + k * 32);
+#pragma unroll
+                        for (int t = 0; t < MT; ++t) {
+                            const uint64_t ad = ptx::sw128_desc(a_addr + t * C::A_TILE + k * 32);
+                            ptx::mma_bf16(d + t * ACC_COLS, ad, bd, idesc, (kb | k) != 0);
+                            if (!GATE_UP)
+                                ptx::mma_bf16(d + t * ACC_COLS, ad, ptx::sw128_desc(b_addr + C::B_TILE + k * 32),
+                                              idesc, 1);
+                        }
                     }
                     ptx::mma_commit(empty + stage);
                     if (++stage == C::STAGES) {
@@ -269,13 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + acc * ACC_COLS;
+            for (int t = 0; t < MT && it.m * MT + t < args.tiles; ++t) {
+            const int tile = it.m * MT + t;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (acc * MT + t) * ACC_COLS;
             for (int c0 = 0; c0 < it.n; c0 += 32) {
                 uint32_t r[32];
                 ptx::tmem_ld32(tbase + c0, r);
                 ptx::tmem_wait_ld();
                 if (GATE_UP) {
-                    const int neuron = it.m * 64 + 16 * q + (lane & 15);
+                    const int neuron = tile * 64 + 16 * q + (lane & 15);
                     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(lane < 16 ? args.out0 : args.out1);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -288,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             dst[(int64_t)(it.p0 + c0 + j) * args.I + neuron] = lane < 16 ? hi : lo;
                     }
                 } else {
-                    const int h = it.m * BM + 32 * q + lane;
+                    const int h = tile * BM + 32 * q + lane;
                     float *z = reinterpret_cast<float *>(args.out0);
                     if (h < args.H) {
 #pragma unroll
@@ -296,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c0 + j < it.n) z[(int64_t)(it.p0 + c0 + j) * args.H + h] = __uint_as_float(r[j]);
                     }
                 }
+            }
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -348,14 +362,14 @@ cudaError_t make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
 // H, 16 rows, gate|up, group of 16 neurons, expert).  A {64, 16, 2, 4, 1}
 // box at {k0, 0, 0, 4m, e} is neurons 64m..64m+63 of expert e laid out as
 // 4 x (16 gate rows, 16 up rows), 128-byte swizzled.
-cudaError_t make_gate_up_map(CUtensorMap *map, const void *base, int E, int I, int H)
+cudaError_t make_gate_up_map(CUtensorMap *map, const void *base, int E, int I, int H, uint32_t groups)
 {
     EncodeTiledFn enc = encoder();
     if (!enc) return cudaErrorNotSupported;
     const cuuint64_t row = (cuuint64_t)H * 2;
     const cuuint64_t dims[5] = {(cuuint64_t)H, 16, 2, (cuuint64_t)I / 16, (cuuint64_t)E};
     const cuuint64_t strides[4] = {row, row * I, row * 16, row * 2 * I};
-    const cuuint32_t box[5] = {BK, 16, 2, 4, 1};
+    const cuuint32_t box[5] = {BK, 16, 2, groups, 1};
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -393,11 +407,14 @@ cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chu
                                 int ctas, cudaStream_t s)
 {
     CUtensorMap tA, tBs, tB;
-    cudaError_t e = make_gate_up_map(&tA, wgu, E, I, H);
+    // groups of 16 neurons per box: MT tiles of 4, but never more than the tensor has
+    const uint32_t groups = (uint32_t)(4 * MT < I / 16 ? 4 * MT : I / 16);
+    cudaError_t e = make_gate_up_map(&tA, wgu, E, I, H, groups);
     if (e == cudaSuccess) e = make_map(&tBs, xs, n_assign, H, SMALL_ROWS);
     if (e == cudaSuccess) e = make_map(&tB, xs, n_assign, H, NMAX);
     if (e != cudaSuccess) return e;
-    GemmArgs a{chunks, nchunks, offs, H, I, H, I / 64, act_hi, act_lo};
+    GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK * 2, act_hi,
+               act_lo};
     grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<true>::SMEM, s>>>(
         tA, tBs, tB, tBs, tB, a);
     return cudaPeekAtLastError();
@@ -408,13 +425,15 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
                              int ctas, cudaStream_t s)
 {
     CUtensorMap tA, tB0s, tB0, tB1s, tB1;
-    cudaError_t e = make_map(&tA, wd, (uint64_t)E * H, I, BM);
+    const uint32_t a_rows = (uint32_t)((int64_t)BM * MT < (int64_t)E * H ? BM * MT : E * H);
+    cudaError_t e = make_map(&tA, wd, (uint64_t)E * H, I, a_rows);
     if (e == cudaSuccess) e = make_map(&tB0s, act_hi, n_assign, I, SMALL_ROWS);
     if (e == cudaSuccess) e = make_map(&tB0, act_hi, n_assign, I, NMAX);
     if (e == cudaSuccess) e = make_map(&tB1s, act_lo, n_assign, I, SMALL_ROWS);
     if (e == cudaSuccess) e = make_map(&tB1, act_lo, n_assign, I, NMAX);
     if (e != cudaSuccess) return e;
-    GemmArgs a{chunks, nchunks, offs, H, I, I, (H + BM - 1) / BM, z, nullptr};
+    const int tiles = (H + BM - 1) / BM;
+    GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, (int)a_rows * BK * 2, z, nullptr};
     grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(
         tA, tB0s, tB0, tB1s, tB1, a);
     return cudaPeekAtLastError();
