@@ -59,8 +59,6 @@ constexpr int BK = 64;                   // K elements per stage: one 128-byte s
 constexpr int NMAX = kGemmChunkMax;      // tokens per chunk (MMA N <= NMAX)
 constexpr int ACC_COLS = 64;             // TMEM columns per accumulator (>= NMAX)
 constexpr int SMALL_ROWS = 16;           // B box for chunks of at most 16 rows
-constexpr int MT = 2;                    // weight tiles per item (share one token tile)
-constexpr int TMEM_COLS = 2 * MT * ACC_COLS;  // double-buffered, one accumulator per tile
 constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain after an abort
@@ -69,7 +67,9 @@ static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulato
 
 template <bool GATE_UP>
 struct Cfg {
-    static constexpr int STAGES = GATE_UP ? 5 : 4;
+    static constexpr int MT = GATE_UP ? 4 : 2;  // weight tiles per item (they share one token tile)
+    static constexpr int TMEM_COLS = 2 * MT * ACC_COLS;  // double-buffered, one accumulator per tile
+    static constexpr int STAGES = GATE_UP ? 3 : 4;
     static constexpr int A_TILE = BM * BK * 2;                            // 16 KB per weight tile
     static constexpr int A_BYTES = MT * A_TILE;
     static constexpr int B_TILE = NMAX * BK * 2;                          // 16 KB per operand
@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tmB0/tmB1: the chunk's token rows (x, or act_hi/act_lo), box 64 x NMAX;
     // tmB0s/tmB1s: the same with a 16-row box, for chunks of <= 16 rows.
     using C = Cfg<GATE_UP>;
+    constexpr int MT = C::MT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -177,8 +178,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t armed[C::STAGES];
             for (int s = 0; s < C::STAGES; ++s) armed[s] = 0;
+            Item nxt = blockIdx.x < total ? decode_item(blockIdx.x, args) : Item{};
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x) {
-                const Item it = decode_item(i, args);
+                const Item it = nxt;
+                if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);  // loads overlap this item
                 const bool small = it.n <= SMALL_ROWS;
                 const uint32_t bytes = args.a_bytes + (small ? SMALL_ROWS : NMAX) * BK * 2 * (GATE_UP ? 1 : 2);
                 for (int kb = 0; kb < KB; ++kb) {
@@ -218,8 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             int li = 0;
+            Item nxt = blockIdx.x < total ? decode_item(blockIdx.x, args) : Item{};
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++li) {
-                const Item it = decode_item(i, args);
+                const Item it = nxt;
+                if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);
                 const uint32_t idesc = ptx::idesc_bf16_f32(BM, pad16(it.n));
                 const int acc = li & 1;
                 const uint32_t aph = (li >> 1) & 1;
@@ -270,8 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         int li = 0;
+        Item nxt = blockIdx.x < total ? decode_item(blockIdx.x, args) : Item{};
         for (int i = blockIdx.x; i < total; i += gridDim.x, ++li) {
-            const Item it = decode_item(i, args);
+            const Item it = nxt;
+            if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);
             const int acc = li & 1;
             const uint32_t aph = (li >> 1) & 1;
             if (!ptx::mbar_wait_bounded(tfull + acc, aph, abort_flag, kWaitLimitNs)) {
@@ -320,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host
@@ -407,6 +414,7 @@ cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chu
                                 int ctas, cudaStream_t s)
 {
     CUtensorMap tA, tBs, tB;
+    constexpr int MT = Cfg<true>::MT;
     // groups of 16 neurons per box: MT tiles of 4, but never more than the tensor has
     const uint32_t groups = (uint32_t)(4 * MT < I / 16 ? 4 * MT : I / 16);
     cudaError_t e = make_gate_up_map(&tA, wgu, E, I, H, groups);
@@ -425,6 +433,7 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
                              int ctas, cudaStream_t s)
 {
     CUtensorMap tA, tB0s, tB0, tB1s, tB1;
+    constexpr int MT = Cfg<false>::MT;
     const uint32_t a_rows = (uint32_t)((int64_t)BM * MT < (int64_t)E * H ? BM * MT : E * H);
     cudaError_t e = make_map(&tA, wd, (uint64_t)E * H, I, a_rows);
     if (e == cudaSuccess) e = make_map(&tB0s, act_hi, n_assign, I, SMALL_ROWS);
