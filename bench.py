@@ -59,6 +59,8 @@ def parse():
     p.add_argument("--E", type=int, default=None, help="fewer experts (profiling-size variant)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
+                   help="force the library's execution path (default: its own choice)")
     p.add_argument("--skip-baseline", action="store_true", help="omit the CPU oracle timing")
     return p.parse_args()
 
@@ -297,12 +299,20 @@ def main():
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
+                 "grouped": m.MOE_PATH_GROUPED}[args.path]
+
+    def new_opts():
+        o = m.moe_ffn_opts()
+        o.path = path_code
+        return o
+
     def call(i, opts=None, idx=None):
         x, L = batches[i]
         m.moe_ffn_forward_ex(x, L, wgu, wd, wl.k, out=out, workspace=ws, topk_idx=idx,
-                             opts=opts, stream=stream)
+                             opts=opts if opts is not None else new_opts(), stream=stream)
 
-    probe = m.moe_ffn_opts()
+    probe = new_opts()
     call(0, probe)
     path, n_stages = probe.path_taken, probe.n_stages
     stage_names = [m.moe_ffn_stage_name(path, s) for s in range(n_stages)]
@@ -350,7 +360,7 @@ def main():
         torch.cuda.synchronize()
         for j in range(K):
             flush.fill_(float(j))
-            o = m.moe_ffn_opts()
+            o = new_opts()
             o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
             call(W + j, o)
         torch.cuda.synchronize()
@@ -365,14 +375,15 @@ def main():
             oh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
             wsh = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev, host=True)
             for i in range(W):
-                m.moe_ffn_forward_host(xh[i], lh[i], wgu, wd, wl.k, oh, wsh, stream=stream)
+                m.moe_ffn_forward_host(xh[i], lh[i], wgu, wd, wl.k, oh, wsh, opts=new_opts(), stream=stream)
             torch.cuda.synchronize()
             e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
             e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
             for j in range(K):
                 flush.fill_(float(j))
                 e_starts[j].record(stream)
-                m.moe_ffn_forward_host(xh[W + j], lh[W + j], wgu, wd, wl.k, oh, wsh, stream=stream)
+                m.moe_ffn_forward_host(xh[W + j], lh[W + j], wgu, wd, wl.k, oh, wsh, opts=new_opts(),
+                                       stream=stream)
                 e_ends[j].record(stream)
             torch.cuda.synchronize()
             e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends))

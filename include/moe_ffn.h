@@ -86,7 +86,7 @@ enum {
 typedef struct moe_ffn_opts {
     /* inputs */
     int32_t path;              /* MOE_PATH_AUTO, _DECODE or _GROUPED */
-    int32_t decode_max_tokens; /* AUTO threshold on T (default 64) */
+    int32_t decode_max_tokens; /* AUTO threshold on T (default 4) */
     int32_t gate_up_warps;     /* decode gate_up: warps per block, 1..16 (default 8) */
     int32_t down_warps;        /* decode down: warps per block, 1..16 (default 8) */
     int32_t gemm_ctas;         /* grouped GEMMs: persistent CTAs (default: one per SM) */
