@@ -42,6 +42,7 @@ FLUSH_BYTES = 512 << 20
 
 # Kernel sources whose change voids a stored ncu traffic figure.
 KERNEL_SOURCES = {
+    "decode_fused": ["decode1.cu"],
     "decode_gate_up": ["decode.cu", "decode1.cu"],
     "decode_down": ["decode.cu", "decode1.cu"],
     "gemm_gate_up": ["grouped_gemm.cu"],
@@ -59,6 +60,9 @@ def parse():
     p.add_argument("--E", type=int, default=None, help="fewer experts (profiling-size variant)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--flush", choices=["write", "write+read"], default="write+read",
+                   help="L2 flush between steps: a write larger than L2, optionally followed by a "
+                        "read that makes the dirty lines' write-back happen before the next step")
     p.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
                    help="force the library's execution path (default: its own choice)")
     p.add_argument("--skip-baseline", action="store_true", help="omit the CPU oracle timing")
@@ -155,6 +159,8 @@ def algorithmic_bytes(wl, T, U):
 def kernel_bytes(kernel, wl, T, U, k):
     """Algorithmic bytes of one launch of a kernel."""
     H, I = wl.H, wl.I
+    if kernel == "decode_fused":  # the whole single-token layer in one kernel
+        return U * 6 * H * I + T * H * 2 + T * wl.E * 4 + T * H * 4 + 2 * T * k * 2 * I * 4
     if kernel == "decode_gate_up":
         return U * 2 * I * H * 2 + T * H * 2 + T * k * I * 4
     if kernel == "decode_down":
@@ -297,6 +303,15 @@ def main():
     ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
     out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sum = torch.empty((), dtype=torch.float32, device=dev)
+
+    def do_flush(j):
+        # write more than L2 holds; then read half of it back, so L2 ends up
+        # full of clean lines and the write-back of the dirty ones happens
+        # here, outside the step's events, not during the next step
+        flush.fill_(float(j))
+        if args.flush == "write+read":
+            torch.sum(flush[: FLUSH_BYTES // 8], dim=0, out=flush_sum)
     stream = torch.cuda.current_stream()
 
     path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
@@ -326,7 +341,7 @@ def main():
     torch.cuda.synchronize()
 
     for i in range(W):
-        flush.fill_(float(i))
+        do_flush((i))
         call(i)
     torch.cuda.synchronize()
 
@@ -338,7 +353,7 @@ def main():
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
         for j in range(K):
-            flush.fill_(float(j))
+            do_flush((j))
             starts[j].record(stream)
             call(W + j)
             ends[j].record(stream)
@@ -359,7 +374,7 @@ def main():
             arrs.append(m.stage_event_array(evs[j]))
         torch.cuda.synchronize()
         for j in range(K):
-            flush.fill_(float(j))
+            do_flush((j))
             o = new_opts()
             o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
             call(W + j, o)
@@ -380,7 +395,7 @@ def main():
             e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
             e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
             for j in range(K):
-                flush.fill_(float(j))
+                do_flush((j))
                 e_starts[j].record(stream)
                 m.moe_ffn_forward_host(xh[W + j], lh[W + j], wgu, wd, wl.k, oh, wsh, opts=new_opts(),
                                        stream=stream)
@@ -423,7 +438,9 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": {1: "decode", 2: "grouped"}.get(path, path),
-                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MB write, not timed)",
+                   "l2": (f"flushed between steps ({FLUSH_BYTES >> 20} MB write"
+                          + (f", then {FLUSH_BYTES >> 21} MB read" if args.flush == "write+read" else "")
+                          + ", not timed)"),
                    "timing": "CUDA events around each step on the launching stream, summed",
                    "parallelism": f"replicas x{world} (independent token streams)"},
         "roofline": roofline,

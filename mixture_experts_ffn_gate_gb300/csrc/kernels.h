@@ -42,6 +42,14 @@ cudaError_t launch_decode1(const void *x, const float *logits, const void *wgu, 
                            int k, int n_sm, float *gu, int32_t *idx_out, float *w_out, float *out, cudaStream_t s,
                            cudaEvent_t between);
 
+// Single-token layer in one cooperative kernel with a grid barrier; flags:
+// kMaxGridCtas 64-bit words of workspace (any contents).
+constexpr int kMaxGridCtas = 1024;
+bool decode1_fused_supported(int H, int I, int E, int k, int n_sm);
+cudaError_t launch_decode1_fused(const void *x, const float *logits, const void *wgu, const void *wd, int H, int I,
+                                 int E, int k, int n_sm, float *gu, unsigned long long *flags, int32_t *idx_out,
+                                 float *w_out, float *out, cudaStream_t s);
+
 // grouped_gemm.cu
 cudaError_t gemm_init_device();
 bool gemm_supported(int H, int I, int E);

@@ -25,7 +25,7 @@ struct Shape {
 // Workspace regions, 256-byte aligned.  The routing/sort region is shared
 // by both paths; the rest is per path and the two overlap.
 struct Layout {
-    size_t idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, common_end;
+    size_t idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, flags, common_end;
     size_t act;                          // decode: act f32 [T*k, I]
     size_t xs, act_hi, act_lo, z;        // grouped
     size_t decode_total, grouped_total, total;
@@ -52,6 +52,7 @@ Layout make_layout(const Shape &s)
     L.ucount = take(4);
     L.chunks = take((size_t)(s.E + ceil_div((int64_t)n, moe::kGemmChunkMax) + 1) * 16);
     L.nchunks = take(4);
+    L.flags = take((size_t)moe::kMaxGridCtas * 8);  // grid-barrier flags of the single-token kernel
     L.common_end = o;
     // decode path: act f32 [T*k, I]; the single-token kernels keep the gate
     // and up dot products there instead, [k, 2I]
@@ -131,7 +132,7 @@ int device_setup(DeviceInfo **info)
 }
 
 const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
-const char *kDecodeT1Stages[] = {"decode_gate_up", "decode_down"};
+const char *kDecodeT1Stages[] = {"decode_fused"};
 const char *kGroupedStages[] = {"router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine"};
 
 // Records stage events around the launches of one call.
@@ -188,14 +189,13 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (path == MOE_PATH_DECODE && T == 1 && moe::decode1_supported(H, I, E, k, dev->n_sm)) {
-        // one token: two kernels that route it themselves, the second a
-        // programmatic dependent of the first
+    if (path == MOE_PATH_DECODE && T == 1 && moe::decode1_fused_supported(H, I, E, k, dev->n_sm)) {
+        // one token: a single cooperative kernel that routes it, streams both
+        // projections' rows and meets at a grid barrier in between
         path = MOE_PATH_DECODE_T1;
-        MOE_TRY(moe::launch_decode1(x, logits, wgu, wd, H, I, E, k, dev->n_sm, (float *)(ws + L.act), idx_out,
-                                    w_out, out, stream, stg.ev ? stg.ev[1] : nullptr));
-        stg.n = 1;
-        MOE_TRY(stg.done(cudaSuccess));
+        MOE_TRY(stg.done(moe::launch_decode1_fused(x, logits, wgu, wd, H, I, E, k, dev->n_sm,
+                                                   (float *)(ws + L.act), (unsigned long long *)(ws + L.flags),
+                                                   idx_out, w_out, out, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
