@@ -9,14 +9,17 @@ decode layer (H=2048, I=768, E=128, top-8) at T=1.  Each rank (torchrun, one
 per GPU) runs its own replica over its own token stream: the calls are
 independent problems, so there is no data-path collective ("scaling": "weak").
 
-Timing: W untimed warm-up steps, then K timed steps bracketed by a barrier and
-cudaDeviceSynchronize.  Between steps a 512 MB buffer is written to flush L2,
-and each step is bracketed by its own CUDA events on the launching stream, so
-the flush is not timed; value = tokens of all ranks / max over ranks of the
-summed step times.  A second pass over the same steps records per-kernel
-events (the library's stage events) for the roofline of the dominant kernel.
-e2e repeats the steps through the host-buffer entry point (pinned inputs
-copied in, output copied out, inside each step's events).
+Timing: the steps run back to back, as a model's layers do, over R layers'
+weights (step j uses layer j % R; R is chosen so that the weights a step
+reads have been streamed out of L2 by the steps in between, i.e. the inputs
+are larger than L2).  W untimed warm-up steps, then the K timed steps as one
+CUDA graph replay (--eager: launched one by one from Python), bracketed by a
+barrier, cudaDeviceSynchronize and CUDA events on the launching stream;
+value = tokens of all ranks / max over ranks of that time.  A second replay
+records the library's stage events between kernels for the roofline of the
+dominant kernel.  cold_call times single calls after an L2 flush each.  e2e
+repeats the steps through the host-buffer entry point, called step by step
+from Python (pinned inputs copied in, output copied out, inside the region).
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -39,6 +42,9 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s; decode HBM TB/s vs peak; T=2048 TFLOPS vs BF16 peak"
 DEFAULT_WORKLOAD = "decode_h2048_i768_e128_k8"
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20            # GB300 L2
+LAYER_MEM_CAP = 72 << 30        # device memory for the layers' weights
+BATCH_MEM_CAP = 2 << 30         # and for the token batches
 
 # Kernel sources whose change voids a stored ncu traffic figure.
 KERNEL_SOURCES = {
@@ -66,6 +72,12 @@ def parse():
     p.add_argument("--path", choices=["auto", "decode", "grouped"], default="auto",
                    help="force the library's execution path (default: its own choice)")
     p.add_argument("--skip-baseline", action="store_true", help="omit the CPU oracle timing")
+    p.add_argument("--layers", type=int, default=None,
+                   help="layers' weights cycled by the steps (default: enough that none is in L2)")
+    p.add_argument("--eager", action="store_true",
+                   help="launch every step from Python instead of replaying a CUDA graph of the steps")
+    p.add_argument("--cold-steps", type=int, default=200,
+                   help="single calls timed after an L2 flush each (secondary figure)")
     return p.parse_args()
 
 
@@ -295,11 +307,21 @@ def main():
 
     dev = torch.device("cuda", local)
     K, W = args.steps, max(3, args.warmup)
-    wgu, wd = synth.make_weights(wl, device=dev)
     bias = synth.make_bias(wl)
+    # Steps run back to back over R layers' weights (step j uses layer j % R),
+    # R chosen so that the weights one step reads were streamed out of L2 by
+    # the steps in between: the inputs are larger than L2 and no step finds
+    # its weights there.  Token batches are fresh per step (cycled past NB).
+    touched = algorithmic_bytes(wl, T, min(wl.E, T * wl.k))
+    R = max(2, math.ceil(3 * L2_BYTES / touched)) if args.layers is None else args.layers
+    R = max(1, min(R, int(LAYER_MEM_CAP // wl.weight_bytes())))
+    layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
+    wgu, wd = layers[0]
+    batch_bytes = T * (wl.H * 2 + wl.E * 4)
+    NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
     # rank r processes calls [r*(W+K), (r+1)*(W+K)) of the token stream
     batches = [synth.make_tokens(wl, T, call=rank * (W + K) + i, device=dev, bias=bias)
-               for i in range(W + K)]
+               for i in range(NB)]
     ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
     out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -312,7 +334,6 @@ def main():
         flush.fill_(float(j))
         if args.flush == "write+read":
             torch.sum(flush[: FLUSH_BYTES // 8], dim=0, out=flush_sum)
-    stream = torch.cuda.current_stream()
 
     path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
                  "grouped": m.MOE_PATH_GROUPED}[args.path]
@@ -322,49 +343,73 @@ def main():
         o.path = path_code
         return o
 
-    def call(i, opts=None, idx=None):
-        x, L = batches[i]
-        m.moe_ffn_forward_ex(x, L, wgu, wd, wl.k, out=out, workspace=ws, topk_idx=idx,
+    def call(j, stream, opts=None, idx=None):
+        x, L = batches[j % NB]
+        lw_gu, lw_d = layers[j % R]
+        m.moe_ffn_forward_ex(x, L, lw_gu, lw_d, wl.k, out=out, workspace=ws, topk_idx=idx,
                              opts=opts if opts is not None else new_opts(), stream=stream)
 
+    stream = torch.cuda.current_stream()
     probe = new_opts()
-    call(0, probe)
+    call(0, stream, probe)
     path, n_stages = probe.path_taken, probe.n_stages
     stage_names = [m.moe_ffn_stage_name(path, s) for s in range(n_stages)]
 
     # unique experts touched per step (routing of each batch, untimed)
     idx_buf = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
-    U = []
-    for i in range(W, W + K):
-        call(i, None, idx_buf)
-        U.append(int(torch.unique(idx_buf).numel()))
+    U_of = {}
+    for j in range(W, W + K):
+        if j % NB not in U_of:
+            call(j, stream, None, idx_buf)
+            U_of[j % NB] = int(torch.unique(idx_buf).numel())
+    U = [U_of[j % NB] for j in range(W, W + K)]
     torch.cuda.synchronize()
 
-    for i in range(W):
-        do_flush((i))
-        call(i)
-    torch.cuda.synchronize()
+    def capture(steps, events=None):
+        """One CUDA graph holding the calls of `steps`, in order."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            s = torch.cuda.current_stream()
+            for n, j in enumerate(steps):
+                o = new_opts()
+                if events is not None:
+                    o.stage_events = m.ctypes.cast(events[n], m.ctypes.c_void_p)
+                call(j, s, o)
+        return g
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    use_graph = not args.eager
+    if use_graph:
+        g_warm = capture(range(W))
+        g_main = capture(range(W, W + K))
+    mark0 = torch.cuda.Event(enable_timing=True)
+    mark1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        # warm-up: W untimed steps
+        if use_graph:
+            g_warm.replay()
+        else:
+            for j in range(W):
+                call(j, stream)
+        torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        for j in range(K):
-            do_flush((j))
-            starts[j].record(stream)
-            call(W + j)
-            ends[j].record(stream)
+        mark0.record(stream)
+        if use_graph:
+            g_main.replay()
+        else:
+            for j in range(W, W + K):
+                call(j, stream)
+        mark1.record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
         if world > 1:
             dist.barrier()
-        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        total_ms = sum(step_ms)
+        total_ms = mark0.elapsed_time(mark1)
 
-        # per-kernel pass over the same steps, stage events between kernels
+        # per-kernel pass over the same steps: the library's stage events
+        # between kernels (captured as event-record nodes when graphs are used)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
                for _ in range(K)]
         arrs = []
@@ -373,36 +418,52 @@ def main():
                 e.record(stream)
             arrs.append(m.stage_event_array(evs[j]))
         torch.cuda.synchronize()
-        for j in range(K):
-            do_flush((j))
-            o = new_opts()
-            o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
-            call(W + j, o)
+        if use_graph:
+            g_stage = capture(range(W, W + K), arrs)
+            g_stage.replay()
+        else:
+            for j in range(K):
+                o = new_opts()
+                o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
+                call(W + j, stream, o)
         torch.cuda.synchronize()
         kern_ms = {name: [evs[j][s].elapsed_time(evs[j][s + 1]) for j in range(K)]
                    for s, name in enumerate(stage_names)}
 
-        # e2e through the host-buffer entry point
+        # cold single calls: L2 flushed before each, each between its own events
+        n_cold = min(K, args.cold_steps)
+        c_starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_cold)]
+        c_ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_cold)]
+        for j in range(n_cold):
+            do_flush(j)
+            c_starts[j].record(stream)
+            call(W + j, stream)
+            c_ends[j].record(stream)
+        torch.cuda.synchronize()
+        cold_ms = [s.elapsed_time(e) for s, e in zip(c_starts, c_ends)]
+
+        # e2e: the host-buffer entry point, called step after step from Python
+        # (pinned inputs copied in and the output copied out inside the region)
         e2e = None
         if not args.no_e2e:
             xh = [b[0].cpu().pin_memory() for b in batches]
             lh = [b[1].cpu().pin_memory() for b in batches]
             oh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
             wsh = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev, host=True)
-            for i in range(W):
-                m.moe_ffn_forward_host(xh[i], lh[i], wgu, wd, wl.k, oh, wsh, opts=new_opts(), stream=stream)
+
+            def host_call(j):
+                lw_gu, lw_d = layers[j % R]
+                m.moe_ffn_forward_host(xh[j % NB], lh[j % NB], lw_gu, lw_d, wl.k, oh, wsh,
+                                       opts=new_opts(), stream=stream)
+            for j in range(W):
+                host_call(j)
             torch.cuda.synchronize()
-            e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-            e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-            for j in range(K):
-                do_flush((j))
-                e_starts[j].record(stream)
-                m.moe_ffn_forward_host(xh[W + j], lh[W + j], wgu, wd, wl.k, oh, wsh, opts=new_opts(),
-                                       stream=stream)
-                e_ends[j].record(stream)
+            mark0.record(stream)
+            for j in range(W, W + K):
+                host_call(j)
+            mark1.record(stream)
             torch.cuda.synchronize()
-            e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends))
-            e2e = {"ms": e2e_ms}
+            e2e = {"ms": mark0.elapsed_time(mark1)}
 
     # max over ranks
     t = torch.tensor([total_ms, e2e["ms"] if e2e else 0.0], dtype=torch.float64, device=dev)
@@ -438,10 +499,13 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": {1: "decode", 2: "grouped"}.get(path, path),
-                   "l2": (f"flushed between steps ({FLUSH_BYTES >> 20} MB write"
-                          + (f", then {FLUSH_BYTES >> 21} MB read" if args.flush == "write+read" else "")
-                          + ", not timed)"),
-                   "timing": "CUDA events around each step on the launching stream, summed",
+                   "layers": R,
+                   "l2": (f"inputs larger than L2: {R} layers' weights "
+                          f"({R * wl.weight_bytes() / 1e9:.1f} GB) cycled step by step, "
+                          f"{touched / 1e6:.0f} MB read per step at most, fresh tokens per step"),
+                   "timing": ("CUDA graph of the K steps replayed once" if use_graph
+                              else "the K steps launched from Python")
+                             + ", CUDA events before and after on the launching stream",
                    "parallelism": f"replicas x{world} (independent token streams)"},
         "roofline": roofline,
         "call_hbm": {"achieved_gbs": whole_call_gbs, "frac_of_measured": whole_call_gbs / peaks["hbm_gbs"],
@@ -449,6 +513,11 @@ def main():
                      "unique_experts_mean": mean_U},
         "tensor": {"tflops": flops / (total_ms / K / 1e3) / 1e12,
                    "frac_of_dense_bf16_peak": flops / (total_ms / K / 1e3) / 1e12 / peaks["bf16_tflops"]},
+        "cold_call": {"us_median": 1e3 * statistics.median(cold_ms), "us_mean": 1e3 * sum(cold_ms) / n_cold,
+                      "calls": n_cold,
+                      "method": (f"L2 flushed before each call ({FLUSH_BYTES >> 20} MB write"
+                                 + (f", then {FLUSH_BYTES >> 21} MB read" if args.flush == "write+read" else "")
+                                 + "), each call between its own CUDA events")},
         "gpu_launches": n_stages * K,
         "stages": stage_names,
         "wall_s": wall,

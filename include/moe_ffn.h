@@ -37,6 +37,9 @@
  *     reaches the point of the call.  The library keeps no pointer after a
  *     call returns; the caller keeps every buffer alive until the stream's
  *     work is done.
+ *   - moe_ffn_forward_ex and moe_ffn_forward_noalloc may be captured into a
+ *     CUDA graph (make one uncaptured call first: it sets up the device);
+ *     replays recompute from the captured buffers' current contents.
  *   - Launch failures are returned as MOE_ERR_CUDA (cudaPeekAtLastError);
  *     faults during execution surface at the caller's next synchronisation.
  *   - Results are deterministic: for the same inputs, path and device the
@@ -94,8 +97,10 @@ typedef struct moe_ffn_opts {
     /* nullable: MOE_MAX_STAGES + 1 created events.  When set, the call
      * records stage_events[0] before its first kernel and stage_events[i+1]
      * after kernel i, on `stream`, so the caller can time each kernel with
-     * cudaEventElapsedTime.  Recording events between kernels can change
-     * how they overlap, so time whole calls without it. */
+     * cudaEventElapsedTime.  Under stream capture they are recorded as
+     * external event nodes, which time the kernels when the graph replays.
+     * Recording events between kernels can change how they overlap, so time
+     * whole calls without it. */
     cudaEvent_t *stage_events;
     /* outputs */
     int32_t n_stages;          /* kernels the call enqueued */

@@ -67,6 +67,18 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// warp_sum of N values at once: the same butterfly per value (same bits as
+// N calls of warp_sum), with the N shuffle chains interleaved.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float (&v)[N])
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < N; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
+    }
+}
+
 // silu(g) * u in FP32 with the library expf.
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 

@@ -1,29 +1,45 @@
-// decode1.cu -- the decode path for a single token (T = 1), as two kernels.
+// decode1.cu -- the decode path for a single token (T = 1), as one kernel.
 //
 // The warp-decode article ("Cursor warp decode 공개 ...", section 핵심 내용)
 // finishes a decode step in two kernels, one warp per output scalar, summing
 // the routed experts' contributions in FP32 with no padding, scatter or
 // per-expert buffers; its section 경쟁 구도 / 비교 keeps the intermediate
-// activation unquantised.  On GB300 the two kernels here are persistent, one
-// CTA of each per SM, and move the weights with bulk copies:
-//   decode1_gate_up: every CTA routes the token itself (the router kernel's
-//     rank-based top-k and softmax, same bits) and owns an equal, contiguous
-//     share of the k*2I gate/up rows of the chosen experts.  Within one expert
-//     those rows are contiguous in memory, so a producer warp moves them into
-//     a shared-memory ring as bulk copies (cp.async.bulk) of whole rows,
-//     about 16 KB each; consumer warps take the rows round-robin and write
-//     each row's dot product with x (FP32) to gu[slot][row].
-//   decode1_down: launched as a programmatic dependent of gate_up, which lets
-//     it go as soon as gate_up has routed.  The two kernels are sized to share
-//     an SM, so the down CTA's producer streams W_down[e_j, h_lo:h_hi, :]
-//     (contiguous per expert; the weights do not depend on gate_up) while
-//     gate_up is still streaming.  Its consumers wait for gate_up, form
-//     act = silu(gate) * up in shared memory (FP32), dot each row with act[j]
-//     and finally sum out[h] = sum_j w_j * part[h][j] in slot order.
+// activation unquantised.  On GB300 a single token's layer is one
+// cooperative launch, one CTA per SM, that moves the weights with bulk
+// copies (cp.async.bulk) into a shared-memory ring:
+//   - every CTA routes the token itself (the router kernel's warp top-k and
+//     softmax, same bits);
+//   - phase A: the CTA owns an equal, contiguous share of the k*I (slot j,
+//     index i) pairs; pair (j, i) is gate row i and up row I+i of expert
+//     sel[j].  For a run of pairs of one slot both row blocks are contiguous
+//     in memory: the producer warp copies them into one ring slot (two bulk
+//     copies), the consumer warps take the pairs round-robin, form both dot
+//     products with x (FP32) and write act = silu(gate) * up to global
+//     memory, already in the two-plane order phase B keeps in shared memory;
+//   - the producer goes straight on to the CTA's W_down rows (dims
+//     [h_lo, h_hi) of each chosen expert, slot after slot; they do not
+//     depend on phase A), so they stream in while the grid meets at a
+//     barrier.  A ring slot takes as many of these rows as fit, across
+//     expert boundaries (one bulk copy per expert run);
+//   - phase B: after the barrier every CTA copies act (k*I FP32) into
+//     shared memory, dots each of its W_down rows with act[j] and sums
+//     out[h] = sum_j w_j * part[h][j] in slot order.
 // Each dot product uses decode.cu's lane split, chunk order, fmaf order and
 // shuffle butterfly, so this path returns the same bits as the general decode
 // path.  Every consumer warp visits every chunk in order, so a ring slot's
 // parity waits are never more than one phase ahead; every wait is bounded.
+//
+// Grid barrier (two hops, every spin bounded): after a CTA-wide barrier one
+// thread of CTA b stores the call's epoch into flags[b] (release).  CTA 0's
+// threads watch those words, one each, and once all hold the epoch CTA 0
+// stores it into the go word (release); one thread of every other CTA
+// watches the go word.  Spins use relaxed loads and end with one acquire
+// load.  The epoch is the launch's odd 64-bit base (drawn at random per
+// process, advanced per launch) plus twice a call counter kept in the flags
+// array: every CTA reads the counter before it arrives and CTA 0 advances it
+// after the barrier, so a CUDA-graph replay, which repeats the base, still
+// gets a fresh epoch.  Stale values from earlier calls never equal a later
+// epoch, so nothing needs zeroing.
 #include <atomic>
 #include <random>
 
@@ -38,21 +54,32 @@ __device__ uint32_t g_decode1_fault_word = 0;
 
 namespace {
 
-// Registers: 2 CTAs x 416 threads x <= 78 fit one SM's 64 K.
-constexpr int kConsumers = 12;
-constexpr int kThreads = 32 * (1 + kConsumers);
-constexpr int kSlotTarget = 16 * 1024;  // bytes per bulk copy (whole rows)
+constexpr int kConsumers = 16;                   // consumer warps per CTA
+constexpr int kThreads = 32 * (1 + kConsumers);  // + the producer warp
+constexpr int kChunkTarget = 32 * 1024;          // gate/up bytes per ring slot (whole row pairs)
+constexpr int kSlotMin = 16 * 1024;
+constexpr int kRowsB = 4;                        // phase B rows per warp task
 constexpr int kMaxSlots = 16;
-constexpr int kSmemCap = 226 * 1024;    // dynamic, one CTA; the per-block limit also covers static smem
-constexpr int kSmemPerSm = 224 * 1024;  // dynamic, both CTAs together
+constexpr int kSmemCap = 226 * 1024;  // dynamic; the per-block limit also covers static smem
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
-__host__ __device__ inline uint32_t align16(uint32_t v) { return (v + 15u) & ~15u; }
+// flags words: [0, kMaxGridCtas) arrivals, then the call counter, then the
+// go word on a 128-byte line of its own
+constexpr int kCallWord = kMaxGridCtas;
+constexpr int kGoWord = kMaxGridCtas + 16;
+static_assert(kGoWord < kDecode1FlagWords, "flags array too small");
 
-// Shared-memory layout: ring | full[slots] | empty[slots] | flag | keys[E] | payload
+enum : uint32_t {
+    FAULT_PRODUCER = 16u,
+    FAULT_PHASE_A = 32u,
+    FAULT_BARRIER = 64u,
+    FAULT_PHASE_B = 128u,
+};
+
+// Shared-memory layout: ring | full[slots] | empty[slots] | flag | vals[E] | payload
 struct Layout {
-    uint32_t full, empty, flag, keys, payload, total;
+    uint32_t full, empty, flag, vals, payload, total;
 };
 
 __host__ __device__ inline Layout layout(int slots, int slot_bytes, int E, uint32_t payload_bytes)
@@ -65,11 +92,16 @@ __host__ __device__ inline Layout layout(int slots, int slot_bytes, int E, uint3
     o += slots * 8;
     L.flag = o;
     o += 16;
-    L.keys = o;
-    o = align16(o + (uint32_t)E * 8);
+    L.vals = o;
+    o += ((uint32_t)E * 4 + 15u) & ~15u;
     L.payload = o;
     L.total = o + payload_bytes;
     return L;
+}
+
+__host__ __device__ inline uint32_t xa_bytes(int H, int I, int k)
+{
+    return (uint32_t)(4 * H > 4 * k * I ? 4 * H : 4 * k * I);  // x in phase A, act in phase B
 }
 
 __device__ __forceinline__ void fail(volatile int *flag, uint32_t bit)
@@ -80,18 +112,6 @@ __device__ __forceinline__ void fail(volatile int *flag, uint32_t bit)
 
 __device__ __forceinline__ uint4 lds16(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
 
-__device__ __forceinline__ void init_ring(uint64_t *full, uint64_t *empty, int slots, volatile int *flag)
-{
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < slots; ++s) {
-            ptx::mbar_init(full + s, 1);
-            ptx::mbar_init(empty + s, kConsumers);
-        }
-        *flag = 0;
-        ptx::fence_barrier_init();
-    }
-}
-
 // The producer waits (bounded) until the last `slots` chunks it issued have
 // landed, so no copy is in flight when the CTA exits.
 __device__ __forceinline__ void drain(uint64_t *full, int slots, int issued)
@@ -101,346 +121,133 @@ __device__ __forceinline__ void drain(uint64_t *full, int slots, int issued)
         ptx::mbar_wait_bounded(full + (c % slots), (uint32_t)(c / slots) & 1, &keep, kDrainNs);
 }
 
-// First row t >= t0 of the CTA's row sequence (starting at lo) that belongs
-// to consumer warp cw (rows go round-robin over the consumer warps).
-__device__ __forceinline__ int first_row(int t0, int lo, int cw)
+// First task of consumer warp cw in a run whose first task has round-robin
+// position `pos` (tasks go round-robin over the consumer warps).
+__device__ __forceinline__ int first_task(int pos, int cw) { return (cw - pos + kConsumers) & (kConsumers - 1); }
+static_assert((kConsumers & (kConsumers - 1)) == 0, "kConsumers must be a power of two");
+
+// Position of act element i of a row in the two-plane order: element 8u+e
+// sits in plane e/4 at 4u + e%4.
+__device__ __forceinline__ int plane_pos(int i, int n) { return ((i >> 2) & 1) * (n / 2) + (i >> 3) * 4 + (i & 3); }
+
+
+// Spin (bounded, relaxed loads) until *p == v, then one acquire load of the
+// same word, which synchronises with the release store that wrote v.
+__device__ __forceinline__ bool wait_word(const unsigned long long *p, unsigned long long v, volatile int *flag,
+                                          uint64_t t_start)
 {
-    const int m = (t0 - lo) % kConsumers;
-    return t0 + ((cw - m) % kConsumers + kConsumers) % kConsumers;
+    for (uint32_t spin = 0; ptx::ld_relaxed_gpu(p) != v; ++spin)
+        if ((spin & 63) == 63 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) return false;
+    return ptx::ld_acquire_gpu(p) == v;
 }
 
-// ------------------------------------------------------------------ gate_up
-// Rows r in [0, k*2I): slot j = r / 2I, row q = r % 2I of expert sel[j]'s
-// [2I, H] block.  A chunk is at most rpc rows and never crosses an expert.
-__device__ __forceinline__ int gu_chunk_end(int t0, int hi, int per_expert, int rpc)
-{
-    const int e_end = (t0 / per_expert + 1) * per_expert;
-    return min(hi, min(e_end, t0 + rpc));
-}
-
-__global__ void __launch_bounds__(kThreads, 2)
-    decode1_gate_up_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
-                           const uint16_t *__restrict__ wgu, int H, int I, int E, int k, int slots, int rpc,
-                           float *__restrict__ gu, int32_t *__restrict__ idx_out, float *__restrict__ w_out)
+__global__ void __launch_bounds__(kThreads, 1)
+    decode1_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits, const uint16_t *__restrict__ wgu,
+                   const uint16_t *__restrict__ wd, int H, int I, int E, int k, int slots, int slot_bytes, int rpc,
+                   int rps, int nh_max, float *__restrict__ act_g, unsigned long long *__restrict__ flags,
+                   unsigned long long epoch_base, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
+                   float *__restrict__ out)
 {
     extern __shared__ __align__(128) uint8_t sm[];
-    const int slot_bytes = rpc * 2 * H;
-    const Layout L = layout(slots, slot_bytes, E, (uint32_t)H * 4);
+    const uint32_t xa = xa_bytes(H, I, k);
+    const Layout L = layout(slots, slot_bytes, E, xa + (uint32_t)nh_max * k * 4);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sm + L.empty);
     volatile int *flag = reinterpret_cast<volatile int *>(sm + L.flag);
     // x in FP32, two planes: element 8u+e sits in plane e/4 at 4u + e%4, so a
     // lane's 8 consecutive elements are two float4 loads that are contiguous
-    // across the warp (no bank conflicts, no per-row unpacking)
+    // across the warp (no bank conflicts, no per-row unpacking).  Phase B
+    // reuses the space for act [k][I], each row in the same two-plane form.
     float *xs = reinterpret_cast<float *>(sm + L.payload);
-    __shared__ int sel[32];
-    __shared__ float wsm[32];
-
-    init_ring(full, empty, slots, flag);
-    route_token_block(logits, E, k, reinterpret_cast<unsigned long long *>(sm + L.keys), sel, wsm);
-    if (blockIdx.x == 0 && threadIdx.x < k) {
-        if (idx_out) idx_out[threadIdx.x] = sel[threadIdx.x];
-        if (w_out) w_out[threadIdx.x] = wsm[threadIdx.x];
-    }
-    pdl_trigger();
-
-    const int per_expert = 2 * I;
-    const int rows = k * per_expert;
-    const int lo = (int)((int64_t)rows * blockIdx.x / gridDim.x);
-    const int hi = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            int c = 0;
-            for (int t0 = lo; t0 < hi; ++c) {
-                const int t1 = gu_chunk_end(t0, hi, per_expert, rpc);
-                const int s = c % slots;
-                if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
-                    fail(flag, 1u);
-                    break;
-                }
-                const int j = t0 / per_expert, q0 = t0 - j * per_expert;
-                const uint32_t bytes = (uint32_t)(t1 - t0) * 2 * H;
-                ptx::mbar_arrive_expect_tx(full + s, bytes);
-                ptx::bulk_load(sm + (size_t)s * slot_bytes, wgu + ((int64_t)sel[j] * per_expert + q0) * H, bytes,
-                               full + s);
-                t0 = t1;
-            }
-            drain(full, slots, c);
-        }
-        return;
-    }
-
-    // consumers stage x while the first copies are in flight
-    for (int u = threadIdx.x - 32; u < H / 8; u += kConsumers * 32) {
-        float f[8];
-        unpack8(ld_nc16(x + (size_t)u * 8), f);
-        *reinterpret_cast<float4 *>(xs + 4 * u) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4 *>(xs + H / 2 + 4 * u) = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    ptx::named_sync(1, kConsumers * 32);
-
-    const int cw = warp - 1;
-    int c = 0;
-    for (int t0 = lo; t0 < hi; ++c) {
-        const int t1 = gu_chunk_end(t0, hi, per_expert, rpc);
-        const int s = c % slots;
-        if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
-            fail(flag, 2u);
-            break;
-        }
-        const uint8_t *chunk = sm + (size_t)s * slot_bytes;
-        for (int t = first_row(t0, lo, cw); t < t1; t += kConsumers) {
-            const uint8_t *row = chunk + (size_t)(t - t0) * 2 * H;
-            float acc = 0.0f;
-#pragma unroll 4
-            for (int h = lane * 8; h < H; h += 256) {
-                float wf[8], xf[8];
-                unpack8(lds16(row + 2 * h), wf);
-                const float4 x0 = *reinterpret_cast<const float4 *>(xs + h / 2);
-                const float4 x1 = *reinterpret_cast<const float4 *>(xs + H / 2 + h / 2);
-                xf[0] = x0.x; xf[1] = x0.y; xf[2] = x0.z; xf[3] = x0.w;
-                xf[4] = x1.x; xf[5] = x1.y; xf[6] = x1.z; xf[7] = x1.w;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc = fmaf(wf[q], xf[q], acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) gu[t] = acc;  // t = j * 2I + q
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty + s);
-        t0 = t1;
-    }
-}
-
-// ------------------------------------------------------------------ down
-// CTA rows: for slot j = 0..k-1, dims h in [h_lo, h_hi) in chunks of at most
-// rpd rows (contiguous in W_down[e_j]).  Row sequence index = j * nh + (h - h_lo).
-__global__ void __launch_bounds__(kThreads, 2)
-    decode1_down_kernel(const float *__restrict__ gu, const float *__restrict__ logits,
-                        const uint16_t *__restrict__ wd, int H, int I, int E, int k, int slots, int rpd, int nh_max,
-                        float *__restrict__ out)
-{
-    extern __shared__ __align__(128) uint8_t sm[];
-    const int slot_bytes = rpd * 2 * I;
-    const Layout L = layout(slots, slot_bytes, E, (uint32_t)(k * I + nh_max * k) * 4);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(sm + L.empty);
-    volatile int *flag = reinterpret_cast<volatile int *>(sm + L.flag);
-    float *act = reinterpret_cast<float *>(sm + L.payload);  // [k][I]
-    float *part = act + (size_t)k * I;                        // [nh][k]
-    __shared__ int sel[32];
-    __shared__ float wsm[32];
-
-    init_ring(full, empty, slots, flag);
-    route_token_block(logits, E, k, reinterpret_cast<unsigned long long *>(sm + L.keys), sel, wsm);
-
-    const int h_lo = (int)((int64_t)H * blockIdx.x / gridDim.x);
-    const int h_hi = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
-    const int nh = h_hi - h_lo;
-    const int cpe = (nh + rpd - 1) / rpd;  // chunks per expert
-    const int n_chunks = k * cpe;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (warp == 0) {
-        // the weights do not depend on gate_up: stream them now
-        if (lane == 0) {
-            int c = 0;
-            for (; c < n_chunks; ++c) {
-                const int j = c / cpe, h0 = h_lo + (c - j * cpe) * rpd;
-                const int nr = min(rpd, h_hi - h0);
-                const int s = c % slots;
-                if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
-                    fail(flag, 4u);
-                    break;
-                }
-                const uint32_t bytes = (uint32_t)nr * 2 * I;
-                ptx::mbar_arrive_expect_tx(full + s, bytes);
-                ptx::bulk_load(sm + (size_t)s * slot_bytes, wd + ((int64_t)sel[j] * H + h0) * I, bytes, full + s);
-            }
-            drain(full, slots, c);
-        }
-        return;
-    }
-
-    // consumers: act = silu(gate) * up for the k slots, from gate_up's output
-    pdl_wait();
-    const int ct = threadIdx.x - 32, n_ct = kConsumers * 32;
-    const int n4 = k * I / 4;
-    for (int v0 = ct; v0 < n4; v0 += 4 * n_ct) {
-        float4 g4[4], u4[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int v = v0 + b * n_ct;
-            if (v < n4) {
-                const int j = (4 * v) / I, i = 4 * v - j * I;
-                g4[b] = *reinterpret_cast<const float4 *>(gu + (size_t)j * 2 * I + i);
-                u4[b] = *reinterpret_cast<const float4 *>(gu + (size_t)j * 2 * I + I + i);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int v = v0 + b * n_ct;
-            if (v < n4) {
-                float4 a;
-                a.x = swiglu(g4[b].x, u4[b].x);
-                a.y = swiglu(g4[b].y, u4[b].y);
-                a.z = swiglu(g4[b].z, u4[b].z);
-                a.w = swiglu(g4[b].w, u4[b].w);
-                // row j in two planes (element 8u+e at plane e/4, offset 4u + e%4)
-                const int j = (4 * v) / I, i = 4 * v - j * I;
-                *reinterpret_cast<float4 *>(act + (size_t)j * I + ((i >> 2) & 1) * (I / 2) + (i >> 3) * 4) = a;
-            }
-        }
-    }
-    ptx::named_sync(1, n_ct);
-
-    const int cw = warp - 1;
-    for (int c = 0; c < n_chunks; ++c) {
-        const int j = c / cpe, h0 = h_lo + (c - j * cpe) * rpd;
-        const int nr = min(rpd, h_hi - h0);
-        const int s = c % slots;
-        if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
-            fail(flag, 8u);
-            break;
-        }
-        const uint8_t *chunk = sm + (size_t)s * slot_bytes;
-        const float *arow = act + (size_t)j * I;
-        const int base = j * nh + (h0 - h_lo);  // row sequence index of the chunk's first row
-        for (int u = first_row(base, 0, cw) - base; u < nr; u += kConsumers) {
-            const uint8_t *row = chunk + (size_t)u * 2 * I;
-            float acc = 0.0f;
-#pragma unroll 4
-            for (int i = lane * 8; i < I; i += 256) {
-                float wf[8];
-                unpack8(lds16(row + 2 * i), wf);
-                const float4 v0 = *reinterpret_cast<const float4 *>(arow + i / 2);
-                const float4 v1 = *reinterpret_cast<const float4 *>(arow + I / 2 + i / 2);
-                const float af[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc = fmaf(wf[q], af[q], acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) part[(h0 - h_lo + u) * k + j] = acc;
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty + s);
-    }
-    ptx::named_sync(1, n_ct);
-    if (*flag) return;
-    for (int q = ct; q < nh; q += n_ct) {
-        float o = 0.0f;
-        for (int j = 0; j < k; ++j) o = fmaf(wsm[j], part[q * k + j], o);
-        out[h_lo + q] = o;
-    }
-}
-
-// ------------------------------------------------------------------ fused
-// The single-token layer in one cooperative launch (all CTAs resident, one
-// per SM).  Each CTA routes the token once; its producer streams first the
-// CTA's share of gate/up rows, then -- without a pause, since W_down does not
-// depend on gate_up -- its W_down rows, through one ring.  The consumers
-// compute the gate/up dot products (gu), meet the other CTAs at a grid-wide
-// barrier, form act = silu(gate) * up in shared memory (reusing the space of
-// x), and finish the down rows, many of which are already in the ring.
-//
-// Grid barrier: CTA b stores the call's epoch (a 64-bit value unique to the
-// call) into flags[b] with release semantics once its gu rows are written,
-// then waits (bounded) until every flags[c] holds the epoch.  Stale values
-// from earlier calls never equal a later epoch, so nothing needs zeroing.
-constexpr int kFusedConsumers = 16;
-constexpr int kFusedThreads = 32 * (1 + kFusedConsumers);
-
-__device__ __forceinline__ int fused_first_row(int t0, int lo, int cw)
-{
-    const int m = (t0 - lo) % kFusedConsumers;
-    return t0 + ((cw - m) % kFusedConsumers + kFusedConsumers) % kFusedConsumers;
-}
-
-__global__ void __launch_bounds__(kFusedThreads, 1)
-    decode1_fused_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
-                         const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int H, int I, int E,
-                         int k, int slots, int slot_bytes, int rpc, int rpd, int nh_max, float *__restrict__ gu,
-                         unsigned long long *__restrict__ flags, unsigned long long epoch,
-                         int32_t *__restrict__ idx_out, float *__restrict__ w_out, float *__restrict__ out)
-{
-    extern __shared__ __align__(128) uint8_t sm[];
-    const uint32_t xa_bytes = (uint32_t)(4 * H > 4 * k * I ? 4 * H : 4 * k * I);  // x, later act
-    const Layout L = layout(slots, slot_bytes, E, xa_bytes + (uint32_t)nh_max * k * 4);
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(sm + L.empty);
-    volatile int *flag = reinterpret_cast<volatile int *>(sm + L.flag);
-    float *xs = reinterpret_cast<float *>(sm + L.payload);   // phase A: x, two planes
-    float *act = xs;                                          // phase B: act [k][I], two planes per row
-    float *part = reinterpret_cast<float *>(sm + L.payload + xa_bytes);  // [nh][k]
+    float *act = xs;
+    float *part = reinterpret_cast<float *>(sm + L.payload + xa);  // [nh][k]
     __shared__ int sel[32];
     __shared__ float wsm[32];
     if (threadIdx.x == 0) {
         for (int s = 0; s < slots; ++s) {
             ptx::mbar_init(full + s, 1);
-            ptx::mbar_init(empty + s, kFusedConsumers);
+            ptx::mbar_init(empty + s, kConsumers);
         }
         *flag = 0;
         ptx::fence_barrier_init();
     }
-    route_token_block(logits, E, k, reinterpret_cast<unsigned long long *>(sm + L.keys), sel, wsm);
+    const unsigned long long calls = *reinterpret_cast<volatile unsigned long long *>(flags + kCallWord);
+    const unsigned long long epoch = epoch_base + 2 * calls;
+    route_token_block(logits, E, k, reinterpret_cast<float *>(sm + L.vals), sel, wsm);  // ends with __syncthreads
     if (blockIdx.x == 0 && threadIdx.x < k) {
         if (idx_out) idx_out[threadIdx.x] = sel[threadIdx.x];
         if (w_out) w_out[threadIdx.x] = wsm[threadIdx.x];
     }
 
-    // phase A rows: [lo, hi) of the k*2I gate/up rows; phase B: output dims
-    // [h_lo, h_hi), all k slots, cpe chunks of <= rpd rows per slot
-    const int per_expert = 2 * I;
-    const int rows = k * per_expert;
-    const int lo = (int)((int64_t)rows * blockIdx.x / gridDim.x);
-    const int hi = (int)((int64_t)rows * (blockIdx.x + 1) / gridDim.x);
+    // Phase A: pairs [lo, hi) of the k*I, pair p = (slot p / I, index p % I),
+    // in chunks of at most rpc pairs that never cross a slot.  Phase B:
+    // output dims [h_lo, h_hi) of all k slots, the row sequence
+    // s -> (slot s / nh, dim h_lo + s % nh), in chunks of rps rows that may
+    // cross slots.  Producer and consumers walk both sequences with running
+    // (slot, index) state.
+    const int pairs = k * I;
+    const int lo = (int)((int64_t)pairs * blockIdx.x / gridDim.x);
+    const int hi = (int)((int64_t)pairs * (blockIdx.x + 1) / gridDim.x);
     const int h_lo = (int)((int64_t)H * blockIdx.x / gridDim.x);
     const int h_hi = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
     const int nh = h_hi - h_lo;
-    const int cpe = (nh + rpd - 1) / rpd;
-    const int nb = k * cpe;
+    const int nrow = k * nh;
+    const int nb = (nrow + rps - 1) / rps;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == 0) {
         if (lane == 0) {
             int c = 0;
             bool ok = true;
-            for (int t0 = lo; t0 < hi && ok; ++c) {
-                const int t1 = gu_chunk_end(t0, hi, per_expert, rpc);
+            int j = lo / I, i0 = lo - j * I;
+            for (int p = lo; p < hi && ok; ++c) {
+                const int n = min(rpc, min(I - i0, hi - p));
                 const int s = c % slots;
                 if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
-                    fail(flag, 16u);
+                    fail(flag, FAULT_PRODUCER);
                     ok = false;
                     break;
                 }
-                const int j = t0 / per_expert, q0 = t0 - j * per_expert;
-                const uint32_t bytes = (uint32_t)(t1 - t0) * 2 * H;
-                ptx::mbar_arrive_expect_tx(full + s, bytes);
-                ptx::bulk_load(sm + (size_t)s * slot_bytes, wgu + ((int64_t)sel[j] * per_expert + q0) * H, bytes,
-                               full + s);
-                t0 = t1;
+                const uint32_t bytes = (uint32_t)n * 2 * H;  // one block: gate or up rows
+                const uint16_t *gate = wgu + ((int64_t)sel[j] * 2 * I + i0) * H;
+                ptx::mbar_arrive_expect_tx(full + s, 2 * bytes);
+                ptx::bulk_load(sm + (size_t)s * slot_bytes, gate, bytes, full + s);
+                ptx::bulk_load(sm + (size_t)s * slot_bytes + bytes, gate + (int64_t)I * H, bytes, full + s);
+                p += n;
+                i0 += n;
+                if (i0 == I) {
+                    i0 = 0;
+                    ++j;
+                }
             }
+            int jj = 0, rr = 0;
             for (int q = 0; q < nb && ok; ++q, ++c) {
-                const int j = q / cpe, h0 = h_lo + (q - j * cpe) * rpd;
-                const int nr = min(rpd, h_hi - h0);
+                const int len_q = min(rps, nrow - q * rps);
                 const int s = c % slots;
                 if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
-                    fail(flag, 16u);
+                    fail(flag, FAULT_PRODUCER);
                     ok = false;
                     break;
                 }
-                const uint32_t bytes = (uint32_t)nr * 2 * I;
-                ptx::mbar_arrive_expect_tx(full + s, bytes);
-                ptx::bulk_load(sm + (size_t)s * slot_bytes, wd + ((int64_t)sel[j] * H + h0) * I, bytes, full + s);
+                ptx::mbar_arrive_expect_tx(full + s, (uint32_t)len_q * 2 * I);
+                for (int off = 0; off < len_q;) {  // one copy per expert run
+                    const int len = min(len_q - off, nh - rr);
+                    ptx::bulk_load(sm + (size_t)s * slot_bytes + (size_t)off * 2 * I,
+                                   wd + ((int64_t)sel[jj] * H + h_lo + rr) * I, (uint32_t)len * 2 * I, full + s);
+                    off += len;
+                    rr += len;
+                    if (rr == nh) {
+                        rr = 0;
+                        ++jj;
+                    }
+                }
             }
             drain(full, slots, c);
         }
         return;
     }
 
-    const int ct = threadIdx.x - 32, n_ct = kFusedConsumers * 32;
+    const int ct = threadIdx.x - 32, n_ct = kConsumers * 32;
     const int cw = warp - 1;
     for (int u = ct; u < H / 8; u += n_ct) {
         float f[8];
@@ -450,175 +257,172 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     ptx::named_sync(1, n_ct);
 
-    // phase A: gate/up row dot products
+    // phase A: gate and up dot products of each pair, act to global memory
     int c = 0;
-    for (int t0 = lo; t0 < hi; ++c) {
-        const int t1 = gu_chunk_end(t0, hi, per_expert, rpc);
-        const int s = c % slots;
-        if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
-            fail(flag, 32u);
-            break;
-        }
-        const uint8_t *chunk = sm + (size_t)s * slot_bytes;
-        for (int t = fused_first_row(t0, lo, cw); t < t1; t += kFusedConsumers) {
-            const uint8_t *row = chunk + (size_t)(t - t0) * 2 * H;
-            float acc = 0.0f;
-#pragma unroll 4
-            for (int h = lane * 8; h < H; h += 256) {
-                float wf[8];
-                unpack8(lds16(row + 2 * h), wf);
-                const float4 x0 = *reinterpret_cast<const float4 *>(xs + h / 2);
-                const float4 x1 = *reinterpret_cast<const float4 *>(xs + H / 2 + h / 2);
-                const float xf[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc = fmaf(wf[q], xf[q], acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) gu[t] = acc;
-        }
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(empty + s);
-        t0 = t1;
-    }
-
-    // grid barrier: every CTA's gu rows written and visible
-    __threadfence();
-    ptx::named_sync(1, n_ct);
-    if (ct == 0 && !*flag) ptx::st_release_gpu(flags + blockIdx.x, epoch);
-    // consumer thread ct watches the flags of CTAs ct, ct + n_ct, ... (all in parallel)
-    const uint64_t t_start = ptx::globaltimer_ns();
-    for (int b = ct; b < (int)gridDim.x && !*flag; b += n_ct) {
-        for (uint32_t spin = 0; ptx::ld_acquire_gpu(flags + b) != epoch; ++spin) {
-            if ((spin & 63) == 63 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) {
-                if (!*flag) fail(flag, 64u);
+    {
+        int j = lo / I, i0 = lo - j * I, pos = 0;
+        for (int p = lo; p < hi; ++c) {
+            const int n = min(rpc, min(I - i0, hi - p));
+            const int s = c % slots;
+            if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
+                fail(flag, FAULT_PHASE_A);
                 break;
             }
+            const uint8_t *chunk = sm + (size_t)s * slot_bytes;
+            for (int m = first_task(pos, cw); m < n; m += kConsumers) {
+                const uint8_t *grow = chunk + (size_t)m * 2 * H;
+                const uint8_t *urow = grow + (size_t)n * 2 * H;
+                float ag = 0.0f, au = 0.0f;
+#pragma unroll 4
+                for (int h = lane * 8; h < H; h += 256) {
+                    float gf[8], uf[8];
+                    unpack8(lds16(grow + 2 * h), gf);
+                    unpack8(lds16(urow + 2 * h), uf);
+                    const float4 x0 = *reinterpret_cast<const float4 *>(xs + h / 2);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(xs + H / 2 + h / 2);
+                    const float xf[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        ag = fmaf(gf[q], xf[q], ag);
+                        au = fmaf(uf[q], xf[q], au);
+                    }
+                }
+                float gu2[2] = {ag, au};
+                warp_sum_n(gu2);
+                if (lane == 0) act_g[(size_t)j * I + plane_pos(i0 + m, I)] = swiglu(gu2[0], gu2[1]);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty + s);
+            p += n;
+            pos = (pos + n) & (kConsumers - 1);
+            i0 += n;
+            if (i0 == I) {
+                i0 = 0;
+                ++j;
+            }
         }
     }
+
+    // grid barrier: every CTA's act values written and visible
     ptx::named_sync(1, n_ct);
-    __threadfence();
+    const uint64_t t_start = ptx::globaltimer_ns();
+    if (ct == 0 && !*flag) ptx::st_release_gpu(flags + blockIdx.x, epoch);
+    if (blockIdx.x == 0) {
+        for (int b = ct; b < (int)gridDim.x && !*flag; b += n_ct)
+            if (!wait_word(flags + b, epoch, flag, t_start)) fail(flag, FAULT_BARRIER);
+        ptx::named_sync(1, n_ct);
+        if (ct == 0 && !*flag) ptx::st_release_gpu(flags + kGoWord, epoch);
+    } else if (ct == 0 && !*flag) {
+        if (!wait_word(flags + kGoWord, epoch, flag, t_start)) fail(flag, FAULT_BARRIER);
+    }
+    ptx::named_sync(1, n_ct);
+    if (blockIdx.x == 0 && ct == 0) flags[kCallWord] = calls + 1;
     if (*flag) return;
 
-    // act = silu(gate) * up for the k slots, two planes per row (x's space)
+    // act of all k slots into shared memory (x's space), eight 16-byte loads
+    // in flight per thread
     const int n4 = k * I / 4;
-    for (int v0 = ct; v0 < n4; v0 += 4 * n_ct) {
-        float4 g4[4], u4[4];
+    for (int v0 = ct; v0 < n4; v0 += 8 * n_ct) {
+        float4 a4[8];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int v = v0 + b * n_ct;
-            if (v < n4) {
-                const int j = (4 * v) / I, i = 4 * v - j * I;
-                g4[b] = __ldcg(reinterpret_cast<const float4 *>(gu + (size_t)j * 2 * I + i));
-                u4[b] = __ldcg(reinterpret_cast<const float4 *>(gu + (size_t)j * 2 * I + I + i));
-            }
-        }
+        for (int b = 0; b < 8; ++b)
+            if (v0 + b * n_ct < n4) a4[b] = __ldcg(reinterpret_cast<const float4 *>(act_g) + v0 + b * n_ct);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int v = v0 + b * n_ct;
-            if (v < n4) {
-                const int j = (4 * v) / I, i = 4 * v - j * I;
-                float4 a;
-                a.x = swiglu(g4[b].x, u4[b].x);
-                a.y = swiglu(g4[b].y, u4[b].y);
-                a.z = swiglu(g4[b].z, u4[b].z);
-                a.w = swiglu(g4[b].w, u4[b].w);
-                *reinterpret_cast<float4 *>(act + (size_t)j * I + ((i >> 2) & 1) * (I / 2) + (i >> 3) * 4) = a;
-            }
-        }
+        for (int b = 0; b < 8; ++b)
+            if (v0 + b * n_ct < n4) reinterpret_cast<float4 *>(act)[v0 + b * n_ct] = a4[b];
     }
     ptx::named_sync(1, n_ct);
 
-    // phase B: W_down rows
+    // phase B: W_down rows.  Within a run of one slot's rows, groups of up
+    // to kRowsB consecutive rows share the act loads; the groups go
+    // round-robin over the consumer warps, counted across runs and chunks.
+    int jj = 0, rr = 0, pos = 0;
     for (int q = 0; q < nb; ++q, ++c) {
-        const int j = q / cpe, h0 = h_lo + (q - j * cpe) * rpd;
-        const int nr = min(rpd, h_hi - h0);
+        const int len_q = min(rps, nrow - q * rps);
         const int s = c % slots;
         if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
-            fail(flag, 128u);
+            fail(flag, FAULT_PHASE_B);
             break;
         }
         const uint8_t *chunk = sm + (size_t)s * slot_bytes;
-        const float *arow = act + (size_t)j * I;
-        const int base = j * nh + (h0 - h_lo);
-        for (int u = fused_first_row(base, 0, cw) - base; u < nr; u += kFusedConsumers) {
-            const uint8_t *row = chunk + (size_t)u * 2 * I;
-            float acc = 0.0f;
-#pragma unroll 4
-            for (int i = lane * 8; i < I; i += 256) {
-                float wf[8];
-                unpack8(lds16(row + 2 * i), wf);
-                const float4 v0 = *reinterpret_cast<const float4 *>(arow + i / 2);
-                const float4 v1 = *reinterpret_cast<const float4 *>(arow + I / 2 + i / 2);
-                const float af[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        for (int off = 0; off < len_q;) {
+            const int len = min(len_q - off, nh - rr);  // rows [rr, rr + len) of slot jj
+            const int ng = (len + kRowsB - 1) / kRowsB;
+            const float *arow = act + (size_t)jj * I;
+            for (int g = first_task(pos, cw); g < ng; g += kConsumers) {
+                const int u0 = g * kRowsB, nu = min(kRowsB, len - u0);
+                // rows past the group's end repeat its first row (in bounds,
+                // results dropped), so every row runs the same code
+                const uint8_t *rowp[kRowsB];
 #pragma unroll
-                for (int qq = 0; qq < 8; ++qq) acc = fmaf(wf[qq], af[qq], acc);
+                for (int r = 0; r < kRowsB; ++r)
+                    rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
+                float acc[kRowsB];
+#pragma unroll
+                for (int r = 0; r < kRowsB; ++r) acc[r] = 0.0f;
+#pragma unroll 2
+                for (int i = lane * 8; i < I; i += 256) {
+                    const float4 v0 = *reinterpret_cast<const float4 *>(arow + i / 2);
+                    const float4 v1 = *reinterpret_cast<const float4 *>(arow + I / 2 + i / 2);
+                    const float af[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    uint4 wv[kRowsB];
+#pragma unroll
+                    for (int r = 0; r < kRowsB; ++r) wv[r] = lds16(rowp[r] + 2 * i);
+#pragma unroll
+                    for (int r = 0; r < kRowsB; ++r) {
+                        float wf[8];
+                        unpack8(wv[r], wf);
+#pragma unroll
+                        for (int qq = 0; qq < 8; ++qq) acc[r] = fmaf(wf[qq], af[qq], acc[r]);
+                    }
+                }
+                warp_sum_n(acc);
+                if (lane == 0) {
+#pragma unroll
+                    for (int r = 0; r < kRowsB; ++r)
+                        if (r < nu) part[(rr + u0 + r) * k + jj] = acc[r];
+                }
             }
-            acc = warp_sum(acc);
-            if (lane == 0) part[(h0 - h_lo + u) * k + j] = acc;
+            pos = (pos + ng) & (kConsumers - 1);
+            off += len;
+            rr += len;
+            if (rr == nh) {
+                rr = 0;
+                ++jj;
+            }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + s);
     }
     ptx::named_sync(1, n_ct);
     if (*flag) return;
-    for (int qh = ct; qh < nh; qh += n_ct) {
+    for (int r = ct; r < nh; r += n_ct) {
         float o = 0.0f;
-        for (int j = 0; j < k; ++j) o = fmaf(wsm[j], part[qh * k + j], o);
-        out[h_lo + qh] = o;
+        for (int j = 0; j < k; ++j) o = fmaf(wsm[j], part[r * k + j], o);
+        out[h_lo + r] = o;
     }
 }
 
-// Ring geometry of both kernels: whole rows per slot (about kSlotTarget
-// bytes), and as many slots as fit -- preferably with both kernels' CTAs on
-// one SM together, otherwise each alone.
+// Geometry: phase A copies rpc whole gate/up row pairs (about kChunkTarget
+// bytes); a slot holds the larger of that, kSlotMin and one W_down row, and
+// phase B fills each slot with rps = slot / 2I rows.  As many slots as fit in
+// shared memory beside the payload.
 struct Plan {
-    int rpc, rpd, slots_a, slots_b, nh_max;
-    uint32_t payload_a, payload_b;
-    bool together;
+    int rpc, rps, slot_bytes, slots, nh_max;
+    uint32_t payload;
 };
 
 Plan plan_for(int H, int I, int E, int k, int n_sm)
 {
     Plan p;
     p.nh_max = (H + n_sm - 1) / n_sm;
-    p.rpc = kSlotTarget / (2 * H) > 0 ? kSlotTarget / (2 * H) : 1;
-    p.rpd = kSlotTarget / (2 * I) > 0 ? kSlotTarget / (2 * I) : 1;
-    if (p.rpd > p.nh_max) p.rpd = p.nh_max > 0 ? p.nh_max : 1;
-    const int sa = p.rpc * 2 * H, sb = p.rpd * 2 * I;
-    p.payload_a = (uint32_t)H * 4;
-    p.payload_b = (uint32_t)(k * I + p.nh_max * k) * 4;
-    const int fa = (int)layout(0, sa, E, p.payload_a).total + 2 * kMaxSlots * 8;
-    const int fb = (int)layout(0, sb, E, p.payload_b).total + 2 * kMaxSlots * 8;
-    const auto cap = [](int n) { return n > kMaxSlots ? kMaxSlots : n; };
-    // together: split the ring bytes in proportion to the weight bytes (2:1)
-    const int ring = kSmemPerSm - fa - fb;
-    p.slots_a = cap(ring * 2 / 3 / sa);
-    p.slots_b = cap((ring - p.slots_a * sa) / sb);
-    p.together = p.slots_a >= 2 && p.slots_b >= 2;
-    if (!p.together) {
-        p.slots_a = cap((kSmemCap - fa) / sa);
-        p.slots_b = cap((kSmemCap - fb) / sb);
-    }
-    return p;
-}
-
-// Fused kernel geometry: one ring for both phases, slots sized for the larger
-// of a gate/up chunk and a down chunk.
-struct FusedPlan {
-    int rpc, rpd, slot_bytes, slots, nh_max;
-    uint32_t payload;
-};
-
-FusedPlan fused_plan_for(int H, int I, int E, int k, int n_sm)
-{
-    FusedPlan p;
-    p.nh_max = (H + n_sm - 1) / n_sm;
-    p.rpc = kSlotTarget / (2 * H) > 0 ? kSlotTarget / (2 * H) : 1;
-    p.rpd = kSlotTarget / (2 * I) > 0 ? kSlotTarget / (2 * I) : 1;
-    if (p.rpd > p.nh_max) p.rpd = p.nh_max > 0 ? p.nh_max : 1;
-    p.slot_bytes = p.rpc * 2 * H > p.rpd * 2 * I ? p.rpc * 2 * H : p.rpd * 2 * I;
-    const int xa = 4 * H > 4 * k * I ? 4 * H : 4 * k * I;
-    p.payload = (uint32_t)(xa + p.nh_max * k * 4);
+    p.rpc = kChunkTarget / (4 * H) > 0 ? kChunkTarget / (4 * H) : 1;
+    const int a = p.rpc * 4 * H;
+    int slot = a > kSlotMin ? a : kSlotMin;
+    if (2 * I > slot) slot = 2 * I;
+    p.rps = slot / (2 * I);
+    p.slot_bytes = slot;
+    p.payload = xa_bytes(H, I, k) + (uint32_t)(p.nh_max * k * 4);
     const int fixed = (int)layout(0, p.slot_bytes, E, p.payload).total + 2 * kMaxSlots * 8;
     const int n = (kSmemCap - fixed) / p.slot_bytes;
     p.slots = n > kMaxSlots ? kMaxSlots : n;
@@ -627,9 +431,9 @@ FusedPlan fused_plan_for(int H, int I, int E, int k, int n_sm)
 
 std::atomic<unsigned long long> g_epoch{0};
 
-// A value unique to this call: a 64-bit counter whose start is drawn at random
-// once per process, so flags left in a workspace by earlier calls (or by
-// another process) do not match it.
+// A value unique to this launch: a 64-bit counter whose start is drawn at
+// random once per process, so flags left in a workspace by earlier calls (or
+// by another process) do not match it.
 unsigned long long next_epoch()
 {
     static const unsigned long long base = [] {
@@ -641,20 +445,20 @@ unsigned long long next_epoch()
 
 }  // namespace
 
-bool decode1_fused_supported(int H, int I, int E, int k, int n_sm)
+bool decode1_supported(int H, int I, int E, int k, int n_sm)
 {
     if (n_sm > kMaxGridCtas) return false;
-    return fused_plan_for(H, I, E, k, n_sm).slots >= 2;
+    return plan_for(H, I, E, k, n_sm).slots >= 2;
 }
 
-cudaError_t launch_decode1_fused(const void *x, const float *logits, const void *wgu, const void *wd, int H, int I,
-                                 int E, int k, int n_sm, float *gu, unsigned long long *flags, int32_t *idx_out,
-                                 float *w_out, float *out, cudaStream_t s)
+cudaError_t launch_decode1(const void *x, const float *logits, const void *wgu, const void *wd, int H, int I, int E,
+                           int k, int n_sm, float *act, unsigned long long *flags, int32_t *idx_out, float *w_out,
+                           float *out, cudaStream_t s)
 {
-    const FusedPlan p = fused_plan_for(H, I, E, k, n_sm);
+    const Plan p = plan_for(H, I, E, k, n_sm);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_sm);
-    cfg.blockDim = dim3(kFusedThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = layout(p.slots, p.slot_bytes, E, p.payload).total;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -662,8 +466,8 @@ cudaError_t launch_decode1_fused(const void *x, const float *logits, const void 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode1_fused_kernel, (const uint16_t *)x, logits, (const uint16_t *)wgu,
-                              (const uint16_t *)wd, H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rpd, p.nh_max, gu,
+    return cudaLaunchKernelEx(&cfg, decode1_kernel, (const uint16_t *)x, logits, (const uint16_t *)wgu,
+                              (const uint16_t *)wd, H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, act,
                               flags, next_epoch(), idx_out, w_out, out);
 }
 
@@ -677,49 +481,7 @@ cudaError_t read_decode1_fault_word(uint32_t *flags, bool clear)
 
 cudaError_t decode1_init_device()
 {
-    for (const void *kern : {(const void *)decode1_gate_up_kernel, (const void *)decode1_down_kernel,
-                             (const void *)decode1_fused_kernel}) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
-        if (e == cudaSuccess)  // ask for the largest shared-memory carveout so both CTAs fit
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     (int)cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-}
-
-bool decode1_supported(int H, int I, int E, int k, int n_sm)
-{
-    const Plan p = plan_for(H, I, E, k, n_sm);
-    return p.slots_a >= 2 && p.slots_b >= 2;
-}
-
-cudaError_t launch_decode1(const void *x, const float *logits, const void *wgu, const void *wd, int H, int I, int E,
-                           int k, int n_sm, float *gu, int32_t *idx_out, float *w_out, float *out, cudaStream_t s,
-                           cudaEvent_t between)
-{
-    const Plan p = plan_for(H, I, E, k, n_sm);
-    const size_t smem_a = layout(p.slots_a, p.rpc * 2 * H, E, p.payload_a).total;
-    decode1_gate_up_kernel<<<n_sm, kThreads, smem_a, s>>>((const uint16_t *)x, logits, (const uint16_t *)wgu, H, I,
-                                                          E, k, p.slots_a, p.rpc, gu, idx_out, w_out);
-    cudaError_t e = cudaPeekAtLastError();
-    if (e != cudaSuccess) return e;
-    if (between) {
-        e = cudaEventRecord(between, s);
-        if (e != cudaSuccess) return e;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)n_sm);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = layout(p.slots_b, p.rpd * 2 * I, E, p.payload_b).total;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode1_down_kernel, (const float *)gu, logits, (const uint16_t *)wd, H, I, E, k,
-                              p.slots_b, p.rpd, p.nh_max, out);
+    return cudaFuncSetAttribute(decode1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
 }
 
 }  // namespace moe

@@ -52,7 +52,7 @@ Layout make_layout(const Shape &s)
     L.ucount = take(4);
     L.chunks = take((size_t)(s.E + ceil_div((int64_t)n, moe::kGemmChunkMax) + 1) * 16);
     L.nchunks = take(4);
-    L.flags = take((size_t)moe::kMaxGridCtas * 8);  // grid-barrier flags of the single-token kernel
+    L.flags = take((size_t)moe::kDecode1FlagWords * 8);  // single-token kernel: grid-barrier state
     L.common_end = o;
     // decode path: act f32 [T*k, I]; the single-token kernels keep the gate
     // and up dot products there instead, [k, 2I]
@@ -135,20 +135,30 @@ const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"
 const char *kDecodeT1Stages[] = {"decode_fused"};
 const char *kGroupedStages[] = {"router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine"};
 
-// Records stage events around the launches of one call.
+// Records stage events around the launches of one call.  While the stream is
+// being captured into a CUDA graph the records become external event-record
+// nodes, so the events still time the graph's kernels when it is replayed.
 struct Stages {
     cudaEvent_t *ev;
     cudaStream_t s;
     int n = 0;
+    cudaError_t record(cudaEvent_t e)
+    {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t r = cudaStreamIsCapturing(s, &cs);
+        if (r != cudaSuccess) return r;
+        return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                                                   : cudaEventRecord(e, s);
+    }
     cudaError_t begin()
     {
-        return ev ? cudaEventRecord(ev[0], s) : cudaSuccess;
+        return ev ? record(ev[0]) : cudaSuccess;
     }
     cudaError_t done(cudaError_t launch)
     {
         if (launch != cudaSuccess) return launch;
         ++n;
-        return ev ? cudaEventRecord(ev[n], s) : cudaSuccess;
+        return ev ? record(ev[n]) : cudaSuccess;
     }
 };
 
@@ -189,11 +199,11 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (path == MOE_PATH_DECODE && T == 1 && moe::decode1_fused_supported(H, I, E, k, dev->n_sm)) {
+    if (path == MOE_PATH_DECODE && T == 1 && moe::decode1_supported(H, I, E, k, dev->n_sm)) {
         // one token: a single cooperative kernel that routes it, streams both
         // projections' rows and meets at a grid barrier in between
         path = MOE_PATH_DECODE_T1;
-        MOE_TRY(stg.done(moe::launch_decode1_fused(x, logits, wgu, wd, H, I, E, k, dev->n_sm,
+        MOE_TRY(stg.done(moe::launch_decode1(x, logits, wgu, wd, H, I, E, k, dev->n_sm,
                                                    (float *)(ws + L.act), (unsigned long long *)(ws + L.flags),
                                                    idx_out, w_out, out, stream)));
         if (opts) {

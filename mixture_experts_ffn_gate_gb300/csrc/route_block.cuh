@@ -1,37 +1,116 @@
 // route_block.cuh -- top-k selection and softmax weights for one token,
-// computed by a whole thread block.  Used by the router kernel and by the
-// single-token decode kernels, which route their token themselves; both give
-// the same bits.
+// computed by one warp.  Used by the router kernel and by the single-token
+// decode kernels, which route their token themselves; both give the same
+// bits.
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-// Every thread of the block must call this.  keys: E x 8 bytes of shared
-// memory; sel[k] and w[k] (shared) receive the chosen experts in slot order
-// and their softmax weights.  Ranking uses a strict total order (larger
-// logit first, the smaller index on ties, -0.0 == +0.0), so the ranks below
-// k are exactly the k slots.
-__device__ __forceinline__ void route_token_block(const float *__restrict__ l, int E, int k,
-                                                  unsigned long long *keys, int *sel, float *w)
+// One warp routes one token under a strict total order -- a larger logit
+// first, on equal logits the smaller index (-0.0 == +0.0).  The key of
+// expert e is the 64-bit (logit_key << 32) | ~e: keys are unique and 0 lies
+// below every key.  The warp copies the E logits into `vals` (E words of
+// shared memory owned by the warp, eight loads in flight per lane).  For
+// k <= kRouteList each lane keeps the kRouteList largest of its own keys
+// (e = lane + 32 i) in a sorted register list; k rounds then take the warp
+// maximum of the list heads (redux on the high, then the low half) and the
+// winning lane pops its head.  Larger k rescans the lane's keys below the
+// last winner instead.  Lane j < k returns the expert of slot j and its
+// softmax weight (the softmax over the k chosen logits, shifted by the
+// largest).
+constexpr int kRouteList = 8;
+
+__device__ __forceinline__ unsigned long long route_key(float f, int e)
 {
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        keys[e] = ((unsigned long long)logit_key(__ldg(l + e)) << 32) | (uint32_t)(0xffffffffu - (uint32_t)e);
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const unsigned long long me = keys[e];
-        int r = 0;
-        for (int j = 0; j < E; ++j) r += keys[j] > me;
-        if (r < k) sel[r] = e;
+    return ((unsigned long long)logit_key(f) << 32) | (uint32_t)~(uint32_t)e;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v)
+{
+    const uint32_t hi = (uint32_t)(v >> 32);
+    const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? (uint32_t)v : 0u);
+    return ((unsigned long long)mhi << 32) | mlo;
+}
+
+__device__ __forceinline__ void route_token_warp(const float *__restrict__ l, int E, int k, float *vals, int &sel_j,
+                                                 float &w_j)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned long long list[kRouteList];
+#pragma unroll
+    for (int q = 0; q < kRouteList; ++q) list[q] = 0;
+    for (int e0 = 0; e0 < E; e0 += 256) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = e0 + 32 * q + lane;
+            if (e < E) v[q] = __ldg(l + e);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = e0 + 32 * q + lane;
+            if (e < E) {
+                vals[e] = v[q];
+                // insert into the descending list: new[i] = max(old[i], min(old[i-1], x))
+                const unsigned long long x = route_key(v[q], e);
+#pragma unroll
+                for (int i = kRouteList - 1; i > 0; --i) {
+                    const unsigned long long m = list[i - 1] < x ? list[i - 1] : x;
+                    list[i] = list[i] > m ? list[i] : m;
+                }
+                list[0] = list[0] > x ? list[0] : x;
+            }
+        }
     }
-    __syncthreads();
+    sel_j = 0;
+    if (k <= kRouteList) {
+        for (int r = 0; r < k; ++r) {
+            const unsigned long long m = warp_max_key(list[0]);
+            if (lane == r) sel_j = (int)~(uint32_t)m;
+            if (list[0] == m) {
+#pragma unroll
+                for (int i = 0; i < kRouteList - 1; ++i) list[i] = list[i + 1];
+                list[kRouteList - 1] = 0;
+            }
+        }
+    } else {
+        unsigned long long best = list[0];
+        for (int r = 0; r < k; ++r) {
+            const unsigned long long m = warp_max_key(best);
+            if (lane == r) sel_j = (int)~(uint32_t)m;
+            if (best == m) {
+                best = 0;
+                for (int e = lane; e < E; e += 32) {
+                    const unsigned long long x = route_key(vals[e], e);
+                    if (x < m && x > best) best = x;
+                }
+            }
+        }
+    }
+    __syncwarp();
+    const float l0 = vals[__shfl_sync(0xffffffffu, sel_j, 0)];
+    const float ex = lane < k ? expf(vals[sel_j] - l0) : 0.0f;
+    const float s = warp_sum(ex);
+    w_j = lane < k ? ex / s : 0.0f;
+}
+
+// Block-wide form: warp 0 routes, every thread of the block must call this;
+// vals: E words of shared memory; sel[k] and w[k] (shared) receive the chosen
+// experts in slot order and their softmax weights.
+__device__ __forceinline__ void route_token_block(const float *__restrict__ l, int E, int k, float *vals, int *sel,
+                                                  float *w)
+{
     if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const float l0 = __ldg(l + sel[0]);
-        const float ex = lane < k ? expf(__ldg(l + sel[lane]) - l0) : 0.0f;
-        const float s = warp_sum(ex);
-        if (lane < k) w[lane] = ex / s;
+        int e;
+        float wt;
+        route_token_warp(l, E, k, vals, e, wt);
+        if (threadIdx.x < k) {
+            sel[threadIdx.x] = e;
+            w[threadIdx.x] = wt;
+        }
     }
     __syncthreads();
 }

@@ -15,26 +15,29 @@
 namespace moe {
 
 // ---------------------------------------------------------------- router
-// One block per token.  Each thread ranks its logits against all E with a
-// strict total order (larger logit first, smaller index on ties), so the k
-// ranks below k are a permutation of the slots and slot j holds the j-th
-// pick.  Warp 0 then forms the softmax over the k chosen logits.
-__global__ void __launch_bounds__(256) router_kernel(const float *__restrict__ logits, int E, int k,
-                                                     int32_t *__restrict__ idx, float *__restrict__ w,
-                                                     int32_t *__restrict__ idx_copy,
-                                                     float *__restrict__ w_copy)
+// One warp per token (route_token_warp): k rounds of a warp-wide maximum
+// under a strict total order (larger logit first, smaller index on ties), so
+// slot j holds the j-th pick; then the softmax over the k chosen logits.
+constexpr int kRouterWarps = 8;
+
+__global__ void __launch_bounds__(32 * kRouterWarps) router_kernel(const float *__restrict__ logits, int T, int E,
+                                                                   int k, int32_t *__restrict__ idx,
+                                                                   float *__restrict__ w,
+                                                                   int32_t *__restrict__ idx_copy,
+                                                                   float *__restrict__ w_copy)
 {
-    extern __shared__ unsigned long long keys[];  // [E]
-    __shared__ int sel[32];
-    __shared__ float wt[32];
-    const int t = blockIdx.x;
-    route_token_block(logits + (int64_t)t * E, E, k, keys, sel, wt);
-    if (threadIdx.x < k) {
-        const int j = threadIdx.x;
-        idx[(int64_t)t * k + j] = sel[j];
-        w[(int64_t)t * k + j] = wt[j];
-        if (idx_copy) idx_copy[(int64_t)t * k + j] = sel[j];
-        if (w_copy) w_copy[(int64_t)t * k + j] = wt[j];
+    extern __shared__ float vals[];  // [kRouterWarps][E]
+    const int t = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int e;
+    float wt;
+    route_token_warp(logits + (int64_t)t * E, E, k, vals + (threadIdx.x >> 5) * E, e, wt);
+    const int j = threadIdx.x & 31;
+    if (j < k) {
+        idx[(int64_t)t * k + j] = e;
+        w[(int64_t)t * k + j] = wt;
+        if (idx_copy) idx_copy[(int64_t)t * k + j] = e;
+        if (w_copy) w_copy[(int64_t)t * k + j] = wt;
     }
 }
 
@@ -187,8 +190,8 @@ __global__ void combine_kernel(const float *__restrict__ z, const float *__restr
 cudaError_t launch_router(const float *logits, int T, int E, int k, int32_t *idx, float *w, int32_t *idx_copy,
                           float *w_copy, cudaStream_t s)
 {
-    const int threads = E >= 256 ? 256 : ((E + 31) / 32) * 32;
-    router_kernel<<<T, threads, (size_t)E * sizeof(unsigned long long), s>>>(logits, E, k, idx, w, idx_copy, w_copy);
+    router_kernel<<<(unsigned)ceil_div(T, kRouterWarps), 32 * kRouterWarps, (size_t)kRouterWarps * E * 4, s>>>(
+        logits, T, E, k, idx, w, idx_copy, w_copy);
     return cudaPeekAtLastError();
 }
 

@@ -81,13 +81,16 @@ def _randn(shape, std, device, seed):
     return t
 
 
-def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=None):
+def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=None, layer=0):
     """Expert weights (w_gate_up [E,2I,H], w_down [E,H,I]) as BF16 on device.
 
     H, I, E default to the workload's; tests pass smaller ones to reuse the
     recipe at other sizes.  ``experts`` (a list of expert ids) draws only
     those blocks, in that order, with the same seeds as the full set.
+    ``layer`` > 0 draws another layer's weights (same distribution, other
+    seeds), for running calls over several layers.
     """
+    tag = () if layer == 0 else ("layer", layer)
     H = H or wl.H
     I = I or wl.I
     E = E or wl.E
@@ -96,9 +99,9 @@ def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=
     wd = torch.empty((len(ids), H, I), dtype=torch.bfloat16, device=device)
     for j, e in enumerate(ids):
         wgu[j] = _randn((2 * I, H), 1.0 / math.sqrt(H), device,
-                        seed_for(wl.name, H, I, "w_gate_up", e)).to(torch.bfloat16)
+                        seed_for(wl.name, H, I, "w_gate_up", e, *tag)).to(torch.bfloat16)
         wd[j] = _randn((H, I), 1.0 / math.sqrt(I), device,
-                       seed_for(wl.name, H, I, "w_down", e)).to(torch.bfloat16)
+                       seed_for(wl.name, H, I, "w_down", e, *tag)).to(torch.bfloat16)
     return wgu, wd
 
 

@@ -199,3 +199,45 @@ def test_errors_from_device_pointers():
     with pytest.raises(m.MoeFfnError) as ei:
         m.moe_ffn_forward_ex(x, L, wgu, wd, k, workspace=small)
     assert ei.value.status == m.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.parametrize("T,path", [(1, "decode"), (4, "decode"), (64, "grouped")])
+def test_cuda_graph_replay_matches_eager(T, path):
+    """A call captured into a CUDA graph recomputes, on every replay, what an
+    eager call gives for the buffers' current contents (the single-token
+    kernel's grid barrier must not reuse a stale epoch on replays)."""
+    H, I, E, k = 512, 256, 32, 8
+    wl = gu.custom(T, H, I, E, k, 1.0, name="graph")
+    inputs = [gu.make_layer(wl, T, call=c)[:2] for c in range(3)]
+    _, _, wgu, wd = gu.make_layer(wl, T)
+    refs = [gu.run_gpu(x, L, wgu, wd, k, path)[0] for x, L in inputs]
+    xb, lb = inputs[0][0].clone(), inputs[0][1].clone()
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = m.new_workspace(T, H, I, E, k)
+    o = m.moe_ffn_opts()
+    o.path = gu.PATHS[path]
+    m.moe_ffn_forward_ex(xb, lb, wgu, wd, k, out=out, workspace=ws, opts=o)
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
+    for e in evs:
+        e.record()
+    arr = m.stage_event_array(evs)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        oc = m.moe_ffn_opts()
+        oc.path = gu.PATHS[path]
+        oc.stage_events = m.ctypes.cast(arr, m.ctypes.c_void_p)
+        m.moe_ffn_forward_ex(xb, lb, wgu, wd, k, out=out, workspace=ws, opts=oc,
+                             stream=torch.cuda.current_stream())
+    if T == 1:
+        assert oc.path_taken == m.MOE_PATH_DECODE_T1
+    for r in range(12):
+        c = r % 3
+        xb.copy_(inputs[c][0])
+        lb.copy_(inputs[c][1])
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.cpu(), refs[c]), (r, c)
+    for i in range(oc.n_stages):
+        assert evs[i].elapsed_time(evs[i + 1]) >= 0.0
