@@ -30,16 +30,17 @@
 // parity waits are never more than one phase ahead; every wait is bounded.
 //
 // Grid barrier (two hops, every spin bounded): after a CTA-wide barrier one
-// thread of CTA b stores the call's epoch into flags[b] (release).  CTA 0's
-// threads watch those words, one each, and once all hold the epoch CTA 0
-// stores it into the go word (release); one thread of every other CTA
-// watches the go word.  Spins use relaxed loads and end with one acquire
-// load.  The epoch is the launch's odd 64-bit base (drawn at random per
-// process, advanced per launch) plus twice a call counter kept in the flags
-// array: every CTA reads the counter before it arrives and CTA 0 advances it
-// after the barrier, so a CUDA-graph replay, which repeats the base, still
-// gets a fresh epoch.  Stale values from earlier calls never equal a later
-// epoch, so nothing needs zeroing.
+// thread of CTA b stores the low 32 bits of the call's epoch into arrival
+// word b (release).  In CTA 0, thread t watches words 4t..4t+3 with 16-byte
+// relaxed loads until all hold the epoch, then issues an acq_rel fence; after
+// a CTA-wide barrier CTA 0 stores the epoch into the go word (release), which
+// one thread of every other CTA watches the same way.  The epoch is the launch's odd 64-bit
+// base (drawn at random per process, advanced per launch) plus twice a call
+// counter kept in the flags array: every CTA reads the counter before it
+// arrives and CTA 0 advances it after the barrier, so a CUDA-graph replay,
+// which repeats the base, still gets a fresh epoch.  Stale words from earlier
+// calls never equal a later epoch (within 2^31 calls), so nothing needs
+// zeroing.
 #include <atomic>
 #include <random>
 
@@ -64,8 +65,9 @@ constexpr int kSmemCap = 226 * 1024;  // dynamic; the per-block limit also cover
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
-// flags words: [0, kMaxGridCtas) arrivals, then the call counter, then the
-// go word on a 128-byte line of its own
+// flags (64-bit words): [0, kMaxGridCtas / 2) hold the kMaxGridCtas 32-bit
+// arrival words, then the call counter, then the go word on a 128-byte line
+// of its own
 constexpr int kCallWord = kMaxGridCtas;
 constexpr int kGoWord = kMaxGridCtas + 16;
 static_assert(kGoWord < kDecode1FlagWords, "flags array too small");
@@ -131,14 +133,53 @@ static_assert((kConsumers & (kConsumers - 1)) == 0, "kConsumers must be a power 
 __device__ __forceinline__ int plane_pos(int i, int n) { return ((i >> 2) & 1) * (n / 2) + (i >> 3) * 4 + (i & 3); }
 
 
-// Spin (bounded, relaxed loads) until *p == v, then one acquire load of the
-// same word, which synchronises with the release store that wrote v.
-__device__ __forceinline__ bool wait_word(const unsigned long long *p, unsigned long long v, volatile int *flag,
-                                          uint64_t t_start)
+// Spin (bounded, 16-byte relaxed loads) until the first n (<= 4) of the four
+// words at p all hold v, then an acq_rel fence, which synchronises with the
+// release stores that wrote them.
+__device__ __forceinline__ bool wait_words4(const uint32_t *p, int n, uint32_t v, volatile int *flag,
+                                            uint64_t t_start)
 {
-    for (uint32_t spin = 0; ptx::ld_relaxed_gpu(p) != v; ++spin)
+    for (uint32_t spin = 0;; ++spin) {
+        const uint4 w = ptx::ld_relaxed_gpu_v4(p);
+        if (w.x == v && (n < 2 || w.y == v) && (n < 3 || w.z == v) && (n < 4 || w.w == v)) break;
         if ((spin & 63) == 63 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) return false;
-    return ptx::ld_acquire_gpu(p) == v;
+    }
+    ptx::fence_acq_rel_gpu();
+    return true;
+}
+
+// Dot products of up to kRowsB W_down rows (rowp, BF16 in shared memory) with
+// one act row (two-plane FP32 in shared memory); rows past nu repeat a valid
+// row and are dropped.  Row r's result goes to part[r * k] (lane 0).  Each
+// row keeps decode.cu's lane split, fmaf order and butterfly.
+__device__ __forceinline__ void down_rows(const uint8_t *const (&rowp)[kRowsB], const float *arow, int I, int lane,
+                                          int nu, float *part, int k)
+{
+    float acc[kRowsB];
+#pragma unroll
+    for (int r = 0; r < kRowsB; ++r) acc[r] = 0.0f;
+#pragma unroll 2
+    for (int i = lane * 8; i < I; i += 256) {
+        const float4 v0 = *reinterpret_cast<const float4 *>(arow + i / 2);
+        const float4 v1 = *reinterpret_cast<const float4 *>(arow + I / 2 + i / 2);
+        const float af[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint4 wv[kRowsB];
+#pragma unroll
+        for (int r = 0; r < kRowsB; ++r) wv[r] = lds16(rowp[r] + 2 * i);
+#pragma unroll
+        for (int r = 0; r < kRowsB; ++r) {
+            float wf[8];
+            unpack8(wv[r], wf);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[r] = fmaf(wf[q], af[q], acc[r]);
+        }
+    }
+    warp_sum_n(acc);
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < kRowsB; ++r)
+            if (r < nu) part[r * k] = acc[r];
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -305,19 +346,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // grid barrier: every CTA's act values written and visible
     ptx::named_sync(1, n_ct);
-    const uint64_t t_start = ptx::globaltimer_ns();
-    if (ct == 0 && !*flag) ptx::st_release_gpu(flags + blockIdx.x, epoch);
-    if (blockIdx.x == 0) {
-        for (int b = ct; b < (int)gridDim.x && !*flag; b += n_ct)
-            if (!wait_word(flags + b, epoch, flag, t_start)) fail(flag, FAULT_BARRIER);
-        ptx::named_sync(1, n_ct);
-        if (ct == 0 && !*flag) ptx::st_release_gpu(flags + kGoWord, epoch);
-    } else if (ct == 0 && !*flag) {
-        if (!wait_word(flags + kGoWord, epoch, flag, t_start)) fail(flag, FAULT_BARRIER);
+    {
+        uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
+        const uint32_t e32 = (uint32_t)epoch;
+        const uint64_t t_start = ptx::globaltimer_ns();
+        uint32_t *go = reinterpret_cast<uint32_t *>(flags + kGoWord);
+        if (ct == 0 && !*flag) ptx::st_release_gpu(arrive + blockIdx.x, e32);
+        if (blockIdx.x == 0) {
+            for (int v = ct; 4 * v < (int)gridDim.x && !*flag; v += n_ct)
+                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start))
+                    fail(flag, FAULT_BARRIER);
+            ptx::named_sync(1, n_ct);
+            if (ct == 0 && !*flag) ptx::st_release_gpu(go, e32);
+        } else if (ct == 0 && !*flag) {
+            if (!wait_words4(go, 1, e32, flag, t_start)) fail(flag, FAULT_BARRIER);
+        }
     }
-    ptx::named_sync(1, n_ct);
+    // every consumer leaves, or none: a producer fault can set the flag at any time
+    const bool stop = ptx::named_sync_or(1, n_ct, *flag != 0);
     if (blockIdx.x == 0 && ct == 0) flags[kCallWord] = calls + 1;
-    if (*flag) return;
+    if (stop) return;
 
     // act of all k slots into shared memory (x's space), eight 16-byte loads
     // in flight per thread
@@ -333,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::named_sync(1, n_ct);
 
-    // phase B: W_down rows.  Within a run of one slot's rows, groups of up
-    // to kRowsB consecutive rows share the act loads; the groups go
-    // round-robin over the consumer warps, counted across runs and chunks.
+    // phase B: W_down rows, chunk by chunk.  Within a run of one slot's rows,
+    // groups of up to kRowsB consecutive rows share the act loads; the groups
+    // go round-robin over the consumer warps, counted across runs and chunks.
     int jj = 0, rr = 0, pos = 0;
     for (int q = 0; q < nb; ++q, ++c) {
         const int len_q = min(rps, nrow - q * rps);
@@ -348,40 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int off = 0; off < len_q;) {
             const int len = min(len_q - off, nh - rr);  // rows [rr, rr + len) of slot jj
             const int ng = (len + kRowsB - 1) / kRowsB;
-            const float *arow = act + (size_t)jj * I;
             for (int g = first_task(pos, cw); g < ng; g += kConsumers) {
                 const int u0 = g * kRowsB, nu = min(kRowsB, len - u0);
-                // rows past the group's end repeat its first row (in bounds,
-                // results dropped), so every row runs the same code
                 const uint8_t *rowp[kRowsB];
 #pragma unroll
                 for (int r = 0; r < kRowsB; ++r)
                     rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
-                float acc[kRowsB];
-#pragma unroll
-                for (int r = 0; r < kRowsB; ++r) acc[r] = 0.0f;
-#pragma unroll 2
-                for (int i = lane * 8; i < I; i += 256) {
-                    const float4 v0 = *reinterpret_cast<const float4 *>(arow + i / 2);
-                    const float4 v1 = *reinterpret_cast<const float4 *>(arow + I / 2 + i / 2);
-                    const float af[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                    uint4 wv[kRowsB];
-#pragma unroll
-                    for (int r = 0; r < kRowsB; ++r) wv[r] = lds16(rowp[r] + 2 * i);
-#pragma unroll
-                    for (int r = 0; r < kRowsB; ++r) {
-                        float wf[8];
-                        unpack8(wv[r], wf);
-#pragma unroll
-                        for (int qq = 0; qq < 8; ++qq) acc[r] = fmaf(wf[qq], af[qq], acc[r]);
-                    }
-                }
-                warp_sum_n(acc);
-                if (lane == 0) {
-#pragma unroll
-                    for (int r = 0; r < kRowsB; ++r)
-                        if (r < nu) part[(rr + u0 + r) * k + jj] = acc[r];
-                }
+                down_rows(rowp, act + (size_t)jj * I, I, lane, nu, part + (size_t)(rr + u0) * k + jj, k);
             }
             pos = (pos + ng) & (kConsumers - 1);
             off += len;
@@ -394,8 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(empty + s);
     }
-    ptx::named_sync(1, n_ct);
-    if (*flag) return;
+    if (ptx::named_sync_or(1, n_ct, *flag != 0)) return;
     for (int r = ct; r < nh; r += n_ct) {
         float o = 0.0f;
         for (int j = 0; j < k; ++j) o = fmaf(wsm[j], part[r * k + j], o);
