@@ -48,9 +48,9 @@ BATCH_MEM_CAP = 2 << 30         # and for the token batches
 
 # Kernel sources whose change voids a stored ncu traffic figure.
 KERNEL_SOURCES = {
-    "decode_fused": ["decode1.cu"],
-    "decode_gate_up": ["decode.cu", "decode1.cu"],
-    "decode_down": ["decode.cu", "decode1.cu"],
+    "decode_fused": ["decode_fused.cu"],
+    "decode_gate_up": ["decode.cu"],
+    "decode_down": ["decode.cu"],
     "gemm_gate_up": ["grouped_gemm.cu"],
     "gemm_down": ["grouped_gemm.cu"],
 }
@@ -171,8 +171,8 @@ def algorithmic_bytes(wl, T, U):
 def kernel_bytes(kernel, wl, T, U, k):
     """Algorithmic bytes of one launch of a kernel."""
     H, I = wl.H, wl.I
-    if kernel == "decode_fused":  # the whole single-token layer in one kernel
-        return U * 6 * H * I + T * H * 2 + T * wl.E * 4 + T * H * 4 + 2 * T * k * 2 * I * 4
+    if kernel == "decode_fused":  # the whole layer in one kernel; act written and read back once
+        return U * 6 * H * I + T * H * 2 + T * wl.E * 4 + T * H * 4 + 2 * T * k * I * 4
     if kernel == "decode_gate_up":
         return U * 2 * I * H * 2 + T * H * 2 + T * k * I * 4
     if kernel == "decode_down":

@@ -75,9 +75,10 @@ enum {
     MOE_PATH_AUTO = 0,    /* decode for T <= decode_max_tokens, else grouped */
     MOE_PATH_DECODE = 1,  /* warp per output scalar, weights streamed once   */
     MOE_PATH_GROUPED = 2, /* counting sort + tcgen05 grouped GEMMs + combine */
-    MOE_PATH_DECODE_T1 = 3 /* reported only (path_taken): the decode path for
-                              T == 1, two kernels that route the token
-                              themselves; same results as MOE_PATH_DECODE */
+    MOE_PATH_DECODE_FUSED = 3 /* reported only (path_taken): the decode path
+                                 for T <= 4 as one kernel that routes the
+                                 tokens itself; same results as
+                                 MOE_PATH_DECODE */
 };
 
 #define MOE_MAX_STAGES 8
@@ -104,7 +105,7 @@ typedef struct moe_ffn_opts {
     cudaEvent_t *stage_events;
     /* outputs */
     int32_t n_stages;          /* kernels the call enqueued */
-    int32_t path_taken;        /* MOE_PATH_DECODE, _DECODE_T1 or _GROUPED */
+    int32_t path_taken;        /* MOE_PATH_DECODE, _DECODE_FUSED or _GROUPED */
     int32_t reserved_out[2];
 } moe_ffn_opts;
 

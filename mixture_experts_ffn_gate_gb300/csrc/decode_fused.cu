@@ -1,0 +1,664 @@
+// decode_fused.cu -- the decode path for a few tokens (T <= 4), as one kernel.
+//
+// The warp-decode article ("Cursor warp decode 공개 ...", section 핵심 내용)
+// finishes a decode step in two kernels, one warp per output scalar, summing
+// the routed experts' contributions in FP32 with no padding, scatter or
+// per-expert buffers; its section 경쟁 구도 / 비교 keeps the intermediate
+// activation unquantised.  On GB300 a decode step of up to four tokens is one
+// cooperative launch, one CTA per SM, that moves the weights with bulk copies
+// (cp.async.bulk) into a shared-memory ring:
+//   - every CTA routes the tokens itself (the router kernel's warp top-k and
+//     softmax, same bits) and lists the touched experts in ascending order,
+//     each with its assignments a = t*k + j in ascending order, so every
+//     touched expert's weights are streamed once;
+//   - phase A: the CTA owns an equal, contiguous share of the U*I (expert u,
+//     index i) pairs; pair (u, i) is gate row i and up row I+i of expert u.
+//     For a run of pairs of one expert both row blocks are contiguous in
+//     memory: the producer warp copies them into one ring slot (two bulk
+//     copies), the consumer warps take the pairs round-robin, form both dot
+//     products with every token the expert serves (x in FP32) and write
+//     act = silu(gate) * up per assignment to global memory, in the two-plane
+//     order phase B keeps in shared memory;
+//   - the producer goes straight on to the CTA's W_down rows (dims
+//     [h_lo, h_hi) of each touched expert, expert after expert; they do not
+//     depend on phase A), so they stream in while the grid meets at a
+//     barrier.  A ring slot takes as many of these rows as fit, across
+//     expert boundaries (one bulk copy per expert run);
+//   - phase B: after the barrier the CTA copies every assignment's act row
+//     into shared memory, dots each of its W_down rows with the act rows of
+//     the expert's assignments and finally sums
+//     out[t, h] = sum_j w[t, j] * part[h][t*k + j] in slot order.
+// The kernel takes a call only if all T*k act rows fit in shared memory beside
+// a ring of at least kMinSlots slots; other small-T calls use decode.cu.
+// Each dot product uses decode.cu's lane split, chunk order, fmaf order and
+// shuffle butterfly, so this path returns the same bits as the general decode
+// path.  Every consumer warp visits every chunk and every expert boundary in
+// order, so a ring slot's parity waits are never more than one phase ahead
+// and the CTA-wide barriers match; every wait is bounded.
+//
+// Grid barrier (two hops, every spin bounded): after a CTA-wide barrier one
+// thread of CTA b stores the low 32 bits of the call's epoch into arrival
+// word b (release).  In CTA 0, thread t watches words 4t..4t+3 with 16-byte
+// relaxed loads until all hold the epoch, then issues an acq_rel fence; after
+// a CTA-wide barrier CTA 0 stores the epoch into the go word (release), which
+// one thread of every other CTA watches the same way.  The epoch is the
+// launch's odd 64-bit base (drawn at random per process, advanced per launch)
+// plus twice a call counter kept in the flags array: every CTA reads the
+// counter before it arrives and CTA 0 advances it after the barrier, so a
+// CUDA-graph replay, which repeats the base, still gets a fresh epoch.  Stale
+// words from earlier calls never equal a later epoch (within 2^31 calls), so
+// nothing needs zeroing.
+#include <atomic>
+#include <random>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "route_block.cuh"
+#include "sm100_ptx.cuh"
+
+namespace moe {
+
+__device__ uint32_t g_decode_fused_fault_word = 0;
+
+namespace {
+
+// Consumer warps per CTA.  With the producer warp that makes 16 warps, four
+// per SM sub-partition, so each thread can hold 128 registers (a 17th warp
+// would take a fifth slot on one sub-partition and cut that to 96).
+constexpr int kConsumers = 15;
+constexpr int kThreads = 32 * (1 + kConsumers);  // + the producer warp
+constexpr int kChunkTarget = 32 * 1024;          // gate/up bytes per ring slot (whole row pairs)
+constexpr int kSlotMin = 16 * 1024;
+constexpr int kMaxSlots = 16;
+constexpr int kSmemCap = 224 * 1024;  // dynamic; the per-block limit also covers the static tables
+constexpr int kMaxTokens = 4;
+constexpr int kMaxAsg = 64;           // T * k
+constexpr int kMinSlots = 5;          // ring slots the kernel needs beside the act rows
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 200000000ull;
+
+// flags (64-bit words): [0, kMaxGridCtas / 2) hold the kMaxGridCtas 32-bit
+// arrival words, then the call counter, then the go word on a 128-byte line
+// of its own
+constexpr int kCallWord = kMaxGridCtas;
+constexpr int kGoWord = kMaxGridCtas + 16;
+static_assert(kGoWord < kDecodeFusedFlagWords, "flags array too small");
+
+enum : uint32_t {
+    FAULT_PRODUCER = 16u,
+    FAULT_PHASE_A = 32u,
+    FAULT_BARRIER = 64u,
+    FAULT_PHASE_B = 128u,
+};
+
+// Shared-memory layout: ring | full[slots] | empty[slots] | flag | payload.
+// The payload holds x [T][H] FP32 (phase A) and, in the same space, the act
+// rows [T*k][I] FP32 of phase B; then part [nh][T*k].
+struct Layout {
+    uint32_t full, empty, flag, payload, total;
+};
+
+__host__ __device__ inline Layout layout(int slots, int slot_bytes, uint32_t payload_bytes)
+{
+    Layout L;
+    uint32_t o = (uint32_t)slots * slot_bytes;
+    L.full = o;
+    o += slots * 8;
+    L.empty = o;
+    o += slots * 8;
+    L.flag = o;
+    o += 16;
+    L.payload = o;
+    L.total = o + payload_bytes;
+    return L;
+}
+
+__host__ __device__ inline uint32_t xa_bytes(int T, int H, int I, int k)
+{
+    const uint32_t xb = (uint32_t)(4 * T * H), ab = (uint32_t)(4 * T * k * I);
+    return xb > ab ? xb : ab;
+}
+
+__device__ __forceinline__ void fail(volatile int *flag, uint32_t bit)
+{
+    if (!*flag) atomicOr(&g_decode_fused_fault_word, bit);
+    *flag = 1;
+}
+
+__device__ __forceinline__ uint4 lds16(const void *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// The producer waits (bounded) until the last `slots` chunks it issued have
+// landed, so no copy is in flight when the CTA exits.
+__device__ __forceinline__ void drain(uint64_t *full, int slots, int issued)
+{
+    const volatile int keep = 0;
+    for (int c = issued - 1; c >= 0 && c >= issued - slots; --c)
+        ptx::mbar_wait_bounded(full + (c % slots), (uint32_t)(c / slots) & 1, &keep, kDrainNs);
+}
+
+// First task of consumer warp cw in a run whose first task has round-robin
+// position `pos` (tasks go round-robin over the consumer warps).
+__device__ __forceinline__ int first_task(int pos, int cw) { return (cw - pos + kConsumers) % kConsumers; }
+
+// Position of element i of a row of n in the two-plane order: element 8u+e
+// sits in plane e/4 at 4u + e%4.
+__device__ __forceinline__ int plane_pos(int i, int n) { return ((i >> 2) & 1) * (n / 2) + (i >> 3) * 4 + (i & 3); }
+
+// Spin (bounded, 16-byte relaxed loads) until the first n (<= 4) of the four
+// words at p all hold v, then an acq_rel fence, which synchronises with the
+// release stores that wrote them.
+__device__ __forceinline__ bool wait_words4(const uint32_t *p, int n, uint32_t v, volatile int *flag,
+                                            uint64_t t_start)
+{
+    for (uint32_t spin = 0;; ++spin) {
+        const uint4 w = ptx::ld_relaxed_gpu_v4(p);
+        if (w.x == v && (n < 2 || w.y == v) && (n < 3 || w.z == v) && (n < 4 || w.w == v)) break;
+        if ((spin & 63) == 63 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) return false;
+    }
+    ptx::fence_acq_rel_gpu();
+    return true;
+}
+
+// Gate and up dot products of one row pair (BF16 in shared memory) with the
+// x rows of the expert's NB tokens (two-plane FP32 in shared memory); lane 0
+// writes act = silu(gate) * up of assignment asg[b] at column col of its
+// global act row.  Each dot product keeps decode.cu's lane split, fmaf
+// order and butterfly.
+template <int NB>
+__device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t *urow, const float *const *xr, int H,
+                                             int lane, const int *asg, float *act_g, int I, int col)
+{
+    float acc[2 * NB];
+#pragma unroll
+    for (int q = 0; q < 2 * NB; ++q) acc[q] = 0.0f;
+#pragma unroll 4
+    for (int h = lane * 8; h < H; h += 256) {
+        float gf[8], uf[8];
+        unpack8(lds16(grow + 2 * h), gf);
+        unpack8(lds16(urow + 2 * h), uf);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(xr[b] + h / 2);
+            const float4 x1 = *reinterpret_cast<const float4 *>(xr[b] + H / 2 + h / 2);
+            const float xf[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                acc[b] = fmaf(gf[q], xf[q], acc[b]);
+                acc[NB + b] = fmaf(uf[q], xf[q], acc[NB + b]);
+            }
+        }
+    }
+    warp_sum_n(acc);
+    if (lane == 0) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) act_g[(size_t)asg[b] * I + col] = swiglu(acc[b], acc[NB + b]);
+    }
+}
+
+// Phase B rows per warp task when a row serves NB assignments: NB * rows <= 4.
+__host__ __device__ constexpr int rows_for(int nb) { return nb >= 3 ? 1 : 4 / nb; }
+
+// Dot products of up to RB W_down rows (rowp, BF16 in shared memory; rows
+// past nu repeat a valid row and are dropped) with the act rows arow[b] of
+// the expert's NB assignments (two-plane FP32 in shared memory).  Lane 0
+// stores row r, assignment b to part[r * A + asg[b]].  Each dot product
+// keeps decode.cu's lane split, fmaf order and butterfly.
+template <int NB>
+__device__ __forceinline__ void down_rows(const uint8_t *const *rowp, const float *const *arow, int I, int lane,
+                                          int nu, const int *asg, float *part, int A)
+{
+    constexpr int RB = rows_for(NB);
+    float acc[RB * NB];
+#pragma unroll
+    for (int q = 0; q < RB * NB; ++q) acc[q] = 0.0f;
+#pragma unroll 2
+    for (int i = lane * 8; i < I; i += 256) {
+        float af[NB][8];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const float4 v0 = *reinterpret_cast<const float4 *>(arow[b] + i / 2);
+            const float4 v1 = *reinterpret_cast<const float4 *>(arow[b] + I / 2 + i / 2);
+            af[b][0] = v0.x; af[b][1] = v0.y; af[b][2] = v0.z; af[b][3] = v0.w;
+            af[b][4] = v1.x; af[b][5] = v1.y; af[b][6] = v1.z; af[b][7] = v1.w;
+        }
+        uint4 wv[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) wv[r] = lds16(rowp[r] + 2 * i);
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            float wf[8];
+            unpack8(wv[r], wf);
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[r * NB + b] = fmaf(wf[q], af[b][q], acc[r * NB + b]);
+        }
+    }
+    warp_sum_n(acc);
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                if (r < nu) part[r * A + asg[b]] = acc[r * NB + b];
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_fused_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
+                        const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int T, int H, int I, int E,
+                        int k, int slots, int slot_bytes, int rpc, int rps, int nh_max, float *__restrict__ act_g,
+                        unsigned long long *__restrict__ flags, unsigned long long epoch_base,
+                        int32_t *__restrict__ idx_out, float *__restrict__ w_out, float *__restrict__ out)
+{
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int A = T * k;
+    const uint32_t xa = xa_bytes(T, H, I, k);
+    const Layout L = layout(slots, slot_bytes, xa + (uint32_t)nh_max * A * 4);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(sm + L.empty);
+    volatile int *flag = reinterpret_cast<volatile int *>(sm + L.flag);
+    // x in FP32, two planes per token row: element 8u+e sits in plane e/4 at
+    // 4u + e%4, so a lane's 8 consecutive elements are two float4 loads that
+    // are contiguous across the warp (no bank conflicts, no unpacking)
+    float *xs = reinterpret_cast<float *>(sm + L.payload);
+    float *abuf = xs;  // phase B: act of all assignments [A][I]
+    float *part = reinterpret_cast<float *>(sm + L.payload + xa);          // [nh][A]
+    __shared__ int s_sel[kMaxAsg], s_asg[kMaxAsg], s_uexp[kMaxAsg], s_ubeg[kMaxAsg + 1], s_U;
+    __shared__ int8_t s_rlog[kMaxAsg];  // per touched expert: log2 of the phase B rows per task
+    __shared__ int s_xoff[kMaxAsg];     // per sorted assignment: its token's offset in xs
+    __shared__ float s_w[kMaxAsg];
+    __shared__ uint32_t s_key[kMaxAsg];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < slots; ++s) {
+            ptx::mbar_init(full + s, 1);
+            ptx::mbar_init(empty + s, kConsumers);
+        }
+        *flag = 0;
+        ptx::fence_barrier_init();
+    }
+    const unsigned long long calls = *reinterpret_cast<volatile unsigned long long *>(flags + kCallWord);
+    const unsigned long long epoch = epoch_base + 2 * calls;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // routing: consumer warp 1 + t routes token t (scratch: the ring)
+    if (warp >= 1 && warp <= T) {
+        const int t = warp - 1;
+        int e;
+        float wt;
+        route_token_warp(logits + (int64_t)t * E, E, k, reinterpret_cast<float *>(sm) + (size_t)t * E, e, wt);
+        if (lane < k) {
+            s_sel[t * k + lane] = e;
+            s_w[t * k + lane] = wt;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < A) {
+        const int a = threadIdx.x;
+        if (blockIdx.x == 0) {
+            if (idx_out) idx_out[a] = s_sel[a];
+            if (w_out) w_out[a] = s_w[a];
+        }
+        s_key[a] = ((uint32_t)s_sel[a] << 8) | (uint32_t)a;  // unique: (expert, assignment)
+        if (T == 1) {  // one token: its k experts are distinct, slot order will do
+            s_uexp[a] = s_sel[a];
+            s_ubeg[a] = a;
+            s_asg[a] = a;
+            if (a == 0) {
+                s_U = k;
+                s_ubeg[k] = k;
+            }
+        }
+    }
+    __syncthreads();
+    if (T > 1 && threadIdx.x < A) {  // rank sort of the keys
+        const uint32_t key = s_key[threadIdx.x];
+        int r = 0;
+        for (int b = 0; b < A; ++b) r += s_key[b] < key;
+        s_asg[r] = (int)key;
+    }
+    if (T > 1) __syncthreads();
+    if (T > 1 && warp == 0) {  // touched experts, ascending; then keep only the assignment in s_asg
+        int base = 0;
+        for (int r0 = 0; r0 < A; r0 += 32) {
+            const int r = r0 + lane;
+            const uint32_t key = r < A ? (uint32_t)s_asg[r] : 0u;
+            const bool nw = r < A && (r == 0 || (key >> 8) != ((uint32_t)s_asg[r - 1] >> 8));
+            const uint32_t m = __ballot_sync(0xffffffffu, nw);
+            if (nw) {
+                const int u = base + __popc(m & ((1u << lane) - 1u));
+                s_uexp[u] = (int)(key >> 8);
+                s_ubeg[u] = r;
+            }
+            base += __popc(m);
+        }
+        __syncwarp();
+        for (int r = lane; r < A; r += 32) s_asg[r] = s_asg[r] & 0xff;
+        if (lane == 0) {
+            s_U = base;
+            s_ubeg[base] = A;
+        }
+    }
+    if (T > 1) __syncthreads();
+    const int U = s_U;
+    if (threadIdx.x < U) {
+        const int na = s_ubeg[threadIdx.x + 1] - s_ubeg[threadIdx.x];
+        s_rlog[threadIdx.x] = (int8_t)(rows_for(na) == 4 ? 2 : rows_for(na) == 2 ? 1 : 0);
+    }
+    if (threadIdx.x < A) s_xoff[threadIdx.x] = s_asg[threadIdx.x] / k * H;
+    __syncthreads();
+
+    // Phase A: pairs [lo, hi) of the U*I, pair p = (expert p / I, index p % I),
+    // in chunks of at most rpc pairs that never cross an expert.  Phase B:
+    // output dims [h_lo, h_hi) of all U experts, the row sequence
+    // s -> (expert s / nh, dim h_lo + s % nh), in chunks of rps rows that may
+    // cross experts.  Producer and consumers walk both sequences with running
+    // (expert, index) state.
+    const int pairs = U * I;
+    const int lo = (int)((int64_t)pairs * blockIdx.x / gridDim.x);
+    const int hi = (int)((int64_t)pairs * (blockIdx.x + 1) / gridDim.x);
+    const int h_lo = (int)((int64_t)H * blockIdx.x / gridDim.x);
+    const int h_hi = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+    const int nh = h_hi - h_lo;
+    const int nrow = U * nh;
+    const int nb = (nrow + rps - 1) / rps;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int c = 0;
+            bool ok = true;
+            int u = lo / I, i0 = lo - u * I;
+            for (int p = lo; p < hi && ok; ++c) {
+                const int n = min(rpc, min(I - i0, hi - p));
+                const int s = c % slots;
+                if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
+                    fail(flag, FAULT_PRODUCER);
+                    ok = false;
+                    break;
+                }
+                const uint32_t bytes = (uint32_t)n * 2 * H;  // one block: gate or up rows
+                const uint16_t *gate = wgu + ((int64_t)s_uexp[u] * 2 * I + i0) * H;
+                ptx::mbar_arrive_expect_tx(full + s, 2 * bytes);
+                ptx::bulk_load(sm + (size_t)s * slot_bytes, gate, bytes, full + s);
+                ptx::bulk_load(sm + (size_t)s * slot_bytes + bytes, gate + (int64_t)I * H, bytes, full + s);
+                p += n;
+                i0 += n;
+                if (i0 == I) {
+                    i0 = 0;
+                    ++u;
+                }
+            }
+            int uu = 0, rr = 0;
+            for (int q = 0; q < nb && ok; ++q, ++c) {
+                const int len_q = min(rps, nrow - q * rps);
+                const int s = c % slots;
+                if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
+                    fail(flag, FAULT_PRODUCER);
+                    ok = false;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(full + s, (uint32_t)len_q * 2 * I);
+                for (int off = 0; off < len_q;) {  // one copy per expert run
+                    const int len = min(len_q - off, nh - rr);
+                    ptx::bulk_load(sm + (size_t)s * slot_bytes + (size_t)off * 2 * I,
+                                   wd + ((int64_t)s_uexp[uu] * H + h_lo + rr) * I, (uint32_t)len * 2 * I, full + s);
+                    off += len;
+                    rr += len;
+                    if (rr == nh) {
+                        rr = 0;
+                        ++uu;
+                    }
+                }
+            }
+            drain(full, slots, c);
+        }
+        return;
+    }
+
+    const int ct = threadIdx.x - 32, n_ct = kConsumers * 32;
+    const int cw = warp - 1;
+    for (int v = ct; v < T * H / 8; v += n_ct) {  // x of all tokens, two planes per row
+        const int t = v / (H / 8), uh = v - t * (H / 8);
+        float f[8];
+        unpack8(ld_nc16(x + (size_t)v * 8), f);
+        float *row = xs + (size_t)t * H;
+        *reinterpret_cast<float4 *>(row + 4 * uh) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4 *>(row + H / 2 + 4 * uh) = make_float4(f[4], f[5], f[6], f[7]);
+    }
+    ptx::named_sync(1, n_ct);
+
+    // phase A: for each pair, gate and up dot products with every token of
+    // the expert; act per assignment to global memory
+    int c = 0;
+    {
+        int u = lo / I, i0 = lo - u * I, pos = 0;
+        for (int p = lo; p < hi; ++c) {
+            const int n = min(rpc, min(I - i0, hi - p));
+            const int s = c % slots;
+            if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
+                fail(flag, FAULT_PHASE_A);
+                break;
+            }
+            const uint8_t *chunk = sm + (size_t)s * slot_bytes;
+            int m = first_task(pos, cw);
+            if (m < n) {  // every warp walks every chunk: set up only with work
+                const int a0 = s_ubeg[u], na = s_ubeg[u + 1] - a0;  // 1 <= na <= T <= NT
+                const float *xr[NT];
+#pragma unroll
+                for (int b = 0; b < NT; ++b) xr[b] = xs + s_xoff[a0 + (b < na ? b : 0)];
+                for (; m < n; m += kConsumers) {
+                    const uint8_t *grow = chunk + (size_t)m * 2 * H;
+                    const uint8_t *urow = grow + (size_t)n * 2 * H;
+                    const int col = plane_pos(i0 + m, I);
+                    if (na == 1) gate_up_pair<1>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                    if constexpr (NT >= 2) {
+                        if (na == 2) gate_up_pair<2>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                    }
+                    if constexpr (NT >= 4) {
+                        if (na == 3) gate_up_pair<3>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                        if (na == 4) gate_up_pair<4>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(empty + s);
+            p += n;
+            pos = (pos + n) % kConsumers;
+            i0 += n;
+            if (i0 == I) {
+                i0 = 0;
+                ++u;
+            }
+        }
+    }
+
+    // grid barrier: every CTA's act values written and visible
+    ptx::named_sync(1, n_ct);
+    {
+        uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
+        uint32_t *go = reinterpret_cast<uint32_t *>(flags + kGoWord);
+        const uint32_t e32 = (uint32_t)epoch;
+        const uint64_t t_start = ptx::globaltimer_ns();
+        if (ct == 0 && !*flag) ptx::st_release_gpu(arrive + blockIdx.x, e32);
+        if (blockIdx.x == 0) {
+            for (int v = ct; 4 * v < (int)gridDim.x && !*flag; v += n_ct)
+                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start))
+                    fail(flag, FAULT_BARRIER);
+            ptx::named_sync(1, n_ct);
+            if (ct == 0 && !*flag) ptx::st_release_gpu(go, e32);
+        } else if (ct == 0 && !*flag) {
+            if (!wait_words4(go, 1, e32, flag, t_start)) fail(flag, FAULT_BARRIER);
+        }
+    }
+    // every consumer leaves, or none: a producer fault can set the flag at any time
+    const bool stop = ptx::named_sync_or(1, n_ct, *flag != 0);
+    if (blockIdx.x == 0 && ct == 0) flags[kCallWord] = calls + 1;
+    if (stop) return;
+
+    // phase B: W_down rows, chunk by chunk.  Within a run of one expert's
+    // rows, groups of up to rows_for(na) consecutive rows share the act
+    // loads; the groups go round-robin over the consumer warps, counted across
+    // runs and chunks.  First every assignment's act row into shared memory.
+    {
+        const int n4 = A * I / 4;
+        for (int v0 = ct; v0 < n4; v0 += 4 * n_ct) {
+            float4 a4[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (v0 + b * n_ct < n4) a4[b] = __ldcg(reinterpret_cast<const float4 *>(act_g) + v0 + b * n_ct);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (v0 + b * n_ct < n4) reinterpret_cast<float4 *>(abuf)[v0 + b * n_ct] = a4[b];
+        }
+        ptx::named_sync(1, n_ct);
+        bool ok = true;
+        int uu = 0, rr = 0, pos = 0;
+        for (int q = 0; q < nb; ++q, ++c) {
+            const int len_q = min(rps, nrow - q * rps);
+            const int s = c % slots;
+            if (ok && !ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
+                fail(flag, FAULT_PHASE_B);
+                ok = false;
+            }
+            const uint8_t *chunk = sm + (size_t)s * slot_bytes;
+            for (int off = 0; off < len_q;) {
+                // rows [rr, rr + len) of expert uu; every warp walks every run,
+                // so keep this bookkeeping cheap and do the rest only with work
+                const int len = min(len_q - off, nh - rr);
+                const int lg = s_rlog[uu];  // log2 of the rows per task
+                const int ng = (len + (1 << lg) - 1) >> lg;
+                int g = first_task(pos, cw);
+                if (ok && g < ng) {
+                    const int a0 = s_ubeg[uu], na = s_ubeg[uu + 1] - a0;
+                    const float *arow[NT];
+#pragma unroll
+                    for (int b = 0; b < NT; ++b) arow[b] = abuf + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
+                    float *pr = part + (size_t)rr * A;
+                    for (; g < ng; g += kConsumers) {
+                        const int u0 = g << lg, nu = min(1 << lg, len - u0);
+                        const uint8_t *rowp[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
+                        if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                        if constexpr (NT >= 2) {
+                            if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                        }
+                        if constexpr (NT >= 4) {
+                            if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                            if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                        }
+                    }
+                }
+                pos = (pos + ng) % kConsumers;
+                off += len;
+                rr += len;
+                if (rr == nh) {
+                    rr = 0;
+                    ++uu;
+                }
+            }
+            __syncwarp();
+            if (ok && lane == 0) ptx::mbar_arrive(empty + s);
+        }
+    }
+    if (ptx::named_sync_or(1, n_ct, *flag != 0)) return;
+    for (int v = ct; v < T * nh; v += n_ct) {
+        const int t = v / nh, r = v - t * nh;
+        float o = 0.0f;
+        for (int j = 0; j < k; ++j) o = fmaf(s_w[t * k + j], part[r * A + t * k + j], o);
+        out[(size_t)t * H + h_lo + r] = o;
+    }
+}
+
+// Geometry: phase A copies rpc whole gate/up row pairs (about kChunkTarget
+// bytes); a slot holds the larger of that, kSlotMin and one W_down row, and
+// phase B fills each slot with rps = slot / 2I rows.  As many slots as fit in
+// shared memory beside the payload.
+struct Plan {
+    int nt, rpc, rps, slot_bytes, slots, nh_max;
+    uint32_t payload;
+};
+
+Plan plan_for(int T, int H, int I, int k, int n_sm)
+{
+    Plan p;
+    p.nt = T <= 1 ? 1 : T <= 2 ? 2 : 4;
+    p.nh_max = (H + n_sm - 1) / n_sm;
+    p.rpc = kChunkTarget / (4 * H) > 0 ? kChunkTarget / (4 * H) : 1;
+    const int a = p.rpc * 4 * H;
+    int slot = a > kSlotMin ? a : kSlotMin;
+    if (2 * I > slot) slot = 2 * I;
+    p.rps = slot / (2 * I);
+    p.slot_bytes = slot;
+    p.payload = xa_bytes(T, H, I, k) + (uint32_t)(p.nh_max * T * k * 4);
+    const int fixed = (int)layout(0, p.slot_bytes, p.payload).total + 2 * kMaxSlots * 8;
+    const int n = (kSmemCap - fixed) / p.slot_bytes;
+    p.slots = n > kMaxSlots ? kMaxSlots : n;
+    return p;
+}
+
+std::atomic<unsigned long long> g_epoch{0};
+
+// A value unique to this launch: a 64-bit counter whose start is drawn at
+// random once per process, so flags left in a workspace by earlier calls (or
+// by another process) do not match it.
+unsigned long long next_epoch()
+{
+    static const unsigned long long base = [] {
+        std::random_device rd;
+        return ((unsigned long long)rd() << 32) ^ rd() ^ 0x9e3779b97f4a7c15ull;
+    }();
+    return base + 2 * g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+}
+
+}  // namespace
+
+bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm)
+{
+    if (T < 1 || T > kMaxTokens || T * k > kMaxAsg || n_sm > kMaxGridCtas) return false;
+    const Plan p = plan_for(T, H, I, k, n_sm);
+    return p.slots >= kMinSlots && (int64_t)T * E * 4 <= (int64_t)p.slots * p.slot_bytes;  // routing scratch
+}
+
+cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
+                                int I, int E, int k, int n_sm, float *act, unsigned long long *flags,
+                                int32_t *idx_out, float *w_out, float *out, cudaStream_t s)
+{
+    const Plan p = plan_for(T, H, I, k, n_sm);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_sm);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = layout(p.slots, p.slot_bytes, p.payload).total;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto kern = p.nt == 1 ? decode_fused_kernel<1> : p.nt == 2 ? decode_fused_kernel<2> : decode_fused_kernel<4>;
+    return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
+                              H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, act, flags, next_epoch(),
+                              idx_out, w_out, out);
+}
+
+cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(flags, g_decode_fused_fault_word, sizeof(uint32_t));
+    if (e != cudaSuccess || !clear) return e;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_decode_fused_fault_word, &zero, sizeof(uint32_t));
+}
+
+cudaError_t decode_fused_init_device()
+{
+    for (const void *kern : {(const void *)decode_fused_kernel<1>, (const void *)decode_fused_kernel<2>,
+                             (const void *)decode_fused_kernel<4>}) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

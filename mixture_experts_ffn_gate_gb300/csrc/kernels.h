@@ -32,17 +32,18 @@ cudaError_t launch_decode_down(const float *act, const void *wd, const float *w,
                                const int32_t *ucount, const int32_t *offs, const int32_t *perm, int T, int H,
                                int I, int k, int warps, float *out, cudaStream_t s);
 
-// decode1.cu: the single-token layer in one cooperative kernel with a grid
-// barrier.  act: [k][I] FP32 scratch; flags: kDecode1FlagWords 64-bit words of
-// workspace (any contents; the kernel keeps its barrier state there).
+// decode_fused.cu: a decode step of up to four tokens in one cooperative
+// kernel with a grid barrier.  act: [T*k][I] FP32 scratch; flags:
+// kDecodeFusedFlagWords 64-bit words of workspace (any contents; the kernel
+// keeps its barrier state there).
 constexpr int kMaxGridCtas = 1024;
-constexpr int kDecode1FlagWords = kMaxGridCtas + 32;
-cudaError_t decode1_init_device();
-cudaError_t read_decode1_fault_word(uint32_t *flags, bool clear);
-bool decode1_supported(int H, int I, int E, int k, int n_sm);
-cudaError_t launch_decode1(const void *x, const float *logits, const void *wgu, const void *wd, int H, int I, int E,
-                           int k, int n_sm, float *act, unsigned long long *flags, int32_t *idx_out, float *w_out,
-                           float *out, cudaStream_t s);
+constexpr int kDecodeFusedFlagWords = kMaxGridCtas + 32;
+cudaError_t decode_fused_init_device();
+cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear);
+bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm);
+cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
+                                int I, int E, int k, int n_sm, float *act, unsigned long long *flags,
+                                int32_t *idx_out, float *w_out, float *out, cudaStream_t s);
 
 // grouped_gemm.cu
 cudaError_t gemm_init_device();

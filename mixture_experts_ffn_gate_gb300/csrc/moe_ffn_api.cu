@@ -52,10 +52,10 @@ Layout make_layout(const Shape &s)
     L.ucount = take(4);
     L.chunks = take((size_t)(s.E + ceil_div((int64_t)n, moe::kGemmChunkMax) + 1) * 16);
     L.nchunks = take(4);
-    L.flags = take((size_t)moe::kDecode1FlagWords * 8);  // single-token kernel: grid-barrier state
+    L.flags = take((size_t)moe::kDecodeFusedFlagWords * 8);  // fused decode kernel: grid-barrier state
     L.common_end = o;
-    // decode path: act f32 [T*k, I]; the single-token kernels keep the gate
-    // and up dot products there instead, [k, 2I]
+    // decode path: act f32 [T*k, I] (the general decode kernels and the
+    // fused decode kernel)
     L.act = take(n * (size_t)s.I * 8);
     L.decode_total = o;
     // grouped path
@@ -123,7 +123,7 @@ int device_setup(DeviceInfo **info)
         if (cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::routing_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::decode_init_device() != cudaSuccess) return MOE_ERR_CUDA;
-        if (moe::decode1_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::decode_fused_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::gemm_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         d.ready = true;
     }
@@ -132,7 +132,7 @@ int device_setup(DeviceInfo **info)
 }
 
 const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
-const char *kDecodeT1Stages[] = {"decode_fused"};
+const char *kDecodeFusedStages[] = {"decode_fused"};
 const char *kGroupedStages[] = {"router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine"};
 
 // Records stage events around the launches of one call.  While the stream is
@@ -199,13 +199,14 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (path == MOE_PATH_DECODE && T == 1 && moe::decode1_supported(H, I, E, k, dev->n_sm)) {
-        // one token: a single cooperative kernel that routes it, streams both
-        // projections' rows and meets at a grid barrier in between
-        path = MOE_PATH_DECODE_T1;
-        MOE_TRY(stg.done(moe::launch_decode1(x, logits, wgu, wd, H, I, E, k, dev->n_sm,
-                                                   (float *)(ws + L.act), (unsigned long long *)(ws + L.flags),
-                                                   idx_out, w_out, out, stream)));
+    if (path == MOE_PATH_DECODE && moe::decode_fused_supported(T, H, I, E, k, dev->n_sm)) {
+        // a few tokens: one cooperative kernel that routes them, streams both
+        // projections' rows of the touched experts and meets at a grid
+        // barrier in between
+        path = MOE_PATH_DECODE_FUSED;
+        MOE_TRY(stg.done(moe::launch_decode_fused(x, logits, wgu, wd, T, H, I, E, k, dev->n_sm,
+                                                  (float *)(ws + L.act), (unsigned long long *)(ws + L.flags),
+                                                  idx_out, w_out, out, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
@@ -357,8 +358,8 @@ const char *moe_ffn_stage_name(int path, int stage)
     if (stage < 0) return nullptr;
     if (path == MOE_PATH_DECODE && stage < (int)(sizeof kDecodeStages / sizeof *kDecodeStages))
         return kDecodeStages[stage];
-    if (path == MOE_PATH_DECODE_T1 && stage < (int)(sizeof kDecodeT1Stages / sizeof *kDecodeT1Stages))
-        return kDecodeT1Stages[stage];
+    if (path == MOE_PATH_DECODE_FUSED && stage < (int)(sizeof kDecodeFusedStages / sizeof *kDecodeFusedStages))
+        return kDecodeFusedStages[stage];
     if (path == MOE_PATH_GROUPED && stage < (int)(sizeof kGroupedStages / sizeof *kGroupedStages))
         return kGroupedStages[stage];
     return nullptr;
@@ -369,8 +370,8 @@ int moe_ffn_device_faults(uint32_t *flags, int clear)
     if (!flags) return MOE_ERR_INVALID_ARG;
     uint32_t gemm = 0, decode = 0;
     if (moe::read_fault_word(&gemm, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
-    if (moe::read_decode1_fault_word(&decode, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
-    *flags = gemm | (decode << 8);  // bits 0-7: grouped GEMMs, 8-15: single-token decode
+    if (moe::read_decode_fused_fault_word(&decode, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
+    *flags = gemm | (decode << 8);  // bits 0-7: grouped GEMMs, 8-15: fused decode
     return MOE_OK;
 }
 

@@ -1,7 +1,6 @@
 // route_block.cuh -- top-k selection and softmax weights for one token,
-// computed by one warp.  Used by the router kernel and by the single-token
-// decode kernels, which route their token themselves; both give the same
-// bits.
+// computed by one warp.  Used by the router kernel and by the fused decode
+// kernel, which routes its tokens itself; both give the same bits.
 #pragma once
 
 #include "common.cuh"

@@ -26,7 +26,7 @@ MOE_ERR_TIMEOUT = 6
 MOE_PATH_AUTO = 0
 MOE_PATH_DECODE = 1
 MOE_PATH_GROUPED = 2
-MOE_PATH_DECODE_T1 = 3  # reported only: the decode path for one token (two kernels)
+MOE_PATH_DECODE_FUSED = 3  # reported only: the decode path for T <= 4 as one kernel
 MOE_MAX_STAGES = 8
 
 EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",

@@ -50,7 +50,7 @@ def run_gpu(x, logits, wgu, wd, k, path="decode", **opt_fields):
     out = m.moe_ffn_forward_ex(x, logits, wgu, wd, k, topk_idx=idx, topk_w=w, opts=o)
     torch.cuda.synchronize()
     if T:
-        want = {m.MOE_PATH_DECODE: (m.MOE_PATH_DECODE, m.MOE_PATH_DECODE_T1),
+        want = {m.MOE_PATH_DECODE: (m.MOE_PATH_DECODE, m.MOE_PATH_DECODE_FUSED),
                 m.MOE_PATH_GROUPED: (m.MOE_PATH_GROUPED,)}.get(o.path)
         assert want is None or o.path_taken in want, (o.path, o.path_taken)
     return out.cpu(), idx.cpu(), w.cpu()

@@ -64,7 +64,7 @@ def test_stage_names(L):
     from mixture_experts_ffn_gate_gb300 import moe_ffn as m
     assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE, i) for i in range(5)] == \
         ["router", "sort", "decode_gate_up", "decode_down", None]
-    assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE_T1, i) for i in range(2)] == ["decode_fused", None]
+    assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE_FUSED, i) for i in range(2)] == ["decode_fused", None]
     assert m.moe_ffn_stage_name(m.MOE_PATH_GROUPED, 3) == "gemm_gate_up"
     assert m.moe_ffn_stage_name(m.MOE_PATH_AUTO, 0) is None
     assert m.moe_ffn_stage_name(m.MOE_PATH_DECODE, -1) is None

@@ -170,8 +170,9 @@ def test_plain_forward_and_host_entry_match_ex():
     assert torch.equal(plain, ref) and torch.equal(oh, ref.cpu())
 
 
-def test_stage_events_time_each_kernel():
-    T, H, I, E, k = 4, 256, 128, 8, 2
+@pytest.mark.parametrize("T,path,stages", [(3, "decode", 1), (8, "decode", 4), (8, "grouped", 6)])
+def test_stage_events_time_each_kernel(T, path, stages):
+    H, I, E, k = 256, 128, 8, 2
     wl = gu.custom(T, H, I, E, k, name="events")
     x, L, wgu, wd = gu.make_layer(wl, T)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
@@ -179,10 +180,11 @@ def test_stage_events_time_each_kernel():
         e.record()
     arr = m.stage_event_array(evs)
     o = m.moe_ffn_opts()
+    o.path = gu.PATHS[path]
     o.stage_events = m.ctypes.cast(arr, m.ctypes.c_void_p)
     m.moe_ffn_forward_ex(x, L, wgu, wd, k, opts=o)
     torch.cuda.synchronize()
-    assert o.n_stages == 4
+    assert o.n_stages == stages
     for i in range(o.n_stages):
         assert evs[i].elapsed_time(evs[i + 1]) >= 0.0
 
@@ -201,10 +203,10 @@ def test_errors_from_device_pointers():
     assert ei.value.status == m.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
-@pytest.mark.parametrize("T,path", [(1, "decode"), (4, "decode"), (64, "grouped")])
+@pytest.mark.parametrize("T,path", [(1, "decode"), (3, "decode"), (8, "decode"), (64, "grouped")])
 def test_cuda_graph_replay_matches_eager(T, path):
     """A call captured into a CUDA graph recomputes, on every replay, what an
-    eager call gives for the buffers' current contents (the single-token
+    eager call gives for the buffers' current contents (the fused decode
     kernel's grid barrier must not reuse a stale epoch on replays)."""
     H, I, E, k = 512, 256, 32, 8
     wl = gu.custom(T, H, I, E, k, 1.0, name="graph")
@@ -229,8 +231,8 @@ def test_cuda_graph_replay_matches_eager(T, path):
         oc.stage_events = m.ctypes.cast(arr, m.ctypes.c_void_p)
         m.moe_ffn_forward_ex(xb, lb, wgu, wd, k, out=out, workspace=ws, opts=oc,
                              stream=torch.cuda.current_stream())
-    if T == 1:
-        assert oc.path_taken == m.MOE_PATH_DECODE_T1
+    if path == "decode":
+        assert oc.path_taken == (m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_DECODE)
     for r in range(12):
         c = r % 3
         xb.copy_(inputs[c][0])
