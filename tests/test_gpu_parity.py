@@ -243,3 +243,33 @@ def test_cuda_graph_replay_matches_eager(T, path):
         assert torch.equal(out.cpu(), refs[c]), (r, c)
     for i in range(oc.n_stages):
         assert evs[i].elapsed_time(evs[i + 1]) >= 0.0
+
+
+# Fused decode kernel (T <= 4): tokens that share experts.  Each touched
+# expert is streamed once and dotted with every token it serves; the result
+# must match the oracle and, bit for bit, the general decode kernels (T > 4
+# forced through the decode path uses them) on the same tokens.
+@pytest.mark.parametrize("T,share", [(2, "all"), (3, "some"), (4, "all"), (4, "some"), (4, "none")])
+def test_fused_decode_shared_experts(T, share):
+    H, I, E, k = 512, 256, 32, 8
+    wl = gu.custom(T, H, I, E, k, 0.0, name="fused_share")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    L = L.clone()
+    if share == "all":        # every token picks the same k experts, in the same order
+        L[:] = L[0]
+    elif share == "some":     # tokens 1.. reuse token 0's two best experts
+        L[1:, :] -= 10.0
+        top2 = torch.topk(L[0], 2).indices
+        L[1:, top2] = L[0, top2] + 20.0
+    else:                     # disjoint expert sets
+        L[:] = -10.0
+        for t in range(T):
+            L[t, t * k:(t + 1) * k] = torch.arange(k, 0, -1, dtype=torch.float32, device=L.device)
+    out, idx, w = gu.run_gpu(x, L, wgu, wd, k, "decode")
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what=f"T={T} {share}")
+    # the same tokens inside a batch of 8 go through the general decode kernels
+    x8 = torch.cat([x, x[:1].expand(8 - T, H)]).contiguous()
+    L8 = torch.cat([L, L[:1].expand(8 - T, E)]).contiguous()
+    out8, idx8, _ = gu.run_gpu(x8, L8, wgu, wd, k, "decode")
+    assert torch.equal(idx8[:T], idx)
+    assert torch.equal(out8[:T], out)
