@@ -273,3 +273,21 @@ def test_fused_decode_shared_experts(T, share):
     out8, idx8, _ = gu.run_gpu(x8, L8, wgu, wd, k, "decode")
     assert torch.equal(idx8[:T], idx)
     assert torch.equal(out8[:T], out)
+
+
+# Fused decode kernel at the edges of its shape range: H = 64 (most CTAs own
+# no output dimension), I = 64, E = 1024 experts, k = 32, and T * k = 64
+# assignments (its maximum).  Compared with the oracle and, bit for bit,
+# with the same tokens through the general decode kernels.
+@pytest.mark.parametrize("T,H,I,E,k", [(1, 64, 64, 1024, 32), (1, 128, 64, 40, 1), (4, 64, 128, 64, 16),
+                                       (2, 192, 320, 7, 7), (3, 1024, 64, 256, 8)])
+def test_fused_decode_edges(T, H, I, E, k):
+    wl = gu.custom(T, H, I, E, k, 1.0, name="fused_edge")
+    x, L, wgu, wd = gu.make_layer(wl, T)
+    out, idx, w = gu.run_gpu(x, L, wgu, wd, k, "decode")
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what=str((T, H, I, E, k)))
+    x8 = torch.cat([x, x[:1].expand(8 - T, H)]).contiguous()
+    L8 = torch.cat([L, L[:1].expand(8 - T, E)]).contiguous()
+    out8, idx8, _ = gu.run_gpu(x8, L8, wgu, wd, k, "decode")
+    assert torch.equal(idx8[:T], idx)
+    assert torch.equal(out8[:T], out)
