@@ -9,8 +9,10 @@
 // of at most kGemmChunkMax rows.
 //
 // Both GEMMs put the expert's weight rows on the MMA's M side (M = 128) and
-// the chunk's tokens on the N side (N = chunk rounded up to 16, <= 128), so
-// a skewed or tiny expert load never pads the weight tile:
+// the chunk's tokens on the N side (N = chunk rounded up to 16, <= 64), so
+// a skewed or tiny expert load never pads the weight tile.  A work item is
+// one chunk against MT weight tiles of one expert (gate_up 4, down 3), which
+// share the chunk's token tile:
 //   gate_up: D[128 x N] = W_gu[e][rows] . xs[chunk]^T, K = H.  The 128 rows of
 //            a tile are 4 groups of (16 gate rows i.., 16 up rows I+i..), so
 //            each epilogue warp holds gate and up of the same 16 neurons in
@@ -67,12 +69,19 @@ static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulato
 
 template <bool GATE_UP>
 struct Cfg {
-    static constexpr int MT = GATE_UP ? 4 : 2;  // weight tiles per item (they share one token tile)
+    static constexpr int MT = GATE_UP ? 4 : 3;  // weight tiles per item (they share one token tile)
     static constexpr int TMEM_COLS = 2 * MT * ACC_COLS;  // double-buffered, one accumulator per tile
-    static constexpr int STAGES = GATE_UP ? 3 : 4;
+    // tcgen05.alloc takes a power of two of at least 32 columns
+    static constexpr int TMEM_ALLOC = TMEM_COLS <= 32    ? 32
+                                      : TMEM_COLS <= 64  ? 64
+                                      : TMEM_COLS <= 128 ? 128
+                                      : TMEM_COLS <= 256 ? 256
+                                                         : 512;
+    static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
+    static constexpr int STAGES = 3;
     static constexpr int A_TILE = BM * BK * 2;                            // 16 KB per weight tile
     static constexpr int A_BYTES = MT * A_TILE;
-    static constexpr int B_TILE = NMAX * BK * 2;                          // 16 KB per operand
+    static constexpr int B_TILE = NMAX * BK * 2;                          // 8 KB per operand
     static constexpr int B_BYTES = B_TILE * (GATE_UP ? 1 : 2);            // x | act_hi + act_lo
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int BAR_BYTES = 256;
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tmA: gate_up -- 5-D view of W_gu [E][2][I/16][16][H] (dims innermost
     //      first: H, 16 rows, gate|up, row group, expert) whose {64,16,2,4,1}
     //      box is one 128-row tile of 4 x (16 gate rows, 16 up rows);
-    //      down -- 2-D [E*H, I], box 64 x 128.
+    //      down -- 3-D [E][H][I], box 64 x 128 x 1 (one tile).
     // tmB0/tmB1: the chunk's token rows (x, or act_hi/act_lo), box 64 x NMAX;
     // tmB0s/tmB1s: the same with a 16-row box, for chunks of <= 16 rows.
     using C = Cfg<GATE_UP>;
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (warp == 1) {
-        ptx::tmem_alloc(tmem_slot, C::TMEM_COLS);
+        ptx::tmem_alloc(tmem_slot, C::TMEM_ALLOC);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -194,12 +203,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++armed[stage];
                     const int k0 = kb * BK;
                     uint8_t *a = sA + stage * C::A_BYTES;
-                    // MT tiles in one box; tiles past the expert's end read 0
-                    // (gate_up) or the next expert's rows (down), never stored
-                    if (GATE_UP)
+                    // MT tiles: one box (gate_up) or one box per tile (down);
+                    // rows past the expert's end read 0 and are never stored
+                    if (GATE_UP) {
                         ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4 * MT, it.e, full + stage);
-                    else
-                        ptx::tma_load_2d(a, &tmA, k0, it.e * args.H + it.m * BM * MT, full + stage);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < MT; ++t)
+                            ptx::tma_load_3d(a + t * C::A_TILE, &tmA, k0, (it.m * MT + t) * BM, it.e, full + stage);
+                    }
                     uint8_t *b = sB + stage * C::B_BYTES;
                     ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
                     if (!GATE_UP) ptx::tma_load_2d(b + C::B_TILE, small ? &tmB1s : &tmB1, k0, it.p0, full + stage);
@@ -327,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_ALLOC);
 }
 
 // ---------------------------------------------------------------- host
@@ -360,6 +372,22 @@ cudaError_t make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
     const cuuint32_t box[2] = {BK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// W_down [E, H, I] as a 3-D map (I, H, E), box 64 x 128 rows x 1 expert: one
+// weight tile; rows past H read 0.
+cudaError_t make_down_map(CUtensorMap *map, const void *base, int E, int H, int I)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
+    const cuuint64_t strides[2] = {(cuuint64_t)I * 2, (cuuint64_t)I * 2 * H};
+    const cuuint32_t box[3] = {BK, BM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -434,15 +462,14 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
 {
     CUtensorMap tA, tB0s, tB0, tB1s, tB1;
     constexpr int MT = Cfg<false>::MT;
-    const uint32_t a_rows = (uint32_t)((int64_t)BM * MT < (int64_t)E * H ? BM * MT : E * H);
-    cudaError_t e = make_map(&tA, wd, (uint64_t)E * H, I, a_rows);
+    cudaError_t e = make_down_map(&tA, wd, E, H, I);
     if (e == cudaSuccess) e = make_map(&tB0s, act_hi, n_assign, I, SMALL_ROWS);
     if (e == cudaSuccess) e = make_map(&tB0, act_hi, n_assign, I, NMAX);
     if (e == cudaSuccess) e = make_map(&tB1s, act_lo, n_assign, I, SMALL_ROWS);
     if (e == cudaSuccess) e = make_map(&tB1, act_lo, n_assign, I, NMAX);
     if (e != cudaSuccess) return e;
     const int tiles = (H + BM - 1) / BM;
-    GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, (int)a_rows * BK * 2, z, nullptr};
+    GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, MT * BM * BK * 2, z, nullptr};
     grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(
         tA, tB0s, tB0, tB1s, tB1, a);
     return cudaPeekAtLastError();
