@@ -150,7 +150,12 @@ int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32,
  * the forward pass and the device->host copy of the output on `stream`;
  * out_host is valid after the stream is synchronised.  The workspace
  * (device, at least moe_ffn_host_workspace_bytes) also holds the staged
- * inputs and output.
+ * inputs and output.  When the three host buffers are page-locked and mapped
+ * (cudaHostAlloc, cudaMallocHost, torch's pin_memory), 16-byte aligned and
+ * at most 1 MiB together, the kernels read the inputs and write the output
+ * in place through the host link instead (no separate copies; same
+ * results); the caller must not touch them until the stream reaches the
+ * end of the call.
  */
 size_t moe_ffn_host_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E,
                                     int64_t k);

@@ -305,6 +305,26 @@ size_t moe_ffn_host_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, 
            make_layout(s).total;
 }
 
+namespace {
+
+// Inputs and output of at most this many bytes are read and written by the
+// kernels in place when the host buffers are page-locked and mapped; larger
+// ones are copied (the grouped path reads each token row k times).
+constexpr size_t kDirectIoBytes = 1 << 20;
+
+// The device address of page-locked, mapped host memory, or null.
+const void *mapped_host(const void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+}  // namespace
+
 int moe_ffn_forward_host(const void *x_host, const float *logits_host, const void *w_gate_up_bf16,
                          const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
                          float *out_host, void *workspace, size_t workspace_bytes, moe_ffn_opts *opts,
@@ -326,6 +346,16 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host, const voi
     if (workspace_bytes < moe_ffn_host_workspace_bytes(T, H, I, E, k)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     char *p = (char *)workspace;
     const size_t xb = (size_t)(T * H * 2), lb = (size_t)(T * E * 4), ob = (size_t)(T * H * 4);
+    if (xb + lb + ob <= kDirectIoBytes) {
+        // small and page-locked: the kernels read x and the logits and write
+        // out through the host link (NVLink-C2C on GB300), no copies
+        const void *xd = mapped_host(x_host), *ld = mapped_host(logits_host), *od = mapped_host(out_host);
+        if (xd && ld && od && aligned16(xd) && aligned16(ld) && aligned16(od)) {
+            char *ws = p + align256(xb) + align256(lb) + align256(ob);
+            return run_forward(xd, (const float *)ld, w_gate_up_bf16, w_down_bf16, s, (float *)od, ws,
+                               make_layout(s), nullptr, nullptr, opts, stream);
+        }
+    }
     void *x_dev = p;
     auto *l_dev = (float *)(p + align256(xb));
     auto *o_dev = (float *)(p + align256(xb) + align256(lb));

@@ -155,19 +155,28 @@ def test_auto_path_choice():
         assert o.n_stages == (4 if want == m.MOE_PATH_DECODE else 6)
 
 
-def test_plain_forward_and_host_entry_match_ex():
-    T, H, I, E, k = 6, 512, 192, 16, 4
+@pytest.mark.parametrize("T", [1, 6, 200])
+def test_plain_forward_and_host_entry_match_ex(T):
+    """moe_ffn_forward and moe_ffn_forward_host give moe_ffn_forward_ex's
+    bits: host buffers page-locked (small calls read and write them in
+    place, large ones copy) and pageable (always copied)."""
+    H, I, E, k = 512, 192, 16, 4
     wl = gu.custom(T, H, I, E, k, name="entries")
     x, L, wgu, wd = gu.make_layer(wl, T)
     ref = m.moe_ffn_forward_ex(x, L, wgu, wd, k)
     plain = m.moe_ffn_forward(x, L, wgu, wd, k)
-    xh = x.cpu().pin_memory()
-    lh = L.cpu().pin_memory()
-    oh = torch.empty((T, H), dtype=torch.float32).pin_memory()
-    ws = m.new_workspace(T, H, I, E, k, host=True)
-    m.moe_ffn_forward_host(xh, lh, wgu, wd, k, oh, ws)
     torch.cuda.synchronize()
-    assert torch.equal(plain, ref) and torch.equal(oh, ref.cpu())
+    assert torch.equal(plain, ref)
+    ws = m.new_workspace(T, H, I, E, k, host=True)
+    for pinned in (True, False):
+        xh, lh = x.cpu(), L.cpu()
+        oh = torch.full((T, H), float("nan"), dtype=torch.float32)
+        if pinned:
+            xh, lh, oh = xh.pin_memory(), lh.pin_memory(), oh.pin_memory()
+        for _ in range(3):
+            m.moe_ffn_forward_host(xh, lh, wgu, wd, k, oh, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(oh, ref.cpu()), pinned
 
 
 @pytest.mark.parametrize("T,path,stages", [(3, "decode", 1), (8, "decode", 4), (8, "grouped", 6)])
