@@ -81,6 +81,27 @@ def parse():
     return p.parse_args()
 
 
+def rank_calls(rank, W, K):
+    """Call indices of the token stream that rank processes: disjoint per
+    rank, so the replicas work on independent tokens."""
+    return range(rank * (W + K), (rank + 1) * (W + K))
+
+
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of the per-rank values; every rank gets it."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_tokens_per_s(T, K, world, max_ms):
+    """Tokens of all ranks over the slowest rank's time (weak scaling)."""
+    return T * K * world / (max_ms / 1e3)
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -319,9 +340,9 @@ def main():
     wgu, wd = layers[0]
     batch_bytes = T * (wl.H * 2 + wl.E * 4)
     NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
-    # rank r processes calls [r*(W+K), (r+1)*(W+K)) of the token stream
-    batches = [synth.make_tokens(wl, T, call=rank * (W + K) + i, device=dev, bias=bias)
-               for i in range(NB)]
+    # rank r processes its own calls of the token stream
+    calls = rank_calls(rank, W, K)
+    batches = [synth.make_tokens(wl, T, call=calls[i], device=dev, bias=bias) for i in range(NB)]
     ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
     out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -466,10 +487,7 @@ def main():
             e2e = {"ms": mark0.elapsed_time(mark1)}
 
     # max over ranks
-    t = torch.tensor([total_ms, e2e["ms"] if e2e else 0.0], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_max = float(t[0]), float(t[1])
+    total_ms, e2e_max = max_over_ranks([total_ms, e2e["ms"] if e2e else 0.0], world, dev)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -477,7 +495,7 @@ def main():
 
     peaks = load_peaks()
     tokens = T * K * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_tokens_per_s(T, K, world, total_ms)
     mean_U = sum(U) / len(U)
     call_bytes = sum(algorithmic_bytes(wl, T, u) for u in U) / K
     flops = 6.0 * wl.H * wl.I * T * wl.k
@@ -523,7 +541,7 @@ def main():
         "wall_s": wall,
     }
     if e2e is not None:
-        line["e2e"] = {"value": tokens / (e2e_max / 1e3), "unit": "tokens/s",
+        line["e2e"] = {"value": whole_job_tokens_per_s(T, K, world, e2e_max), "unit": "tokens/s",
                        "h2d_bytes_per_step": T * wl.H * 2 + T * wl.E * 4,
                        "d2h_bytes_per_step": T * wl.H * 4}
     line["clocks"] = clocks.summary()
