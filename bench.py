@@ -293,9 +293,33 @@ def cpu_baseline(wl, T, wgu_dev, wd_dev, bias):
     t0 = time.perf_counter()
     oracle.forward(xb, L, wgu, wd, wl.k, expert_map=emap, nthreads=cores)
     dt = time.perf_counter() - t0
+    # the same oracle on one thread, on the first tokens of the sample (~5 s)
+    n1 = max(1, min(got, int(15e9 / per_token)))
+    t1 = time.perf_counter()
+    oracle.forward(xb[:n1], L[:n1], wgu, wd, wl.k, expert_map=emap, nthreads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": got / dt, "unit": "tokens/s", "cores": min(cores, got), "kind": "oracle",
             "sample": f"{got} fresh seeded tokens of the workload in one oracle call "
-                      f"({len(used)} experts), {dt:.1f} s"}
+                      f"({len(used)} experts), {dt:.1f} s",
+            "cpu": cpu_model(),
+            "single_thread": {"value": n1 / dt1, "unit": "tokens/s", "sample": f"the first {n1} tokens, {dt1:.1f} s"}}
+
+
+def cpu_model():
+    """The host CPU's name as /proc/cpuinfo or lscpu give it."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
 
 
 def main():

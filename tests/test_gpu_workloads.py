@@ -68,6 +68,8 @@ def test_workload_against_oracle(name, T, n_sample):
 
 
 @pytest.mark.parametrize("name,T,runs", [("decode_h2048_i768_e128_k8", 1, 100),
+                                          ("decode_h2048_i768_e128_k8", 2, 100),
+                                          ("decode_h4096_i1536_e128_k8_bias", 4, 100),
                                           ("decode_h7168_i2048_e384_k8_bias", 32, 100),
                                           ("fwd_t2048_h6144_i2048_e256_k8_bias", 2048, 100)],
                          ids=lambda v: str(v))
