@@ -24,12 +24,13 @@
 //     depend on phase A), so they stream in while the grid meets at a
 //     barrier.  A ring slot takes as many of these rows as fit, across
 //     expert boundaries (one bulk copy per expert run);
-//   - phase B: after the barrier the CTA copies every assignment's act row
-//     into shared memory, dots each of its W_down rows with the act rows of
-//     the expert's assignments and finally sums
-//     out[t, h] = sum_j w[t, j] * part[h][t*k + j] in slot order.
-// The kernel takes a call only if all T*k act rows fit in shared memory beside
-// a ring of at least kMinSlots slots; other small-T calls use decode.cu.
+//   - phase B: after the barrier the CTA dots each of its W_down rows with
+//     the act rows of the expert's assignments and finally sums
+//     out[t, h] = sum_j w[t, j] * part[h][t*k + j] in slot order.  The act
+//     rows are first copied into shared memory when all T*k of them fit
+//     beside a ring of kMinSlots slots; otherwise they are read from global
+//     memory as needed (one expert's rows at a time, so they stay in L1).
+// Calls whose ring would still be shorter than kMinSlots use decode.cu.
 // Each dot product uses decode.cu's lane split, chunk order, fmaf order and
 // shuffle butterfly, so this path returns the same bits as the general decode
 // path.  Every consumer warp visits every chunk and every expert boundary in
@@ -73,7 +74,7 @@ constexpr int kMaxSlots = 16;
 constexpr int kSmemCap = 224 * 1024;  // dynamic; the per-block limit also covers the static tables
 constexpr int kMaxTokens = 4;
 constexpr int kMaxAsg = 64;           // T * k
-constexpr int kMinSlots = 5;          // ring slots the kernel needs beside the act rows
+constexpr int kMinSlots = 5;          // ring slots the kernel needs (measured: 4 are too few)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
@@ -93,7 +94,7 @@ enum : uint32_t {
 
 // Shared-memory layout: ring | full[slots] | empty[slots] | flag | payload.
 // The payload holds x [T][H] FP32 (phase A) and, in the same space, the act
-// rows [T*k][I] FP32 of phase B; then part [nh][T*k].
+// rows [T*k][I] FP32 of phase B if they are staged; then part [nh][T*k].
 struct Layout {
     uint32_t full, empty, flag, payload, total;
 };
@@ -113,9 +114,9 @@ __host__ __device__ inline Layout layout(int slots, int slot_bytes, uint32_t pay
     return L;
 }
 
-__host__ __device__ inline uint32_t xa_bytes(int T, int H, int I, int k)
+__host__ __device__ inline uint32_t xa_bytes(int T, int H, int I, int k, bool act_in_smem)
 {
-    const uint32_t xb = (uint32_t)(4 * T * H), ab = (uint32_t)(4 * T * k * I);
+    const uint32_t xb = (uint32_t)(4 * T * H), ab = act_in_smem ? (uint32_t)(4 * T * k * I) : 0u;
     return xb > ab ? xb : ab;
 }
 
@@ -248,13 +249,14 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
                         const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int T, int H, int I, int E,
-                        int k, int slots, int slot_bytes, int rpc, int rps, int nh_max, float *__restrict__ act_g,
+                        int k, int slots, int slot_bytes, int rpc, int rps, int nh_max, int act_in_smem,
+                        float *__restrict__ act_g,
                         unsigned long long *__restrict__ flags, unsigned long long epoch_base,
                         int32_t *__restrict__ idx_out, float *__restrict__ w_out, float *__restrict__ out)
 {
     extern __shared__ __align__(128) uint8_t sm[];
     const int A = T * k;
-    const uint32_t xa = xa_bytes(T, H, I, k);
+    const uint32_t xa = xa_bytes(T, H, I, k, act_in_smem != 0);
     const Layout L = layout(slots, slot_bytes, xa + (uint32_t)nh_max * A * 4);
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sm + L.empty);
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loads; the groups go round-robin over the consumer warps, counted across
     // runs and chunks.  First every assignment's act row into shared memory.
     {
-        const int n4 = A * I / 4;
+        const int n4 = act_in_smem ? A * I / 4 : 0;
         for (int v0 = ct; v0 < n4; v0 += 4 * n_ct) {
             float4 a4[4];
 #pragma unroll
@@ -533,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int a0 = s_ubeg[uu], na = s_ubeg[uu + 1] - a0;
                     const float *arow[NT];
 #pragma unroll
-                    for (int b = 0; b < NT; ++b) arow[b] = abuf + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
+                    for (int b = 0; b < NT; ++b)
+                        arow[b] = (act_in_smem ? abuf : act_g) + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
                     float *pr = part + (size_t)rr * A;
                     for (; g < ng; g += kConsumers) {
                         const int u0 = g << lg, nu = min(1 << lg, len - u0);
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // phase B fills each slot with rps = slot / 2I rows.  As many slots as fit in
 // shared memory beside the payload.
 struct Plan {
-    int nt, rpc, rps, slot_bytes, slots, nh_max;
+    int nt, rpc, rps, slot_bytes, slots, nh_max, act_in_smem;
     uint32_t payload;
 };
 
@@ -592,10 +595,14 @@ Plan plan_for(int T, int H, int I, int k, int n_sm)
     if (2 * I > slot) slot = 2 * I;
     p.rps = slot / (2 * I);
     p.slot_bytes = slot;
-    p.payload = xa_bytes(T, H, I, k) + (uint32_t)(p.nh_max * T * k * 4);
-    const int fixed = (int)layout(0, p.slot_bytes, p.payload).total + 2 * kMaxSlots * 8;
-    const int n = (kSmemCap - fixed) / p.slot_bytes;
-    p.slots = n > kMaxSlots ? kMaxSlots : n;
+    for (int staged = 1; staged >= 0; --staged) {  // act rows in shared memory if the ring keeps kMinSlots
+        p.act_in_smem = staged;
+        p.payload = xa_bytes(T, H, I, k, staged != 0) + (uint32_t)(p.nh_max * T * k * 4);
+        const int fixed = (int)layout(0, p.slot_bytes, p.payload).total + 2 * kMaxSlots * 8;
+        const int n = (kSmemCap - fixed) / p.slot_bytes;
+        p.slots = n > kMaxSlots ? kMaxSlots : n;
+        if (p.slots >= kMinSlots) break;
+    }
     return p;
 }
 
@@ -639,8 +646,8 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
     cfg.numAttrs = 1;
     auto kern = p.nt == 1 ? decode_fused_kernel<1> : p.nt == 2 ? decode_fused_kernel<2> : decode_fused_kernel<4>;
     return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
-                              H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, act, flags, next_epoch(),
-                              idx_out, w_out, out);
+                              H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, flags,
+                              next_epoch(), idx_out, w_out, out);
 }
 
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)

@@ -289,7 +289,8 @@ def test_fused_decode_shared_experts(T, share):
 # assignments (its maximum).  Compared with the oracle and, bit for bit,
 # with the same tokens through the general decode kernels.
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 64, 64, 1024, 32), (1, 128, 64, 40, 1), (4, 64, 128, 64, 16),
-                                       (2, 192, 320, 7, 7), (3, 1024, 64, 256, 8)])
+                                       (2, 192, 320, 7, 7), (3, 1024, 64, 256, 8),
+                                       (4, 512, 1024, 64, 16)])  # act rows too large to stage: read in place
 def test_fused_decode_edges(T, H, I, E, k):
     wl = gu.custom(T, H, I, E, k, 1.0, name="fused_edge")
     x, L, wgu, wd = gu.make_layer(wl, T)
