@@ -112,7 +112,9 @@ typedef struct moe_ffn_opts {
 /*
  * The layer forward pass.  Uses a stream-ordered temporary workspace
  * (cudaMallocAsync / cudaFreeAsync on `stream`), so it is safe on several
- * streams at once.  Returns MOE_ERR_NO_MEMORY if that allocation fails.
+ * streams at once, and keeps no state between calls (its decode calls always
+ * meet at the grid barrier).  Returns MOE_ERR_NO_MEMORY if that allocation
+ * fails.
  */
 int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32,
                     const void *w_gate_up_bf16, const void *w_down_bf16,
@@ -130,7 +132,14 @@ size_t moe_ffn_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E,
  * The forward pass with a caller-owned workspace (256-byte aligned, at least
  * moe_ffn_workspace_bytes), optional routing outputs and options.  With a
  * workspace the call allocates nothing and is reentrant; two calls that
- * share a workspace must be ordered on one stream.
+ * share a workspace must be ordered on one stream.  The workspace needs no
+ * initialisation, and any memory (whatever it held before) can become one.
+ * The library keeps state in it between calls (the decode path for T <= 4
+ * keeps a call counter and tagged scratch there, at offsets that depend only
+ * on k and I, so calls with any T may share it): do not write to it while it
+ * serves as a workspace.  A workspace's first decode call for a given shape
+ * meets at a grid barrier and prepares that state; later ones skip the
+ * barrier.
  *   topk_idx_out  nullable int32 [T,k]: the chosen experts, slot order.
  *   topk_w_out    nullable float [T,k]: their softmax weights.
  *   opts          nullable; see moe_ffn_opts.
@@ -181,8 +190,9 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host,
  * address (set-up, once per device, with that device current); make that
  * first call before any stream capture.  All calls share the array: calls
  * whose GPU work overlaps (other streams, unordered host threads) race and
- * return wrong results, so order them on one stream.  Nothing in the array
- * needs to start at zero; each call writes every byte it later reads.
+ * return wrong results, so order them on one stream.  The array serves as
+ * the workspace of moe_ffn_forward_ex, with the state that keeps between
+ * calls.
  */
 #define MOE_FFN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int moe_ffn_forward_noalloc(const void *x_bf16, const float *router_logits_f32,

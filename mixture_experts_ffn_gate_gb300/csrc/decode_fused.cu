@@ -21,13 +21,13 @@
 //     order phase B keeps in shared memory;
 //   - the producer goes straight on to the CTA's W_down rows (dims
 //     [h_lo, h_hi) of each touched expert, expert after expert; they do not
-//     depend on phase A), so they stream in while the grid meets at a
-//     barrier.  A ring slot takes as many of these rows as fit, across
+//     depend on phase A), so they stream in while the act rows are
+//     exchanged.  A ring slot takes as many of these rows as fit, across
 //     expert boundaries (one bulk copy per expert run);
-//   - phase B: after the barrier the CTA dots each of its W_down rows with
-//     the act rows of the expert's assignments and finally sums
-//     out[t, h] = sum_j w[t, j] * part[h][t*k + j] in slot order.  The act
-//     rows are first copied into shared memory when all T*k of them fit
+//   - phase B: once every act value is visible the CTA dots each of its
+//     W_down rows with the act rows of the expert's assignments and finally
+//     sums out[t, h] = sum_j w[t, j] * part[h][t*k + j] in slot order.  The
+//     act rows are first copied into shared memory when all T*k of them fit
 //     beside a ring of kMinSlots slots; otherwise they are read from global
 //     memory as needed (one expert's rows at a time, so they stay in L1).
 // Calls whose ring would still be shorter than kMinSlots use decode.cu.
@@ -37,19 +37,33 @@
 // order, so a ring slot's parity waits are never more than one phase ahead
 // and the CTA-wide barriers match; every wait is bounded.
 //
-// Grid barrier (two hops, every spin bounded): after a CTA-wide barrier one
-// thread of CTA b stores the low 32 bits of the call's epoch into arrival
-// word b (release).  In CTA 0, thread t watches words 4t..4t+3 with 16-byte
-// relaxed loads until all hold the epoch, then issues an acq_rel fence; after
-// a CTA-wide barrier CTA 0 stores the epoch into the go word (release), which
-// one thread of every other CTA watches the same way.  The epoch is the
-// launch's odd 64-bit base (drawn at random per process, advanced per launch)
-// plus twice a call counter kept in the flags array: every CTA reads the
-// counter before it arrives and CTA 0 advances it after the barrier, so a
-// CUDA-graph replay, which repeats the base, still gets a fresh epoch.  Stale
-// words from earlier calls never equal a later epoch (within 2^31 calls), so
-// nothing needs zeroing.
-#include <atomic>
+// Exchange of the act rows between phase A and phase B, in one of two ways.
+// Every call has an epoch: a 64-bit salt drawn at random once per process
+// plus twice a call counter kept in the workspace's flags array; every CTA
+// reads the counter at its start and it is advanced once per call after all
+// CTAs have read it, so no two calls on one flags array (eager or replayed
+// from a CUDA graph) share an epoch within 2^31 calls.
+//   - Grid barrier (two hops, every spin bounded): after a CTA-wide barrier
+//     one thread of CTA b stores the low 32 bits of the epoch into arrival
+//     word b (release).  In CTA 0, thread t watches words 4t..4t+3 with
+//     16-byte relaxed loads until all hold the epoch, then issues an acq_rel
+//     fence; after a CTA-wide barrier CTA 0 stores the epoch into the go word
+//     (release), which one thread of every other CTA watches the same way,
+//     and advances the counter.  Stale words never equal a later epoch, so
+//     nothing needs zeroing.
+//   - Tagged act (no barrier), for calls that stage the act rows in shared
+//     memory: phase A writes each act value as one 64-bit word, epoch << 32
+//     | float bits, into a tag region of the workspace, and phase B re-reads
+//     the words (64-bit relaxed loads, single-copy atomic against the 64-bit
+//     stores) until all carry the epoch: the data is its own flag, one hop
+//     instead of the barrier's two plus the copy.  Every CTA stores the epoch
+//     in its arrival word at its start; CTA 0's producer warp advances the
+//     counter once all have.  A tag region is used only after a barrier call
+//     on the same flags array has zeroed it and set the check word (a key
+//     xor the flags address) and the size word, so its words hold zeros or
+//     tags of earlier calls, which never equal the epoch (zero cannot: the
+//     epoch is odd).  Memory that held other data thus never stands in for
+//     an act value; only the check word could match by chance (2^-64).
 #include <random>
 
 #include "common.cuh"
@@ -79,11 +93,15 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
 // flags (64-bit words): [0, kMaxGridCtas / 2) hold the kMaxGridCtas 32-bit
-// arrival words, then the call counter, then the go word on a 128-byte line
-// of its own
+// arrival words, then the call counter, the tag-region check word and the
+// tag-region size (64-bit words known to hold no live tag), then the go
+// word on a 128-byte line of its own
 constexpr int kCallWord = kMaxGridCtas;
+constexpr int kCheckWord = kMaxGridCtas + 1;
+constexpr int kSizeWord = kMaxGridCtas + 2;
 constexpr int kGoWord = kMaxGridCtas + 16;
 static_assert(kGoWord < kDecodeFusedFlagWords, "flags array too small");
+constexpr unsigned long long kCheckKey = 0x6d6f652d7461672dull;  // xor the flags address
 
 enum : uint32_t {
     FAULT_PRODUCER = 16u,
@@ -163,11 +181,13 @@ __device__ __forceinline__ bool wait_words4(const uint32_t *p, int n, uint32_t v
 // Gate and up dot products of one row pair (BF16 in shared memory) with the
 // x rows of the expert's NB tokens (two-plane FP32 in shared memory); lane 0
 // writes act = silu(gate) * up of assignment asg[b] at column col of its
-// global act row.  Each dot product keeps decode.cu's lane split, fmaf
-// order and butterfly.
+// global act row: as a plain float in act_g, or, when act_t is set, as one
+// 64-bit word (tag << 32 | float bits) in act_t.  Each dot product keeps
+// decode.cu's lane split, fmaf order and butterfly.
 template <int NB>
 __device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t *urow, const float *const *xr, int H,
-                                             int lane, const int *asg, float *act_g, int I, int col)
+                                             int lane, const int *asg, float *act_g, unsigned long long *act_t,
+                                             uint32_t tag, int I, int col)
 {
     float acc[2 * NB];
 #pragma unroll
@@ -192,7 +212,14 @@ __device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t 
     warp_sum_n(acc);
     if (lane == 0) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) act_g[(size_t)asg[b] * I + col] = swiglu(acc[b], acc[NB + b]);
+        for (int b = 0; b < NB; ++b) {
+            const float a = swiglu(acc[b], acc[NB + b]);
+            const size_t at = (size_t)asg[b] * I + col;
+            if (act_t)
+                ptx::st_relaxed_gpu(act_t + at, ((unsigned long long)tag << 32) | __float_as_uint(a));
+            else
+                act_g[at] = a;
+        }
     }
 }
 
@@ -250,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
                         const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int T, int H, int I, int E,
                         int k, int slots, int slot_bytes, int rpc, int rps, int nh_max, int act_in_smem,
-                        float *__restrict__ act_g,
-                        unsigned long long *__restrict__ flags, unsigned long long epoch_base,
+                        float *__restrict__ act_g, unsigned long long *__restrict__ act_t,
+                        unsigned long long *__restrict__ flags, unsigned long long epoch_salt,
                         int32_t *__restrict__ idx_out, float *__restrict__ w_out, float *__restrict__ out)
 {
     extern __shared__ __align__(128) uint8_t sm[];
@@ -280,8 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         *flag = 0;
         ptx::fence_barrier_init();
     }
-    const unsigned long long calls = *reinterpret_cast<volatile unsigned long long *>(flags + kCallWord);
-    const unsigned long long epoch = epoch_base + 2 * calls;
+    // this call's epoch and exchange mode, from words that no CTA changes
+    // before every CTA has read them
+    const volatile unsigned long long *vflags = flags;
+    const unsigned long long calls = vflags[kCallWord];
+    const uint32_t e32 = (uint32_t)(epoch_salt + 2 * calls);
+    const bool tag_region = act_in_smem && act_t;  // this call may use, or prepare, the tag region
+    const bool tagged = tag_region && vflags[kCheckWord] == (kCheckKey ^ (unsigned long long)flags) &&
+                        vflags[kSizeWord] >= (unsigned long long)(T * k) * I;
+    uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
+    if (tagged && threadIdx.x == 0) ptx::st_relaxed_gpu(arrive + blockIdx.x, e32);  // "read the counter"
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // routing: consumer warp 1 + t routes token t (scratch: the ring)
@@ -367,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb = (nrow + rps - 1) / rps;
 
     if (warp == 0) {
+        int c = 0;
         if (lane == 0) {
-            int c = 0;
             bool ok = true;
             int u = lo / I, i0 = lo - u * I;
             for (int p = lo; p < hi && ok; ++c) {
@@ -413,8 +448,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            drain(full, slots, c);
         }
+        __syncwarp();
+        if (tagged && blockIdx.x == 0) {
+            // no grid barrier in this call: advance the call counter once
+            // every CTA has read it (its arrival word holds the epoch).  It
+            // is advanced even after a failed wait, so that no later call
+            // reuses this epoch.
+            const uint64_t t_start = ptx::globaltimer_ns();
+            for (int v = lane; 4 * v < (int)gridDim.x && !*flag; v += 32)
+                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start))
+                    fail(flag, FAULT_BARRIER);
+            __syncwarp();
+            if (lane == 0) flags[kCallWord] = calls + 1;
+        }
+        if (lane == 0) drain(full, slots, c);
         return;
     }
 
@@ -431,7 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::named_sync(1, n_ct);
 
     // phase A: for each pair, gate and up dot products with every token of
-    // the expert; act per assignment to global memory
+    // the expert; act per assignment to global memory (tagged
+    // words when this call exchanges act without a grid barrier)
+    unsigned long long *const act_w = tagged ? act_t : nullptr;
     int c = 0;
     {
         int u = lo / I, i0 = lo - u * I, pos = 0;
@@ -453,13 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t *grow = chunk + (size_t)m * 2 * H;
                     const uint8_t *urow = grow + (size_t)n * 2 * H;
                     const int col = plane_pos(i0 + m, I);
-                    if (na == 1) gate_up_pair<1>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                    if (na == 1) gate_up_pair<1>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
                     if constexpr (NT >= 2) {
-                        if (na == 2) gate_up_pair<2>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                        if (na == 2) gate_up_pair<2>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
                     }
                     if constexpr (NT >= 4) {
-                        if (na == 3) gate_up_pair<3>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
-                        if (na == 4) gate_up_pair<4>(grow, urow, xr, H, lane, s_asg + a0, act_g, I, col);
+                        if (na == 3) gate_up_pair<3>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                        if (na == 4) gate_up_pair<4>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
                     }
                 }
             }
@@ -475,12 +525,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // grid barrier: every CTA's act values written and visible
+    // Exchange of the act rows.  Tagged: no grid barrier; phase B polls the
+    // tagged words until every one carries this call's epoch.  Otherwise the
+    // grid meets at the two-hop barrier, and a call that could use the tag
+    // region first clears its share of it (zero never equals an epoch, which
+    // is odd) so that CTA 0 can then mark the region as usable.
+    const int nact = A * I;
+    if (!tagged && tag_region) {
+        const int w_lo = (int)((int64_t)nact * blockIdx.x / gridDim.x);
+        const int w_hi = (int)((int64_t)nact * (blockIdx.x + 1) / gridDim.x);
+        for (int v = w_lo + ct; v < w_hi; v += n_ct) act_t[v] = 0ull;
+    }
     ptx::named_sync(1, n_ct);
-    {
-        uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
+    if (!tagged) {  // grid barrier: every CTA's act values written and visible
         uint32_t *go = reinterpret_cast<uint32_t *>(flags + kGoWord);
-        const uint32_t e32 = (uint32_t)epoch;
         const uint64_t t_start = ptx::globaltimer_ns();
         if (ct == 0 && !*flag) ptx::st_release_gpu(arrive + blockIdx.x, e32);
         if (blockIdx.x == 0) {
@@ -495,7 +553,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // every consumer leaves, or none: a producer fault can set the flag at any time
     const bool stop = ptx::named_sync_or(1, n_ct, *flag != 0);
-    if (blockIdx.x == 0 && ct == 0) flags[kCallWord] = calls + 1;
+    if (!tagged && blockIdx.x == 0 && ct == 0) {
+        // past the barrier every CTA has read the flags and cleared its share
+        flags[kCallWord] = calls + 1;
+        if (tag_region && !stop) {
+            const unsigned long long key = kCheckKey ^ (unsigned long long)flags;
+            const unsigned long long had = vflags[kCheckWord] == key ? vflags[kSizeWord] : 0ull;
+            flags[kSizeWord] = had > (unsigned long long)nact ? had : (unsigned long long)nact;
+            flags[kCheckWord] = key;
+        }
+    }
     if (stop) return;
 
     // phase B: W_down rows, chunk by chunk.  Within a run of one expert's
@@ -503,15 +570,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loads; the groups go round-robin over the consumer warps, counted across
     // runs and chunks.  First every assignment's act row into shared memory.
     {
-        const int n4 = act_in_smem ? A * I / 4 : 0;
-        for (int v0 = ct; v0 < n4; v0 += 4 * n_ct) {
-            float4 a4[4];
+        if (tagged) {
+            // each thread takes 16-byte words (two tagged values) eight at a
+            // time and re-reads the ones that do not yet carry the epoch
+            const int nw = nact / 2;
+            const uint64_t t_start = ptx::globaltimer_ns();
+            for (int v0 = ct; v0 < nw; v0 += 8 * n_ct) {
+                uint32_t need = 0;
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                if (v0 + b * n_ct < n4) a4[b] = __ldcg(reinterpret_cast<const float4 *>(act_g) + v0 + b * n_ct);
+                for (int j = 0; j < 8; ++j)
+                    if (v0 + j * n_ct < nw) need |= 1u << j;
+                for (uint32_t spin = 0; need; ++spin) {
+                    ulonglong2 w[8];
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                if (v0 + b * n_ct < n4) reinterpret_cast<float4 *>(abuf)[v0 + b * n_ct] = a4[b];
+                    for (int j = 0; j < 8; ++j)
+                        if ((need >> j) & 1u) w[j] = ptx::ld_relaxed_gpu_v2u64(act_t + 2 * (size_t)(v0 + j * n_ct));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (((need >> j) & 1u) && (uint32_t)(w[j].x >> 32) == e32 && (uint32_t)(w[j].y >> 32) == e32) {
+                            need &= ~(1u << j);
+                            reinterpret_cast<float2 *>(abuf)[v0 + j * n_ct] =
+                                make_float2(__uint_as_float((uint32_t)w[j].x), __uint_as_float((uint32_t)w[j].y));
+                        }
+                    if (need && (spin & 15) == 15 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) {
+                        fail(flag, FAULT_BARRIER);
+                        break;
+                    }
+                }
+                if (*flag) break;
+            }
+        } else if (act_in_smem) {
+            const int n4 = nact / 4;
+            for (int v0 = ct; v0 < n4; v0 += 4 * n_ct) {
+                float4 a4[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if (v0 + b * n_ct < n4) a4[b] = __ldcg(reinterpret_cast<const float4 *>(act_g) + v0 + b * n_ct);
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if (v0 + b * n_ct < n4) reinterpret_cast<float4 *>(abuf)[v0 + b * n_ct] = a4[b];
+            }
         }
         ptx::named_sync(1, n_ct);
         bool ok = true;
@@ -606,18 +704,18 @@ Plan plan_for(int T, int H, int I, int k, int n_sm)
     return p;
 }
 
-std::atomic<unsigned long long> g_epoch{0};
-
-// A value unique to this launch: a 64-bit counter whose start is drawn at
-// random once per process, so flags left in a workspace by earlier calls (or
-// by another process) do not match it.
-unsigned long long next_epoch()
+// The odd 64-bit salt of every epoch, drawn at random once per process.  A
+// call's epoch is salt + 2 * (the flags array's call counter), so the calls
+// on one flags array, eager or replayed from a CUDA graph, never repeat an
+// epoch within 2^31 calls, and words left by another process or by other
+// data match one only by chance (2^-32 per word).
+unsigned long long epoch_salt()
 {
-    static const unsigned long long base = [] {
+    static const unsigned long long salt = [] {
         std::random_device rd;
-        return ((unsigned long long)rd() << 32) ^ rd() ^ 0x9e3779b97f4a7c15ull;
+        return (((unsigned long long)rd() << 32) ^ rd() ^ 0x9e3779b97f4a7c15ull) | 1ull;
     }();
-    return base + 2 * g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    return salt;
 }
 
 }  // namespace
@@ -629,9 +727,16 @@ bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm)
     return p.slots >= kMinSlots && (int64_t)T * E * 4 <= (int64_t)p.slots * p.slot_bytes;  // routing scratch
 }
 
+size_t decode_fused_tag_words(int k, int I)
+{
+    const int a = kMaxTokens * k < kMaxAsg ? kMaxTokens * k : kMaxAsg;
+    return (size_t)a * I;
+}
+
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
-                                int I, int E, int k, int n_sm, float *act, unsigned long long *flags,
-                                int32_t *idx_out, float *w_out, float *out, cudaStream_t s)
+                                int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
+                                unsigned long long *flags, int32_t *idx_out, float *w_out, float *out,
+                                cudaStream_t s)
 {
     const Plan p = plan_for(T, H, I, k, n_sm);
     cudaLaunchConfig_t cfg = {};
@@ -640,14 +745,14 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
     cfg.dynamicSmemBytes = layout(p.slots, p.slot_bytes, p.payload).total;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
+    attr[0].id = cudaLaunchAttributeCooperative;  // both act exchanges need every CTA resident
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     auto kern = p.nt == 1 ? decode_fused_kernel<1> : p.nt == 2 ? decode_fused_kernel<2> : decode_fused_kernel<4>;
     return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
-                              H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, flags,
-                              next_epoch(), idx_out, w_out, out);
+                              H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, act_tag,
+                              flags, epoch_salt(), idx_out, w_out, out);
 }
 
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)

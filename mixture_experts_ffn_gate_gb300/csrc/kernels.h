@@ -33,17 +33,20 @@ cudaError_t launch_decode_down(const float *act, const void *wd, const float *w,
                                int I, int k, int warps, float *out, cudaStream_t s);
 
 // decode_fused.cu: a decode step of up to four tokens in one cooperative
-// kernel with a grid barrier.  act: [T*k][I] FP32 scratch; flags:
-// kDecodeFusedFlagWords 64-bit words of workspace (any contents; the kernel
-// keeps its barrier state there).
+// kernel.  act: [T*k][I] FP32 scratch; flags: kDecodeFusedFlagWords 64-bit
+// words and act_tag: decode_fused_tag_words(k, I) 64-bit words, both kept by
+// the kernel between calls (any initial contents) and written by nothing
+// else; act_tag may be null (every call then meets at a grid barrier).
 constexpr int kMaxGridCtas = 1024;
 constexpr int kDecodeFusedFlagWords = kMaxGridCtas + 32;
 cudaError_t decode_fused_init_device();
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear);
 bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm);
+size_t decode_fused_tag_words(int k, int I);
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
-                                int I, int E, int k, int n_sm, float *act, unsigned long long *flags,
-                                int32_t *idx_out, float *w_out, float *out, cudaStream_t s);
+                                int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
+                                unsigned long long *flags, int32_t *idx_out, float *w_out, float *out,
+                                cudaStream_t s);
 
 // grouped_gemm.cu
 cudaError_t gemm_init_device();

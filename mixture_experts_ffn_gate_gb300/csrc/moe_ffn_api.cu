@@ -22,10 +22,14 @@ struct Shape {
     int64_t T, H, I, E, k;
 };
 
-// Workspace regions, 256-byte aligned.  The routing/sort region is shared
-// by both paths; the rest is per path and the two overlap.
+// Workspace regions, 256-byte aligned.  First the fused decode kernel's
+// state, which it keeps between calls: its flags and its tag region, at the
+// same offsets for every T (they depend only on k and I), so calls with
+// different T on one workspace share them and no other region overlaps
+// them.  Then the routing/sort region, shared by both paths; the rest is per
+// path and the two overlap.
 struct Layout {
-    size_t idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, flags, common_end;
+    size_t flags, act_tag, idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, common_end;
     size_t act;                          // decode: act f32 [T*k, I]
     size_t xs, act_hi, act_lo, z;        // grouped
     size_t decode_total, grouped_total, total;
@@ -43,6 +47,8 @@ Layout make_layout(const Shape &s)
         o = align256(o + bytes);
         return at;
     };
+    L.flags = take((size_t)moe::kDecodeFusedFlagWords * 8);
+    L.act_tag = take(moe::decode_fused_tag_words((int)s.k, (int)s.I) * 8);
     L.idx = take(n * 4);
     L.w = take(n * 4);
     L.offs = take((size_t)(s.E + 1) * 4);
@@ -52,11 +58,10 @@ Layout make_layout(const Shape &s)
     L.ucount = take(4);
     L.chunks = take((size_t)(s.E + ceil_div((int64_t)n, moe::kGemmChunkMax) + 1) * 16);
     L.nchunks = take(4);
-    L.flags = take((size_t)moe::kDecodeFusedFlagWords * 8);  // fused decode kernel: grid-barrier state
     L.common_end = o;
-    // decode path: act f32 [T*k, I] (the general decode kernels and the
-    // fused decode kernel)
-    L.act = take(n * (size_t)s.I * 8);
+    // decode path: act f32 [T*k, I] (the general decode kernels, and the
+    // fused decode kernel when it meets at its grid barrier)
+    L.act = take(n * (size_t)s.I * 4);
     L.decode_total = o;
     // grouped path
     o = L.common_end;
@@ -168,8 +173,12 @@ struct Stages {
         if (e_ != cudaSuccess) return MOE_ERR_CUDA;  \
     } while (0)
 
+// keep_state: the workspace is the caller's and keeps its contents between
+// calls, so the fused decode kernel may use its tag region (a workspace
+// allocated for one call is not: its memory may have held anything since).
 int run_forward(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s, float *out,
-                char *ws, const Layout &L, int32_t *idx_out, float *w_out, moe_ffn_opts *opts, cudaStream_t stream)
+                char *ws, const Layout &L, bool keep_state, int32_t *idx_out, float *w_out, moe_ffn_opts *opts,
+                cudaStream_t stream)
 {
     DeviceInfo *dev = nullptr;
     int st = device_setup(&dev);
@@ -201,12 +210,13 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
     MOE_TRY(stg.begin());
     if (path == MOE_PATH_DECODE && moe::decode_fused_supported(T, H, I, E, k, dev->n_sm)) {
         // a few tokens: one cooperative kernel that routes them, streams both
-        // projections' rows of the touched experts and meets at a grid
-        // barrier in between
+        // projections' rows of the touched experts and exchanges the act
+        // rows in between
         path = MOE_PATH_DECODE_FUSED;
-        MOE_TRY(stg.done(moe::launch_decode_fused(x, logits, wgu, wd, T, H, I, E, k, dev->n_sm,
-                                                  (float *)(ws + L.act), (unsigned long long *)(ws + L.flags),
-                                                  idx_out, w_out, out, stream)));
+        MOE_TRY(stg.done(moe::launch_decode_fused(
+            x, logits, wgu, wd, T, H, I, E, k, dev->n_sm, (float *)(ws + L.act),
+            keep_state ? (unsigned long long *)(ws + L.act_tag) : nullptr, (unsigned long long *)(ws + L.flags),
+            idx_out, w_out, out, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
@@ -254,10 +264,14 @@ size_t moe_ffn_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64
     return make_layout(s).total;
 }
 
-int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
-                       const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
-                       float *out_f32, void *workspace, size_t workspace_bytes, int32_t *topk_idx_out,
-                       float *topk_w_out, moe_ffn_opts *opts, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+int forward_ex(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+               const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, float *out_f32,
+               void *workspace, size_t workspace_bytes, bool keep_state, int32_t *topk_idx_out, float *topk_w_out,
+               moe_ffn_opts *opts, cudaStream_t stream)
 {
     Shape s{T, H, I, E, k};
     int st = check_args(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, s, out_f32);
@@ -275,7 +289,20 @@ int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32, const
     const Layout L = make_layout(s);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
     return run_forward(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, s, out_f32, (char *)workspace, L,
-                       topk_idx_out, topk_w_out, opts, stream);
+                       keep_state, topk_idx_out, topk_w_out, opts, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+                       const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                       float *out_f32, void *workspace, size_t workspace_bytes, int32_t *topk_idx_out,
+                       float *topk_w_out, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    return forward_ex(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, T, H, I, E, k, out_f32, workspace,
+                      workspace_bytes, true, topk_idx_out, topk_w_out, opts, stream);
 }
 
 int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
@@ -291,8 +318,8 @@ int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32, const vo
         cudaGetLastError();
         return MOE_ERR_NO_MEMORY;
     }
-    st = moe_ffn_forward_ex(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, T, H, I, E, k, out_f32, ws,
-                            bytes, nullptr, nullptr, nullptr, stream);
+    st = forward_ex(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, T, H, I, E, k, out_f32, ws, bytes,
+                    false, nullptr, nullptr, nullptr, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && st == MOE_OK) st = MOE_ERR_CUDA;
     return st;
 }
@@ -351,19 +378,21 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host, const voi
         // out through the host link (NVLink-C2C on GB300), no copies
         const void *xd = mapped_host(x_host), *ld = mapped_host(logits_host), *od = mapped_host(out_host);
         if (xd && ld && od && aligned16(xd) && aligned16(ld) && aligned16(od)) {
-            char *ws = p + align256(xb) + align256(lb) + align256(ob);
-            return run_forward(xd, (const float *)ld, w_gate_up_bf16, w_down_bf16, s, (float *)od, ws,
-                               make_layout(s), nullptr, nullptr, opts, stream);
+            return run_forward(xd, (const float *)ld, w_gate_up_bf16, w_down_bf16, s, (float *)od, p,
+                               make_layout(s), true, nullptr, nullptr, opts, stream);
         }
     }
-    void *x_dev = p;
-    auto *l_dev = (float *)(p + align256(xb));
-    auto *o_dev = (float *)(p + align256(xb) + align256(lb));
-    char *ws = p + align256(xb) + align256(lb) + align256(ob);
+    // the device workspace first, so the fused decode kernel's state sits at
+    // the same place for every T; then the staged inputs and output
     const Layout L = make_layout(s);
+    char *ws = p;
+    void *x_dev = p + L.total;
+    auto *l_dev = (float *)(p + L.total + align256(xb));
+    auto *o_dev = (float *)(p + L.total + align256(xb) + align256(lb));
     if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpyAsync(l_dev, logits_host, lb, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    st = run_forward(x_dev, l_dev, w_gate_up_bf16, w_down_bf16, s, o_dev, ws, L, nullptr, nullptr, opts, stream);
+    st = run_forward(x_dev, l_dev, w_gate_up_bf16, w_down_bf16, s, o_dev, ws, L, true, nullptr, nullptr, opts,
+                     stream);
     if (st != MOE_OK) return st;
     if (cudaMemcpyAsync(out_host, o_dev, ob, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;

@@ -14,9 +14,9 @@
 // library and stays there until the process exits.  All calls share it, so
 // two calls whose work overlaps on the GPU (different streams, or different
 // host threads without ordering) race on it and give wrong results: order
-// them on one stream.  Nothing in it has to start at zero -- every byte a
-// call reads, the same call has written first -- so calls never clear it,
-// and whatever the last call left there is simply overwritten.
+// them on one stream.  It is the workspace of moe_ffn_forward_ex, so it also
+// holds the state that path keeps between calls; nothing in it has to start
+// at zero.
 #include <mutex>
 
 #include "moe_ffn.h"

@@ -137,6 +137,25 @@ __device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const uint32_t *p)
     return v;
 }
 
+// Two 64-bit words; each is read whole (single-copy atomic against a 64-bit
+// store to it), the pair is not.
+__device__ __forceinline__ ulonglong2 ld_relaxed_gpu_v2u64(const unsigned long long *p)
+{
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0,%1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long *p)

@@ -254,6 +254,75 @@ def test_cuda_graph_replay_matches_eager(T, path):
         assert evs[i].elapsed_time(evs[i + 1]) >= 0.0
 
 
+@pytest.mark.parametrize("T,I", [(1, 256), (4, 1024)], ids=["tagged_act", "grid_barrier"])
+def test_eager_calls_and_graph_replays_interleaved(T, I):
+    """Eager calls and replays of one captured call, interleaved on one
+    workspace, each compute their own tokens.  Regression: when a call's
+    epoch was a per-launch base plus the device call counter, the replay
+    that followed an eager call that followed a replay repeated that eager
+    call's epoch, and the fused decode kernel's grid barrier passed on its
+    stale arrival words.  T=1 exchanges act through tagged words once the
+    workspace is prepared, T=4 with I=1024 (act rows too large to stage)
+    always meets at the grid barrier."""
+    H, E, k = 512, 32, 8
+    wl = gu.custom(T, H, I, E, k, 1.0, name="interleave")
+    inputs = [gu.make_layer(wl, T, call=c)[:2] for c in range(6)]
+    _, _, wgu, wd = gu.make_layer(wl, T)
+    refs = [m.moe_ffn_forward(x, L, wgu, wd, k).cpu() for x, L in inputs]  # keeps no state
+    xb, lb = inputs[0][0].clone(), inputs[0][1].clone()
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = m.new_workspace(T, H, I, E, k)
+
+    def set_inputs(c):
+        xb.copy_(inputs[c][0])
+        lb.copy_(inputs[c][1])
+        out.fill_(float("nan"))
+
+    set_inputs(0)
+    o = m.moe_ffn_opts()
+    m.moe_ffn_forward_ex(xb, lb, wgu, wd, k, out=out, workspace=ws, opts=o)
+    torch.cuda.synchronize()
+    assert o.path_taken == m.MOE_PATH_DECODE_FUSED
+    assert torch.equal(out.cpu(), refs[0])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        m.moe_ffn_forward_ex(xb, lb, wgu, wd, k, out=out, workspace=ws, stream=torch.cuda.current_stream())
+    steps = ["replay", "eager", "replay", "eager", "eager", "replay", "replay", "eager", "replay"]
+    for i, how in enumerate(steps):
+        c = (i + 1) % len(inputs)
+        set_inputs(c)
+        if how == "replay":
+            g.replay()
+        else:
+            m.moe_ffn_forward_ex(xb, lb, wgu, wd, k, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.cpu(), refs[c]), (i, how)
+
+
+def test_fused_decode_state_in_a_shared_workspace():
+    """One workspace, filled with random bytes first, serves decode calls of
+    T = 1..4 (the fused kernel, whose state sits at the same offsets for
+    every T) and grouped calls in between.  The first call, and every call
+    whose act rows outgrow the prepared tag region, meets at the grid barrier
+    and prepares it; the others exchange act through tagged words.  Every
+    output matches, bit for bit, a call that keeps no state."""
+    H, I, E, k = 512, 256, 32, 8
+    seq = [1, 1, 2, 2, 1, 40, 3, 3, 4, 6, 4, 2, 1, 1]
+    _, _, wgu, wd = gu.make_layer(gu.custom(1, H, I, E, k, 1.0, name="shared_ws"), 1)
+    nbytes = max(m.moe_ffn_workspace_bytes(T, H, I, E, k) for T in seq)
+    ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda")
+    for step, T in enumerate(seq):
+        x, L = synth.make_tokens(gu.custom(T, H, I, E, k, 1.0, name="shared_ws"), T, call=step)
+        x, L = x.cuda(), L.cuda()
+        ref = m.moe_ffn_forward(x, L, wgu, wd, k).cpu()
+        out = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+        o = m.moe_ffn_opts()
+        m.moe_ffn_forward_ex(x, L, wgu, wd, k, out=out, workspace=ws, opts=o)
+        torch.cuda.synchronize()
+        assert o.path_taken == (m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_GROUPED), (T, o.path_taken)
+        assert torch.equal(out.cpu(), ref), (step, T)
+
+
 # Fused decode kernel (T <= 4): tokens that share experts.  Each touched
 # expert is streamed once and dotted with every token it serves; the result
 # must match the oracle and, bit for bit, the general decode kernels (T > 4
