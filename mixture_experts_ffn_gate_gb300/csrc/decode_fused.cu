@@ -33,9 +33,11 @@
 // Calls whose ring would still be shorter than kMinSlots use decode.cu.
 // Each dot product uses decode.cu's lane split, chunk order, fmaf order and
 // shuffle butterfly, so this path returns the same bits as the general decode
-// path.  Every consumer warp visits every chunk and every expert boundary in
-// order, so a ring slot's parity waits are never more than one phase ahead
-// and the CTA-wide barriers match; every wait is bounded.
+// path.  Every consumer warp visits every chunk in order (in phase B it reads
+// the chunk's descriptor, written by the producer, and walks the chunk's
+// expert runs only if one of its row groups lies there), so a ring slot's
+// parity waits are never more than one phase ahead and the CTA-wide barriers
+// match; every wait is bounded.
 //
 // Exchange of the act rows between phase A and phase B, in one of two ways.
 // Every call has an epoch: a 64-bit salt drawn at random once per process
@@ -299,6 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_xoff[kMaxAsg];     // per sorted assignment: its token's offset in xs
     __shared__ float s_w[kMaxAsg];
     __shared__ uint32_t s_key[kMaxAsg];
+    // per ring slot, for its phase B chunk: first group id, number of
+    // groups, expert and row of the chunk's first row (written by the
+    // producer before it arms the slot's full barrier)
+    __shared__ int4 s_desc[kMaxSlots];
     if (threadIdx.x == 0) {
         for (int s = 0; s < slots; ++s) {
             ptx::mbar_init(full + s, 1);
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++u;
                 }
             }
-            int uu = 0, rr = 0;
+            int uu = 0, rr = 0, gq = 0;  // next row to copy; groups before this chunk
             for (int q = 0; q < nb && ok; ++q, ++c) {
                 const int len_q = min(rps, nrow - q * rps);
                 const int s = c % slots;
@@ -435,6 +441,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                int ngq = 0;  // groups of the chunk: each run's rows in groups of 1 << s_rlog
+                for (int off = 0, u2 = uu, r2 = rr; off < len_q;) {
+                    const int len = min(len_q - off, nh - r2), lg = s_rlog[u2];
+                    ngq += (len + (1 << lg) - 1) >> lg;
+                    off += len;
+                    r2 += len;
+                    if (r2 == nh) {
+                        r2 = 0;
+                        ++u2;
+                    }
+                }
+                s_desc[s] = make_int4(gq, ngq, uu, rr);
+                gq += ngq;
+                // the arrive releases the descriptor to the consumers that wait on the slot
                 ptx::mbar_arrive_expect_tx(full + s, (uint32_t)len_q * 2 * I);
                 for (int off = 0; off < len_q;) {  // one copy per expert run
                     const int len = min(len_q - off, nh - rr);
@@ -613,51 +633,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::named_sync(1, n_ct);
         bool ok = true;
-        int uu = 0, rr = 0, pos = 0;
         for (int q = 0; q < nb; ++q, ++c) {
-            const int len_q = min(rps, nrow - q * rps);
             const int s = c % slots;
             if (ok && !ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
                 fail(flag, FAULT_PHASE_B);
                 ok = false;
             }
-            const uint8_t *chunk = sm + (size_t)s * slot_bytes;
-            for (int off = 0; off < len_q;) {
-                // rows [rr, rr + len) of expert uu; every warp walks every run,
-                // so keep this bookkeeping cheap and do the rest only with work
-                const int len = min(len_q - off, nh - rr);
-                const int lg = s_rlog[uu];  // log2 of the rows per task
-                const int ng = (len + (1 << lg) - 1) >> lg;
-                int g = first_task(pos, cw);
-                if (ok && g < ng) {
-                    const int a0 = s_ubeg[uu], na = s_ubeg[uu + 1] - a0;
-                    const float *arow[NT];
+            const int4 d = s_desc[s];
+            // groups are numbered across runs and chunks; group g goes to warp
+            // g % kConsumers.  A warp with none in this chunk skips its runs.
+            int g = d.x + (cw - d.x % kConsumers + kConsumers) % kConsumers;
+            if (ok && g < d.x + d.y) {
+                const uint8_t *chunk = sm + (size_t)s * slot_bytes;
+                const int len_q = min(rps, nrow - q * rps);
+                int uu = d.z, rr = d.w, gb = d.x;
+                for (int off = 0; off < len_q && g < d.x + d.y;) {
+                    // rows [rr, rr + len) of expert uu: groups [gb, gb + ng)
+                    const int len = min(len_q - off, nh - rr);
+                    const int lg = s_rlog[uu];  // log2 of the rows per group
+                    const int ng = (len + (1 << lg) - 1) >> lg;
+                    if (g < gb + ng) {
+                        const int a0 = s_ubeg[uu], na = s_ubeg[uu + 1] - a0;
+                        const float *arow[NT];
 #pragma unroll
-                    for (int b = 0; b < NT; ++b)
-                        arow[b] = (act_in_smem ? abuf : act_g) + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
-                    float *pr = part + (size_t)rr * A;
-                    for (; g < ng; g += kConsumers) {
-                        const int u0 = g << lg, nu = min(1 << lg, len - u0);
-                        const uint8_t *rowp[4];
+                        for (int b = 0; b < NT; ++b)
+                            arow[b] = (act_in_smem ? abuf : act_g) + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
+                        float *pr = part + (size_t)rr * A;
+                        for (; g < gb + ng; g += kConsumers) {
+                            const int u0 = (g - gb) << lg, nu = min(1 << lg, len - u0);
+                            const uint8_t *rowp[4];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r)
-                            rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
-                        if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
-                        if constexpr (NT >= 2) {
-                            if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
-                        }
-                        if constexpr (NT >= 4) {
-                            if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
-                            if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                            for (int r = 0; r < 4; ++r)
+                                rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
+                            if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                            if constexpr (NT >= 2) {
+                                if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                            }
+                            if constexpr (NT >= 4) {
+                                if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                                if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                            }
                         }
                     }
-                }
-                pos = (pos + ng) % kConsumers;
-                off += len;
-                rr += len;
-                if (rr == nh) {
-                    rr = 0;
-                    ++uu;
+                    gb += ng;
+                    off += len;
+                    rr += len;
+                    if (rr == nh) {
+                        rr = 0;
+                        ++uu;
+                    }
                 }
             }
             __syncwarp();
