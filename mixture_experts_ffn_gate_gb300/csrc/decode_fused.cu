@@ -157,6 +157,20 @@ __device__ __forceinline__ void drain(uint64_t *full, int slots, int issued)
         ptx::mbar_wait_bounded(full + (c % slots), (uint32_t)(c / slots) & 1, &keep, kDrainNs);
 }
 
+// Position in the ring of the next chunk: slot and the parity of the slot's
+// current phase, advanced without divisions.
+struct RingPos {
+    int s = 0;
+    uint32_t par = 0;
+    __device__ __forceinline__ void next(int slots)
+    {
+        if (++s == slots) {
+            s = 0;
+            par ^= 1u;
+        }
+    }
+};
+
 // First task of consumer warp cw in a run whose first task has round-robin
 // position `pos` (tasks go round-robin over the consumer warps).
 __device__ __forceinline__ int first_task(int pos, int cw) { return (cw - pos + kConsumers) % kConsumers; }
@@ -411,11 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c = 0;
         if (lane == 0) {
             bool ok = true;
+            RingPos rp;
             int u = lo / I, i0 = lo - u * I;
-            for (int p = lo; p < hi && ok; ++c) {
+            for (int p = lo; p < hi && ok; ++c, rp.next(slots)) {
                 const int n = min(rpc, min(I - i0, hi - p));
-                const int s = c % slots;
-                if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
+                const int s = rp.s;
+                if (!ptx::mbar_wait_bounded(empty + s, rp.par ^ 1u, flag, kWaitNs)) {
                     fail(flag, FAULT_PRODUCER);
                     ok = false;
                     break;
@@ -433,10 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             int uu = 0, rr = 0, gq = 0;  // next row to copy; groups before this chunk
-            for (int q = 0; q < nb && ok; ++q, ++c) {
+            for (int q = 0; q < nb && ok; ++q, ++c, rp.next(slots)) {
                 const int len_q = min(rps, nrow - q * rps);
-                const int s = c % slots;
-                if (!ptx::mbar_wait_bounded(empty + s, ((uint32_t)(c / slots) & 1) ^ 1, flag, kWaitNs)) {
+                const int s = rp.s;
+                if (!ptx::mbar_wait_bounded(empty + s, rp.par ^ 1u, flag, kWaitNs)) {
                     fail(flag, FAULT_PRODUCER);
                     ok = false;
                     break;
@@ -502,13 +517,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the expert; act per assignment to global memory (tagged
     // words when this call exchanges act without a grid barrier)
     unsigned long long *const act_w = tagged ? act_t : nullptr;
-    int c = 0;
+    RingPos rp;
     {
         int u = lo / I, i0 = lo - u * I, pos = 0;
-        for (int p = lo; p < hi; ++c) {
+        for (int p = lo; p < hi; rp.next(slots)) {
             const int n = min(rpc, min(I - i0, hi - p));
-            const int s = c % slots;
-            if (!ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
+            const int s = rp.s;
+            if (!ptx::mbar_wait_bounded(full + s, rp.par, flag, kWaitNs)) {
                 fail(flag, FAULT_PHASE_A);
                 break;
             }
@@ -633,9 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::named_sync(1, n_ct);
         bool ok = true;
-        for (int q = 0; q < nb; ++q, ++c) {
-            const int s = c % slots;
-            if (ok && !ptx::mbar_wait_bounded(full + s, (uint32_t)(c / slots) & 1, flag, kWaitNs)) {
+        for (int q = 0; q < nb; ++q, rp.next(slots)) {
+            const int s = rp.s;
+            if (ok && !ptx::mbar_wait_bounded(full + s, rp.par, flag, kWaitNs)) {
                 fail(flag, FAULT_PHASE_B);
                 ok = false;
             }
