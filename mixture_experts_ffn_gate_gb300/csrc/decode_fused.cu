@@ -67,6 +67,7 @@
 //     epoch is odd).  Memory that held other data thus never stands in for
 //     an act value; only the check word could match by chance (2^-64).
 #include <random>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -647,61 +648,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         ptx::named_sync(1, n_ct);
-        bool ok = true;
-        for (int q = 0; q < nb; ++q, rp.next(slots)) {
-            const int s = rp.s;
-            if (ok && !ptx::mbar_wait_bounded(full + s, rp.par, flag, kWaitNs)) {
-                fail(flag, FAULT_PHASE_B);
-                ok = false;
-            }
-            const int4 d = s_desc[s];
-            // groups are numbered across runs and chunks; group g goes to warp
-            // g % kConsumers.  A warp with none in this chunk skips its runs.
-            int g = d.x + (cw - d.x % kConsumers + kConsumers) % kConsumers;
-            if (ok && g < d.x + d.y) {
-                const uint8_t *chunk = sm + (size_t)s * slot_bytes;
-                const int len_q = min(rps, nrow - q * rps);
-                int uu = d.z, rr = d.w, gb = d.x;
-                for (int off = 0; off < len_q && g < d.x + d.y;) {
-                    // rows [rr, rr + len) of expert uu: groups [gb, gb + ng)
-                    const int len = min(len_q - off, nh - rr);
-                    const int lg = s_rlog[uu];  // log2 of the rows per group
-                    const int ng = (len + (1 << lg) - 1) >> lg;
-                    if (g < gb + ng) {
-                        const int a0 = s_ubeg[uu], na = s_ubeg[uu + 1] - a0;
-                        const float *arow[NT];
+        // Two instances of the loop: with the act rows staged, their loads are
+        // plain shared-memory loads (one pointer type for the compiler);
+        // otherwise global loads through L1.
+        auto rows_b = [&](auto staged) {
+            const float *const act_base = decltype(staged)::value ? abuf : act_g;
+            bool ok = true;
+            for (int q = 0; q < nb; ++q, rp.next(slots)) {
+                const int s = rp.s;
+                if (ok && !ptx::mbar_wait_bounded(full + s, rp.par, flag, kWaitNs)) {
+                    fail(flag, FAULT_PHASE_B);
+                    ok = false;
+                }
+                const int4 d = s_desc[s];
+                // groups are numbered across runs and chunks; group g goes to warp
+                // g % kConsumers.  A warp with none in this chunk skips its runs.
+                int g = d.x + (cw - d.x % kConsumers + kConsumers) % kConsumers;
+                if (ok && g < d.x + d.y) {
+                    const uint8_t *chunk = sm + (size_t)s * slot_bytes;
+                    const int len_q = min(rps, nrow - q * rps);
+                    int uu = d.z, rr = d.w, gb = d.x;
+                    for (int off = 0; off < len_q && g < d.x + d.y;) {
+                        // rows [rr, rr + len) of expert uu: groups [gb, gb + ng)
+                        const int len = min(len_q - off, nh - rr);
+                        const int lg = s_rlog[uu];  // log2 of the rows per group
+                        const int ng = (len + (1 << lg) - 1) >> lg;
+                        if (g < gb + ng) {
+                            const int a0 = s_ubeg[uu], na = s_ubeg[uu + 1] - a0;
+                            const float *arow[NT];
 #pragma unroll
-                        for (int b = 0; b < NT; ++b)
-                            arow[b] = (act_in_smem ? abuf : act_g) + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
-                        float *pr = part + (size_t)rr * A;
-                        for (; g < gb + ng; g += kConsumers) {
-                            const int u0 = (g - gb) << lg, nu = min(1 << lg, len - u0);
-                            const uint8_t *rowp[4];
+                            for (int b = 0; b < NT; ++b)
+                                arow[b] = act_base + (size_t)s_asg[a0 + (b < na ? b : 0)] * I;
+                            float *pr = part + (size_t)rr * A;
+                            for (; g < gb + ng; g += kConsumers) {
+                                const int u0 = (g - gb) << lg, nu = min(1 << lg, len - u0);
+                                const uint8_t *rowp[4];
 #pragma unroll
-                            for (int r = 0; r < 4; ++r)
-                                rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
-                            if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
-                            if constexpr (NT >= 2) {
-                                if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
-                            }
-                            if constexpr (NT >= 4) {
-                                if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
-                                if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pr + (size_t)u0 * A, A);
+                                for (int r = 0; r < 4; ++r)
+                                    rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
+                                float *const pu = pr + (size_t)u0 * A;
+                                if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                if constexpr (NT >= 2) {
+                                    if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                }
+                                if constexpr (NT >= 4) {
+                                    if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                }
                             }
                         }
-                    }
-                    gb += ng;
-                    off += len;
-                    rr += len;
-                    if (rr == nh) {
-                        rr = 0;
-                        ++uu;
+                        gb += ng;
+                        off += len;
+                        rr += len;
+                        if (rr == nh) {
+                            rr = 0;
+                            ++uu;
+                        }
                     }
                 }
+                __syncwarp();
+                if (ok && lane == 0) ptx::mbar_arrive(empty + s);
             }
-            __syncwarp();
-            if (ok && lane == 0) ptx::mbar_arrive(empty + s);
-        }
+        };
+        if (act_in_smem)
+            rows_b(std::true_type{});
+        else
+            rows_b(std::false_type{});
     }
     if (ptx::named_sync_or(1, n_ct, *flag != 0)) return;
     for (int v = ct; v < T * nh; v += n_ct) {
