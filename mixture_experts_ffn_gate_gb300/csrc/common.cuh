@@ -79,6 +79,38 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N])
     }
 }
 
+// warp_sum of N values (N a power of two <= 32) with the same butterfly, so
+// every total has the same bits, but at each of the first log2(N) levels a
+// lane keeps half of its values (the upper half if its lane bit for that
+// level is set) and receives its partner's copy of that half: N - 1 + 5 -
+// log2(N) shuffles instead of 5 N.  Value s ends in lanes
+// [s * 32 / N, (s + 1) * 32 / N), each holding the same bits; the return is
+// the lane's own total.
+template <int N>
+__device__ __forceinline__ float warp_sum_split(float (&v)[N], int lane)
+{
+    static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
+    constexpr int L = N == 1 ? 0 : N == 2 ? 1 : N == 4 ? 2 : N == 8 ? 3 : N == 16 ? 4 : 5;
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+        const int o = 16 >> j, h = (N >> j) / 2;
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 >> L; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
+}
+
+// Smallest power of two >= n (n >= 1).
+__host__ __device__ constexpr int pow2_ceil(int n) { return n <= 1 ? 1 : 2 * pow2_ceil((n + 1) / 2); }
+
 // silu(g) * u in FP32 with the library expf.
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 

@@ -196,19 +196,21 @@ __device__ __forceinline__ bool wait_words4(const uint32_t *p, int n, uint32_t v
 }
 
 // Gate and up dot products of one row pair (BF16 in shared memory) with the
-// x rows of the expert's NB tokens (two-plane FP32 in shared memory); lane 0
-// writes act = silu(gate) * up of assignment asg[b] at column col of its
-// global act row: as a plain float in act_g, or, when act_t is set, as one
-// 64-bit word (tag << 32 | float bits) in act_t.  Each dot product keeps
-// decode.cu's lane split, fmaf order and butterfly.
+// x rows of the expert's NB tokens (two-plane FP32 in shared memory); one lane
+// per token writes act = silu(gate) * up of assignment asg[b] at column col
+// of its global act row: as a plain float in act_g, or, when act_t is set, as
+// one 64-bit word (tag << 32 | float bits) in act_t.  Each dot product keeps
+// decode.cu's lane split, fmaf order and butterfly (split over the lanes,
+// same pairs and bits).
 template <int NB>
 __device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t *urow, const float *const *xr, int H,
                                              int lane, const int *asg, float *act_g, unsigned long long *act_t,
                                              uint32_t tag, int I, int col)
 {
-    float acc[2 * NB];
+    constexpr int N = pow2_ceil(2 * NB);  // gate of token b in slot b, up in slot NB + b
+    float acc[N];
 #pragma unroll
-    for (int q = 0; q < 2 * NB; ++q) acc[q] = 0.0f;
+    for (int q = 0; q < N; ++q) acc[q] = 0.0f;
 #pragma unroll 4
     for (int h = lane * 8; h < H; h += 256) {
         float gf[8], uf[8];
@@ -226,17 +228,32 @@ __device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t 
             }
         }
     }
-    warp_sum_n(acc);
-    if (lane == 0) {
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const float a = swiglu(acc[b], acc[NB + b]);
-            const size_t at = (size_t)asg[b] * I + col;
-            if (act_t)
-                ptx::st_relaxed_gpu(act_t + at, ((unsigned long long)tag << 32) | __float_as_uint(a));
-            else
-                act_g[at] = a;
-        }
+    // the butterfly's totals: for one token the plain butterfly (every lane
+    // ends with gate and up), for more split over the lanes, where the first
+    // lane of gate slot b fetches up slot NB + b from NB * 32 / N lanes up
+    float t, u;
+    int b;
+    bool writer;
+    if constexpr (NB == 1) {
+        warp_sum_n(acc);
+        t = acc[0];
+        u = acc[1];
+        b = 0;
+        writer = lane == 0;
+    } else {
+        constexpr int W = 32 / N;
+        t = warp_sum_split(acc, lane);
+        u = __shfl_sync(0xffffffffu, t, (lane + NB * W) & 31);
+        b = lane / W;
+        writer = lane % W == 0 && b < NB;
+    }
+    if (writer) {
+        const float a = swiglu(t, u);
+        const size_t at = (size_t)asg[b] * I + col;
+        if (act_t)
+            ptx::st_relaxed_gpu(act_t + at, ((unsigned long long)tag << 32) | __float_as_uint(a));
+        else
+            act_g[at] = a;
     }
 }
 
@@ -245,17 +262,19 @@ __host__ __device__ constexpr int rows_for(int nb) { return nb >= 3 ? 1 : 4 / nb
 
 // Dot products of up to RB W_down rows (rowp, BF16 in shared memory; rows
 // past nu repeat a valid row and are dropped) with the act rows arow[b] of
-// the expert's NB assignments (two-plane FP32 in shared memory).  Lane 0
-// stores row r, assignment b to part[r * A + asg[b]].  Each dot product
-// keeps decode.cu's lane split, fmaf order and butterfly.
+// the expert's NB assignments (two-plane FP32 in shared memory).  One lane
+// per (row r, assignment b) stores it to part[r * A + asg[b]].  Each dot
+// product keeps decode.cu's lane split, fmaf order and butterfly (split over
+// the lanes, same pairs and bits).
 template <int NB>
 __device__ __forceinline__ void down_rows(const uint8_t *const *rowp, const float *const *arow, int I, int lane,
                                           int nu, const int *asg, float *part, int A)
 {
     constexpr int RB = rows_for(NB);
-    float acc[RB * NB];
+    constexpr int N = pow2_ceil(RB * NB);  // row r, assignment b in slot r * NB + b
+    float acc[N];
 #pragma unroll
-    for (int q = 0; q < RB * NB; ++q) acc[q] = 0.0f;
+    for (int q = 0; q < N; ++q) acc[q] = 0.0f;
 #pragma unroll 2
     for (int i = lane * 8; i < I; i += 256) {
         float af[NB][8];
@@ -279,14 +298,12 @@ __device__ __forceinline__ void down_rows(const uint8_t *const *rowp, const floa
                 for (int q = 0; q < 8; ++q) acc[r * NB + b] = fmaf(wf[q], af[b][q], acc[r * NB + b]);
         }
     }
-    warp_sum_n(acc);
-    if (lane == 0) {
-#pragma unroll
-        for (int r = 0; r < RB; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-                if (r < nu) part[r * A + asg[b]] = acc[r * NB + b];
-    }
+    // the butterfly's totals, split over the lanes; the first lane of slot
+    // r * NB + b stores it
+    constexpr int W = 32 / N;
+    const float t = warp_sum_split(acc, lane);
+    const int slot = lane / W, r = slot / NB, b = slot - r * NB;
+    if (lane % W == 0 && slot < RB * NB && r < nu) part[r * A + asg[b]] = t;
 }
 
 template <int NT>
