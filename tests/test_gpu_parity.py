@@ -355,11 +355,15 @@ def test_fused_decode_shared_experts(T, share):
 
 # Fused decode kernel at the edges of its shape range: H = 64 (most CTAs own
 # no output dimension), I = 64, E = 1024 experts, k = 32, and T * k = 64
-# assignments (its maximum).  Compared with the oracle and, bit for bit,
-# with the same tokens through the general decode kernels.
+# assignments (its maximum); and one token on the 2048-hidden geometry (six
+# W_down chunks of 21 rows per CTA, experts crossing chunk boundaries),
+# I = 1024 and I = 320 (a short last 256-element step).  Compared with the
+# oracle and, bit for bit, with the same tokens through the general decode
+# kernels.
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 64, 64, 1024, 32), (1, 128, 64, 40, 1), (4, 64, 128, 64, 16),
                                        (2, 192, 320, 7, 7), (3, 1024, 64, 256, 8),
-                                       (4, 512, 1024, 64, 16)])  # act rows too large to stage: read in place
+                                       (4, 512, 1024, 64, 16),  # act rows too large to stage: read in place
+                                       (1, 2048, 768, 32, 8), (1, 512, 1024, 16, 4), (1, 256, 320, 8, 2)])
 def test_fused_decode_edges(T, H, I, E, k):
     wl = gu.custom(T, H, I, E, k, 1.0, name="fused_edge")
     x, L, wgu, wd = gu.make_layer(wl, T)
