@@ -114,7 +114,7 @@ enum : uint32_t {
 };
 
 // Shared-memory layout: ring | full[slots] | empty[slots] | flag | payload.
-// The payload holds x [T][H] FP32 (phase A) and, in the same space, the act
+// The payload holds x [T][H] BF16 (phase A) and, in the same space, the act
 // rows [T*k][I] FP32 of phase B if they are staged; then part [nh][T*k].
 struct Layout {
     uint32_t full, empty, flag, payload, total;
@@ -137,7 +137,7 @@ __host__ __device__ inline Layout layout(int slots, int slot_bytes, uint32_t pay
 
 __host__ __device__ inline uint32_t xa_bytes(int T, int H, int I, int k, bool act_in_smem)
 {
-    const uint32_t xb = (uint32_t)(4 * T * H), ab = act_in_smem ? (uint32_t)(4 * T * k * I) : 0u;
+    const uint32_t xb = (uint32_t)(2 * T * H), ab = act_in_smem ? (uint32_t)(4 * T * k * I) : 0u;
     return xb > ab ? xb : ab;
 }
 
@@ -196,16 +196,17 @@ __device__ __forceinline__ bool wait_words4(const uint32_t *p, int n, uint32_t v
 }
 
 // Gate and up dot products of one row pair (BF16 in shared memory) with the
-// x rows of the expert's NB tokens (two-plane FP32 in shared memory); one lane
+// x rows of the expert's NB tokens (BF16 in shared memory, widened to FP32
+// exactly); one lane
 // per token writes act = silu(gate) * up of assignment asg[b] at column col
 // of its global act row: as a plain float in act_g, or, when act_t is set, as
 // one 64-bit word (tag << 32 | float bits) in act_t.  Each dot product keeps
 // decode.cu's lane split, fmaf order and butterfly (split over the lanes,
 // same pairs and bits).
 template <int NB>
-__device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t *urow, const float *const *xr, int H,
-                                             int lane, const int *asg, float *act_g, unsigned long long *act_t,
-                                             uint32_t tag, int I, int col)
+__device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t *urow, const uint16_t *const *xr,
+                                             int H, int lane, const int *asg, float *act_g,
+                                             unsigned long long *act_t, uint32_t tag, int I, int col)
 {
     constexpr int N = pow2_ceil(2 * NB);  // gate of token b in slot b, up in slot NB + b
     float acc[N];
@@ -218,9 +219,8 @@ __device__ __forceinline__ void gate_up_pair(const uint8_t *grow, const uint8_t 
         unpack8(lds16(urow + 2 * h), uf);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const float4 x0 = *reinterpret_cast<const float4 *>(xr[b] + h / 2);
-            const float4 x1 = *reinterpret_cast<const float4 *>(xr[b] + H / 2 + h / 2);
-            const float xf[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            float xf[8];
+            unpack8(lds16(xr[b] + h), xf);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 acc[b] = fmaf(gf[q], xf[q], acc[b]);
@@ -322,11 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(sm + L.empty);
     volatile int *flag = reinterpret_cast<volatile int *>(sm + L.flag);
-    // x in FP32, two planes per token row: element 8u+e sits in plane e/4 at
-    // 4u + e%4, so a lane's 8 consecutive elements are two float4 loads that
-    // are contiguous across the warp (no bank conflicts, no unpacking)
-    float *xs = reinterpret_cast<float *>(sm + L.payload);
-    float *abuf = xs;  // phase B: act of all assignments [A][I]
+    // x as BF16 rows: a lane's 8 consecutive elements are one 16-byte load,
+    // contiguous across the warp
+    uint16_t *xs = reinterpret_cast<uint16_t *>(sm + L.payload);
+    float *abuf = reinterpret_cast<float *>(sm + L.payload);  // phase B: act of all assignments [A][I]
     float *part = reinterpret_cast<float *>(sm + L.payload + xa);          // [nh][A]
     __shared__ int s_sel[kMaxAsg], s_asg[kMaxAsg], s_uexp[kMaxAsg], s_ubeg[kMaxAsg + 1], s_U;
     __shared__ int8_t s_rlog[kMaxAsg];  // per touched expert: log2 of the phase B rows per task
@@ -521,14 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int ct = threadIdx.x - 32, n_ct = kConsumers * 32;
     const int cw = warp - 1;
-    for (int v = ct; v < T * H / 8; v += n_ct) {  // x of all tokens, two planes per row
-        const int t = v / (H / 8), uh = v - t * (H / 8);
-        float f[8];
-        unpack8(ld_nc16(x + (size_t)v * 8), f);
-        float *row = xs + (size_t)t * H;
-        *reinterpret_cast<float4 *>(row + 4 * uh) = make_float4(f[0], f[1], f[2], f[3]);
-        *reinterpret_cast<float4 *>(row + H / 2 + 4 * uh) = make_float4(f[4], f[5], f[6], f[7]);
-    }
+    for (int v = ct; v < T * H / 8; v += n_ct)  // x of all tokens, 16 bytes at a time
+        reinterpret_cast<uint4 *>(xs)[v] = ld_nc16(x + (size_t)v * 8);
     ptx::named_sync(1, n_ct);
 
     // phase A: for each pair, gate and up dot products with every token of
@@ -549,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int m = first_task(pos, cw);
             if (m < n) {  // every warp walks every chunk: set up only with work
                 const int a0 = s_ubeg[u], na = s_ubeg[u + 1] - a0;  // 1 <= na <= T <= NT
-                const float *xr[NT];
+                const uint16_t *xr[NT];
 #pragma unroll
                 for (int b = 0; b < NT; ++b) xr[b] = xs + s_xoff[a0 + (b < na ? b : 0)];
                 for (; m < n; m += kConsumers) {
