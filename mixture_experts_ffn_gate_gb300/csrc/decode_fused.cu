@@ -345,16 +345,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         *flag = 0;
         ptx::fence_barrier_init();
     }
-    // this call's epoch and exchange mode, from words that no CTA changes
-    // before every CTA has read them
+    // this call's epoch and exchange mode come from words that no CTA
+    // changes before every CTA has read them: thread 0 (not a routing warp)
+    // reads them while the tokens are routed and shares them through shared
+    // memory after the barrier that ends the routing
     const volatile unsigned long long *vflags = flags;
-    const unsigned long long calls = vflags[kCallWord];
-    const uint32_t e32 = (uint32_t)(epoch_salt + 2 * calls);
-    const bool tag_region = act_in_smem && act_t;  // this call may use, or prepare, the tag region
-    const bool tagged = tag_region && vflags[kCheckWord] == (kCheckKey ^ (unsigned long long)flags) &&
-                        vflags[kSizeWord] >= (unsigned long long)(T * k) * I;
-    uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
-    if (tagged && threadIdx.x == 0) ptx::st_relaxed_gpu(arrive + blockIdx.x, e32);  // "read the counter"
+    __shared__ unsigned long long s_flags[3];  // call counter, check word, size word
+    if (threadIdx.x == 0) {
+        s_flags[0] = vflags[kCallWord];
+        s_flags[1] = vflags[kCheckWord];
+        s_flags[2] = vflags[kSizeWord];
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // routing: consumer warp 1 + t routes token t (scratch: the ring)
@@ -423,6 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x < A) s_xoff[threadIdx.x] = s_asg[threadIdx.x] / k * H;
     __syncthreads();
+
+    const unsigned long long calls = s_flags[0];
+    const uint32_t e32 = (uint32_t)(epoch_salt + 2 * calls);
+    const bool tag_region = act_in_smem && act_t;  // this call may use, or prepare, the tag region
+    const bool tagged = tag_region && s_flags[1] == (kCheckKey ^ (unsigned long long)flags) &&
+                        s_flags[2] >= (unsigned long long)(T * k) * I;
+    uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
+    if (tagged && threadIdx.x == 0) ptx::st_relaxed_gpu(arrive + blockIdx.x, e32);  // "read the counter"
 
     // Phase A: pairs [lo, hi) of the U*I, pair p = (expert p / I, index p % I),
     // in chunks of at most rpc pairs that never cross an expert.  Phase B:
@@ -605,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         flags[kCallWord] = calls + 1;
         if (tag_region && !stop) {
             const unsigned long long key = kCheckKey ^ (unsigned long long)flags;
-            const unsigned long long had = vflags[kCheckWord] == key ? vflags[kSizeWord] : 0ull;
+            const unsigned long long had = s_flags[1] == key ? s_flags[2] : 0ull;
             flags[kSizeWord] = had > (unsigned long long)nact ? had : (unsigned long long)nact;
             flags[kCheckWord] = key;
         }
