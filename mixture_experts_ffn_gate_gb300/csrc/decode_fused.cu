@@ -16,7 +16,8 @@
 //     For a run of pairs of one expert both row blocks are contiguous in
 //     memory: the producer warp copies them into one ring slot (two bulk
 //     copies), the consumer warps take the pairs round-robin, form both dot
-//     products with every token the expert serves (x in FP32) and write
+//     products with every token the expert serves (x staged in shared memory
+//     as BF16, widened to FP32 at use) and write
 //     act = silu(gate) * up per assignment to global memory, in the two-plane
 //     order phase B keeps in shared memory;
 //   - the producer goes straight on to the CTA's W_down rows (dims
