@@ -158,6 +158,15 @@ __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Programmatic dependent launch: let the next launch on the stream be
+// scheduled; wait until the previous launch has completed and its writes are
+// visible (returns at once when the kernel was not launched as a dependent).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long *p)
 {
     unsigned long long v;
