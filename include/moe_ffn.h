@@ -42,6 +42,13 @@
  *     replays recompute from the captured buffers' current contents.
  *   - Launch failures are returned as MOE_ERR_CUDA (cudaPeekAtLastError);
  *     faults during execution surface at the caller's next synchronisation.
+ *   - The fused decode kernel (T <= 4) is launched as a programmatic
+ *     dependent (cudaLaunchAttributeProgrammaticStreamSerialization): it
+ *     waits for the preceding work on `stream` to complete before it reads
+ *     anything, and lets the following launch be scheduled early; a kernel
+ *     the caller launches after it with that attribute must, as programmatic
+ *     dependent launch requires, call griddepcontrol.wait
+ *     (cudaGridDependencySynchronize) before reading this call's outputs.
  *   - Results are deterministic: for the same inputs, path and device the
  *     output bits do not change from run to run or with the launch knobs in
  *     moe_ffn_opts.  The two paths (decode, grouped) are each deterministic
