@@ -101,6 +101,12 @@ constexpr int kMinSlots = 5;          // ring slots the kernel needs (measured: 
 // layers at four tokens (about 31 experts) run 4% and 7.6% faster, while at
 // 8 and 16 experts the rotation gains nothing.
 constexpr int kRotateAbove = 16;
+// Tagged act words (16 bytes each) a consumer thread polls per batch, for up
+// to two tokens and for more: under the weight stream an L2 round trip takes
+// 1-2 us, so the fewer batches the better; 16 cover two tokens' 2 x 8 x 768
+// act values of the 2048-hidden layer in one batch, and the four-token
+// instance keeps 8 (16 would spill there).
+constexpr int kPollWordsFew = 16, kPollWordsMany = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
@@ -643,22 +649,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs and chunks.  First every assignment's act row into shared memory.
     {
         if (tagged) {
-            // each thread takes 16-byte words (two tagged values) eight at a
-            // time and re-reads the ones that do not yet carry the epoch
+            // each thread takes 16-byte words (two tagged values) kPollWords
+            // at a time and re-reads the ones that do not yet carry the epoch
+            constexpr int kPollWords = NT <= 2 ? kPollWordsFew : kPollWordsMany;
             const int nw = nact / 2;
             const uint64_t t_start = ptx::globaltimer_ns();
-            for (int v0 = ct; v0 < nw; v0 += 8 * n_ct) {
+            for (int v0 = ct; v0 < nw; v0 += kPollWords * n_ct) {
                 uint32_t need = 0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < kPollWords; ++j)
                     if (v0 + j * n_ct < nw) need |= 1u << j;
                 for (uint32_t spin = 0; need; ++spin) {
-                    ulonglong2 w[8];
+                    ulonglong2 w[kPollWords];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < kPollWords; ++j)
                         if ((need >> j) & 1u) w[j] = ptx::ld_relaxed_gpu_v2u64(act_t + 2 * (size_t)(v0 + j * n_ct));
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < kPollWords; ++j)
                         if (((need >> j) & 1u) && (uint32_t)(w[j].x >> 32) == e32 && (uint32_t)(w[j].y >> 32) == e32) {
                             need &= ~(1u << j);
                             reinterpret_cast<float2 *>(abuf)[v0 + j * n_ct] =
