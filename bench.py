@@ -21,6 +21,15 @@ dominant kernel.  cold_call times single calls after an L2 flush each.  e2e
 repeats the steps through the host-buffer entry point, called step by step
 from Python (pinned inputs copied in, output copied out, inside the region).
 
+After the headline line's figures (at one GPU), every other configuration
+of the layer the metric names (the 2048-hidden decode layer at T=2, the
+4096-hidden one at T=1/4/16/64, the 7168-hidden one at T=1/8/32 and the
+T=2048 training-size forward) is measured the same way, W warm-up and K
+timed steps each over its own layers' weights drawn on the GPU, and reported
+in the line's "supplementary" array: us per call, tokens/s, the whole
+call's HBM fraction, the dominant kernel's roofline and the TFLOP/s against
+dense BF16 peak and against min(peak, HBM peak x flop/byte).
+
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
 """
@@ -78,6 +87,8 @@ def parse():
                    help="launch every step from Python instead of replaying a CUDA graph of the steps")
     p.add_argument("--cold-steps", type=int, default=200,
                    help="single calls timed after an L2 flush each (secondary figure)")
+    p.add_argument("--no-supplementary", action="store_true",
+                   help="omit the other configurations' rows (measured after the headline line)")
     return p.parse_args()
 
 
@@ -322,6 +333,225 @@ def cpu_model():
     return platform.machine()
 
 
+# Every other configuration the metric names, measured by the same command
+# after the headline line: a short timed run each (weights drawn on the GPU,
+# no oracle timing), reported in the line's "supplementary" array.
+SUPPLEMENTARY = [
+    ("decode_h2048_i768_e128_k8", (2,)),
+    ("decode_h4096_i1536_e128_k8_bias", (1, 4, 16, 64)),
+    ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
+    ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),
+]
+
+
+def layer_count(wl, T, layers_arg):
+    """Layers' weights the steps cycle through: enough that the weights one
+    step reads were streamed out of L2 by the steps in between."""
+    touched = algorithmic_bytes(wl, T, min(wl.E, T * wl.k))
+    R = max(2, math.ceil(3 * L2_BYTES / touched)) if layers_arg is None else layers_arg
+    return max(1, min(R, int(LAYER_MEM_CAP // wl.weight_bytes()))), touched
+
+
+class Measure:
+    """One workload at one T on this rank: the steps cycle through the given
+    layers' weights over fresh token batches on one workspace.  timed() runs
+    W warm-up steps and times K steps as one CUDA-graph replay (or eager
+    launches); stages() replays them with the library's stage events between
+    kernels; summary() gives the figures of one line."""
+
+    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager):
+        import torch
+        from mixture_experts_ffn_gate_gb300 import moe_ffn as m
+        from mixture_experts_ffn_gate_gb300 import synth
+        self.m, self.torch = m, torch
+        self.wl, self.T, self.dev, self.K, self.W = wl, T, dev, K, W
+        self.path_code, self.layers, self.R = path_code, layers, len(layers)
+        self.eager = eager
+        batch_bytes = T * (wl.H * 2 + wl.E * 4)
+        self.NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
+        calls = rank_calls(rank, W, K)   # rank r processes its own calls of the token stream
+        self.batches = [synth.make_tokens(wl, T, call=calls[i], device=dev, bias=bias)
+                        for i in range(self.NB)]
+        self.ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
+        self.out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream()
+        probe = self.new_opts()
+        self.call(0, self.stream, probe)
+        self.path, self.n_stages = probe.path_taken, probe.n_stages
+        self.stage_names = [m.moe_ffn_stage_name(self.path, s) for s in range(self.n_stages)]
+        # unique experts touched per step (routing of each batch, untimed)
+        idx_buf = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
+        U_of = {}
+        for j in range(W, W + K):
+            if j % self.NB not in U_of:
+                self.call(j, self.stream, None, idx_buf)
+                U_of[j % self.NB] = int(torch.unique(idx_buf).numel())
+        self.U = [U_of[j % self.NB] for j in range(W, W + K)]
+        torch.cuda.synchronize()
+        if not eager:
+            self.g_warm = self.capture(range(W))
+            self.g_main = self.capture(range(W, W + K))
+
+    def new_opts(self):
+        o = self.m.moe_ffn_opts()
+        o.path = self.path_code
+        return o
+
+    def call(self, j, stream, opts=None, idx=None):
+        x, L = self.batches[j % self.NB]
+        lw_gu, lw_d = self.layers[j % self.R]
+        self.m.moe_ffn_forward_ex(x, L, lw_gu, lw_d, self.wl.k, out=self.out, workspace=self.ws,
+                                  topk_idx=idx, opts=opts if opts is not None else self.new_opts(),
+                                  stream=stream)
+
+    def capture(self, steps, events=None):
+        """One CUDA graph holding the calls of `steps`, in order."""
+        torch, m = self.torch, self.m
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            s = torch.cuda.current_stream()
+            for n, j in enumerate(steps):
+                o = self.new_opts()
+                if events is not None:
+                    o.stage_events = m.ctypes.cast(events[n], m.ctypes.c_void_p)
+                self.call(j, s, o)
+        return g
+
+    def timed(self, world):
+        """W untimed warm-up steps, then the K timed steps between a barrier,
+        device synchronisation and CUDA events on the launching stream.
+        Returns (ms for the K steps, host wall seconds)."""
+        torch = self.torch
+        import torch.distributed as dist
+        W, K = self.W, self.K
+        if self.eager:
+            for j in range(W):
+                self.call(j, self.stream)
+        else:
+            self.g_warm.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        mark0 = torch.cuda.Event(enable_timing=True)
+        mark1 = torch.cuda.Event(enable_timing=True)
+        t_wall = time.perf_counter()
+        mark0.record(self.stream)
+        if self.eager:
+            for j in range(W, W + K):
+                self.call(j, self.stream)
+        else:
+            self.g_main.replay()
+        mark1.record(self.stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+        if world > 1:
+            dist.barrier()
+        return mark0.elapsed_time(mark1), wall
+
+    def stages(self):
+        """Mean ms of each kernel over the K steps, from the library's stage
+        events (captured as event-record nodes when graphs are used)."""
+        torch, m = self.torch, self.m
+        K, W = self.K, self.W
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
+               for _ in range(K)]
+        arrs = []
+        for j in range(K):
+            for e in evs[j]:
+                e.record(self.stream)
+            arrs.append(m.stage_event_array(evs[j]))
+        torch.cuda.synchronize()
+        if self.eager:
+            for j in range(K):
+                o = self.new_opts()
+                o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
+                self.call(W + j, self.stream, o)
+        else:
+            g = self.capture(range(W, W + K), arrs)
+            g.replay()
+        torch.cuda.synchronize()
+        return {name: sum(evs[j][s].elapsed_time(evs[j][s + 1]) for j in range(K)) / K
+                for s, name in enumerate(self.stage_names)}
+
+    def summary(self, total_ms, kern_avg, peaks, world):
+        """Throughput, the whole call's HBM fraction, the dominant kernel's
+        roofline and the tensor figures of one workload line."""
+        wl, T, K = self.wl, self.T, self.K
+        call_bytes = sum(algorithmic_bytes(wl, T, u) for u in self.U) / K
+        flops = 6.0 * wl.H * wl.I * T * wl.k
+        ms_call = total_ms / K
+        # dominant kernel = largest share of the per-kernel pass.  When a step
+        # is a single kernel, its launches are the timed region itself, so
+        # their mean duration is at most the timed region / K; the
+        # stage-event replay (event nodes between launches) would charge the
+        # event overhead to it.
+        dom = max(kern_avg, key=kern_avg.get)
+        one_kernel = len(kern_avg) == 1
+        dom_ms = ms_call if one_kernel else kern_avg[dom]
+        dom_bytes = sum(kernel_bytes(dom, wl, T, u, wl.k) for u in self.U) / K
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": stored_traffic(dom, wl.name, T),
+                    "peak_source": f"{peaks['source']} HBM copy (burst)",
+                    "algorithmic_bytes_per_launch": dom_bytes,
+                    "kernel_time": ("timed region / K (one kernel per step)" if one_kernel
+                                    else "stage events between kernels, CUDA-graph replay"),
+                    "kernel_us": {n: round(1e3 * v, 3) for n, v in kern_avg.items()}}
+        gbs = call_bytes / (ms_call / 1e3) / 1e9
+        tflops = flops / (ms_call / 1e3) / 1e12
+        intensity = flops / call_bytes
+        attainable = min(peaks["bf16_tflops"], peaks["hbm_gbs"] * 1e9 * intensity / 1e12)
+        return {
+            "value": whole_job_tokens_per_s(T, K, world, total_ms),
+            "ms_per_step": ms_call,
+            "path": {1: "decode", 2: "grouped", 3: "decode_fused"}.get(self.path, self.path),
+            "roofline": roofline,
+            "call_hbm": {"achieved_gbs": gbs, "frac_of_measured": gbs / peaks["hbm_gbs"],
+                         "frac_of_8tbs_spec": gbs / 8000.0, "bytes_per_call": call_bytes,
+                         "unique_experts_mean": sum(self.U) / K},
+            "tensor": {"tflops": tflops, "frac_of_dense_bf16_peak": tflops / peaks["bf16_tflops"],
+                       "flop_per_byte": intensity, "attainable_tflops": attainable,
+                       "frac_of_attainable": tflops / attainable,
+                       "attainable": "min(dense BF16 peak, measured HBM copy peak x flop/byte)"},
+        }
+
+
+def supplementary_rows(args, dev, peaks, skip):
+    """The other configurations, one short timed run each (W warm-up and K
+    timed steps as for the headline line); weights are shared by the T of a
+    workload and freed before the next workload."""
+    import gc
+
+    import torch
+    from mixture_experts_ffn_gate_gb300 import synth
+    rows = []
+    for name, Ts in SUPPLEMENTARY:
+        wl = synth.WORKLOADS[name]
+        Ts = [T for T in Ts if (name, T) != skip]
+        if not Ts:
+            continue
+        R = max(layer_count(wl, T, args.layers)[0] for T in Ts)
+        layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
+        bias = synth.make_bias(wl)
+        for T in Ts:
+            run = Measure(wl, T, dev, args.steps, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
+                args.path], layers, bias, 0, args.eager)
+            with ClockSampler(dev.index or 0) as clocks:
+                total_ms, _ = run.timed(1)
+                kern = run.stages()
+            row = {"workload": name, "T": T, "layers": R}
+            row.update(run.summary(total_ms, kern, peaks, 1))
+            row["clocks"] = clocks.summary()
+            rows.append(row)
+            del run
+        del layers
+        gc.collect()
+        torch.cuda.empty_cache()
+    return rows
+
+
 def main():
     args = parse()
     from mixture_experts_ffn_gate_gb300 import synth
@@ -354,22 +584,13 @@ def main():
     dev = torch.device("cuda", local)
     K, W = args.steps, max(3, args.warmup)
     bias = synth.make_bias(wl)
-    # Steps run back to back over R layers' weights (step j uses layer j % R),
-    # R chosen so that the weights one step reads were streamed out of L2 by
-    # the steps in between: the inputs are larger than L2 and no step finds
-    # its weights there.  Token batches are fresh per step (cycled past NB).
-    touched = algorithmic_bytes(wl, T, min(wl.E, T * wl.k))
-    R = max(2, math.ceil(3 * L2_BYTES / touched)) if args.layers is None else args.layers
-    R = max(1, min(R, int(LAYER_MEM_CAP // wl.weight_bytes())))
+    R, touched = layer_count(wl, T, args.layers)
     layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
     wgu, wd = layers[0]
-    batch_bytes = T * (wl.H * 2 + wl.E * 4)
-    NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
-    # rank r processes its own calls of the token stream
-    calls = rank_calls(rank, W, K)
-    batches = [synth.make_tokens(wl, T, call=calls[i], device=dev, bias=bias) for i in range(NB)]
-    ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
-    out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
+    path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
+                 "grouped": m.MOE_PATH_GROUPED}[args.path]
+    run = Measure(wl, T, dev, K, W, path_code, layers, bias, rank, args.eager)
+    stream = run.stream
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sum = torch.empty((), dtype=torch.float32, device=dev)
 
@@ -381,100 +602,9 @@ def main():
         if args.flush == "write+read":
             torch.sum(flush[: FLUSH_BYTES // 8], dim=0, out=flush_sum)
 
-    path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
-                 "grouped": m.MOE_PATH_GROUPED}[args.path]
-
-    def new_opts():
-        o = m.moe_ffn_opts()
-        o.path = path_code
-        return o
-
-    def call(j, stream, opts=None, idx=None):
-        x, L = batches[j % NB]
-        lw_gu, lw_d = layers[j % R]
-        m.moe_ffn_forward_ex(x, L, lw_gu, lw_d, wl.k, out=out, workspace=ws, topk_idx=idx,
-                             opts=opts if opts is not None else new_opts(), stream=stream)
-
-    stream = torch.cuda.current_stream()
-    probe = new_opts()
-    call(0, stream, probe)
-    path, n_stages = probe.path_taken, probe.n_stages
-    stage_names = [m.moe_ffn_stage_name(path, s) for s in range(n_stages)]
-
-    # unique experts touched per step (routing of each batch, untimed)
-    idx_buf = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
-    U_of = {}
-    for j in range(W, W + K):
-        if j % NB not in U_of:
-            call(j, stream, None, idx_buf)
-            U_of[j % NB] = int(torch.unique(idx_buf).numel())
-    U = [U_of[j % NB] for j in range(W, W + K)]
-    torch.cuda.synchronize()
-
-    def capture(steps, events=None):
-        """One CUDA graph holding the calls of `steps`, in order."""
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, capture_error_mode="thread_local"):
-            s = torch.cuda.current_stream()
-            for n, j in enumerate(steps):
-                o = new_opts()
-                if events is not None:
-                    o.stage_events = m.ctypes.cast(events[n], m.ctypes.c_void_p)
-                call(j, s, o)
-        return g
-
-    use_graph = not args.eager
-    if use_graph:
-        g_warm = capture(range(W))
-        g_main = capture(range(W, W + K))
-    mark0 = torch.cuda.Event(enable_timing=True)
-    mark1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
-        # warm-up: W untimed steps
-        if use_graph:
-            g_warm.replay()
-        else:
-            for j in range(W):
-                call(j, stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter()
-        mark0.record(stream)
-        if use_graph:
-            g_main.replay()
-        else:
-            for j in range(W, W + K):
-                call(j, stream)
-        mark1.record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t_wall
-        if world > 1:
-            dist.barrier()
-        total_ms = mark0.elapsed_time(mark1)
-
-        # per-kernel pass over the same steps: the library's stage events
-        # between kernels (captured as event-record nodes when graphs are used)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
-               for _ in range(K)]
-        arrs = []
-        for j in range(K):
-            for e in evs[j]:
-                e.record(stream)
-            arrs.append(m.stage_event_array(evs[j]))
-        torch.cuda.synchronize()
-        if use_graph:
-            g_stage = capture(range(W, W + K), arrs)
-            g_stage.replay()
-        else:
-            for j in range(K):
-                o = new_opts()
-                o.stage_events = m.ctypes.cast(arrs[j], m.ctypes.c_void_p)
-                call(W + j, stream, o)
-        torch.cuda.synchronize()
-        kern_ms = {name: [evs[j][s].elapsed_time(evs[j][s + 1]) for j in range(K)]
-                   for s, name in enumerate(stage_names)}
+        total_ms, wall = run.timed(world)
+        kern_avg = run.stages()
 
         # cold single calls: L2 flushed before each, each between its own events
         n_cold = min(K, args.cold_steps)
@@ -483,7 +613,7 @@ def main():
         for j in range(n_cold):
             do_flush(j)
             c_starts[j].record(stream)
-            call(W + j, stream)
+            run.call(W + j, stream)
             c_ends[j].record(stream)
         torch.cuda.synchronize()
         cold_ms = [s.elapsed_time(e) for s, e in zip(c_starts, c_ends)]
@@ -492,15 +622,18 @@ def main():
         # (pinned inputs copied in and the output copied out inside the region)
         e2e = None
         if not args.no_e2e:
-            xh = [b[0].cpu().pin_memory() for b in batches]
-            lh = [b[1].cpu().pin_memory() for b in batches]
+            NB = run.NB
+            xh = [b[0].cpu().pin_memory() for b in run.batches]
+            lh = [b[1].cpu().pin_memory() for b in run.batches]
             oh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
             wsh = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev, host=True)
 
             def host_call(j):
                 lw_gu, lw_d = layers[j % R]
                 m.moe_ffn_forward_host(xh[j % NB], lh[j % NB], lw_gu, lw_d, wl.k, oh, wsh,
-                                       opts=new_opts(), stream=stream)
+                                       opts=run.new_opts(), stream=stream)
+            mark0 = torch.cuda.Event(enable_timing=True)
+            mark1 = torch.cuda.Event(enable_timing=True)
             for j in range(W):
                 host_call(j)
             torch.cuda.synchronize()
@@ -519,57 +652,31 @@ def main():
         return
 
     peaks = load_peaks()
-    tokens = T * K * world
-    value = whole_job_tokens_per_s(T, K, world, total_ms)
-    mean_U = sum(U) / len(U)
-    call_bytes = sum(algorithmic_bytes(wl, T, u) for u in U) / K
-    flops = 6.0 * wl.H * wl.I * T * wl.k
-    # dominant kernel = largest share of the per-kernel pass.  When a step is
-    # a single kernel, its launches are the timed region itself, so their
-    # mean duration is at most the timed region / K; the stage-event replay
-    # (event nodes between launches) would charge the event overhead to it.
-    kern_avg = {n: sum(v) / len(v) for n, v in kern_ms.items()}
-    dom = max(kern_avg, key=kern_avg.get)
-    one_kernel = len(kern_avg) == 1
-    dom_ms = total_ms / K if one_kernel else kern_avg[dom]
-    dom_bytes = sum(kernel_bytes(dom, wl, T, u, wl.k) for u in U) / K
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    traffic = stored_traffic(dom, wl.name, T)
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                "peak_source": f"{peaks['source']} HBM copy (burst)",
-                "algorithmic_bytes_per_launch": dom_bytes,
-                "kernel_time": ("timed region / K (one kernel per step)" if one_kernel
-                                else "stage events between kernels, CUDA-graph replay"),
-                "kernel_us": {n: round(1e3 * v, 3) for n, v in kern_avg.items()}}
-    whole_call_gbs = call_bytes / (total_ms / K / 1e3) / 1e9
+    head = run.summary(total_ms, kern_avg, peaks, world)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "path": {1: "decode", 2: "grouped"}.get(path, path),
+                   "path": head["path"],
                    "layers": R,
                    "l2": (f"inputs larger than L2: {R} layers' weights "
                           f"({R * wl.weight_bytes() / 1e9:.1f} GB) cycled step by step, "
                           f"{touched / 1e6:.0f} MB read per step at most, fresh tokens per step"),
-                   "timing": ("CUDA graph of the K steps replayed once" if use_graph
-                              else "the K steps launched from Python")
+                   "timing": ("the K steps launched from Python" if args.eager
+                              else "CUDA graph of the K steps replayed once")
                              + ", CUDA events before and after on the launching stream",
                    "parallelism": f"replicas x{world} (independent token streams)"},
-        "roofline": roofline,
-        "call_hbm": {"achieved_gbs": whole_call_gbs, "frac_of_measured": whole_call_gbs / peaks["hbm_gbs"],
-                     "frac_of_8tbs_spec": whole_call_gbs / 8000.0, "bytes_per_call": call_bytes,
-                     "unique_experts_mean": mean_U},
-        "tensor": {"tflops": flops / (total_ms / K / 1e3) / 1e12,
-                   "frac_of_dense_bf16_peak": flops / (total_ms / K / 1e3) / 1e12 / peaks["bf16_tflops"]},
+        "roofline": head["roofline"],
+        "call_hbm": head["call_hbm"],
+        "tensor": head["tensor"],
         "cold_call": {"us_median": 1e3 * statistics.median(cold_ms), "us_mean": 1e3 * sum(cold_ms) / n_cold,
                       "calls": n_cold,
                       "method": (f"L2 flushed before each call ({FLUSH_BYTES >> 20} MB write"
                                  + (f", then {FLUSH_BYTES >> 21} MB read" if args.flush == "write+read" else "")
                                  + "), each call between its own CUDA events")},
-        "gpu_launches": n_stages * K,
-        "stages": stage_names,
+        "gpu_launches": run.n_stages * K,
+        "stages": run.stage_names,
         "wall_s": wall,
     }
     if e2e is not None:
@@ -579,6 +686,10 @@ def main():
     line["clocks"] = clocks.summary()
     if world == 1 and not args.skip_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T, wgu, wd, bias)
+    if world == 1 and not args.no_supplementary:
+        del run, layers, wgu, wd, flush
+        torch.cuda.empty_cache()
+        line["supplementary"] = supplementary_rows(args, dev, peaks, skip=(wl.name, T))
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

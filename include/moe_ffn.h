@@ -101,7 +101,16 @@ typedef struct moe_ffn_opts {
     int32_t gate_up_warps;     /* decode gate_up: warps per block, 1..16 (default 8) */
     int32_t down_warps;        /* decode down: warps per block, 1..16 (default 8) */
     int32_t gemm_ctas;         /* grouped GEMMs: persistent CTAs (default: one per SM) */
-    int32_t reserved_in[3];    /* must be zero */
+    /* Test hooks of the fused decode kernel (MOE_PATH_DECODE_FUSED calls
+     * only; ignored by the other kernels).  test_wait_limit_us bounds each
+     * of its device-side waits (0: 2 s).  test_skip_arrival != 0 makes its
+     * last CTA skip its arrival at the grid barrier, so that the barrier's
+     * bounded waits run out: the call then writes no output and sets its
+     * bit in the device fault word (moe_ffn_device_faults), and the next
+     * call on the workspace is correct.  Leave both at zero in production. */
+    int32_t test_wait_limit_us;
+    int32_t test_skip_arrival;
+    int32_t reserved_in[1];    /* must be zero */
     /* nullable: MOE_MAX_STAGES + 1 created events.  When set, the call
      * records stage_events[0] before its first kernel and stage_events[i+1]
      * after kernel i, on `stream`, so the caller can time each kernel with
@@ -110,6 +119,11 @@ typedef struct moe_ffn_opts {
      * Recording events between kernels can change how they overlap, so time
      * whole calls without it. */
     cudaEvent_t *stage_events;
+    /* nullable DEVICE int32: a call that takes MOE_PATH_DECODE_FUSED stores
+     * (asynchronously, on `stream`) how its CTAs exchanged the act rows:
+     * 1 = at a grid barrier (which prepares the workspace's tagged state),
+     * 2 = through tagged words, without a barrier.  Other paths leave it. */
+    int32_t *exchange_out;
     /* outputs */
     int32_t n_stages;          /* kernels the call enqueued */
     int32_t path_taken;        /* MOE_PATH_DECODE, _DECODE_FUSED or _GROUPED */
@@ -139,18 +153,24 @@ size_t moe_ffn_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E,
  * The forward pass with a caller-owned workspace (256-byte aligned, at least
  * moe_ffn_workspace_bytes), optional routing outputs and options.  With a
  * workspace the call allocates nothing and is reentrant; two calls that
- * share a workspace must be ordered on one stream.  The workspace needs no
- * initialisation, and any memory (whatever it held before) can become one.
- * The library keeps state in it between calls (the decode path for T <= 4
- * keeps a call counter and tagged scratch there, at offsets that depend only
- * on k and I, so calls with any T may share it): do not write to it while it
- * serves as a workspace.  A workspace's first decode call for a given shape
- * meets at a grid barrier and prepares that state; later ones skip the
- * barrier.
+ * share a workspace must be ordered on one stream.  The library keeps state in it between calls: the decode path for T <= 4
+ * keeps a call counter and tagged scratch at its start.  Calls of any shape
+ * may share a workspace (if it is large enough for each): every call lowers
+ * the state's record of how much scratch is prepared to what its own other
+ * data leave untouched, so a decode call trusts only scratch that no call
+ * has overwritten since a barrier call cleared it.  A decode call whose
+ * scratch is not prepared meets at a grid barrier and prepares it; the
+ * following ones of that shape skip the barrier.  Memory that never served
+ * as a workspace needs no initialisation.  Do not write to a workspace
+ * between its calls; if its memory holds other data in between (lent to
+ * another use, or freed and allocated again), zero its first
+ * MOE_FFN_WORKSPACE_STATE_BYTES bytes (e.g. cudaMemsetAsync on `stream`)
+ * before its next call, which discards the state.
  *   topk_idx_out  nullable int32 [T,k]: the chosen experts, slot order.
  *   topk_w_out    nullable float [T,k]: their softmax weights.
  *   opts          nullable; see moe_ffn_opts.
  */
+#define MOE_FFN_WORKSPACE_STATE_BYTES ((size_t)16384)
 int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32,
                        const void *w_gate_up_bf16, const void *w_down_bf16,
                        int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
@@ -166,7 +186,8 @@ int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32,
  * the forward pass and the device->host copy of the output on `stream`;
  * out_host is valid after the stream is synchronised.  The workspace
  * (device, at least moe_ffn_host_workspace_bytes) also holds the staged
- * inputs and output.  When the three host buffers are page-locked and mapped
+ * inputs and output, and keeps the same state, under the same rules, as
+ * moe_ffn_forward_ex's.  When the three host buffers are page-locked and mapped
  * (cudaHostAlloc, cudaMallocHost, torch's pin_memory), 16-byte aligned and
  * at most 1 MiB together, the kernels read the inputs and write the output
  * in place through the host link instead (no separate copies; same
@@ -194,7 +215,8 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host,
  * allocates nothing.  Shapes whose workspace (moe_ffn_workspace_bytes)
  * exceeds that size return MOE_ERR_WORKSPACE_TOO_SMALL before anything is
  * enqueued.  The first call on each device looks up the array's device
- * address (set-up, once per device, with that device current); make that
+ * address (set-up, once per device, with that device current, and again if
+ * the device's context changes, e.g. after cudaDeviceReset); make that
  * first call before any stream capture.  All calls share the array: calls
  * whose GPU work overlaps (other streams, unordered host threads) race and
  * return wrong results, so order them on one stream.  The array serves as

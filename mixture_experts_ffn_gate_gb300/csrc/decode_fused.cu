@@ -62,12 +62,20 @@
 //     stores) until all carry the epoch: the data is its own flag, one hop
 //     instead of the barrier's two plus the copy.  Every CTA stores the epoch
 //     in its arrival word at its start; CTA 0's producer warp advances the
-//     counter once all have.  A tag region is used only after a barrier call
-//     on the same flags array has zeroed it and set the check word (a key
-//     xor the flags address) and the size word, so its words hold zeros or
-//     tags of earlier calls, which never equal the epoch (zero cannot: the
-//     epoch is odd).  Memory that held other data thus never stands in for
-//     an act value; only the check word could match by chance (2^-64).
+//     counter once all have.  A call trusts its T*k*I words of the tag
+//     region only when the check word (a key xor the flags address) is set
+//     and the size word is at least T*k*I.  The size word counts the leading
+//     words of the region that hold nothing but zeros and tags of earlier
+//     calls, which never equal the epoch (zero cannot: the epoch is odd):
+//     a barrier call zeroes its T*k*I words before it raises the size word
+//     to cover them, and every call on the workspace lowers the size word
+//     to its tag_cap, the words of the region before the call's first other
+//     region, because a call with a smaller k*I places its routing, act or
+//     gathered rows inside the region of a larger one (this kernel does so
+//     in CTA 0 once every CTA has read the flags; the other paths' router
+//     kernel before anything else).  So memory that held other data never
+//     stands in for an act value, whatever shapes share the workspace; only
+//     the check word could match by chance (2^-64) in fresh memory.
 #include <random>
 #include <type_traits>
 
@@ -107,7 +115,6 @@ constexpr int kRotateAbove = 16;
 // act values of the 2048-hidden layer in one batch, and the four-token
 // instance keeps 8 (16 would spill there).
 constexpr int kPollWordsFew = 16, kPollWordsMany = 8;
-constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
 // flags (64-bit words): [0, kMaxGridCtas / 2) hold the kMaxGridCtas 32-bit
@@ -116,7 +123,7 @@ constexpr uint64_t kDrainNs = 200000000ull;
 // word on a 128-byte line of its own
 constexpr int kCallWord = kMaxGridCtas;
 constexpr int kCheckWord = kMaxGridCtas + 1;
-constexpr int kSizeWord = kMaxGridCtas + 2;
+constexpr int kSizeWord = kDecodeFusedSizeWord;
 constexpr int kGoWord = kMaxGridCtas + 16;
 static_assert(kGoWord < kDecodeFusedFlagWords, "flags array too small");
 constexpr unsigned long long kCheckKey = 0x6d6f652d7461672dull;  // xor the flags address
@@ -199,12 +206,12 @@ __device__ __forceinline__ int plane_pos(int i, int n) { return ((i >> 2) & 1) *
 // words at p all hold v, then an acq_rel fence, which synchronises with the
 // release stores that wrote them.
 __device__ __forceinline__ bool wait_words4(const uint32_t *p, int n, uint32_t v, volatile int *flag,
-                                            uint64_t t_start)
+                                            uint64_t t_start, uint64_t wait_ns)
 {
     for (uint32_t spin = 0;; ++spin) {
         const uint4 w = ptx::ld_relaxed_gpu_v4(p);
         if (w.x == v && (n < 2 || w.y == v) && (n < 3 || w.z == v) && (n < 4 || w.w == v)) break;
-        if ((spin & 63) == 63 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) return false;
+        if ((spin & 63) == 63 && (*flag || ptx::globaltimer_ns() - t_start > wait_ns)) return false;
     }
     ptx::fence_acq_rel_gpu();
     return true;
@@ -327,8 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int T, int H, int I, int E,
                         int k, int slots, int slot_bytes, int rpc, int rps, int nh_max, int act_in_smem,
                         float *__restrict__ act_g, unsigned long long *__restrict__ act_t,
-                        unsigned long long *__restrict__ flags, unsigned long long epoch_salt,
-                        int32_t *__restrict__ idx_out, float *__restrict__ w_out, float *__restrict__ out)
+                        unsigned long long tag_cap, unsigned long long *__restrict__ flags,
+                        unsigned long long epoch_salt, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
+                        float *__restrict__ out, int32_t *__restrict__ exchange_out, uint64_t wait_ns,
+                        int skip_arrival)
 {
     extern __shared__ __align__(128) uint8_t sm[];
     const int A = T * k;
@@ -448,10 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const unsigned long long calls = s_flags[0];
     const uint32_t e32 = (uint32_t)(epoch_salt + 2 * calls);
     const bool tag_region = act_in_smem && act_t;  // this call may use, or prepare, the tag region
-    const bool tagged = tag_region && s_flags[1] == (kCheckKey ^ (unsigned long long)flags) &&
+    const unsigned long long check_key = kCheckKey ^ (unsigned long long)flags;
+    const bool tagged = tag_region && !skip_arrival && s_flags[1] == check_key &&
                         s_flags[2] >= (unsigned long long)(T * k) * I;
     uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
     if (tagged && threadIdx.x == 0) ptx::st_relaxed_gpu(arrive + blockIdx.x, e32);  // "read the counter"
+    if (exchange_out && blockIdx.x == 0 && threadIdx.x == 0) *exchange_out = tagged ? 2 : 1;
 
     // Phase A: pairs [lo, hi) of the U*I, pair p = (expert p / I, index p % I),
     // in chunks of at most rpc pairs that never cross an expert.  Phase B:
@@ -479,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int p = lo; p < hi && ok; ++c, rp.next(slots)) {
                 const int n = min(rpc, min(I - i0, hi - p));
                 const int s = rp.s;
-                if (!ptx::mbar_wait_bounded(empty + s, rp.par ^ 1u, flag, kWaitNs)) {
+                if (!ptx::mbar_wait_bounded(empty + s, rp.par ^ 1u, flag, wait_ns)) {
                     fail(flag, FAULT_PRODUCER);
                     ok = false;
                     break;
@@ -500,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < nb && ok; ++q, ++c, rp.next(slots)) {
                 const int len_q = min(rps, nrow - q * rps);
                 const int s = rp.s;
-                if (!ptx::mbar_wait_bounded(empty + s, rp.par ^ 1u, flag, kWaitNs)) {
+                if (!ptx::mbar_wait_bounded(empty + s, rp.par ^ 1u, flag, wait_ns)) {
                     fail(flag, FAULT_PRODUCER);
                     ok = false;
                     break;
@@ -541,10 +552,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // reuses this epoch.
             const uint64_t t_start = ptx::globaltimer_ns();
             for (int v = lane; 4 * v < (int)gridDim.x && !*flag; v += 32)
-                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start))
+                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start, wait_ns))
                     fail(flag, FAULT_BARRIER);
             __syncwarp();
-            if (lane == 0) flags[kCallWord] = calls + 1;
+            if (lane == 0) {
+                flags[kCallWord] = calls + 1;
+                if (s_flags[2] > tag_cap) flags[kSizeWord] = tag_cap;
+            }
         }
         if (lane == 0) drain(full, slots, c);
         return;
@@ -566,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = lo; p < hi; rp.next(slots)) {
             const int n = min(rpc, min(I - i0, hi - p));
             const int s = rp.s;
-            if (!ptx::mbar_wait_bounded(full + s, rp.par, flag, kWaitNs)) {
+            if (!ptx::mbar_wait_bounded(full + s, rp.par, flag, wait_ns)) {
                 fail(flag, FAULT_PHASE_A);
                 break;
             }
@@ -618,28 +632,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!tagged) {  // grid barrier: every CTA's act values written and visible
         uint32_t *go = reinterpret_cast<uint32_t *>(flags + kGoWord);
         const uint64_t t_start = ptx::globaltimer_ns();
-        if (ct == 0 && !*flag) ptx::st_release_gpu(arrive + blockIdx.x, e32);
+        // (the test hook: the last CTA does not arrive, so the waits run out)
+        const bool arrives = !(skip_arrival && blockIdx.x == gridDim.x - 1);
+        if (ct == 0 && !*flag && arrives) ptx::st_release_gpu(arrive + blockIdx.x, e32);
         if (blockIdx.x == 0) {
             for (int v = ct; 4 * v < (int)gridDim.x && !*flag; v += n_ct)
-                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start))
+                if (!wait_words4(arrive + 4 * v, min(4, (int)gridDim.x - 4 * v), e32, flag, t_start, wait_ns))
                     fail(flag, FAULT_BARRIER);
             ptx::named_sync(1, n_ct);
             if (ct == 0 && !*flag) ptx::st_release_gpu(go, e32);
         } else if (ct == 0 && !*flag) {
-            if (!wait_words4(go, 1, e32, flag, t_start)) fail(flag, FAULT_BARRIER);
+            if (!wait_words4(go, 1, e32, flag, t_start, wait_ns)) fail(flag, FAULT_BARRIER);
         }
     }
     // every consumer leaves, or none: a producer fault can set the flag at any time
     const bool stop = ptx::named_sync_or(1, n_ct, *flag != 0);
     if (!tagged && blockIdx.x == 0 && ct == 0) {
         // past the barrier every CTA has read the flags and cleared its share
+        // (or, after a failed wait, may still be clearing it: then the size
+        // word is not raised).  The act rows of a call that reads them in
+        // place lie past tag_cap, like every other region of this call.
         flags[kCallWord] = calls + 1;
-        if (tag_region && !stop) {
-            const unsigned long long key = kCheckKey ^ (unsigned long long)flags;
-            const unsigned long long had = s_flags[1] == key ? s_flags[2] : 0ull;
-            flags[kSizeWord] = had > (unsigned long long)nact ? had : (unsigned long long)nact;
-            flags[kCheckWord] = key;
-        }
+        unsigned long long size = s_flags[1] == check_key ? s_flags[2] : 0ull;
+        if (tag_region && !stop && size < (unsigned long long)nact) size = (unsigned long long)nact;
+        flags[kSizeWord] = size < tag_cap ? size : tag_cap;
+        if (tag_region && !stop) flags[kCheckWord] = check_key;
     }
     if (stop) return;
 
@@ -671,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             reinterpret_cast<float2 *>(abuf)[v0 + j * n_ct] =
                                 make_float2(__uint_as_float((uint32_t)w[j].x), __uint_as_float((uint32_t)w[j].y));
                         }
-                    if (need && (spin & 15) == 15 && (*flag || ptx::globaltimer_ns() - t_start > kWaitNs)) {
+                    if (need && (spin & 15) == 15 && (*flag || ptx::globaltimer_ns() - t_start > wait_ns)) {
                         fail(flag, FAULT_BARRIER);
                         break;
                     }
@@ -699,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int q = 0; q < nb; ++q, rp.next(slots)) {
                 const int s = rp.s;
-                if (ok && !ptx::mbar_wait_bounded(full + s, rp.par, flag, kWaitNs)) {
+                if (ok && !ptx::mbar_wait_bounded(full + s, rp.par, flag, wait_ns)) {
                     fail(flag, FAULT_PHASE_B);
                     ok = false;
                 }
@@ -836,7 +853,8 @@ size_t decode_fused_tag_words(int k, int I)
 
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
-                                unsigned long long *flags, int32_t *idx_out, float *w_out, float *out,
+                                unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
+                                float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
                                 cudaStream_t s)
 {
     const Plan p = plan_for(T, H, I, k, n_sm);
@@ -858,7 +876,8 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
     auto kern = p.nt == 1 ? decode_fused_kernel<1> : p.nt == 2 ? decode_fused_kernel<2> : decode_fused_kernel<4>;
     return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
                               H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, act_tag,
-                              flags, epoch_salt(), idx_out, w_out, out);
+                              tag_cap, flags, epoch_salt(), idx_out, w_out, out, exchange_out, (uint64_t)wait_ns,
+                              skip_arrival);
 }
 
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)

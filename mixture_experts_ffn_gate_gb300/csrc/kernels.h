@@ -11,8 +11,11 @@ constexpr int kGemmChunkMax = 64;
 
 // routing.cu
 cudaError_t routing_init_device();
+// tag_size (nullable): the fused decode kernel's size word in a workspace
+// that keeps its state; the router lowers it to tag_cap (the call's other
+// regions start that many 64-bit words into the tag region).
 cudaError_t launch_router(const float *logits, int T, int E, int k, int32_t *idx, float *w, int32_t *idx_copy,
-                          float *w_copy, cudaStream_t s);
+                          float *w_copy, unsigned long long *tag_size, unsigned long long tag_cap, cudaStream_t s);
 size_t sort_smem_bytes(int E);
 cudaError_t launch_sort(const int32_t *idx, int n_assign, int E, int chunk_max, int32_t *offs, int32_t *perm,
                         int32_t *pos, int32_t *uexp, int32_t *ucount, int4 *chunks, int32_t *nchunks,
@@ -34,19 +37,35 @@ cudaError_t launch_decode_down(const float *act, const void *wd, const float *w,
 
 // decode_fused.cu: a decode step of up to four tokens in one cooperative
 // kernel.  act: [T*k][I] FP32 scratch; flags: kDecodeFusedFlagWords 64-bit
-// words and act_tag: decode_fused_tag_words(k, I) 64-bit words, both kept by
-// the kernel between calls (any initial contents) and written by nothing
-// else; act_tag may be null (every call then meets at a grid barrier).
+// words and act_tag: the tag region, both kept between calls (any initial
+// contents); act_tag may be null (every call then meets at a grid barrier).
+// Word kDecodeFusedSizeWord of flags counts the leading words of the tag
+// region known to hold only zeros and tags.  Every call on a workspace that
+// keeps state lowers it to its tag_cap, the 64-bit words of the tag region
+// before the call's first other region: the fused kernel itself, and the
+// router kernel on the other paths.
 constexpr int kMaxGridCtas = 1024;
 constexpr int kDecodeFusedFlagWords = kMaxGridCtas + 32;
+constexpr int kDecodeFusedSizeWord = kMaxGridCtas + 2;
 cudaError_t decode_fused_init_device();
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear);
 bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm);
 size_t decode_fused_tag_words(int k, int I);
+// exchange_out (nullable, device): CTA 0 stores 1 when the call met at the
+// grid barrier, 2 when it exchanged tagged act words.  wait_ns bounds every
+// wait; skip_arrival (a test hook) makes the last CTA skip its arrival at
+// the grid barrier, so the call's waits run out and it reports a fault.
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
-                                unsigned long long *flags, int32_t *idx_out, float *w_out, float *out,
+                                unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
+                                float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
                                 cudaStream_t s);
+constexpr unsigned long long kDecodeFusedWaitNs = 2000000000ull;  // default bound of its waits
+
+// moe_ffn_api.cu: an identifier of the calling thread's current CUDA
+// context (0 if none can be had), so that per-device set-up is redone in a
+// new context, e.g. after cudaDeviceReset.
+unsigned long long current_context_id();
 
 // grouped_gemm.cu
 cudaError_t gemm_init_device();

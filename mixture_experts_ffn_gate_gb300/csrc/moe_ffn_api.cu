@@ -23,13 +23,16 @@ struct Shape {
 };
 
 // Workspace regions, 256-byte aligned.  First the fused decode kernel's
-// state, which it keeps between calls: its flags and its tag region, at the
-// same offsets for every T (they depend only on k and I), so calls with
-// different T on one workspace share them and no other region overlaps
-// them.  Then the routing/sort region, shared by both paths; the rest is per
-// path and the two overlap.
+// state, which it keeps between calls: its flags (at offset 0 for every
+// shape) and its tag region (right after them, its length depending on k
+// and I), so calls of one k and I with any T share them and no other region
+// of theirs overlaps them; a call of another shape may place its regions in
+// a larger shape's tag region, which is why every call lowers the flags'
+// size word to its own tag capacity (tag_cap).  Then the routing/sort
+// region, shared by both paths; the rest is per path and the two overlap.
 struct Layout {
     size_t flags, act_tag, idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, common_end;
+    unsigned long long tag_cap;          // 64-bit words from act_tag to the next region
     size_t act;                          // decode: act f32 [T*k, I]
     size_t xs, act_hi, act_lo, z;        // grouped
     size_t decode_total, grouped_total, total;
@@ -50,6 +53,7 @@ Layout make_layout(const Shape &s)
     L.flags = take((size_t)moe::kDecodeFusedFlagWords * 8);
     L.act_tag = take(moe::decode_fused_tag_words((int)s.k, (int)s.I) * 8);
     L.idx = take(n * 4);
+    L.tag_cap = (L.idx - L.act_tag) / 8;
     L.w = take(n * 4);
     L.offs = take((size_t)(s.E + 1) * 4);
     L.perm = take(n * 4);
@@ -105,14 +109,18 @@ int check_opts(const moe_ffn_opts *o)
     if (o->gate_up_warps < 0 || o->gate_up_warps > 16) return MOE_ERR_INVALID_ARG;
     if (o->down_warps < 0 || o->down_warps > 16) return MOE_ERR_INVALID_ARG;
     if (o->gemm_ctas < 0) return MOE_ERR_INVALID_ARG;
+    if (o->test_wait_limit_us < 0 || o->test_skip_arrival < 0) return MOE_ERR_INVALID_ARG;
     for (int r : o->reserved_in)
         if (r != 0) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
 }
 
-// Per-device one-time set-up: kernel attributes and the SM count.
+// Per-device set-up: kernel attributes and the SM count, done once per
+// device and context (a new context, e.g. after cudaDeviceReset, has lost
+// the kernel attributes).
 struct DeviceInfo {
     bool ready = false;
+    unsigned long long ctx = 0;
     int n_sm = 0;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -124,12 +132,16 @@ int device_setup(DeviceInfo **info)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     DeviceInfo &d = g_dev[dev];
-    if (!d.ready) {
+    const unsigned long long ctx = moe::current_context_id();
+    if (!d.ready || d.ctx != ctx) {
+        d.ready = false;
         if (cudaDeviceGetAttribute(&d.n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::routing_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::decode_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::decode_fused_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::gemm_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        // the attribute calls above created the context if there was none
+        d.ctx = moe::current_context_id();
         d.ready = true;
     }
     *info = &d;
@@ -213,17 +225,24 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
         // projections' rows of the touched experts and exchanges the act
         // rows in between
         path = MOE_PATH_DECODE_FUSED;
+        const unsigned long long wait_ns = (opts && opts->test_wait_limit_us)
+                                               ? 1000ull * (unsigned long long)opts->test_wait_limit_us
+                                               : moe::kDecodeFusedWaitNs;
         MOE_TRY(stg.done(moe::launch_decode_fused(
             x, logits, wgu, wd, T, H, I, E, k, dev->n_sm, (float *)(ws + L.act),
-            keep_state ? (unsigned long long *)(ws + L.act_tag) : nullptr, (unsigned long long *)(ws + L.flags),
-            idx_out, w_out, out, stream)));
+            keep_state ? (unsigned long long *)(ws + L.act_tag) : nullptr, L.tag_cap,
+            (unsigned long long *)(ws + L.flags), idx_out, w_out, out, opts ? opts->exchange_out : nullptr, wait_ns,
+            opts ? opts->test_skip_arrival : 0, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
         }
         return MOE_OK;
     }
-    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, idx_out, w_out, stream)));
+    // on a workspace that keeps state, the router also tells the fused
+    // decode kernel's state which words this call's other regions overwrite
+    auto *tag_size = keep_state ? (unsigned long long *)(ws + L.flags) + moe::kDecodeFusedSizeWord : nullptr;
+    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, idx_out, w_out, tag_size, L.tag_cap, stream)));
     if (path == MOE_PATH_DECODE) {
         auto *act = (float *)(ws + L.act);
         MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
@@ -254,6 +273,40 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 }
 
 }  // namespace
+
+namespace moe {
+
+unsigned long long current_context_id()
+{
+    // the driver's cuCtxGetCurrent and cuCtxGetId, fetched through the
+    // runtime (the library does not link libcuda); CUresult 0 is success
+    using get_current_fn = int (*)(void **);
+    using get_id_fn = int (*)(void *, unsigned long long *);
+    static get_current_fn get_current = nullptr;
+    static get_id_fn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) == cudaSuccess &&
+            r1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) == cudaSuccess &&
+            r2 == cudaDriverEntryPointSuccess) {
+            get_current = (get_current_fn)p;
+            get_id = (get_id_fn)q;
+        }
+        cudaGetLastError();
+    });
+    void *ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+    return id;
+}
+
+}  // namespace moe
+
+static_assert(MOE_FFN_WORKSPACE_STATE_BYTES >= (size_t)moe::kDecodeFusedFlagWords * 8,
+              "the state bytes must cover the fused decode kernel's flags");
 
 extern "C" {
 

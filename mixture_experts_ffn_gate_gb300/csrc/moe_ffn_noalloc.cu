@@ -15,10 +15,12 @@
 // two calls whose work overlaps on the GPU (different streams, or different
 // host threads without ordering) race on it and give wrong results: order
 // them on one stream.  It is the workspace of moe_ffn_forward_ex, so it also
-// holds the state that path keeps between calls; nothing in it has to start
-// at zero.
+// holds the state that path keeps between calls, under the same rules:
+// calls of any shape may follow one another, nothing in it has to start at
+// zero, and no one else writes to it.
 #include <mutex>
 
+#include "kernels.h"
 #include "moe_ffn.h"
 
 namespace {
@@ -30,8 +32,16 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch per device.  In host code the array's
 // name only stands in for the symbol; its device address comes from
-// cudaGetSymbolAddress, taken once per device with that device current.
-void *g_scratch_addr[kMaxDevices];
+// cudaGetSymbolAddress, taken once per device with that device current.  The
+// address belongs to the context that loaded the library's module, so it is
+// looked up again when the current context changes (after cudaDeviceReset
+// the module is loaded anew and the array may sit elsewhere, with fresh
+// contents).
+struct Scratch {
+    void *addr = nullptr;
+    unsigned long long ctx = 0;
+};
+Scratch g_scratch[kMaxDevices];
 std::mutex g_scratch_mutex;
 
 int scratch_address(void **addr)
@@ -39,15 +49,18 @@ int scratch_address(void **addr)
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    Scratch &sc = g_scratch[dev];
+    if (!sc.addr || sc.ctx != moe::current_context_id()) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
+            sc.addr = nullptr;
             return MOE_ERR_CUDA;
         }
-        g_scratch_addr[dev] = p;
+        sc.addr = p;
+        sc.ctx = moe::current_context_id();  // the lookup above made the context current if none was
     }
-    *addr = g_scratch_addr[dev];
+    *addr = sc.addr;
     return MOE_OK;
 }
 

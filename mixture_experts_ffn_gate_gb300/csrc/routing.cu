@@ -20,13 +20,21 @@ namespace moe {
 // slot j holds the j-th pick; then the softmax over the k chosen logits.
 constexpr int kRouterWarps = 8;
 
+//
+// On a workspace that keeps the fused decode kernel's state, block 0 also
+// lowers that kernel's size word to tag_cap: this call's other regions
+// (routing, act, gathered rows ...) start tag_cap words into the tag region,
+// and a later fused call must not take what they leave there for tags.
 __global__ void __launch_bounds__(32 * kRouterWarps) router_kernel(const float *__restrict__ logits, int T, int E,
                                                                    int k, int32_t *__restrict__ idx,
                                                                    float *__restrict__ w,
                                                                    int32_t *__restrict__ idx_copy,
-                                                                   float *__restrict__ w_copy)
+                                                                   float *__restrict__ w_copy,
+                                                                   unsigned long long *__restrict__ tag_size,
+                                                                   unsigned long long tag_cap)
 {
     extern __shared__ float vals[];  // [kRouterWarps][E]
+    if (tag_size && blockIdx.x == 0 && threadIdx.x == 0 && *tag_size > tag_cap) *tag_size = tag_cap;
     const int t = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
     if (t >= T) return;
     int e;
@@ -188,10 +196,10 @@ __global__ void combine_kernel(const float *__restrict__ z, const float *__restr
 
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_router(const float *logits, int T, int E, int k, int32_t *idx, float *w, int32_t *idx_copy,
-                          float *w_copy, cudaStream_t s)
+                          float *w_copy, unsigned long long *tag_size, unsigned long long tag_cap, cudaStream_t s)
 {
     router_kernel<<<(unsigned)ceil_div(T, kRouterWarps), 32 * kRouterWarps, (size_t)kRouterWarps * E * 4, s>>>(
-        logits, T, E, k, idx, w, idx_copy, w_copy);
+        logits, T, E, k, idx, w, idx_copy, w_copy, tag_size, tag_cap);
     return cudaPeekAtLastError();
 }
 

@@ -35,15 +35,23 @@ EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",
 
 # Size of the library's fixed scratch array used by moe_ffn_forward_noalloc.
 MOE_FFN_NOALLOC_SCRATCH_BYTES = 16 << 20
+# Leading bytes of a workspace that hold the state kept between calls.
+MOE_FFN_WORKSPACE_STATE_BYTES = 16384
+
+# Values moe_ffn_opts.exchange_out receives from a fused decode call.
+EXCHANGE_BARRIER = 1
+EXCHANGE_TAGGED = 2
 
 
 class moe_ffn_opts(ctypes.Structure):
     """Mirror of ``struct moe_ffn_opts``."""
     _fields_ = [("path", ctypes.c_int32), ("decode_max_tokens", ctypes.c_int32),
                 ("gate_up_warps", ctypes.c_int32), ("down_warps", ctypes.c_int32),
-                ("gemm_ctas", ctypes.c_int32), ("reserved_in", ctypes.c_int32 * 3),
-                ("stage_events", ctypes.c_void_p), ("n_stages", ctypes.c_int32),
-                ("path_taken", ctypes.c_int32), ("reserved_out", ctypes.c_int32 * 2)]
+                ("gemm_ctas", ctypes.c_int32), ("test_wait_limit_us", ctypes.c_int32),
+                ("test_skip_arrival", ctypes.c_int32), ("reserved_in", ctypes.c_int32 * 1),
+                ("stage_events", ctypes.c_void_p), ("exchange_out", ctypes.c_void_p),
+                ("n_stages", ctypes.c_int32), ("path_taken", ctypes.c_int32),
+                ("reserved_out", ctypes.c_int32 * 2)]
 
 
 class MoeFfnError(RuntimeError):
@@ -186,11 +194,16 @@ def moe_ffn_forward_noalloc(x, logits, w_gate_up, w_down, k: int, out=None, stre
 
 
 def new_workspace(T, H, I, E, k, device="cuda", host=False):
-    """A workspace tensor big enough for this shape (256-byte aligned)."""
+    """A workspace tensor big enough for this shape (256-byte aligned).
+
+    Its state bytes are zeroed: torch's caching allocator may hand out
+    memory that served as another workspace and then held other data."""
     n = (moe_ffn_host_workspace_bytes if host else moe_ffn_workspace_bytes)(T, H, I, E, k)
     if n == 0:
         raise MoeFfnError(MOE_ERR_UNSUPPORTED_SHAPE, "workspace size")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:MOE_FFN_WORKSPACE_STATE_BYTES].zero_()
+    return ws
 
 
 def moe_ffn_forward_ex(x, logits, w_gate_up, w_down, k: int, out=None, workspace=None,

@@ -72,9 +72,11 @@ def test_stage_names(L):
 
 def test_opts_struct_layout():
     from mixture_experts_ffn_gate_gb300 import moe_ffn as m
-    # int32 x 8, pointer, int32 x 4 (LP64)
-    assert ctypes.sizeof(m.moe_ffn_opts) == 56
+    # int32 x 8, two pointers, int32 x 4 (LP64)
+    assert ctypes.sizeof(m.moe_ffn_opts) == 64
     assert m.moe_ffn_opts.stage_events.offset == 32
+    assert m.moe_ffn_opts.exchange_out.offset == 40
+    assert m.moe_ffn_opts.n_stages.offset == 48
 
 
 def test_workspace_bytes(L):
@@ -113,14 +115,15 @@ def test_argument_checks(L, case, want):
 def test_bad_opts_rejected(L):
     from mixture_experts_ffn_gate_gb300 import moe_ffn as m
     for field, val in (("path", 3), ("gate_up_warps", 17), ("down_warps", -1), ("gemm_ctas", -2),
-                       ("decode_max_tokens", -1)):
+                       ("decode_max_tokens", -1), ("test_wait_limit_us", -1),
+                       ("test_skip_arrival", -3)):
         o = m.moe_ffn_opts()
         setattr(o, field, val)
         st = L.moe_ffn_forward_ex(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 8, 2, FAKE, FAKE, 1 << 40,
                                   None, None, ctypes.byref(o), None)
         assert st == m.MOE_ERR_INVALID_ARG, field
     o = m.moe_ffn_opts()
-    o.reserved_in[1] = 7
+    o.reserved_in[0] = 7
     assert L.moe_ffn_forward_ex(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 8, 2, FAKE, FAKE, 1 << 40,
                                 None, None, ctypes.byref(o), None) == m.MOE_ERR_INVALID_ARG
 

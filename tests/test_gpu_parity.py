@@ -69,6 +69,74 @@ def test_exact_ties_and_signed_zero(path):
     gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what="ties")
 
 
+def _tie_logits(T, E, seed):
+    """Logits drawn from {-1, -0.0, +0.0, 1}: ties everywhere, and signed
+    zeros that must compare equal."""
+    g = torch.Generator().manual_seed(seed)
+    vals = torch.tensor([-1.0, -0.0, 0.0, 1.0])
+    return vals[torch.randint(0, 4, (T, E), generator=g)].contiguous()
+
+
+def _fused_and_general_agree(x, L, wgu, wd, k):
+    """The tokens (T <= 4) through the fused decode kernel, checked against
+    the oracle, and bit for bit against the same tokens inside a batch of
+    eight, which the general decode kernels (router kernel included) take."""
+    T, H = x.shape
+    E = L.shape[1]
+    o = m.moe_ffn_opts()
+    o.path = m.MOE_PATH_DECODE
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    out = m.moe_ffn_forward_ex(x, L, wgu, wd, k, topk_idx=idx, topk_w=w, opts=o)
+    torch.cuda.synchronize()
+    assert o.path_taken == m.MOE_PATH_DECODE_FUSED
+    out, idx, w = out.cpu(), idx.cpu(), w.cpu()
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what=f"fused T={T} k={k}")
+    x8 = torch.cat([x, x[:1].expand(8 - T, H)]).contiguous()
+    L8 = torch.cat([L, L[:1].expand(8 - T, E)]).contiguous()
+    out8, idx8, w8 = gu.run_gpu(x8, L8, wgu, wd, k, "decode")
+    assert torch.equal(idx8[:T], idx)
+    assert torch.equal(w8[:T], w)
+    assert torch.equal(out8[:T], out)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4])
+def test_ties_and_signed_zero_through_the_fused_kernel(T):
+    """The tie rule (lower index wins, -0.0 == +0.0) where the headline
+    decode calls route: inside the fused decode kernel."""
+    H, I, E, k = 256, 128, 16, 5
+    wl = gu.custom(T, H, I, E, k, name="fused_ties")
+    x, _, wgu, wd = gu.make_layer(wl, T)
+    L = _tie_logits(T, E, seed=10 + T)
+    L[0, 3] = -0.0          # a signed zero on a likely winner's tie
+    L[0, 2] = 0.0
+    _fused_and_general_agree(x, L.cuda(), wgu, wd, k)
+
+
+@pytest.mark.parametrize("T,k", [(4, 9), (4, 16), (1, 32), (2, 32)])
+def test_ties_in_the_rescan_branch(T, k):
+    """k > 8 selects by rescanning the lane's keys below the last winner
+    (the register list holds eight); with tied logits the keys still order
+    by index.  Through the fused kernel and the router kernel."""
+    H, I, E = 128, 64, 64
+    wl = gu.custom(T, H, I, E, k, name="rescan_ties")
+    x, _, wgu, wd = gu.make_layer(wl, T)
+    L = _tie_logits(T, E, seed=100 + k + T).cuda()
+    _fused_and_general_agree(x, L, wgu, wd, k)
+
+
+@pytest.mark.parametrize("path", PATH_IDS)
+@pytest.mark.parametrize("k", [9, 16, 32])
+def test_ties_in_the_rescan_branch_many_tokens(path, k):
+    """The router kernel's rescan branch over 40 tokens of tied logits."""
+    T, H, I, E = 40, 128, 64, 64
+    wl = gu.custom(T, H, I, E, k, name="rescan_ties_many")
+    x, _, wgu, wd = gu.make_layer(wl, T)
+    L = _tie_logits(T, E, seed=200 + k).cuda()
+    out, idx, w = gu.run_gpu(x, L, wgu, wd, k, path)
+    gu.assert_accepted(out, idx, w, *gu.oracle_ref(x, L, wgu, wd, k), what=f"rescan k={k}")
+
+
 @pytest.mark.parametrize("path", PATH_IDS)
 def test_zero_input_gives_zero(path):
     T, H, I, E, k = 7, 256, 128, 8, 2
