@@ -40,22 +40,30 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/*.cu and link libmoeffn.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+# Opt-in instrumented variant: the fused decode kernel records per-CTA clock
+# stamps (read back with moe_ffn_debug_fused_timeline), built apart from the
+# library the tests and the benchmark load.
+TIMELINE_FLAGS = ("-DMOE_FUSED_TIMELINE",)
+TIMELINE_BUILD = os.path.join(PKG, "_build_timeline")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str = BUILD) -> str:
+    """Compile every csrc/*.cu and link libmoeffn.so into out_dir; returns its path."""
+    lib = os.path.join(out_dir, "libmoeffn.so")
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,15 +75,23 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_timeline(force: bool = False) -> str:
+    """The instrumented variant (see TIMELINE_FLAGS); returns its path."""
+    return build(force=force, extra_flags=TIMELINE_FLAGS, out_dir=TIMELINE_BUILD)
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True))
+    if "--timeline" in sys.argv:
+        print(build_timeline(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose=True))

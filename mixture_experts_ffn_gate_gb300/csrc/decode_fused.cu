@@ -88,6 +88,29 @@ namespace moe {
 
 __device__ uint32_t g_decode_fused_fault_word = 0;
 
+// Opt-in timeline (build with -DMOE_FUSED_TIMELINE): each CTA records SM
+// clock stamps of its phase boundaries and of every ring chunk's arrival as
+// consumer warp 0 sees it, overwritten by every launch, read back with
+// moe_ffn_debug_fused_timeline.  Slots per CTA (clock64 unless noted):
+// 0 entry, 1 past griddepcontrol.wait, 2 routing done, 3 first copy issued,
+// 4 last gate/up copy issued, 5 last W_down copy issued, 6 phase A done,
+// 7 act exchange done, 8 act rows staged, 9 phase B done, 10 output
+// written, 11 producer drained, 12 chunks seen, 13 phase A chunks, 16..55
+// chunk c's full barrier passed, 56/57 token 0's routing warp before/after
+// its selection, 58 flag words read, 62 globaltimer at the end, 63
+// globaltimer at entry.  The compiler may move a clock read across a block
+// barrier, so stamps right after one are approximate.
+#ifdef MOE_FUSED_TIMELINE
+constexpr int kTimelineSlots = 64;
+constexpr int kTimelineChunks = 40;
+__device__ unsigned long long g_fused_timeline[kMaxGridCtas * kTimelineSlots];
+#define MOE_TL(i) (g_fused_timeline[blockIdx.x * kTimelineSlots + (i)] = (unsigned long long)clock64())
+#define MOE_TL_SET(i, v) (g_fused_timeline[blockIdx.x * kTimelineSlots + (i)] = (unsigned long long)(v))
+#else
+#define MOE_TL(i) ((void)0)
+#define MOE_TL_SET(i, v) ((void)0)
+#endif
+
 namespace {
 
 // Consumer warps per CTA.  With the producer warp that makes 16 warps, four
@@ -360,12 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // groups, expert and row of the chunk's first row (written by the
     // producer before it arms the slot's full barrier)
     __shared__ int4 s_desc[kMaxSlots];
+    if (threadIdx.x == 0) {
+        MOE_TL_SET(63, ptx::globaltimer_ns());
+        MOE_TL(0);
+    }
     // Launched with programmatic stream serialization: the next launch on
     // the stream may be scheduled from here on (its CTAs take an SM as one
     // of these exits), and nothing written by the previous launch -- the
     // caller's inputs included -- is read before it has completed.
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+    if (threadIdx.x == 0) MOE_TL(1);
     if (threadIdx.x == 0) {
         for (int s = 0; s < slots; ++s) {
             ptx::mbar_init(full + s, 1);
@@ -384,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_flags[0] = vflags[kCallWord];
         s_flags[1] = vflags[kCheckWord];
         s_flags[2] = vflags[kSizeWord];
+#ifdef MOE_FUSED_TIMELINE
+        if (s_flags[0] != ~0ull) MOE_TL(58);  // after the loads returned
+#endif
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -392,7 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = warp - 1;
         int e;
         float wt;
+        if (t == 0 && lane == 0) MOE_TL(56);
         route_token_warp(logits + (int64_t)t * E, E, k, reinterpret_cast<float *>(sm) + (size_t)t * E, e, wt);
+#ifdef MOE_FUSED_TIMELINE
+        if (t == 0 && lane == 0 && wt != -1.0f) MOE_TL(57);
+#endif
         if (lane < k) {
             s_sel[t * k + lane] = e;
             s_w[t * k + lane] = wt;
@@ -453,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x < A) s_xoff[threadIdx.x] = s_asg[threadIdx.x] / k * H;
     __syncthreads();
+    if (threadIdx.x == 0) MOE_TL(2);
 
     const unsigned long long calls = s_flags[0];
     const uint32_t e32 = (uint32_t)(epoch_salt + 2 * calls);
@@ -500,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::mbar_arrive_expect_tx(full + s, 2 * bytes);
                 ptx::bulk_load(sm + (size_t)s * slot_bytes, gate, bytes, full + s);
                 ptx::bulk_load(sm + (size_t)s * slot_bytes + bytes, gate + (int64_t)I * H, bytes, full + s);
+                if (c == 0) MOE_TL(3);
                 p += n;
                 i0 += n;
                 if (i0 == I) {
@@ -507,6 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++u;
                 }
             }
+            MOE_TL(4);
+            MOE_TL_SET(13, c);
             int uu = u_first, rr = 0, gq = 0;  // next row to copy; groups before this chunk
             for (int q = 0; q < nb && ok; ++q, ++c, rp.next(slots)) {
                 const int len_q = min(rps, nrow - q * rps);
@@ -544,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (lane == 0) MOE_TL(5);
         __syncwarp();
         if (tagged && blockIdx.x == 0) {
             // no grid barrier in this call: advance the call counter once
@@ -560,7 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (s_flags[2] > tag_cap) flags[kSizeWord] = tag_cap;
             }
         }
-        if (lane == 0) drain(full, slots, c);
+        if (lane == 0) {
+            drain(full, slots, c);
+            MOE_TL(11);
+        }
         return;
     }
 
@@ -575,6 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // words when this call exchanges act without a grid barrier)
     unsigned long long *const act_w = tagged ? act_t : nullptr;
     RingPos rp;
+#ifdef MOE_FUSED_TIMELINE
+    int pos_c = 0;  // chunks consumer warp 0 has seen
+#endif
     {
         int u = lo / I, i0 = lo - u * I, pos = 0;
         for (int p = lo; p < hi; rp.next(slots)) {
@@ -584,6 +630,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fail(flag, FAULT_PHASE_A);
                 break;
             }
+#ifdef MOE_FUSED_TIMELINE
+            if (ct == 0 && pos_c < kTimelineChunks) MOE_TL(16 + pos_c);
+            ++pos_c;
+#endif
             const uint8_t *chunk = sm + (size_t)s * slot_bytes;
             int m = first_task(pos, cw);
             if (m < n) {  // every warp walks every chunk: set up only with work
@@ -623,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // region first clears its share of it (zero never equals an epoch, which
     // is odd) so that CTA 0 can then mark the region as usable.
     const int nact = A * I;
+    if (ct == 0) MOE_TL(6);
     if (!tagged && tag_region) {
         const int w_lo = (int)((int64_t)nact * blockIdx.x / gridDim.x);
         const int w_hi = (int)((int64_t)nact * (blockIdx.x + 1) / gridDim.x);
@@ -659,6 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tag_region && !stop) flags[kCheckWord] = check_key;
     }
     if (stop) return;
+    if (ct == 0) MOE_TL(7);
 
     // phase B: W_down rows, chunk by chunk.  Within a run of one expert's
     // rows, groups of up to rows_for(na) consecutive rows share the act
@@ -708,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         ptx::named_sync(1, n_ct);
+        if (ct == 0) MOE_TL(8);
         // Two instances of the loop: with the act rows staged, their loads are
         // plain shared-memory loads (one pointer type for the compiler);
         // otherwise global loads through L1.
@@ -720,6 +773,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fail(flag, FAULT_PHASE_B);
                     ok = false;
                 }
+#ifdef MOE_FUSED_TIMELINE
+                if (ct == 0 && pos_c < kTimelineChunks) MOE_TL(16 + pos_c);
+                ++pos_c;
+#endif
                 const int4 d = s_desc[s];
                 // groups are numbered across runs and chunks; group g goes to warp
                 // g % kConsumers.  A warp with none in this chunk skips its runs.
@@ -775,6 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
             rows_b(std::false_type{});
     }
+    if (ct == 0) MOE_TL(9);
     if (ptx::named_sync_or(1, n_ct, *flag != 0)) return;
     for (int v = ct; v < T * nh; v += n_ct) {
         const int t = v / nh, r = v - t * nh;
@@ -782,6 +840,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < k; ++j) o = fmaf(s_w[t * k + j], part[r * A + t * k + j], o);
         out[(size_t)t * H + h_lo + r] = o;
     }
+#ifdef MOE_FUSED_TIMELINE
+    if (ct == 0) {
+        MOE_TL(10);
+        MOE_TL_SET(12, pos_c);
+        MOE_TL_SET(62, ptx::globaltimer_ns());
+    }
+#endif
 }
 
 // Geometry: phase A copies rpc whole gate/up row pairs (about kChunkTarget,
@@ -887,6 +952,23 @@ cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)
     const uint32_t zero = 0;
     return cudaMemcpyToSymbol(g_decode_fused_fault_word, &zero, sizeof(uint32_t));
 }
+
+}  // namespace moe
+
+#ifdef MOE_FUSED_TIMELINE
+// Copies the timeline of the last fused decode launch (n_ctas x 64 words,
+// layout above) to host memory; only in builds with -DMOE_FUSED_TIMELINE.
+extern "C" int moe_ffn_debug_fused_timeline(unsigned long long *host, int n_ctas)
+{
+    if (!host || n_ctas < 1 || n_ctas > moe::kMaxGridCtas) return 1;
+    return cudaMemcpyFromSymbol(host, moe::g_fused_timeline,
+                                (size_t)n_ctas * moe::kTimelineSlots * sizeof(unsigned long long)) == cudaSuccess
+               ? 0
+               : 3;
+}
+#endif
+
+namespace moe {
 
 cudaError_t decode_fused_init_device()
 {

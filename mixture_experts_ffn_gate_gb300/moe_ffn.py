@@ -65,7 +65,9 @@ _lock = threading.Lock()
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The library this process loads: MOE_FFN_LIB if set (e.g. the
+    instrumented timeline build), else the in-tree build."""
+    return os.environ.get("MOE_FFN_LIB") or _build.LIB
 
 
 def lib():
@@ -73,11 +75,12 @@ def lib():
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_build.LIB):
+            path = lib_path()
+            if not os.path.exists(path):
                 raise RuntimeError(
-                    f"{_build.LIB} is missing: build it with "
+                    f"{path} is missing: build it with "
                     "`python -c 'import __graft_entry__ as g; g.build()'`")
-            L = ctypes.CDLL(_build.LIB)
+            L = ctypes.CDLL(path)
             vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
             L.moe_ffn_forward.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
             L.moe_ffn_workspace_bytes.argtypes = [i64] * 5
@@ -98,6 +101,9 @@ def lib():
             for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
                       L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc):
                 f.restype = i32
+            if hasattr(L, "moe_ffn_debug_fused_timeline"):   # instrumented build only
+                L.moe_ffn_debug_fused_timeline.argtypes = [vp, i32]
+                L.moe_ffn_debug_fused_timeline.restype = i32
             _lib = L
     return _lib
 

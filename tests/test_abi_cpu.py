@@ -150,3 +150,15 @@ def test_product_and_oracle_share_no_code():
         if f.endswith((".py", ".c", ".h")):
             src = open(f).read()
             assert "mixture_experts_ffn_gate_gb300" not in src and "moe_ffn.h" not in src, f
+
+
+def test_timeline_build_is_separate_and_exports_its_reader(L):
+    """The instrumented build of the fused decode kernel (-DMOE_FUSED_TIMELINE)
+    compiles on its own and exports the stamp reader; the product library
+    exports no such symbol (its kernels carry no stamps)."""
+    from mixture_experts_ffn_gate_gb300 import _build
+    path = _build.build_timeline()
+    assert os.path.dirname(path) != os.path.dirname(_build.LIB)
+    T = ctypes.CDLL(path)
+    assert hasattr(T, "moe_ffn_debug_fused_timeline")
+    assert not hasattr(L, "moe_ffn_debug_fused_timeline")
