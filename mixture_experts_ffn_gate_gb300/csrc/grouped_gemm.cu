@@ -22,9 +22,13 @@
 //            bits of the FP32 intermediate for the down GEMM (split-precision
 //            products as in Markidis et al. 2018, "NVIDIA Tensor Core
 //            Programmability, Performance & Precision").
-//   down:    D[128 x N] = W_down[e][h0:h0+128] . (act_hi + act_lo)[chunk]^T,
-//            K = I, two MMAs per K step into one accumulator; the epilogue
-//            writes z[sorted row, h] in FP32.
+//   down:    D[128 x N] = W_down[e][h0:h0+128] . [act_hi ; act_lo][chunk]^T,
+//            K = I: the chunk's hi rows and then its lo rows form one B tile,
+//            so one MMA per K step reads the weight tile once for both halves
+//            (with a few tokens on N the tensor pipe's time goes into reading
+//            the 128 x 16 weight slice from shared memory, so a second MMA
+//            for the lo half would cost as much as the first); the epilogue
+//            writes z[sorted row, h] = D[:, j] + D[:, box + j] in FP32.
 // Every output element is one MMA chain over K in a fixed order, so results
 // do not depend on the grid size or on which CTA ran which tile.
 //
@@ -70,7 +74,13 @@ static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulato
 template <bool GATE_UP>
 struct Cfg {
     static constexpr int MT = GATE_UP ? 4 : 3;  // weight tiles per item (they share one token tile)
-    static constexpr int TMEM_COLS = 2 * MT * ACC_COLS;  // double-buffered, one accumulator per tile
+    // accumulator columns per weight tile: the chunk's tokens (gate_up), or
+    // its hi rows then its lo rows (down); gate_up double-buffers them so the
+    // epilogue of one item overlaps the MMAs of the next, down (three tiles
+    // of 128 columns) has room for one set
+    static constexpr int TILE_COLS = GATE_UP ? ACC_COLS : 2 * ACC_COLS;
+    static constexpr int ACC_BUFS = GATE_UP ? 2 : 1;
+    static constexpr int TMEM_COLS = ACC_BUFS * MT * TILE_COLS;
     // tcgen05.alloc takes a power of two of at least 32 columns
     static constexpr int TMEM_ALLOC = TMEM_COLS <= 32    ? 32
                                       : TMEM_COLS <= 64  ? 64
@@ -214,7 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t *b = sB + stage * C::B_BYTES;
                     ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
-                    if (!GATE_UP) ptx::tma_load_2d(b + C::B_TILE, small ? &tmB1s : &tmB1, k0, it.p0, full + stage);
+                    // down: the lo rows right after the hi rows (a whole
+                    // number of 1024-byte swizzle groups), one B tile
+                    if (!GATE_UP)
+                        ptx::tma_load_2d(b + (small ? SMALL_ROWS : NMAX) * BK * 2, small ? &tmB1s : &tmB1, k0, it.p0,
+                                         full + stage);
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -237,16 +251,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = blockIdx.x; i < total && !*abort_flag; i += gridDim.x, ++li) {
                 const Item it = nxt;
                 if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);
-                const uint32_t idesc = ptx::idesc_bf16_f32(BM, pad16(it.n));
-                const int acc = li & 1;
-                const uint32_t aph = (li >> 1) & 1;
+                // down: N spans the hi box and the lo rows that matter
+                const int box = it.n <= SMALL_ROWS ? SMALL_ROWS : NMAX;
+                const uint32_t idesc = ptx::idesc_bf16_f32(BM, GATE_UP ? pad16(it.n) : box + pad16(it.n));
+                const int acc = C::ACC_BUFS == 2 ? (li & 1) : 0;
+                const uint32_t aph = C::ACC_BUFS == 2 ? (li >> 1) & 1 : li & 1;
                 if (!ptx::mbar_wait_bounded(tempty + acc, aph ^ 1, abort_flag, kWaitLimitNs)) {
                     if (!*abort_flag) raise_fault(FAULT_GEMM_MMA);
                     *abort_flag = 1;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d = tmem + acc * MT * ACC_COLS;
+                const uint32_t d = tmem + acc * MT * C::TILE_COLS;
                 bool ok = true;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!ptx::mbar_wait_bounded(full + stage, phase, abort_flag, kWaitLimitNs)) {
@@ -264,10 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int t = 0; t < MT; ++t) {
                             const uint64_t ad = ptx::sw128_desc(a_addr + t * C::A_TILE + k * 32);
-                            ptx::mma_bf16(d + t * ACC_COLS, ad, bd, idesc, (kb | k) != 0);
-                            if (!GATE_UP)
-                                ptx::mma_bf16(d + t * ACC_COLS, ad, ptx::sw128_desc(b_addr + C::B_TILE + k * 32),
-                                              idesc, 1);
+                            ptx::mma_bf16(d + t * C::TILE_COLS, ad, bd, idesc, (kb | k) != 0);
                         }
                     }
                     ptx::mma_commit(empty + stage);
@@ -291,8 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = blockIdx.x; i < total; i += gridDim.x, ++li) {
             const Item it = nxt;
             if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);
-            const int acc = li & 1;
-            const uint32_t aph = (li >> 1) & 1;
+            const int acc = C::ACC_BUFS == 2 ? (li & 1) : 0;
+            const uint32_t aph = C::ACC_BUFS == 2 ? (li >> 1) & 1 : li & 1;
             if (!ptx::mbar_wait_bounded(tfull + acc, aph, abort_flag, kWaitLimitNs)) {
                 if (!*abort_flag) raise_fault(FAULT_GEMM_EPILOGUE);
                 *abort_flag = 1;
@@ -301,11 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             for (int t = 0; t < MT && it.m * MT + t < args.tiles; ++t) {
             const int tile = it.m * MT + t;
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (acc * MT + t) * ACC_COLS;
+            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (acc * MT + t) * C::TILE_COLS;
             for (int c0 = 0; c0 < it.n; c0 += 32) {
                 uint32_t r[32];
                 ptx::tmem_ld32(tbase + c0, r);
-                ptx::tmem_wait_ld();
+                if (!GATE_UP) {
+                    // z = hi part + lo part: for a small chunk both sit in
+                    // these 32 columns (lo from column 16), else the lo part
+                    // is 64 columns on
+                    if (it.n > SMALL_ROWS) {
+                        uint32_t rl[32];
+                        ptx::tmem_ld32(tbase + NMAX + c0, rl);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(rl[j]));
+                    } else {
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < SMALL_ROWS; ++j)
+                            r[j] = __float_as_uint(__uint_as_float(r[j]) + __uint_as_float(r[SMALL_ROWS + j]));
+                    }
+                } else {
+                    ptx::tmem_wait_ld();
+                }
                 if (GATE_UP) {
                     const int neuron = tile * 64 + 16 * q + (lane & 15);
                     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(lane < 16 ? args.out0 : args.out1);
