@@ -11,7 +11,9 @@ arrays to it.  BF16 tensors travel as their raw 16-bit patterns (numpy
 ``uint16``), so the oracle reads exactly the bits the GPU reads.
 
 What each step computes, and the passage it follows, is written at the top of
-``moe_oracle.c``.
+``moe_oracle.c``.  The router projection that produces the logits from the
+token activations (``router.py``, plain numpy and ``math.fsum``) is the one
+step written in Python: its definition is an exactly rounded sum.
 """
 from __future__ import annotations
 
@@ -165,3 +167,18 @@ def expert_ffn(x_row, wgu_e, wd_e):
 
 def forward(x, logits, wgu, wd, k, **kw):
     return default().forward(x, logits, wgu, wd, k, **kw)
+
+
+def router_logits(x, w_router, bias=None):
+    """logits float32 [T, E] = round_f32(exact x . W_r^T + b); see router.py."""
+    from .router import router_logits as f
+    return f(x, w_router, bias)
+
+
+def forward_router(x, w_router, bias, wgu, wd, k, **kw):
+    """The layer from the token activations and the router weights: the
+    router projection, then the layer on its logits.  Returns (out, idx, w,
+    logits)."""
+    logits = router_logits(x, w_router, bias)
+    out, idx, w = forward(x, logits, wgu, wd, k, **kw)
+    return out, idx, w, logits
