@@ -28,7 +28,10 @@ T=2048 training-size forward) is measured the same way, W warm-up and K
 timed steps each over its own layers' weights drawn on the GPU, and reported
 in the line's "supplementary" array: us per call, tokens/s, the whole
 call's HBM fraction, the dominant kernel's roofline and the TFLOP/s against
-dense BF16 peak and against min(peak, HBM peak x flop/byte).
+dense BF16 peak and against min(peak, HBM peak x flop/byte).  Two of the
+rows ("entry": moe_ffn_forward_router) run the 2048-hidden decode layer at
+T=1 and 2 with the router projection inside the call (router weights and
+bias passed instead of logits).
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -338,6 +341,7 @@ def cpu_model():
 # no oracle timing), reported in the line's "supplementary" array.
 SUPPLEMENTARY = [
     ("decode_h2048_i768_e128_k8", (2,)),
+    ("decode_h2048_i768_e128_k8+router", (1, 2)),
     ("decode_h4096_i1536_e128_k8_bias", (1, 4, 16, 64)),
     ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),
@@ -359,7 +363,7 @@ class Measure:
     launches); stages() replays them with the library's stage events between
     kernels; summary() gives the figures of one line."""
 
-    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager):
+    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager, routers=None):
         import torch
         from mixture_experts_ffn_gate_gb300 import moe_ffn as m
         from mixture_experts_ffn_gate_gb300 import synth
@@ -367,12 +371,17 @@ class Measure:
         self.wl, self.T, self.dev, self.K, self.W = wl, T, dev, K, W
         self.path_code, self.layers, self.R = path_code, layers, len(layers)
         self.eager = eager
+        # routers: per layer W_r [E, H]; the calls then pass the router
+        # weights and the bias instead of logits (moe_ffn_forward_router)
+        self.routers = routers
+        self.rbias = bias.to(dev) if routers is not None else None
         batch_bytes = T * (wl.H * 2 + wl.E * 4)
         self.NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
         calls = rank_calls(rank, W, K)   # rank r processes its own calls of the token stream
         self.batches = [synth.make_tokens(wl, T, call=calls[i], device=dev, bias=bias)
                         for i in range(self.NB)]
-        self.ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
+        self.ws = (m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev) if routers is None
+                   else m.new_router_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev))
         self.out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
         self.stream = torch.cuda.current_stream()
         probe = self.new_opts()
@@ -400,9 +409,13 @@ class Measure:
     def call(self, j, stream, opts=None, idx=None):
         x, L = self.batches[j % self.NB]
         lw_gu, lw_d = self.layers[j % self.R]
+        opts = opts if opts is not None else self.new_opts()
+        if self.routers is not None:
+            self.m.moe_ffn_forward_router(x, self.routers[j % self.R], self.rbias, lw_gu, lw_d, self.wl.k,
+                                          out=self.out, workspace=self.ws, topk_idx=idx, opts=opts, stream=stream)
+            return
         self.m.moe_ffn_forward_ex(x, L, lw_gu, lw_d, self.wl.k, out=self.out, workspace=self.ws,
-                                  topk_idx=idx, opts=opts if opts is not None else self.new_opts(),
-                                  stream=stream)
+                                  topk_idx=idx, opts=opts, stream=stream)
 
     def capture(self, steps, events=None):
         """One CUDA graph holding the calls of `steps`, in order."""
@@ -479,6 +492,9 @@ class Measure:
         roofline and the tensor figures of one workload line."""
         wl, T, K = self.wl, self.T, self.K
         call_bytes = sum(algorithmic_bytes(wl, T, u) for u in self.U) / K
+        # calls with the router projection inside also read W_r (E*H BF16)
+        router_bytes = wl.E * wl.H * 2 if self.routers is not None else 0
+        call_bytes += router_bytes
         flops = 6.0 * wl.H * wl.I * T * wl.k
         ms_call = total_ms / K
         # dominant kernel = largest share of the per-kernel pass.  When a step
@@ -490,6 +506,8 @@ class Measure:
         one_kernel = len(kern_avg) == 1
         dom_ms = ms_call if one_kernel else kern_avg[dom]
         dom_bytes = sum(kernel_bytes(dom, wl, T, u, wl.k) for u in self.U) / K
+        if dom == "decode_fused":
+            dom_bytes += router_bytes
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
@@ -527,21 +545,26 @@ def supplementary_rows(args, dev, peaks, skip):
     import torch
     from mixture_experts_ffn_gate_gb300 import synth
     rows = []
-    for name, Ts in SUPPLEMENTARY:
+    for entry, Ts in SUPPLEMENTARY:
+        name, _, how = entry.partition("+")
         wl = synth.WORKLOADS[name]
-        Ts = [T for T in Ts if (name, T) != skip]
+        Ts = [T for T in Ts if (entry, T) != skip]
         if not Ts:
             continue
         R = max(layer_count(wl, T, args.layers)[0] for T in Ts)
         layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
+        routers = [synth.make_router(wl, device=dev, layer=r) for r in range(R)] if how == "router" else None
         bias = synth.make_bias(wl)
         for T in Ts:
             run = Measure(wl, T, dev, args.steps, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
-                args.path], layers, bias, 0, args.eager)
+                args.path], layers, bias, 0, args.eager, routers=routers)
             with ClockSampler(dev.index or 0) as clocks:
                 total_ms, _ = run.timed(1)
                 kern = run.stages()
             row = {"workload": name, "T": T, "layers": R}
+            if how == "router":
+                row["entry"] = ("moe_ffn_forward_router: router weights W_r [E,H] ~ N(0,1/H) and the "
+                                "workload's bias passed instead of logits; the projection runs inside the call")
             row.update(run.summary(total_ms, kern, peaks, 1))
             row["clocks"] = clocks.summary()
             rows.append(row)

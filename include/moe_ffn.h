@@ -179,6 +179,41 @@ int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32,
                        moe_ffn_opts *opts, cudaStream_t stream);
 
 /*
+ * The layer with its router projection inside the call: the caller passes
+ * the router weights instead of logits.  "Expert routing" is the step the
+ * warp-decode article (section 배경 및 맥락) places before the experts; here
+ * it is a linear map plus a per-expert bias:
+ *   logits[t][e] = round_f32( sum_h x[t][h] * w_router[e][h] + router_bias[e] ),
+ * the sum of the BF16 products taken exactly (the GPU forms and accumulates
+ * them in FP64, which is exact unless they span more than about 2^40 in
+ * magnitude) and rounded once to FP32, so the logits, and the top-k decided
+ * on them, are a function of the inputs alone.  Then the layer as in
+ * moe_ffn_forward_ex on those logits.
+ *   w_router_bf16  [E, H] BF16, one row per expert (a linear layer's weight).
+ *   router_bias_f32 nullable [E] FP32 (4-byte aligned).
+ *   logits_out     nullable [T, E] FP32: the logits the call computed.
+ * Decode calls (the fused decode kernel, T <= 4) compute the logits inside
+ * that kernel, each CTA a share, exchanged between CTAs through the
+ * workspace: no separate router launch.  Other calls run one router kernel
+ * first.  The FP64 rate of the GPU makes that kernel slow for large T (at
+ * T = 2048, E = 256, H = 6144 it takes milliseconds): batches of that size
+ * are better served by logits from the caller's own GEMM and
+ * moe_ffn_forward_ex.  The workspace (at least
+ * moe_ffn_router_workspace_bytes) is moe_ffn_forward_ex's, with the same
+ * state and rules, plus room for the logits.
+ */
+size_t moe_ffn_router_workspace_bytes(int64_t T, int64_t H, int64_t I,
+                                      int64_t E, int64_t k);
+int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16,
+                           const float *router_bias_f32,
+                           const void *w_gate_up_bf16, const void *w_down_bf16,
+                           int64_t T, int64_t H, int64_t I, int64_t E,
+                           int64_t k, float *out_f32, void *workspace,
+                           size_t workspace_bytes, float *logits_out,
+                           int32_t *topk_idx_out, float *topk_w_out,
+                           moe_ffn_opts *opts, cudaStream_t stream);
+
+/*
  * End-to-end form for callers whose tokens live in host memory: x_host
  * [T,H] bf16, logits_host [T,E] f32 and out_host [T,H] f32 are HOST buffers
  * (page-locked for the copies to be asynchronous); the weights are device

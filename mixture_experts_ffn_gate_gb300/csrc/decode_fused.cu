@@ -76,6 +76,7 @@
 //     kernel before anything else).  So memory that held other data never
 //     stands in for an act value, whatever shapes share the workspace; only
 //     the check word could match by chance (2^-64) in fresh memory.
+#include <atomic>
 #include <random>
 #include <type_traits>
 
@@ -95,10 +96,11 @@ __device__ uint32_t g_decode_fused_fault_word = 0;
 // 0 entry, 1 past griddepcontrol.wait, 2 routing done, 3 first copy issued,
 // 4 last gate/up copy issued, 5 last W_down copy issued, 6 phase A done,
 // 7 act exchange done, 8 act rows staged, 9 phase B done, 10 output
-// written, 11 producer drained, 12 chunks seen, 13 phase A chunks, 16..55
-// chunk c's full barrier passed, 56/57 token 0's routing warp before/after
-// its selection, 58 flag words read, 62 globaltimer at the end, 63
-// globaltimer at entry.  The compiler may move a clock read across a block
+// written, 11 producer drained, 12 chunks seen, 13 phase A chunks, 14/15
+// (calls with the router projection) its slices summed / every logit
+// polled, 16..55 chunk c's full barrier passed, 56/57 token 0's routing
+// warp before/after its selection, 58 flag words read, 62 globaltimer at
+// the end, 63 globaltimer at entry.  The compiler may move a clock read across a block
 // barrier, so stamps right after one are approximate.
 #ifdef MOE_FUSED_TIMELINE
 constexpr int kTimelineSlots = 64;
@@ -139,6 +141,7 @@ constexpr int kRotateAbove = 16;
 // instance keeps 8 (16 would spill there).
 constexpr int kPollWordsFew = 16, kPollWordsMany = 8;
 constexpr uint64_t kDrainNs = 200000000ull;
+constexpr int kLogitReplicas = kDecodeFusedLogitCopies;  // copies of each published router logit
 
 // flags (64-bit words): [0, kMaxGridCtas / 2) hold the kMaxGridCtas 32-bit
 // arrival words, then the call counter, the tag-region check word and the
@@ -152,6 +155,7 @@ static_assert(kGoWord < kDecodeFusedFlagWords, "flags array too small");
 constexpr unsigned long long kCheckKey = 0x6d6f652d7461672dull;  // xor the flags address
 
 enum : uint32_t {
+    FAULT_LOGITS = 8u,
     FAULT_PRODUCER = 16u,
     FAULT_PHASE_A = 32u,
     FAULT_BARRIER = 64u,
@@ -351,7 +355,48 @@ __device__ __forceinline__ void down_rows(const uint8_t *const *rowp, const floa
     if (lane % W == 0 && slot < RB * NB && r < nu) part[r * A + asg[b]] = t;
 }
 
-template <int NT>
+// The router projection's inputs for the ROUTER instantiation: W_r [E][H]
+// BF16, the bias [E] (nullable), the tagged logit words [T*E] (16 bytes
+// each) and the caller's logits output (nullable).
+struct RouterArgs {
+    const uint16_t *wr;
+    const float *bias;
+    unsigned long long *ltag;
+    float *logits_out;
+    unsigned long long nonce;  // fresh for every launch from the host
+};
+
+// A 64-bit mixing function (the finaliser of Steele, Lea and Flood's
+// SplitMix64): every input bit reaches every output bit.
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z)
+{
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+}
+
+// ROUTER: the call passes the router weights instead of logits.  Before it
+// routes, CTA b computes the logits o = b, b + grid, ... of the T*E -- the
+// (logit, 256-element slice) pairs go round-robin over its warps
+// (router_slice_warp), one thread per logit then adds the slices in order
+// (router_logit_sum), the same arithmetic as the router kernel -- and
+// publishes each as a 16-byte word:
+// the call's 64-bit id, then the id's upper half << 32 | the logit's bits.
+// The id mixes a nonce the host draws for every launch with the workspace's
+// call counter, so no two calls of the process share one: replays of a
+// captured launch keep its nonce but each advances the counter, while a
+// workspace whose state was reset (counter back at zero, perhaps at the
+// address of an earlier workspace) gets new nonces.  So a word left by any
+// earlier call never matches, nor, but by chance (2^-96), other data; the
+// words need no preparation.  Each half is single-copy atomic, so a reader
+// that finds both halves carrying the id has the value of this call's store
+// (a half from another store would carry another id's upper half, 2^-32).
+// Every CTA polls all T*E words into its routing scratch and routes from
+// there.  Each logit's word is stored in kLogitReplicas copies and CTA b
+// polls copy b % kLogitReplicas, so the grid's polls spread over that many
+// times more L2 lines (every CTA polls every logit, so one copy would draw
+// all of them to the same few lines).
+template <int NT, bool ROUTER>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
                         const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int T, int H, int I, int E,
@@ -360,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         unsigned long long tag_cap, unsigned long long *__restrict__ flags,
                         unsigned long long epoch_salt, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
                         float *__restrict__ out, int32_t *__restrict__ exchange_out, uint64_t wait_ns,
-                        int skip_arrival)
+                        int skip_arrival, RouterArgs ra)
 {
     extern __shared__ __align__(128) uint8_t sm[];
     const int A = T * k;
@@ -418,13 +463,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    if constexpr (ROUTER) {
+        // x of all tokens into shared memory for phase A, while the
+        // projection below reads x and W_r from global memory
+        for (int v = threadIdx.x; v < T * H / 8; v += kThreads)
+            reinterpret_cast<uint4 *>(xs)[v] = ld_nc16(x + (size_t)v * 8);
+        const int TE = T * E;
+        const int n_mine = TE > (int)blockIdx.x ? (TE - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const int ns = router_slices(H);
+        // slice sums [n_mine][ns] in the ring, after the routing scratch
+        double *slice = reinterpret_cast<double *>(sm + (((size_t)TE * 4 + 15) & ~(size_t)15));
+        for (int u = warp; u < n_mine * ns; u += kThreads / 32) {
+            const int j = u / ns, sl = u - j * ns;
+            const int o = blockIdx.x + j * gridDim.x, t = o / E, e = o - t * E;
+            const double d = router_slice_warp(x + (size_t)t * H, ra.wr + (int64_t)e * H, H, sl, lane);
+            if (lane == 0) slice[u] = d;
+        }
+        __syncthreads();  // slices summed, x staged; thread 0 has read the flag words
+        if (threadIdx.x == 0) MOE_TL(14);
+        const unsigned long long e64 = mix64(ra.nonce ^ (s_flags[0] * 0x9e3779b97f4a7c15ull));
+        const unsigned long long tag_hi = e64 & 0xffffffff00000000ull;
+        if (threadIdx.x < n_mine) {
+            const int j = threadIdx.x, o = blockIdx.x + j * gridDim.x, e = o % E;
+            const float v = router_logit_sum(slice + (size_t)j * ns, ns, ra.bias ? __ldg(ra.bias + e) : 0.0f);
+            if (ra.logits_out) ra.logits_out[o] = v;
+#pragma unroll
+            for (int c = 0; c < kLogitReplicas; ++c)
+                ptx::st_relaxed_gpu_v2u64(ra.ltag + 2 * ((size_t)c * TE + o), e64, tag_hi | __float_as_uint(v));
+        }
+        float *vals = reinterpret_cast<float *>(sm);  // the routing scratch: token t's logits at t * E
+        const unsigned long long *copy = ra.ltag + 2 * (size_t)(blockIdx.x % kLogitReplicas) * TE;
+        const uint64_t t_start = ptx::globaltimer_ns();
+        for (int o = threadIdx.x; o < TE && !*flag; o += kThreads) {
+            for (uint32_t spin = 0;; ++spin) {
+                const ulonglong2 w = ptx::ld_relaxed_gpu_v2u64(copy + 2 * (size_t)o);
+                if (w.x == e64 && (w.y >> 32) == (tag_hi >> 32)) {
+                    vals[o] = __uint_as_float((uint32_t)w.y);
+                    break;
+                }
+                if ((spin & 15) == 15 && (*flag || ptx::globaltimer_ns() - t_start > wait_ns)) {
+                    fail(flag, FAULT_LOGITS);
+                    break;
+                }
+            }
+        }
+        if (__syncthreads_or(*flag != 0)) return;  // no copy has been issued yet
+        if (threadIdx.x == 0) MOE_TL(15);
+    }
+
     // routing: consumer warp 1 + t routes token t (scratch: the ring)
     if (warp >= 1 && warp <= T) {
         const int t = warp - 1;
         int e;
         float wt;
         if (t == 0 && lane == 0) MOE_TL(56);
-        route_token_warp(logits + (int64_t)t * E, E, k, reinterpret_cast<float *>(sm) + (size_t)t * E, e, wt);
+        route_token_warp<ROUTER>(logits + (int64_t)t * E, E, k, reinterpret_cast<float *>(sm) + (size_t)t * E, e,
+                                 wt);
 #ifdef MOE_FUSED_TIMELINE
         if (t == 0 && lane == 0 && wt != -1.0f) MOE_TL(57);
 #endif
@@ -609,9 +703,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int ct = threadIdx.x - 32, n_ct = kConsumers * 32;
     const int cw = warp - 1;
-    for (int v = ct; v < T * H / 8; v += n_ct)  // x of all tokens, 16 bytes at a time
-        reinterpret_cast<uint4 *>(xs)[v] = ld_nc16(x + (size_t)v * 8);
-    ptx::named_sync(1, n_ct);
+    if constexpr (!ROUTER) {  // (the router projection staged x already)
+        for (int v = ct; v < T * H / 8; v += n_ct)  // x of all tokens, 16 bytes at a time
+            reinterpret_cast<uint4 *>(xs)[v] = ld_nc16(x + (size_t)v * 8);
+        ptx::named_sync(1, n_ct);
+    }
 
     // phase A: for each pair, gate and up dot products with every token of
     // the expert; act per assignment to global memory (tagged
@@ -885,6 +981,17 @@ Plan plan_for(int T, int H, int I, int k, int n_sm)
     return p;
 }
 
+// A fresh 64-bit value for every launch that passes router weights: a
+// process-wide counter started at a random point.
+unsigned long long launch_nonce()
+{
+    static std::atomic<unsigned long long> next{[] {
+        std::random_device rd;
+        return ((unsigned long long)rd() << 32) ^ rd();
+    }()};
+    return next.fetch_add(1, std::memory_order_relaxed);
+}
+
 // The odd 64-bit salt of every epoch, drawn at random once per process.  A
 // call's epoch is salt + 2 * (the flags array's call counter), so the calls
 // on one flags array, eager or replayed from a CUDA graph, never repeat an
@@ -910,6 +1017,17 @@ bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm)
     return p.slots >= kMinSlots && (int64_t)T * E * 4 <= (int64_t)p.slots * p.slot_bytes;  // routing scratch
 }
 
+bool decode_fused_router_supported(int T, int H, int I, int E, int k, int n_sm)
+{
+    if (!decode_fused_supported(T, H, I, E, k, n_sm)) return false;
+    // the routing scratch and the slice sums of the CTA's logits fit in the
+    // ring; one thread per logit adds its slices
+    const Plan p = plan_for(T, H, I, k, n_sm);
+    const int64_t n_mine = ((int64_t)T * E + n_sm - 1) / n_sm;
+    const int64_t need = (((int64_t)T * E * 4 + 15) & ~15) + n_mine * router_slices(H) * 8;
+    return n_mine <= kThreads && need <= (int64_t)p.slots * p.slot_bytes;
+}
+
 size_t decode_fused_tag_words(int k, int I)
 {
     const int a = kMaxTokens * k < kMaxAsg ? kMaxTokens * k : kMaxAsg;
@@ -920,7 +1038,7 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
                                 unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
                                 float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
-                                cudaStream_t s)
+                                const FusedRouter *router, cudaStream_t s)
 {
     const Plan p = plan_for(T, H, I, k, n_sm);
     cudaLaunchConfig_t cfg = {};
@@ -938,11 +1056,19 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    auto kern = p.nt == 1 ? decode_fused_kernel<1> : p.nt == 2 ? decode_fused_kernel<2> : decode_fused_kernel<4>;
+    RouterArgs ra{};
+    if (router)
+        ra = RouterArgs{(const uint16_t *)router->wr, router->bias, router->ltag, router->logits_out, launch_nonce()};
+    auto kern = router ? (p.nt == 1   ? decode_fused_kernel<1, true>
+                          : p.nt == 2 ? decode_fused_kernel<2, true>
+                                      : decode_fused_kernel<4, true>)
+                       : (p.nt == 1   ? decode_fused_kernel<1, false>
+                          : p.nt == 2 ? decode_fused_kernel<2, false>
+                                      : decode_fused_kernel<4, false>);
     return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
                               H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, act_tag,
                               tag_cap, flags, epoch_salt(), idx_out, w_out, out, exchange_out, (uint64_t)wait_ns,
-                              skip_arrival);
+                              skip_arrival, ra);
 }
 
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)
@@ -972,8 +1098,10 @@ namespace moe {
 
 cudaError_t decode_fused_init_device()
 {
-    for (const void *kern : {(const void *)decode_fused_kernel<1>, (const void *)decode_fused_kernel<2>,
-                             (const void *)decode_fused_kernel<4>}) {
+    for (const void *kern :
+         {(const void *)decode_fused_kernel<1, false>, (const void *)decode_fused_kernel<2, false>,
+          (const void *)decode_fused_kernel<4, false>, (const void *)decode_fused_kernel<1, true>,
+          (const void *)decode_fused_kernel<2, true>, (const void *)decode_fused_kernel<4, true>}) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
         if (e != cudaSuccess) return e;
     }

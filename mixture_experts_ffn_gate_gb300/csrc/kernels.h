@@ -16,6 +16,11 @@ cudaError_t routing_init_device();
 // regions start that many 64-bit words into the tag region).
 cudaError_t launch_router(const float *logits, int T, int E, int k, int32_t *idx, float *w, int32_t *idx_copy,
                           float *w_copy, unsigned long long *tag_size, unsigned long long tag_cap, cudaStream_t s);
+// logits [T, E] (and logits_copy, nullable) from x [T, H] and the router
+// weights wr [E, H] (BF16) plus bias [E] (nullable): the exact sum rounded
+// once to FP32
+cudaError_t launch_router_gemv(const void *x, const void *wr, const float *bias, int T, int H, int E, float *logits,
+                               float *logits_copy, cudaStream_t s);
 size_t sort_smem_bytes(int E);
 cudaError_t launch_sort(const int32_t *idx, int n_assign, int E, int chunk_max, int32_t *offs, int32_t *perm,
                         int32_t *pos, int32_t *uexp, int32_t *ucount, int4 *chunks, int32_t *nchunks,
@@ -50,16 +55,31 @@ constexpr int kDecodeFusedSizeWord = kMaxGridCtas + 2;
 cudaError_t decode_fused_init_device();
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear);
 bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm);
+// the same for a call that passes the router weights (its projection's
+// scratch must fit too)
+bool decode_fused_router_supported(int T, int H, int I, int E, int k, int n_sm);
 size_t decode_fused_tag_words(int k, int I);
 // exchange_out (nullable, device): CTA 0 stores 1 when the call met at the
 // grid barrier, 2 when it exchanged tagged act words.  wait_ns bounds every
 // wait; skip_arrival (a test hook) makes the last CTA skip its arrival at
 // the grid barrier, so the call's waits run out and it reports a fault.
+// router (nullable): the call passes the router weights instead of logits;
+// the kernel computes the logits itself, exchanges them through ltag
+// (kDecodeFusedLogitCopies copies of T*E words of 16 bytes, any initial
+// contents) and writes them to logits_out (nullable).  `logits` is then not
+// read.
+constexpr int kDecodeFusedLogitCopies = 8;
+struct FusedRouter {
+    const void *wr;       // [E, H] BF16
+    const float *bias;    // [E], nullable
+    unsigned long long *ltag;
+    float *logits_out;
+};
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
                                 unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
                                 float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
-                                cudaStream_t s);
+                                const FusedRouter *router, cudaStream_t s);
 constexpr unsigned long long kDecodeFusedWaitNs = 2000000000ull;  // default bound of its waits
 
 // moe_ffn_api.cu: an identifier of the calling thread's current CUDA

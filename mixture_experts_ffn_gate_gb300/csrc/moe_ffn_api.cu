@@ -36,6 +36,10 @@ struct Layout {
     size_t act;                          // decode: act f32 [T*k, I]
     size_t xs, act_hi, act_lo, z;        // grouped
     size_t decode_total, grouped_total, total;
+    // calls that pass the router weights: the logits [T, E] f32 (paths other
+    // than the fused decode kernel) and the fused kernel's tagged logit words
+    // (copies of [T*E] words of 16 bytes), after everything else
+    size_t rlog, rtag, router_total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -75,6 +79,10 @@ Layout make_layout(const Shape &s)
     L.z = take(n * (size_t)s.H * 4);
     L.grouped_total = o;
     L.total = L.decode_total > L.grouped_total ? L.decode_total : L.grouped_total;
+    o = L.total;
+    L.rlog = take((size_t)(s.T * s.E) * 4);
+    L.rtag = take((size_t)(s.T * s.E) * 16 * moe::kDecodeFusedLogitCopies);
+    L.router_total = o;
     return L;
 }
 
@@ -188,9 +196,13 @@ struct Stages {
 // keep_state: the workspace is the caller's and keeps its contents between
 // calls, so the fused decode kernel may use its tag region (a workspace
 // allocated for one call is not: its memory may have held anything since).
+// wr (nullable): the call passes the router weights [E, H] (and rbias [E],
+// nullable) instead of logits; the logits are computed here (and copied to
+// logits_out, nullable).
 int run_forward(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s, float *out,
                 char *ws, const Layout &L, bool keep_state, int32_t *idx_out, float *w_out, moe_ffn_opts *opts,
-                cudaStream_t stream)
+                cudaStream_t stream, const void *wr = nullptr, const float *rbias = nullptr,
+                float *logits_out = nullptr)
 {
     DeviceInfo *dev = nullptr;
     int st = device_setup(&dev);
@@ -220,7 +232,8 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (path == MOE_PATH_DECODE && moe::decode_fused_supported(T, H, I, E, k, dev->n_sm)) {
+    if (path == MOE_PATH_DECODE && (wr ? moe::decode_fused_router_supported(T, H, I, E, k, dev->n_sm)
+                                       : moe::decode_fused_supported(T, H, I, E, k, dev->n_sm))) {
         // a few tokens: one cooperative kernel that routes them, streams both
         // projections' rows of the touched experts and exchanges the act
         // rows in between
@@ -228,11 +241,12 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
         const unsigned long long wait_ns = (opts && opts->test_wait_limit_us)
                                                ? 1000ull * (unsigned long long)opts->test_wait_limit_us
                                                : moe::kDecodeFusedWaitNs;
+        const moe::FusedRouter fr{wr, rbias, (unsigned long long *)(ws + L.rtag), logits_out};
         MOE_TRY(stg.done(moe::launch_decode_fused(
             x, logits, wgu, wd, T, H, I, E, k, dev->n_sm, (float *)(ws + L.act),
             keep_state ? (unsigned long long *)(ws + L.act_tag) : nullptr, L.tag_cap,
             (unsigned long long *)(ws + L.flags), idx_out, w_out, out, opts ? opts->exchange_out : nullptr, wait_ns,
-            opts ? opts->test_skip_arrival : 0, stream)));
+            opts ? opts->test_skip_arrival : 0, wr ? &fr : nullptr, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
@@ -242,6 +256,10 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
     // on a workspace that keeps state, the router also tells the fused
     // decode kernel's state which words this call's other regions overwrite
     auto *tag_size = keep_state ? (unsigned long long *)(ws + L.flags) + moe::kDecodeFusedSizeWord : nullptr;
+    if (wr) {  // the router projection first; it and the top-k form the "router" stage
+        logits = (const float *)(ws + L.rlog);
+        MOE_TRY(moe::launch_router_gemv(x, wr, rbias, T, H, E, (float *)(ws + L.rlog), logits_out, stream));
+    }
     MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, idx_out, w_out, tag_size, L.tag_cap, stream)));
     if (path == MOE_PATH_DECODE) {
         auto *act = (float *)(ws + L.act);
@@ -356,6 +374,44 @@ int moe_ffn_forward_ex(const void *x_bf16, const float *router_logits_f32, const
 {
     return forward_ex(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, T, H, I, E, k, out_f32, workspace,
                       workspace_bytes, true, topk_idx_out, topk_w_out, opts, stream);
+}
+
+size_t moe_ffn_router_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k)
+{
+    Shape s{T, H, I, E, k};
+    if (check_shape(s) != MOE_OK) return 0;
+    return make_layout(s).router_total;
+}
+
+int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16, const float *router_bias_f32,
+                           const void *w_gate_up_bf16, const void *w_down_bf16, int64_t T, int64_t H, int64_t I,
+                           int64_t E, int64_t k, float *out_f32, void *workspace, size_t workspace_bytes,
+                           float *logits_out, int32_t *topk_idx_out, float *topk_w_out, moe_ffn_opts *opts,
+                           cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    int st = check_shape(s);
+    if (st != MOE_OK) return st;
+    st = check_opts(opts);
+    if (st != MOE_OK) return st;
+    if (opts) {
+        opts->n_stages = 0;
+        opts->path_taken = 0;
+    }
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !w_router_bf16 || !w_gate_up_bf16 || !w_down_bf16 || !out_f32) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(w_router_bf16) || !aligned16(w_gate_up_bf16) || !aligned16(w_down_bf16) ||
+        !aligned16(out_f32))
+        return MOE_ERR_INVALID_ARG;
+    if (router_bias_f32 && ((uintptr_t)router_bias_f32 & 3)) return MOE_ERR_INVALID_ARG;
+    if ((logits_out && !aligned16(logits_out)) || (topk_idx_out && !aligned16(topk_idx_out)) ||
+        (topk_w_out && !aligned16(topk_w_out)))
+        return MOE_ERR_INVALID_ARG;
+    if (!workspace || ((uintptr_t)workspace & 255)) return MOE_ERR_INVALID_ARG;
+    const Layout L = make_layout(s);
+    if (workspace_bytes < L.router_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return run_forward(x_bf16, nullptr, w_gate_up_bf16, w_down_bf16, s, out_f32, (char *)workspace, L, true,
+                       topk_idx_out, topk_w_out, opts, stream, w_router_bf16, router_bias_f32, logits_out);
 }
 
 int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,

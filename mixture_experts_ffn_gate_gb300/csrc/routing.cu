@@ -49,6 +49,27 @@ __global__ void __launch_bounds__(32 * kRouterWarps) router_kernel(const float *
     }
 }
 
+// ---------------------------------------------------------------- router projection
+// logits[t, e] = round_f32(sum_h x[t, h] * W_r[e, h] + b[e]), one warp per
+// logit (router_logit_warp), for calls that pass the router weights instead
+// of logits and do not take the fused decode kernel.
+__global__ void __launch_bounds__(32 * kRouterWarps) router_gemv_kernel(const uint16_t *__restrict__ x,
+                                                                        const uint16_t *__restrict__ wr,
+                                                                        const float *__restrict__ bias, int T,
+                                                                        int H, int E, float *__restrict__ logits,
+                                                                        float *__restrict__ logits_copy)
+{
+    const int64_t o = (int64_t)blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
+    if (o >= (int64_t)T * E) return;
+    const int t = (int)(o / E), e = (int)(o - (int64_t)t * E);
+    const float v = router_logit_warp(x + (int64_t)t * H, wr + (int64_t)e * H, H, bias ? __ldg(bias + e) : 0.0f,
+                                      threadIdx.x & 31);
+    if ((threadIdx.x & 31) == 0) {
+        logits[o] = v;
+        if (logits_copy) logits_copy[o] = v;
+    }
+}
+
 // ---------------------------------------------------------------- sort
 // Single block of SORT_THREADS threads.  Warp q owns a contiguous range of
 // assignments (a = t*k + j).  Pass 1 counts per (warp, expert); a scan turns
@@ -200,6 +221,15 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int32_t *idx
 {
     router_kernel<<<(unsigned)ceil_div(T, kRouterWarps), 32 * kRouterWarps, (size_t)kRouterWarps * E * 4, s>>>(
         logits, T, E, k, idx, w, idx_copy, w_copy, tag_size, tag_cap);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_router_gemv(const void *x, const void *wr, const float *bias, int T, int H, int E, float *logits,
+                               float *logits_copy, cudaStream_t s)
+{
+    const int64_t n = (int64_t)T * E;
+    router_gemv_kernel<<<(unsigned)ceil_div(n, kRouterWarps), 32 * kRouterWarps, 0, s>>>(
+        (const uint16_t *)x, (const uint16_t *)wr, bias, T, H, E, logits, logits_copy);
     return cudaPeekAtLastError();
 }
 

@@ -146,6 +146,13 @@ __device__ __forceinline__ ulonglong2 ld_relaxed_gpu_v2u64(const unsigned long l
     return v;
 }
 
+// Two 64-bit words with one store; each half is single-copy atomic on its
+// own, the pair is not.
+__device__ __forceinline__ void st_relaxed_gpu_v2u64(unsigned long long *p, unsigned long long a, unsigned long long b)
+{
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
 __device__ __forceinline__ void st_relaxed_gpu(unsigned long long *p, unsigned long long v)
 {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");

@@ -31,7 +31,8 @@ MOE_MAX_STAGES = 8
 
 EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",
             "moe_ffn_host_workspace_bytes", "moe_ffn_forward_host", "moe_ffn_status_string",
-            "moe_ffn_stage_name", "moe_ffn_device_faults", "moe_ffn_forward_noalloc"]
+            "moe_ffn_stage_name", "moe_ffn_device_faults", "moe_ffn_forward_noalloc",
+            "moe_ffn_router_workspace_bytes", "moe_ffn_forward_router"]
 
 # Size of the library's fixed scratch array used by moe_ffn_forward_noalloc.
 MOE_FFN_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -98,8 +99,13 @@ def lib():
             L.moe_ffn_stage_name.restype = ctypes.c_char_p
             L.moe_ffn_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
             L.moe_ffn_forward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
+            L.moe_ffn_router_workspace_bytes.argtypes = [i64] * 5
+            L.moe_ffn_router_workspace_bytes.restype = ctypes.c_size_t
+            L.moe_ffn_forward_router.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp,
+                                                 ctypes.c_size_t, vp, vp, vp,
+                                                 ctypes.POINTER(moe_ffn_opts), vp]
             for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
-                      L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc):
+                      L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc, L.moe_ffn_forward_router):
                 f.restype = i32
             if hasattr(L, "moe_ffn_debug_fused_timeline"):   # instrumented build only
                 L.moe_ffn_debug_fused_timeline.argtypes = [vp, i32]
@@ -234,6 +240,53 @@ def moe_ffn_forward_ex(x, logits, w_gate_up, w_down, k: int, out=None, workspace
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(topk_idx),
         _ptr(topk_w), ctypes.byref(opts) if opts is not None else None, _stream(stream)),
         "moe_ffn_forward_ex")
+    return out
+
+
+def moe_ffn_router_workspace_bytes(T, H, I, E, k) -> int:
+    return int(lib().moe_ffn_router_workspace_bytes(T, H, I, E, k))
+
+
+def new_router_workspace(T, H, I, E, k, device="cuda"):
+    """A workspace for moe_ffn_forward_router (state bytes zeroed)."""
+    n = moe_ffn_router_workspace_bytes(T, H, I, E, k)
+    if n == 0:
+        raise MoeFfnError(MOE_ERR_UNSUPPORTED_SHAPE, "workspace size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    ws[:MOE_FFN_WORKSPACE_STATE_BYTES].zero_()
+    return ws
+
+
+def moe_ffn_forward_router(x, w_router, router_bias, w_gate_up, w_down, k: int, out=None,
+                           workspace=None, logits=None, topk_idx=None, topk_w=None,
+                           opts: moe_ffn_opts | None = None, stream=None):
+    """The layer with its router projection inside the call: x bf16 [T,H],
+    w_router bf16 [E,H], router_bias f32 [E] or None; optional outputs
+    logits f32 [T,E], topk_idx int32 / topk_w f32 [T,k].  Returns out."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    I = w_down.shape[2]
+    if tuple(w_router.shape) != (E, H) or tuple(w_gate_up.shape) != (E, 2 * I, H) \
+            or tuple(w_down.shape) != (E, H, I):
+        raise ValueError("shape mismatch")
+    for t, d, n in ((x, torch.bfloat16, "x"), (w_router, torch.bfloat16, "w_router"),
+                    (w_gate_up, torch.bfloat16, "w_gate_up"), (w_down, torch.bfloat16, "w_down")):
+        _dev(t, d, n)
+    if router_bias is not None:
+        _dev(router_bias, torch.float32, "router_bias")
+    for t, d, n in ((logits, torch.float32, "logits"), (topk_idx, torch.int32, "topk_idx"),
+                    (topk_w, torch.float32, "topk_w")):
+        if t is not None:
+            _dev(t, d, n)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = new_router_workspace(T, H, I, E, k, device=x.device)
+    _check(lib().moe_ffn_forward_router(
+        _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k,
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(logits),
+        _ptr(topk_idx), _ptr(topk_w), ctypes.byref(opts) if opts is not None else None,
+        _stream(stream)), "moe_ffn_forward_router")
     return out
 
 

@@ -12,6 +12,8 @@ with ``Tensor.to(torch.bfloat16)``):
 * ``bias``        [E]         ~ N(0, var) drawn once per workload (var 0 = none)
 * ``w_gate_up``   [E, 2I, H]  ~ N(0, 1/H) (fan-in H)            -> BF16
 * ``w_down``      [E, H, I]   ~ N(0, 1/I) (fan-in I)            -> BF16
+* ``w_router``    [E, H]      ~ N(0, 1/H) (fan-in H)            -> BF16
+  (calls that pass the router weights; their logits are x . W_r^T + bias)
 
 ``N(0, v)`` names the variance, so std = sqrt(v).  Each expert's weights come
 from a generator seeded with ``seed_for(workload, tensor, expert)``; token
@@ -103,6 +105,16 @@ def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=
         wd[j] = _randn((H, I), 1.0 / math.sqrt(I), device,
                        seed_for(wl.name, H, I, "w_down", e, *tag)).to(torch.bfloat16)
     return wgu, wd
+
+
+def make_router(wl: Workload, device="cpu", *, H=None, E=None, layer=0):
+    """Router weights W_r [E, H] ~ N(0, 1/H) -> BF16 (a linear layer's
+    weight, one row per expert), for calls that pass the router weights
+    instead of logits; the per-expert bias of such calls is make_bias."""
+    tag = () if layer == 0 else ("layer", layer)
+    H = H or wl.H
+    E = E or wl.E
+    return _randn((E, H), 1.0 / math.sqrt(H), device, seed_for(wl.name, H, E, "w_router", *tag)).to(torch.bfloat16)
 
 
 def make_bias(wl: Workload, E=None, device="cpu"):

@@ -25,7 +25,7 @@ import json
 import os
 import statistics
 
-EVENTS = {1: "past_griddep_wait", 56: "route_start", 57: "route_end", 58: "flags_read", 2: "routed",
+EVENTS = {1: "past_griddep_wait", 14: "router_slices_summed", 15: "router_logits_polled", 56: "route_start", 57: "route_end", 58: "flags_read", 2: "routed",
           3: "first_copy_issued", 4: "last_gate_up_copy_issued", 5: "last_w_down_copy_issued",
           6: "phase_a_done", 7: "exchange_done", 8: "act_staged", 9: "phase_b_done", 10: "out_written",
           11: "producer_drained"}
@@ -37,6 +37,8 @@ def main(argv=None):
     p.add_argument("--T", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--reps", type=int, default=5)
+    p.add_argument("--router", action="store_true",
+                   help="pass router weights instead of logits (moe_ffn_forward_router)")
     args = p.parse_args(argv)
 
     from . import _build
@@ -56,14 +58,20 @@ def main(argv=None):
     layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
     bias = synth.make_bias(wl)
     batches = [synth.make_tokens(wl, T, call=i, device=dev, bias=bias) for i in range(K + 5)]
-    ws = m.new_workspace(T, wl.H, wl.I, wl.E, wl.k)
+    routers = [synth.make_router(wl, device=dev, layer=r) for r in range(R)] if args.router else None
+    ws = (m.new_router_workspace if args.router else m.new_workspace)(T, wl.H, wl.I, wl.E, wl.k)
+    rbias = bias.to(dev)
     out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
 
     def call(j, s):
         x, L = batches[j % len(batches)]
         g, d = layers[j % R]
         o = m.moe_ffn_opts()
-        m.moe_ffn_forward_ex(x, L, g, d, wl.k, out=out, workspace=ws, opts=o, stream=s)
+        if routers is not None:
+            m.moe_ffn_forward_router(x, routers[j % R], rbias, g, d, wl.k, out=out, workspace=ws, opts=o,
+                                     stream=s)
+        else:
+            m.moe_ffn_forward_ex(x, L, g, d, wl.k, out=out, workspace=ws, opts=o, stream=s)
         return o
 
     o = call(0, torch.cuda.current_stream())
@@ -108,7 +116,8 @@ def main(argv=None):
         rows.append(row)
     best = min(rows, key=lambda r: r["us_per_call_instrumented"])
     best["us_per_call_instrumented_median"] = statistics.median(r["us_per_call_instrumented"] for r in rows)
-    print(json.dumps({"workload": args.workload, "T": T, "steps": K, "layers": R, **best}))
+    print(json.dumps({"workload": args.workload, "T": T, "router": args.router, "steps": K, "layers": R,
+                      **best}))
 
 
 if __name__ == "__main__":

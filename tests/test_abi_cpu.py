@@ -162,3 +162,29 @@ def test_timeline_build_is_separate_and_exports_its_reader(L):
     T = ctypes.CDLL(path)
     assert hasattr(T, "moe_ffn_debug_fused_timeline")
     assert not hasattr(L, "moe_ffn_debug_fused_timeline")
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(x=None), 1), (dict(wr=None), 1), (dict(wgu=None), 1), (dict(out=None), 1),
+    (dict(wr=FAKE + 8), 1), (dict(bias=FAKE + 2), 1), (dict(logits=FAKE + 4), 1),
+    (dict(workspace=FAKE + 16), 1), (dict(ws_bytes=1024), 5), (dict(k=9), 1), (dict(H=200), 2),
+    (dict(T=0), 0), (dict(T=0, x=None), 0), (dict(bias=None), None),
+])
+def test_router_entry_argument_checks(L, case, want):
+    a = dict(x=FAKE, wr=FAKE, bias=FAKE, wgu=FAKE, wd=FAKE, T=4, H=256, I=128, E=8, k=2, out=FAKE,
+             workspace=FAKE, ws_bytes=16, logits=None)
+    if want is None:   # only checks that a null bias is accepted: stop at the workspace size
+        a.update(case)
+        want = 5
+    else:
+        a["ws_bytes"] = 1 << 40 if case.get("ws_bytes") is None else case["ws_bytes"]
+        a.update(case)
+    st = L.moe_ffn_forward_router(a["x"], a["wr"], a["bias"], a["wgu"], a["wd"], a["T"], a["H"], a["I"],
+                                  a["E"], a["k"], a["out"], a["workspace"], a["ws_bytes"], a["logits"],
+                                  None, None, None, None)
+    assert st == want
+
+
+def test_router_workspace_bytes(L):
+    assert L.moe_ffn_router_workspace_bytes(4, 256, 128, 8, 2) > L.moe_ffn_workspace_bytes(4, 256, 128, 8, 2)
+    assert L.moe_ffn_router_workspace_bytes(4, 256, 128, 8, 9) == 0
