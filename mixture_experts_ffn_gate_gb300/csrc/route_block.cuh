@@ -11,20 +11,28 @@ namespace moe {
 // first, on equal logits the smaller index (-0.0 == +0.0).  The key of
 // expert e is the 64-bit (logit_key << 32) | ~e: keys are unique and 0 lies
 // below every key.  The warp copies the E logits into `vals` (E words of
-// shared memory owned by the warp, eight loads in flight per lane).  For
-// k <= kRouteList each lane keeps the kRouteList largest of its own keys
-// (e = lane + 32 i) in a sorted register list; k rounds then take the warp
+// shared memory owned by the warp).  Each lane takes its keys (e = lane +
+// 32 i) 8 at a time, sorts them with a sorting network and merges them into
+// a sorted list of its kRouteList largest; k rounds then take the warp
 // maximum of the list heads (redux on the high, then the low half) and the
 // winning lane pops its head.  Larger k rescans the lane's keys below the
 // last winner instead.  Lane j < k returns the expert of slot j and its
 // softmax weight (the softmax over the k chosen logits, shifted by the
-// largest).  With STAGED the logits are already in `vals` (the fused decode
-// kernel's router projection put them there) and `l` is not read.
+// largest, the logits read back from the winning keys).  With STAGED the
+// logits are already in `vals` (the fused decode kernel's router projection
+// put them there) and `l` is not read.
 constexpr int kRouteList = 8;
 
 __device__ __forceinline__ unsigned long long route_key(float f, int e)
 {
     return ((unsigned long long)logit_key(f) << 32) | (uint32_t)~(uint32_t)e;
+}
+
+// The float a logit key came from (-0.0 comes back as +0.0, which no
+// difference of logits can tell apart).
+__device__ __forceinline__ float key_logit(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
 }
 
 __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v)
@@ -35,14 +43,32 @@ __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v)
     return ((unsigned long long)mhi << 32) | mlo;
 }
 
+// a >= b afterwards
+__device__ __forceinline__ void key_order(unsigned long long &a, unsigned long long &b)
+{
+    const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+
+// 8 keys in descending order: a 19-comparator sorting network of depth 6
+__device__ __forceinline__ void sort8_desc(unsigned long long (&x)[8])
+{
+    key_order(x[0], x[2]); key_order(x[1], x[3]); key_order(x[4], x[6]); key_order(x[5], x[7]);
+    key_order(x[0], x[4]); key_order(x[1], x[5]); key_order(x[2], x[6]); key_order(x[3], x[7]);
+    key_order(x[0], x[1]); key_order(x[2], x[3]); key_order(x[4], x[5]); key_order(x[6], x[7]);
+    key_order(x[2], x[4]); key_order(x[3], x[5]);
+    key_order(x[1], x[4]); key_order(x[3], x[6]);
+    key_order(x[1], x[2]); key_order(x[3], x[4]); key_order(x[5], x[6]);
+}
+
 template <bool STAGED = false>
 __device__ __forceinline__ void route_token_warp(const float *__restrict__ l, int E, int k, float *vals, int &sel_j,
                                                  float &w_j)
 {
+    static_assert(kRouteList == 8, "the sorting network below sorts 8 keys");
     const int lane = threadIdx.x & 31;
     unsigned long long list[kRouteList];
-#pragma unroll
-    for (int q = 0; q < kRouteList; ++q) list[q] = 0;
     for (int e0 = 0; e0 < E; e0 += 256) {
         float v[8];
 #pragma unroll
@@ -50,27 +76,41 @@ __device__ __forceinline__ void route_token_warp(const float *__restrict__ l, in
             const int e = e0 + 32 * q + lane;
             if (e < E) v[q] = STAGED ? vals[e] : __ldg(l + e);
         }
+        unsigned long long x[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int e = e0 + 32 * q + lane;
-            if (e < E) {
-                if (!STAGED) vals[e] = v[q];
-                // insert into the descending list: new[i] = max(old[i], min(old[i-1], x))
-                const unsigned long long x = route_key(v[q], e);
+            x[q] = e < E ? route_key(v[q], e) : 0ull;
+            if (!STAGED && e < E) vals[e] = v[q];
+        }
+        sort8_desc(x);
+        if (e0 == 0) {
 #pragma unroll
-                for (int i = kRouteList - 1; i > 0; --i) {
-                    const unsigned long long m = list[i - 1] < x ? list[i - 1] : x;
-                    list[i] = list[i] > m ? list[i] : m;
-                }
-                list[0] = list[0] > x ? list[0] : x;
-            }
+            for (int q = 0; q < 8; ++q) list[q] = x[q];
+        } else {
+            // the 8 largest of two descending lists: the larger of each
+            // list[q], x[7 - q] pair form a bitonic sequence, sorted by a
+            // half-cleaner cascade
+#pragma unroll
+            for (int q = 0; q < 8; ++q) list[q] = list[q] > x[7 - q] ? list[q] : x[7 - q];
+            key_order(list[0], list[4]); key_order(list[1], list[5]);
+            key_order(list[2], list[6]); key_order(list[3], list[7]);
+            key_order(list[0], list[2]); key_order(list[1], list[3]);
+            key_order(list[4], list[6]); key_order(list[5], list[7]);
+            key_order(list[0], list[1]); key_order(list[2], list[3]);
+            key_order(list[4], list[5]); key_order(list[6], list[7]);
         }
     }
     sel_j = 0;
+    uint32_t mine = 0, top = 0;  // logit keys of this lane's slot and of slot 0
     if (k <= kRouteList) {
         for (int r = 0; r < k; ++r) {
             const unsigned long long m = warp_max_key(list[0]);
-            if (lane == r) sel_j = (int)~(uint32_t)m;
+            if (r == 0) top = (uint32_t)(m >> 32);
+            if (lane == r) {
+                sel_j = (int)~(uint32_t)m;
+                mine = (uint32_t)(m >> 32);
+            }
             if (list[0] == m) {
 #pragma unroll
                 for (int i = 0; i < kRouteList - 1; ++i) list[i] = list[i + 1];
@@ -81,7 +121,11 @@ __device__ __forceinline__ void route_token_warp(const float *__restrict__ l, in
         unsigned long long best = list[0];
         for (int r = 0; r < k; ++r) {
             const unsigned long long m = warp_max_key(best);
-            if (lane == r) sel_j = (int)~(uint32_t)m;
+            if (r == 0) top = (uint32_t)(m >> 32);
+            if (lane == r) {
+                sel_j = (int)~(uint32_t)m;
+                mine = (uint32_t)(m >> 32);
+            }
             if (best == m) {
                 best = 0;
                 for (int e = lane; e < E; e += 32) {
@@ -91,10 +135,12 @@ __device__ __forceinline__ void route_token_warp(const float *__restrict__ l, in
             }
         }
     }
-    __syncwarp();
-    const float l0 = vals[__shfl_sync(0xffffffffu, sel_j, 0)];
-    const float ex = lane < k ? expf(vals[sel_j] - l0) : 0.0f;
-    const float s = warp_sum(ex);
+    const float ex = lane < k ? expf(key_logit(mine) - key_logit(top)) : 0.0f;
+    // a butterfly over the 32 lanes, whose first levels only add the zeros
+    // of lanes >= k to lanes < k when k <= 8 (or 16): they are skipped, the
+    // sums of lanes < k keep their bits
+    float s = ex;
+    for (int o = k <= 8 ? 4 : k <= 16 ? 8 : 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     w_j = lane < k ? ex / s : 0.0f;
 }
 
@@ -146,28 +192,5 @@ __device__ __forceinline__ float router_logit_warp(const uint16_t *x, const uint
     for (int s = 0; s < router_slices(H); ++s) acc += router_slice_warp(x, w, H, s, lane);
     return __double2float_rn(acc + (double)bias);
 }
-
-// Block-wide form: warp 0 routes, every thread of the block must call this;
-// vals: E words of shared memory; sel[k] and w[k] (shared) receive the chosen
-// experts in slot order and their softmax weights.
-__device__ __forceinline__ void route_token_block(const float *__restrict__ l, int E, int k, float *vals, int *sel,
-                                                  float *w)
-{
-    if (threadIdx.x < 32) {
-        int e;
-        float wt;
-        route_token_warp(l, E, k, vals, e, wt);
-        if (threadIdx.x < k) {
-            sel[threadIdx.x] = e;
-            w[threadIdx.x] = wt;
-        }
-    }
-    __syncthreads();
-}
-
-// Programmatic dependent launch: wait for the preceding grid's results /
-// allow the next grid to be scheduled.  No-ops without the launch attribute.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 }  // namespace moe
