@@ -12,9 +12,11 @@ independent problems, so there is no data-path collective ("scaling": "weak").
 Timing: the steps run back to back, as a model's layers do, over R layers'
 weights (step j uses layer j % R; R is chosen so that the weights a step
 reads have been streamed out of L2 by the steps in between, i.e. the inputs
-are larger than L2).  W untimed warm-up steps, then the K timed steps as one
-CUDA graph replay (--eager: launched one by one from Python), bracketed by a
-barrier, cudaDeviceSynchronize and CUDA events on the launching stream;
+are larger than L2).  W untimed warm-up steps and one untimed replay of the
+timed graph (its first launch uploads it to the device), then the K timed
+steps as one CUDA graph replay (--eager: launched one by one from Python),
+bracketed by a barrier, cudaDeviceSynchronize and CUDA events on the
+launching stream;
 value = tokens of all ranks / max over ranks of that time.  A second replay
 records the library's stage events between kernels for the roofline of the
 dominant kernel.  cold_call times single calls after an L2 flush each.  e2e
@@ -432,7 +434,11 @@ class Measure:
 
     def timed(self, world):
         """W untimed warm-up steps, then the K timed steps between a barrier,
-        device synchronisation and CUDA events on the launching stream.
+        device synchronisation and CUDA events on the launching stream.  With
+        CUDA graphs the graph of the K steps is also replayed once untimed
+        first: its first launch uploads it to the device and runs about 1.5 us
+        per call slower than every later one, which is what a serving loop
+        replaying one graph sees (warm_steps counts both).
         Returns (ms for the K steps, host wall seconds)."""
         torch = self.torch
         import torch.distributed as dist
@@ -440,8 +446,11 @@ class Measure:
         if self.eager:
             for j in range(W):
                 self.call(j, self.stream)
+            self.warm_steps = W
         else:
             self.g_warm.replay()
+            self.g_main.replay()
+            self.warm_steps = W + K
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -482,6 +491,7 @@ class Measure:
                 self.call(W + j, self.stream, o)
         else:
             g = self.capture(range(W, W + K), arrs)
+            g.replay()   # uploads the graph; the second replay's events count
             g.replay()
         torch.cuda.synchronize()
         return {name: sum(evs[j][s].elapsed_time(evs[j][s + 1]) for j in range(K)) / K
@@ -561,7 +571,7 @@ def supplementary_rows(args, dev, peaks, skip):
             with ClockSampler(dev.index or 0) as clocks:
                 total_ms, _ = run.timed(1)
                 kern = run.stages()
-            row = {"workload": name, "T": T, "layers": R}
+            row = {"workload": name, "T": T, "layers": R, "warmup": run.warm_steps}
             if how == "router":
                 row["entry"] = ("moe_ffn_forward_router: router weights W_r [E,H] ~ N(0,1/H) and the "
                                 "workload's bias passed instead of logits; the projection runs inside the call")
@@ -678,7 +688,8 @@ def main():
     head = run.summary(total_ms, kern_avg, peaks, world)
     line = {
         "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "warmup": run.warm_steps, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": head["path"],
@@ -687,7 +698,8 @@ def main():
                           f"({R * wl.weight_bytes() / 1e9:.1f} GB) cycled step by step, "
                           f"{touched / 1e6:.0f} MB read per step at most, fresh tokens per step"),
                    "timing": ("the K steps launched from Python" if args.eager
-                              else "CUDA graph of the K steps replayed once")
+                              else "CUDA graph of the K steps, replayed once untimed (its first launch "
+                                   "uploads it) and once timed")
                              + ", CUDA events before and after on the launching stream",
                    "parallelism": f"replicas x{world} (independent token streams)"},
         "roofline": head["roofline"],
