@@ -107,6 +107,59 @@ def make_weights(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=
     return wgu, wd
 
 
+MX_BLOCK = 32  # MXFP8: elements per E8M0 scale, along the reduction axis
+
+
+def mx_scale_row_bytes(K: int) -> int:
+    """Bytes per row of an MXFP8 scale array for rows of K elements:
+    K / 32 scales, padded to a multiple of 16 bytes."""
+    return -(-(K // MX_BLOCK) // 16) * 16
+
+
+def _quantize_mx(w: torch.Tensor):
+    """Rows of float32 weights [R, K] -> (E4M3 codes uint8 [R, K], E8M0
+    scales uint8 [R, Ks]): per block of 32, the scale 2^(floor(log2 amax) -
+    8) (amax maps into [256, 512), as the MX specification's conversion
+    recipe does for E4M3, whose largest exponent is 8), then each element
+    divided by it (exact) and rounded to E4M3 (nearest, ties to even),
+    clamped to +-448.  Input generation only: the recipe that turns the
+    seeded Gaussian weights into MXFP8 ones."""
+    R, K = w.shape
+    b = w.view(R, K // MX_BLOCK, MX_BLOCK)
+    amax = b.abs().amax(-1)
+    e = torch.frexp(amax).exponent.to(torch.int32) - 1  # floor(log2 amax) for amax > 0
+    sc = torch.where(amax > 0, e - 8 + 127, torch.full_like(e, 127)).clamp(1, 254)
+    x = torch.ldexp(b, (127 - sc).to(torch.float32).unsqueeze(-1))
+    q = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).view(R, K)
+    s_full = torch.zeros((R, mx_scale_row_bytes(K)), dtype=torch.uint8, device=w.device)
+    s_full[:, : K // MX_BLOCK] = sc.to(torch.uint8)
+    return q, s_full
+
+
+def make_weights_mxfp8(wl: Workload, device="cpu", *, H=None, I=None, E=None, experts=None, layer=0):
+    """MXFP8 expert weights: (wgu_q uint8 [E, 2I, H], wgu_s uint8 [E, 2I,
+    Hs], wd_q uint8 [E, H, I], wd_s uint8 [E, H, Is]) -- the same seeded
+    Gaussian draws as make_weights (N(0, 1/H) and N(0, 1/I)), quantised by
+    _quantize_mx instead of rounded to BF16.  Arguments as for
+    make_weights."""
+    tag = () if layer == 0 else ("layer", layer)
+    H = H or wl.H
+    I = I or wl.I
+    E = E or wl.E
+    ids = list(range(E)) if experts is None else list(experts)
+    n = len(ids)
+    gq = torch.empty((n, 2 * I, H), dtype=torch.uint8, device=device)
+    gs = torch.empty((n, 2 * I, mx_scale_row_bytes(H)), dtype=torch.uint8, device=device)
+    dq = torch.empty((n, H, I), dtype=torch.uint8, device=device)
+    ds = torch.empty((n, H, mx_scale_row_bytes(I)), dtype=torch.uint8, device=device)
+    for j, e in enumerate(ids):
+        gq[j], gs[j] = _quantize_mx(_randn((2 * I, H), 1.0 / math.sqrt(H), device,
+                                           seed_for(wl.name, H, I, "w_gate_up", e, *tag)))
+        dq[j], ds[j] = _quantize_mx(_randn((H, I), 1.0 / math.sqrt(I), device,
+                                           seed_for(wl.name, H, I, "w_down", e, *tag)))
+    return gq, gs, dq, ds
+
+
 def make_router(wl: Workload, device="cpu", *, H=None, E=None, layer=0):
     """Router weights W_r [E, H] ~ N(0, 1/H) -> BF16 (a linear layer's
     weight, one row per expert), for calls that pass the router weights

@@ -7,7 +7,8 @@ never imports the product: the two share no code.
 
 The arithmetic lives in ``moe_oracle.c`` (plain C, IEEE double, no
 ``-ffast-math``).  This module only compiles it with gcc and marshals numpy
-arrays to it.  BF16 tensors travel as their raw 16-bit patterns (numpy
+arrays to it.  MXFP8 expert weights (``mxfp8.py``) are decoded and
+dequantised exactly into BF16 numbers before they reach it.  BF16 tensors travel as their raw 16-bit patterns (numpy
 ``uint16``), so the oracle reads exactly the bits the GPU reads.
 
 What each step computes, and the passage it follows, is written at the top of
@@ -182,3 +183,12 @@ def forward_router(x, w_router, bias, wgu, wd, k, **kw):
     logits = router_logits(x, w_router, bias)
     out, idx, w = forward(x, logits, wgu, wd, k, **kw)
     return out, idx, w, logits
+
+
+def forward_mxfp8(x, logits, wgu_q, wgu_s, wd_q, wd_s, k, **kw):
+    """The layer with MXFP8 expert weights (codes uint8 [Eb, 2I, H] and
+    [Eb, H, I], scales uint8 [Eb, 2I, Hs] and [Eb, H, Is]; see mxfp8.py):
+    the weights dequantised exactly, then the BF16 layer's definition.
+    Returns (out, idx, w)."""
+    from .mxfp8 import dequantize_bf16
+    return forward(x, logits, dequantize_bf16(wgu_q, wgu_s), dequantize_bf16(wd_q, wd_s), k, **kw)
