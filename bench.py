@@ -33,7 +33,9 @@ call's HBM fraction, the dominant kernel's roofline and the TFLOP/s against
 dense BF16 peak and against min(peak, HBM peak x flop/byte).  Two of the
 rows ("entry": moe_ffn_forward_router) run the 2048-hidden decode layer at
 T=1 and 2 with the router projection inside the call (router weights and
-bias passed instead of logits).
+bias passed instead of logits); four ("entry": moe_ffn_forward_mxfp8) run
+the 2048-hidden layer at T=1/2/4 and the 7168-hidden one at T=1 with MXFP8
+expert weights (their bytes counted at 1 + 1/32 per weight).
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -94,6 +96,9 @@ def parse():
                    help="single calls timed after an L2 flush each (secondary figure)")
     p.add_argument("--no-supplementary", action="store_true",
                    help="omit the other configurations' rows (measured after the headline line)")
+    p.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
+                   help="expert weight format of the headline line (mxfp8: moe_ffn_forward_mxfp8, "
+                        "one to four tokens; no e2e or CPU-baseline figures)")
     return p.parse_args()
 
 
@@ -199,17 +204,23 @@ class ClockSampler:
                                                          if r[3].replace(".", "").isdigit())}
 
 
-def algorithmic_bytes(wl, T, U):
+# bytes per expert-weight element: BF16, or MXFP8 (one E4M3 byte plus one
+# E8M0 scale byte per 32 elements; the padding of the scale rows is not
+# counted)
+BPE = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32}
+
+
+def algorithmic_bytes(wl, T, U, bpe=2.0):
     """Per-call algorithmic HBM bytes: each touched expert's weights once
-    (U*6*H*I), x in (T*H*2), logits in (T*E*4), out written (T*H*4)."""
-    return U * 6 * wl.H * wl.I + T * wl.H * 2 + T * wl.E * 4 + T * wl.H * 4
+    (U*3*H*I*bpe), x in (T*H*2), logits in (T*E*4), out written (T*H*4)."""
+    return U * 3 * wl.H * wl.I * bpe + T * wl.H * 2 + T * wl.E * 4 + T * wl.H * 4
 
 
-def kernel_bytes(kernel, wl, T, U, k):
+def kernel_bytes(kernel, wl, T, U, k, bpe=2.0):
     """Algorithmic bytes of one launch of a kernel."""
     H, I = wl.H, wl.I
     if kernel == "decode_fused":  # the whole layer in one kernel; act written and read back once
-        return U * 6 * H * I + T * H * 2 + T * wl.E * 4 + T * H * 4 + 2 * T * k * I * 4
+        return U * 3 * H * I * bpe + T * H * 2 + T * wl.E * 4 + T * H * 4 + 2 * T * k * I * 4
     if kernel == "decode_gate_up":
         return U * 2 * I * H * 2 + T * H * 2 + T * k * I * 4
     if kernel == "decode_down":
@@ -344,16 +355,18 @@ def cpu_model():
 SUPPLEMENTARY = [
     ("decode_h2048_i768_e128_k8", (2,)),
     ("decode_h2048_i768_e128_k8+router", (1, 2)),
+    ("decode_h2048_i768_e128_k8+mxfp8", (1, 2, 4)),
+    ("decode_h7168_i2048_e384_k8_bias+mxfp8", (1,)),
     ("decode_h4096_i1536_e128_k8_bias", (1, 4, 16, 64)),
     ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),
 ]
 
 
-def layer_count(wl, T, layers_arg):
+def layer_count(wl, T, layers_arg, bpe=2.0):
     """Layers' weights the steps cycle through: enough that the weights one
     step reads were streamed out of L2 by the steps in between."""
-    touched = algorithmic_bytes(wl, T, min(wl.E, T * wl.k))
+    touched = algorithmic_bytes(wl, T, min(wl.E, T * wl.k), bpe)
     R = max(2, math.ceil(3 * L2_BYTES / touched)) if layers_arg is None else layers_arg
     return max(1, min(R, int(LAYER_MEM_CAP // wl.weight_bytes()))), touched
 
@@ -365,7 +378,7 @@ class Measure:
     launches); stages() replays them with the library's stage events between
     kernels; summary() gives the figures of one line."""
 
-    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager, routers=None):
+    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager, routers=None, mx=False):
         import torch
         from mixture_experts_ffn_gate_gb300 import moe_ffn as m
         from mixture_experts_ffn_gate_gb300 import synth
@@ -377,6 +390,10 @@ class Measure:
         # weights and the bias instead of logits (moe_ffn_forward_router)
         self.routers = routers
         self.rbias = bias.to(dev) if routers is not None else None
+        # mx: the layers hold MXFP8 weights (codes and scales, four tensors)
+        # and the calls go through moe_ffn_forward_mxfp8
+        self.mx = mx
+        self.bpe = BPE["mxfp8" if mx else "bf16"]
         batch_bytes = T * (wl.H * 2 + wl.E * 4)
         self.NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
         calls = rank_calls(rank, W, K)   # rank r processes its own calls of the token stream
@@ -410,8 +427,12 @@ class Measure:
 
     def call(self, j, stream, opts=None, idx=None):
         x, L = self.batches[j % self.NB]
-        lw_gu, lw_d = self.layers[j % self.R]
         opts = opts if opts is not None else self.new_opts()
+        if self.mx:
+            self.m.moe_ffn_forward_mxfp8(x, L, *self.layers[j % self.R], self.wl.k, out=self.out, workspace=self.ws,
+                                         topk_idx=idx, opts=opts, stream=stream)
+            return
+        lw_gu, lw_d = self.layers[j % self.R]
         if self.routers is not None:
             self.m.moe_ffn_forward_router(x, self.routers[j % self.R], self.rbias, lw_gu, lw_d, self.wl.k,
                                           out=self.out, workspace=self.ws, topk_idx=idx, opts=opts, stream=stream)
@@ -501,7 +522,7 @@ class Measure:
         """Throughput, the whole call's HBM fraction, the dominant kernel's
         roofline and the tensor figures of one workload line."""
         wl, T, K = self.wl, self.T, self.K
-        call_bytes = sum(algorithmic_bytes(wl, T, u) for u in self.U) / K
+        call_bytes = sum(algorithmic_bytes(wl, T, u, self.bpe) for u in self.U) / K
         # calls with the router projection inside also read W_r (E*H BF16)
         router_bytes = wl.E * wl.H * 2 if self.routers is not None else 0
         call_bytes += router_bytes
@@ -515,7 +536,7 @@ class Measure:
         dom = max(kern_avg, key=kern_avg.get)
         one_kernel = len(kern_avg) == 1
         dom_ms = ms_call if one_kernel else kern_avg[dom]
-        dom_bytes = sum(kernel_bytes(dom, wl, T, u, wl.k) for u in self.U) / K
+        dom_bytes = sum(kernel_bytes(dom, wl, T, u, wl.k, self.bpe) for u in self.U) / K
         if dom == "decode_fused":
             dom_bytes += router_bytes
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
@@ -561,13 +582,14 @@ def supplementary_rows(args, dev, peaks, skip):
         Ts = [T for T in Ts if (entry, T) != skip]
         if not Ts:
             continue
-        R = max(layer_count(wl, T, args.layers)[0] for T in Ts)
-        layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
+        R = max(layer_count(wl, T, args.layers, BPE["mxfp8" if how == "mxfp8" else "bf16"])[0] for T in Ts)
+        make = synth.make_weights_mxfp8 if how == "mxfp8" else synth.make_weights
+        layers = [make(wl, device=dev, layer=r) for r in range(R)]
         routers = [synth.make_router(wl, device=dev, layer=r) for r in range(R)] if how == "router" else None
         bias = synth.make_bias(wl)
         for T in Ts:
             run = Measure(wl, T, dev, args.steps, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
-                args.path], layers, bias, 0, args.eager, routers=routers)
+                args.path], layers, bias, 0, args.eager, routers=routers, mx=how == "mxfp8")
             with ClockSampler(dev.index or 0) as clocks:
                 total_ms, _ = run.timed(1)
                 kern = run.stages()
@@ -575,6 +597,10 @@ def supplementary_rows(args, dev, peaks, skip):
             if how == "router":
                 row["entry"] = ("moe_ffn_forward_router: router weights W_r [E,H] ~ N(0,1/H) and the "
                                 "workload's bias passed instead of logits; the projection runs inside the call")
+            if how == "mxfp8":
+                row["entry"] = ("moe_ffn_forward_mxfp8: the same seeded weights quantised to MXFP8 (E4M3 "
+                                "codes, one E8M0 scale per 32 elements along K); bytes per weight 1 + 1/32")
+                row["dtype"] = "mxfp8 weights, bf16 activations, f32 arithmetic"
             row.update(run.summary(total_ms, kern, peaks, 1))
             row["clocks"] = clocks.summary()
             rows.append(row)
@@ -617,12 +643,16 @@ def main():
     dev = torch.device("cuda", local)
     K, W = args.steps, max(3, args.warmup)
     bias = synth.make_bias(wl)
-    R, touched = layer_count(wl, T, args.layers)
-    layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
-    wgu, wd = layers[0]
+    mx = args.weights == "mxfp8"
+    if mx:   # the MXFP8 entry has no host-buffer form; the oracle baseline is the BF16 one
+        args.no_e2e = args.skip_baseline = True
+    R, touched = layer_count(wl, T, args.layers, BPE[args.weights])
+    make = synth.make_weights_mxfp8 if mx else synth.make_weights
+    layers = [make(wl, device=dev, layer=r) for r in range(R)]
+    wgu, wd = (None, None) if mx else layers[0]
     path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
                  "grouped": m.MOE_PATH_GROUPED}[args.path]
-    run = Measure(wl, T, dev, K, W, path_code, layers, bias, rank, args.eager)
+    run = Measure(wl, T, dev, K, W, path_code, layers, bias, rank, args.eager, mx=mx)
     stream = run.stream
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sum = torch.empty((), dtype=torch.float32, device=dev)
@@ -690,12 +720,12 @@ def main():
         "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": run.warm_steps, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "mxfp8 weights, bf16 activations" if mx else "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "path": head["path"],
                    "layers": R,
                    "l2": (f"inputs larger than L2: {R} layers' weights "
-                          f"({R * wl.weight_bytes() / 1e9:.1f} GB) cycled step by step, "
+                          f"({R * wl.weight_bytes() * BPE[args.weights] / 2 / 1e9:.1f} GB) cycled step by step, "
                           f"{touched / 1e6:.0f} MB read per step at most, fresh tokens per step"),
                    "timing": ("the K steps launched from Python" if args.eager
                               else "CUDA graph of the K steps, replayed once untimed (its first launch "

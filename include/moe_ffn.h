@@ -214,6 +214,38 @@ int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16,
                            moe_ffn_opts *opts, cudaStream_t stream);
 
 /*
+ * The layer with MXFP8 expert weights, for decode steps of one to four
+ * tokens.  The Mixture-of-Kittens article ("커서가 MoE 학습 메가커널 믹스처 오브
+ * 키튼스를 아파치 2.0으로 공개했다", section 2.37배는 어떤 기준선과 비교한
+ * 숫자인가) measures the layer with MXFP8 operands; the format is the OCP
+ * Microscaling (MX) specification's MXFP8 with E4M3 elements, applied here
+ * to the expert weights (the activations stay BF16):
+ *   w_gate_up_e4m3  [E, 2I, H] uint8 E4M3 codes (row layout as for BF16),
+ *   w_gate_up_scale [E, 2I, Sh] uint8 E8M0 scales, Sh = MOE_FFN_MX_SCALE_BYTES(H),
+ *   w_down_e4m3     [E, H, I] uint8 E4M3 codes,
+ *   w_down_scale    [E, H, Si] uint8 E8M0 scales, Si = MOE_FFN_MX_SCALE_BYTES(I).
+ * Weight [e, r, c] = E4M3(code) * 2^(scale[e, r, c / 32] - 127); a scale row
+ * holds K / 32 scales, then padding to a multiple of 16 bytes (ignored).
+ * NaN codes (E4M3 S.1111.111, scale 255) are not valid inputs.  Products
+ * and sums are formed in FP32 as in the BF16 path; the results are within
+ * the same tolerance of the FP64 layer on the dequantised weights.
+ * All device pointers 16-byte aligned; the workspace is moe_ffn_forward_ex's
+ * (at least moe_ffn_workspace_bytes, same state rules).  Only the fused
+ * decode kernel is built for this format: shapes it cannot take (T > 4,
+ * or too large for its shared-memory ring) and opts->path other than AUTO
+ * or DECODE return MOE_ERR_UNSUPPORTED_SHAPE, with nothing launched.
+ */
+#define MOE_FFN_MX_SCALE_BYTES(K) ((((K) / 32) + 15) / 16 * 16)
+int moe_ffn_forward_mxfp8(const void *x_bf16, const float *router_logits_f32,
+                          const void *w_gate_up_e4m3, const void *w_gate_up_scale,
+                          const void *w_down_e4m3, const void *w_down_scale,
+                          int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                          float *out_f32, void *workspace,
+                          size_t workspace_bytes, int32_t *topk_idx_out,
+                          float *topk_w_out, moe_ffn_opts *opts,
+                          cudaStream_t stream);
+
+/*
  * End-to-end form for callers whose tokens live in host memory: x_host
  * [T,H] bf16, logits_host [T,E] f32 and out_host [T,H] f32 are HOST buffers
  * (page-locked for the copies to be asynchronous); the weights are device

@@ -80,6 +80,9 @@
 #include <random>
 #include <type_traits>
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "route_block.cuh"
@@ -355,6 +358,149 @@ __device__ __forceinline__ void down_rows(const uint8_t *const *rowp, const floa
     if (lane % W == 0 && slot < RB * NB && r < nu) part[r * A + asg[b]] = t;
 }
 
+// ---- MXFP8 weights (the MX instantiation)
+// E4M3 codes with one E8M0 scale per 32 elements along the reduction axis
+// (the OCP MX specification's MXFP8).  The ring carries the codes and the
+// scale bytes of the rows; each lane takes 16 consecutive elements per step
+// (one 16-byte load), converts them to FP32 exactly (E4M3 -> F16 -> F32),
+// forms its partial sums with the activations in FP32, and adds each partial
+// sum times its block's scale (a power of two, so scaling the partial sum or
+// every weight differ only in FP32 rounding order).
+
+struct MxArgs {
+    const uint8_t *gq, *gs;  // W_gate_up codes [E][2I][H] and scales [E][2I][hs]
+    const uint8_t *dq, *ds;  // W_down codes [E][H][I] and scales [E][H][is]
+    int hs, is;              // scale bytes per row (K / 32 padded to 16)
+};
+
+// 2^(s - 127) as a float: the biased exponent itself for s >= 1, the
+// subnormal 2^-127 for s = 0 (s = 255, NaN in the format, is not an input).
+__device__ __forceinline__ float e8m0_scale(uint32_t s)
+{
+    return __uint_as_float(s ? s << 23 : 0x00400000u);
+}
+
+// 16 E4M3 codes (byte j = element j) to their values in FP32, exactly.
+__device__ __forceinline__ void unpack16_e4m3(const uint4 &v, float (&f)[16])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const __half2_raw r =
+                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> (16 * hf)), __NV_E4M3);
+            const float2 f2 = __half22float2(__half2(r));
+            f[4 * q + 2 * hf] = f2.x;
+            f[4 * q + 2 * hf + 1] = f2.y;
+        }
+}
+
+// gate_up_pair with MXFP8 rows: codes grow/urow, scale rows gsc/usc.
+template <int NB>
+__device__ __forceinline__ void gate_up_pair_mx(const uint8_t *grow, const uint8_t *urow, const uint8_t *gsc,
+                                                const uint8_t *usc, const uint16_t *const *xr, int H, int lane,
+                                                const int *asg, float *act_g, unsigned long long *act_t,
+                                                uint32_t tag, int I, int col)
+{
+    constexpr int N = pow2_ceil(2 * NB);  // gate of token b in slot b, up in slot NB + b
+    float acc[N];
+#pragma unroll
+    for (int q = 0; q < N; ++q) acc[q] = 0.0f;
+#pragma unroll 2
+    for (int h = lane * 16; h < H; h += 512) {
+        float gf[16], uf[16];
+        unpack16_e4m3(lds16(grow + h), gf);
+        unpack16_e4m3(lds16(urow + h), uf);
+        const float sg = e8m0_scale(gsc[h >> 5]), su = e8m0_scale(usc[h >> 5]);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            float xf[16];
+            unpack8(lds16(xr[b] + h), xf);
+            unpack8(lds16(xr[b] + h + 8), xf + 8);
+            float pg = 0.0f, pu = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                pg = fmaf(gf[q], xf[q], pg);
+                pu = fmaf(uf[q], xf[q], pu);
+            }
+            acc[b] = fmaf(pg, sg, acc[b]);
+            acc[NB + b] = fmaf(pu, su, acc[NB + b]);
+        }
+    }
+    float t, u;
+    int b;
+    bool writer;
+    if constexpr (NB == 1) {
+        warp_sum_n(acc);
+        t = acc[0];
+        u = acc[1];
+        b = 0;
+        writer = lane == 0;
+    } else {
+        constexpr int W = 32 / N;
+        t = warp_sum_split(acc, lane);
+        u = __shfl_sync(0xffffffffu, t, (lane + NB * W) & 31);
+        b = lane / W;
+        writer = lane % W == 0 && b < NB;
+    }
+    if (writer) {
+        const float a = swiglu(t, u);
+        const size_t at = (size_t)asg[b] * I + col;
+        if (act_t)
+            ptx::st_relaxed_gpu(act_t + at, ((unsigned long long)tag << 32) | __float_as_uint(a));
+        else
+            act_g[at] = a;
+    }
+}
+
+// down_rows with MXFP8 rows: codes rowp[r], scale rows scp[r].
+template <int NB>
+__device__ __forceinline__ void down_rows_mx(const uint8_t *const *rowp, const uint8_t *const *scp,
+                                             const float *const *arow, int I, int lane, int nu, const int *asg,
+                                             float *part, int A)
+{
+    constexpr int RB = rows_for(NB);
+    constexpr int N = pow2_ceil(RB * NB);  // row r, assignment b in slot r * NB + b
+    float acc[N];
+#pragma unroll
+    for (int q = 0; q < N; ++q) acc[q] = 0.0f;
+    for (int i = lane * 16; i < I; i += 512) {
+        // elements i .. i + 15 of the two-plane act rows: groups i / 8 and
+        // i / 8 + 1, each 4 values in plane 0 and 4 in plane 1
+        float af[NB][16];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            const float *p0 = arow[b] + i / 2, *p1 = arow[b] + I / 2 + i / 2;
+            const float4 v0 = *reinterpret_cast<const float4 *>(p0);
+            const float4 v1 = *reinterpret_cast<const float4 *>(p1);
+            const float4 v2 = *reinterpret_cast<const float4 *>(p0 + 4);
+            const float4 v3 = *reinterpret_cast<const float4 *>(p1 + 4);
+            af[b][0] = v0.x; af[b][1] = v0.y; af[b][2] = v0.z; af[b][3] = v0.w;
+            af[b][4] = v1.x; af[b][5] = v1.y; af[b][6] = v1.z; af[b][7] = v1.w;
+            af[b][8] = v2.x; af[b][9] = v2.y; af[b][10] = v2.z; af[b][11] = v2.w;
+            af[b][12] = v3.x; af[b][13] = v3.y; af[b][14] = v3.z; af[b][15] = v3.w;
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            float wf[16];
+            unpack16_e4m3(lds16(rowp[r] + i), wf);
+            const float sc = e8m0_scale(scp[r][i >> 5]);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                float p = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) p = fmaf(wf[q], af[b][q], p);
+                acc[r * NB + b] = fmaf(p, sc, acc[r * NB + b]);
+            }
+        }
+    }
+    constexpr int W = 32 / N;
+    const float t = warp_sum_split(acc, lane);
+    const int slot = lane / W, r = slot / NB, b = slot - r * NB;
+    if (lane % W == 0 && slot < RB * NB && r < nu) part[r * A + asg[b]] = t;
+}
+
 // The router projection's inputs for the ROUTER instantiation: W_r [E][H]
 // BF16, the bias [E] (nullable), the tagged logit words [T*E] (16 bytes
 // each) and the caller's logits output (nullable).
@@ -396,7 +542,7 @@ __device__ __forceinline__ unsigned long long mix64(unsigned long long z)
 // polls copy b % kLogitReplicas, so the grid's polls spread over that many
 // times more L2 lines (every CTA polls every logit, so one copy would draw
 // all of them to the same few lines).
-template <int NT, bool ROUTER>
+template <int NT, bool ROUTER, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const uint16_t *__restrict__ x, const float *__restrict__ logits,
                         const uint16_t *__restrict__ wgu, const uint16_t *__restrict__ wd, int T, int H, int I, int E,
@@ -405,8 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         unsigned long long tag_cap, unsigned long long *__restrict__ flags,
                         unsigned long long epoch_salt, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
                         float *__restrict__ out, int32_t *__restrict__ exchange_out, uint64_t wait_ns,
-                        int skip_arrival, RouterArgs ra)
+                        int skip_arrival, RouterArgs ra, MxArgs mx)
 {
+    static_assert(!(ROUTER && MX), "the router projection is built for BF16 weights only");
     extern __shared__ __align__(128) uint8_t sm[];
     const int A = T * k;
     const uint32_t xa = xa_bytes(T, H, I, k, act_in_smem != 0);
@@ -625,11 +772,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t bytes = (uint32_t)n * 2 * H;  // one block: gate or up rows
-                const uint16_t *gate = wgu + ((int64_t)s_uexp[u] * 2 * I + i0) * H;
-                ptx::mbar_arrive_expect_tx(full + s, 2 * bytes);
-                ptx::bulk_load(sm + (size_t)s * slot_bytes, gate, bytes, full + s);
-                ptx::bulk_load(sm + (size_t)s * slot_bytes + bytes, gate + (int64_t)I * H, bytes, full + s);
+                if constexpr (MX) {
+                    // gate codes, up codes, gate scales, up scales
+                    const uint32_t bytes = (uint32_t)n * H, sb = (uint32_t)n * mx.hs;
+                    const int64_t r0 = (int64_t)s_uexp[u] * 2 * I + i0;  // first gate row
+                    uint8_t *dst = sm + (size_t)s * slot_bytes;
+                    ptx::mbar_arrive_expect_tx(full + s, 2 * bytes + 2 * sb);
+                    ptx::bulk_load(dst, mx.gq + r0 * H, bytes, full + s);
+                    ptx::bulk_load(dst + bytes, mx.gq + (r0 + I) * H, bytes, full + s);
+                    ptx::bulk_load(dst + 2 * bytes, mx.gs + r0 * mx.hs, sb, full + s);
+                    ptx::bulk_load(dst + 2 * bytes + sb, mx.gs + (r0 + I) * mx.hs, sb, full + s);
+                } else {
+                    const uint32_t bytes = (uint32_t)n * 2 * H;  // one block: gate or up rows
+                    const uint16_t *gate = wgu + ((int64_t)s_uexp[u] * 2 * I + i0) * H;
+                    ptx::mbar_arrive_expect_tx(full + s, 2 * bytes);
+                    ptx::bulk_load(sm + (size_t)s * slot_bytes, gate, bytes, full + s);
+                    ptx::bulk_load(sm + (size_t)s * slot_bytes + bytes, gate + (int64_t)I * H, bytes, full + s);
+                }
                 if (c == 0) MOE_TL(3);
                 p += n;
                 i0 += n;
@@ -663,11 +822,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_desc[s] = make_int4(gq, ngq, uu, rr);
                 gq += ngq;
                 // the arrive releases the descriptor to the consumers that wait on the slot
-                ptx::mbar_arrive_expect_tx(full + s, (uint32_t)len_q * 2 * I);
-                for (int off = 0; off < len_q;) {  // one copy per expert run
+                // MX: the slot holds rps code rows, then their scale rows
+                ptx::mbar_arrive_expect_tx(full + s, (uint32_t)len_q * (MX ? I + mx.is : 2 * I));
+                for (int off = 0; off < len_q;) {  // one copy per expert run (two for MX)
                     const int len = min(len_q - off, nh - rr);
-                    ptx::bulk_load(sm + (size_t)s * slot_bytes + (size_t)off * 2 * I,
-                                   wd + ((int64_t)s_uexp[uu] * H + h_lo + rr) * I, (uint32_t)len * 2 * I, full + s);
+                    const int64_t row = (int64_t)s_uexp[uu] * H + h_lo + rr;
+                    if constexpr (MX) {
+                        uint8_t *dst = sm + (size_t)s * slot_bytes;
+                        ptx::bulk_load(dst + (size_t)off * I, mx.dq + row * I, (uint32_t)len * I, full + s);
+                        ptx::bulk_load(dst + (size_t)rps * I + (size_t)off * mx.is, mx.ds + row * mx.is,
+                                       (uint32_t)len * mx.is, full + s);
+                    } else {
+                        ptx::bulk_load(sm + (size_t)s * slot_bytes + (size_t)off * 2 * I, wd + row * I,
+                                       (uint32_t)len * 2 * I, full + s);
+                    }
                     off += len;
                     rr += len;
                     if (rr == nh) {
@@ -738,16 +906,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int b = 0; b < NT; ++b) xr[b] = xs + s_xoff[a0 + (b < na ? b : 0)];
                 for (; m < n; m += kConsumers) {
-                    const uint8_t *grow = chunk + (size_t)m * 2 * H;
-                    const uint8_t *urow = grow + (size_t)n * 2 * H;
                     const int col = plane_pos(i0 + m, I);
-                    if (na == 1) gate_up_pair<1>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
-                    if constexpr (NT >= 2) {
-                        if (na == 2) gate_up_pair<2>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
-                    }
-                    if constexpr (NT >= 4) {
-                        if (na == 3) gate_up_pair<3>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
-                        if (na == 4) gate_up_pair<4>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                    if constexpr (MX) {
+                        const uint8_t *grow = chunk + (size_t)m * H;
+                        const uint8_t *urow = grow + (size_t)n * H;
+                        const uint8_t *gsc = chunk + (size_t)2 * n * H + (size_t)m * mx.hs;
+                        const uint8_t *usc = gsc + (size_t)n * mx.hs;
+                        if (na == 1)
+                            gate_up_pair_mx<1>(grow, urow, gsc, usc, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                        if constexpr (NT >= 2) {
+                            if (na == 2)
+                                gate_up_pair_mx<2>(grow, urow, gsc, usc, xr, H, lane, s_asg + a0, act_g, act_w, e32, I,
+                                                   col);
+                        }
+                        if constexpr (NT >= 4) {
+                            if (na == 3)
+                                gate_up_pair_mx<3>(grow, urow, gsc, usc, xr, H, lane, s_asg + a0, act_g, act_w, e32, I,
+                                                   col);
+                            if (na == 4)
+                                gate_up_pair_mx<4>(grow, urow, gsc, usc, xr, H, lane, s_asg + a0, act_g, act_w, e32, I,
+                                                   col);
+                        }
+                    } else {
+                        const uint8_t *grow = chunk + (size_t)m * 2 * H;
+                        const uint8_t *urow = grow + (size_t)n * 2 * H;
+                        if (na == 1) gate_up_pair<1>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                        if constexpr (NT >= 2) {
+                            if (na == 2)
+                                gate_up_pair<2>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                        }
+                        if constexpr (NT >= 4) {
+                            if (na == 3)
+                                gate_up_pair<3>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                            if (na == 4)
+                                gate_up_pair<4>(grow, urow, xr, H, lane, s_asg + a0, act_g, act_w, e32, I, col);
+                        }
                     }
                 }
             }
@@ -896,17 +1089,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (; g < gb + ng; g += kConsumers) {
                                 const int u0 = (g - gb) << lg, nu = min(1 << lg, len - u0);
                                 const uint8_t *rowp[4];
-#pragma unroll
-                                for (int r = 0; r < 4; ++r)
-                                    rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
                                 float *const pu = pr + (size_t)u0 * A;
-                                if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
-                                if constexpr (NT >= 2) {
-                                    if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
-                                }
-                                if constexpr (NT >= 4) {
-                                    if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
-                                    if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                if constexpr (MX) {
+                                    const uint8_t *scp[4];
+#pragma unroll
+                                    for (int r = 0; r < 4; ++r) {
+                                        const size_t rw = (size_t)(off + u0 + (r < nu ? r : 0));
+                                        rowp[r] = chunk + rw * I;
+                                        scp[r] = chunk + (size_t)rps * I + rw * mx.is;
+                                    }
+                                    if (na == 1) down_rows_mx<1>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    if constexpr (NT >= 2) {
+                                        if (na == 2) down_rows_mx<2>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    }
+                                    if constexpr (NT >= 4) {
+                                        if (na == 3) down_rows_mx<3>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                        if (na == 4) down_rows_mx<4>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int r = 0; r < 4; ++r)
+                                        rowp[r] = chunk + (size_t)(off + u0 + (r < nu ? r : 0)) * 2 * I;
+                                    if (na == 1) down_rows<1>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    if constexpr (NT >= 2) {
+                                        if (na == 2) down_rows<2>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    }
+                                    if constexpr (NT >= 4) {
+                                        if (na == 3) down_rows<3>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                        if (na == 4) down_rows<4>(rowp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    }
                                 }
                             }
                         }
@@ -947,28 +1158,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Geometry: phase A copies rpc whole gate/up row pairs (about kChunkTarget,
 // or kChunkTargetOne, bytes); a slot holds the larger of that, kSlotMin and
-// one W_down row, and phase B fills each slot with rps = slot / 2I rows.  As
-// many slots as fit in shared memory beside the payload.
+// one W_down row, and phase B fills each slot with rps = slot / (bytes of a
+// W_down row) rows.  As many slots as fit in shared memory beside the
+// payload.  A BF16 row of K elements is 2K bytes; an MXFP8 row is K code
+// bytes plus its scale row (mx_scale_bytes(K)).
 struct Plan {
     int nt, rpc, rps, slot_bytes, slots, nh_max, act_in_smem;
     uint32_t payload;
 };
 
-Plan plan_for(int T, int H, int I, int k, int n_sm)
+Plan plan_for(int T, int H, int I, int k, int n_sm, bool mx = false)
 {
     Plan p;
     p.nt = T <= 1 ? 1 : T <= 2 ? 2 : 4;
     p.nh_max = (H + n_sm - 1) / n_sm;
+    const int pair_bytes = mx ? 2 * (H + mx_scale_bytes(H)) : 4 * H;
+    const int row_bytes = mx ? I + mx_scale_bytes(I) : 2 * I;
     // one token does little work per byte: shorter chunks pipeline better
     // (measured: 2048-hidden layer 22.9 -> 22.1 us), as long as a chunk
     // keeps two pairs; with more tokens per pair, or one pair per chunk,
     // they are slower
-    const int target = (T == 1 && kChunkTargetOne / (4 * H) >= 2) ? kChunkTargetOne : kChunkTarget;
-    p.rpc = target / (4 * H) > 0 ? target / (4 * H) : 1;
-    const int a = p.rpc * 4 * H;
+    const int target = (T == 1 && kChunkTargetOne / pair_bytes >= 2) ? kChunkTargetOne : kChunkTarget;
+    p.rpc = target / pair_bytes > 0 ? target / pair_bytes : 1;
+    const int a = p.rpc * pair_bytes;
     int slot = a > kSlotMin ? a : kSlotMin;
-    if (2 * I > slot) slot = 2 * I;
-    p.rps = slot / (2 * I);
+    if (row_bytes > slot) slot = row_bytes;
+    p.rps = slot / row_bytes;
     p.slot_bytes = slot;
     for (int staged = 1; staged >= 0; --staged) {  // act rows in shared memory if the ring keeps kMinSlots
         p.act_in_smem = staged;
@@ -1008,12 +1223,13 @@ unsigned long long epoch_salt()
 
 }  // namespace
 
-bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm)
+bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm, bool mx)
 {
     if (T < 1 || T > kMaxTokens || T * k > kMaxAsg || n_sm > kMaxGridCtas) return false;
     // the kernel splits pairs and output dims over the CTAs in 32-bit arithmetic
     if ((uint64_t)T * k * I * n_sm >= (1ull << 32) || (uint64_t)H * n_sm >= (1ull << 32)) return false;
-    const Plan p = plan_for(T, H, I, k, n_sm);
+    if (mx && (H % 32 || I % 32)) return false;
+    const Plan p = plan_for(T, H, I, k, n_sm, mx);
     return p.slots >= kMinSlots && (int64_t)T * E * 4 <= (int64_t)p.slots * p.slot_bytes;  // routing scratch
 }
 
@@ -1038,9 +1254,10 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
                                 unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
                                 float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
-                                const FusedRouter *router, cudaStream_t s)
+                                const FusedRouter *router, const FusedMx *mxw, cudaStream_t s)
 {
-    const Plan p = plan_for(T, H, I, k, n_sm);
+    if (router && mxw) return cudaErrorInvalidValue;  // no such instantiation
+    const Plan p = plan_for(T, H, I, k, n_sm, mxw != nullptr);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_sm);
     cfg.blockDim = dim3(kThreads);
@@ -1059,16 +1276,23 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
     RouterArgs ra{};
     if (router)
         ra = RouterArgs{(const uint16_t *)router->wr, router->bias, router->ltag, router->logits_out, launch_nonce()};
-    auto kern = router ? (p.nt == 1   ? decode_fused_kernel<1, true>
-                          : p.nt == 2 ? decode_fused_kernel<2, true>
-                                      : decode_fused_kernel<4, true>)
-                       : (p.nt == 1   ? decode_fused_kernel<1, false>
-                          : p.nt == 2 ? decode_fused_kernel<2, false>
-                                      : decode_fused_kernel<4, false>);
+    MxArgs ma{};
+    if (mxw)
+        ma = MxArgs{(const uint8_t *)mxw->gq, (const uint8_t *)mxw->gs, (const uint8_t *)mxw->dq,
+                    (const uint8_t *)mxw->ds, mx_scale_bytes(H), mx_scale_bytes(I)};
+    auto kern = router ? (p.nt == 1   ? decode_fused_kernel<1, true, false>
+                          : p.nt == 2 ? decode_fused_kernel<2, true, false>
+                                      : decode_fused_kernel<4, true, false>)
+                : mxw  ? (p.nt == 1   ? decode_fused_kernel<1, false, true>
+                          : p.nt == 2 ? decode_fused_kernel<2, false, true>
+                                      : decode_fused_kernel<4, false, true>)
+                       : (p.nt == 1   ? decode_fused_kernel<1, false, false>
+                          : p.nt == 2 ? decode_fused_kernel<2, false, false>
+                                      : decode_fused_kernel<4, false, false>);
     return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
                               H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, act_tag,
                               tag_cap, flags, epoch_salt(), idx_out, w_out, out, exchange_out, (uint64_t)wait_ns,
-                              skip_arrival, ra);
+                              skip_arrival, ra, ma);
 }
 
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)
@@ -1099,9 +1323,11 @@ namespace moe {
 cudaError_t decode_fused_init_device()
 {
     for (const void *kern :
-         {(const void *)decode_fused_kernel<1, false>, (const void *)decode_fused_kernel<2, false>,
-          (const void *)decode_fused_kernel<4, false>, (const void *)decode_fused_kernel<1, true>,
-          (const void *)decode_fused_kernel<2, true>, (const void *)decode_fused_kernel<4, true>}) {
+         {(const void *)decode_fused_kernel<1, false, false>, (const void *)decode_fused_kernel<2, false, false>,
+          (const void *)decode_fused_kernel<4, false, false>, (const void *)decode_fused_kernel<1, true, false>,
+          (const void *)decode_fused_kernel<2, true, false>, (const void *)decode_fused_kernel<4, true, false>,
+          (const void *)decode_fused_kernel<1, false, true>, (const void *)decode_fused_kernel<2, false, true>,
+          (const void *)decode_fused_kernel<4, false, true>}) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
         if (e != cudaSuccess) return e;
     }

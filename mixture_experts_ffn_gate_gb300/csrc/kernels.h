@@ -54,7 +54,8 @@ constexpr int kDecodeFusedFlagWords = kMaxGridCtas + 32;
 constexpr int kDecodeFusedSizeWord = kMaxGridCtas + 2;
 cudaError_t decode_fused_init_device();
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear);
-bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm);
+// mx: with MXFP8 expert weights (FusedMx) instead of BF16 ones
+bool decode_fused_supported(int T, int H, int I, int E, int k, int n_sm, bool mx = false);
 // the same for a call that passes the router weights (its projection's
 // scratch must fit too)
 bool decode_fused_router_supported(int T, int H, int I, int E, int k, int n_sm);
@@ -75,11 +76,20 @@ struct FusedRouter {
     unsigned long long *ltag;
     float *logits_out;
 };
+// mxw (nullable): MXFP8 expert weights -- E4M3 codes gq [E, 2I, H] and dq
+// [E, H, I], E8M0 scales gs [E, 2I, mx_scale_bytes(H)] and ds [E, H,
+// mx_scale_bytes(I)] -- instead of wgu/wd (then not read); not together
+// with router.
+struct FusedMx {
+    const void *gq, *gs, *dq, *ds;
+};
+// Bytes per scale row for rows of K elements: K / 32 scales padded to 16.
+constexpr int mx_scale_bytes(int K) { return (K / 32 + 15) / 16 * 16; }
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
                                 unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
                                 float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
-                                const FusedRouter *router, cudaStream_t s);
+                                const FusedRouter *router, const FusedMx *mxw, cudaStream_t s);
 constexpr unsigned long long kDecodeFusedWaitNs = 2000000000ull;  // default bound of its waits
 
 // moe_ffn_api.cu: an identifier of the calling thread's current CUDA

@@ -198,11 +198,12 @@ struct Stages {
 // allocated for one call is not: its memory may have held anything since).
 // wr (nullable): the call passes the router weights [E, H] (and rbias [E],
 // nullable) instead of logits; the logits are computed here (and copied to
-// logits_out, nullable).
+// logits_out, nullable).  mx (nullable): MXFP8 expert weights instead of
+// wgu/wd; such calls take the fused decode kernel or nothing.
 int run_forward(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s, float *out,
                 char *ws, const Layout &L, bool keep_state, int32_t *idx_out, float *w_out, moe_ffn_opts *opts,
                 cudaStream_t stream, const void *wr = nullptr, const float *rbias = nullptr,
-                float *logits_out = nullptr)
+                float *logits_out = nullptr, const moe::FusedMx *mx = nullptr)
 {
     DeviceInfo *dev = nullptr;
     int st = device_setup(&dev);
@@ -232,8 +233,10 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
+    if (mx && (path != MOE_PATH_DECODE || !moe::decode_fused_supported(T, H, I, E, k, dev->n_sm, true)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (path == MOE_PATH_DECODE && (wr ? moe::decode_fused_router_supported(T, H, I, E, k, dev->n_sm)
-                                       : moe::decode_fused_supported(T, H, I, E, k, dev->n_sm))) {
+                                       : moe::decode_fused_supported(T, H, I, E, k, dev->n_sm, mx != nullptr))) {
         // a few tokens: one cooperative kernel that routes them, streams both
         // projections' rows of the touched experts and exchanges the act
         // rows in between
@@ -246,7 +249,7 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
             x, logits, wgu, wd, T, H, I, E, k, dev->n_sm, (float *)(ws + L.act),
             keep_state ? (unsigned long long *)(ws + L.act_tag) : nullptr, L.tag_cap,
             (unsigned long long *)(ws + L.flags), idx_out, w_out, out, opts ? opts->exchange_out : nullptr, wait_ns,
-            opts ? opts->test_skip_arrival : 0, wr ? &fr : nullptr, stream)));
+            opts ? opts->test_skip_arrival : 0, wr ? &fr : nullptr, mx, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
@@ -412,6 +415,46 @@ int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16, const 
     if (workspace_bytes < L.router_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
     return run_forward(x_bf16, nullptr, w_gate_up_bf16, w_down_bf16, s, out_f32, (char *)workspace, L, true,
                        topk_idx_out, topk_w_out, opts, stream, w_router_bf16, router_bias_f32, logits_out);
+}
+
+int moe_ffn_forward_mxfp8(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_e4m3,
+                          const void *w_gate_up_scale, const void *w_down_e4m3, const void *w_down_scale, int64_t T,
+                          int64_t H, int64_t I, int64_t E, int64_t k, float *out_f32, void *workspace,
+                          size_t workspace_bytes, int32_t *topk_idx_out, float *topk_w_out, moe_ffn_opts *opts,
+                          cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    int st = check_shape(s);
+    if (st != MOE_OK) return st;
+    st = check_opts(opts);
+    if (st != MOE_OK) return st;
+    if (opts) {
+        opts->n_stages = 0;
+        opts->path_taken = 0;
+    }
+    if (T == 0) return MOE_OK;
+    if (!x_bf16 || !router_logits_f32 || !w_gate_up_e4m3 || !w_gate_up_scale || !w_down_e4m3 || !w_down_scale ||
+        !out_f32)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(router_logits_f32) || !aligned16(w_gate_up_e4m3) ||
+        !aligned16(w_gate_up_scale) || !aligned16(w_down_e4m3) || !aligned16(w_down_scale) || !aligned16(out_f32))
+        return MOE_ERR_INVALID_ARG;
+    if ((topk_idx_out && !aligned16(topk_idx_out)) || (topk_w_out && !aligned16(topk_w_out)))
+        return MOE_ERR_INVALID_ARG;
+    if (opts && opts->path != MOE_PATH_AUTO && opts->path != MOE_PATH_DECODE) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!workspace || ((uintptr_t)workspace & 255)) return MOE_ERR_INVALID_ARG;
+    const Layout L = make_layout(s);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    moe_ffn_opts o = opts ? *opts : moe_ffn_opts{};
+    o.path = MOE_PATH_DECODE;
+    const moe::FusedMx mx{w_gate_up_e4m3, w_gate_up_scale, w_down_e4m3, w_down_scale};
+    st = run_forward(x_bf16, router_logits_f32, nullptr, nullptr, s, out_f32, (char *)workspace, L, true, topk_idx_out,
+                     topk_w_out, &o, stream, nullptr, nullptr, nullptr, &mx);
+    if (opts) {
+        opts->n_stages = o.n_stages;
+        opts->path_taken = o.path_taken;
+    }
+    return st;
 }
 
 int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,

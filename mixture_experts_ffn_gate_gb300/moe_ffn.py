@@ -32,7 +32,7 @@ MOE_MAX_STAGES = 8
 EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",
             "moe_ffn_host_workspace_bytes", "moe_ffn_forward_host", "moe_ffn_status_string",
             "moe_ffn_stage_name", "moe_ffn_device_faults", "moe_ffn_forward_noalloc",
-            "moe_ffn_router_workspace_bytes", "moe_ffn_forward_router"]
+            "moe_ffn_router_workspace_bytes", "moe_ffn_forward_router", "moe_ffn_forward_mxfp8"]
 
 # Size of the library's fixed scratch array used by moe_ffn_forward_noalloc.
 MOE_FFN_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -104,8 +104,11 @@ def lib():
             L.moe_ffn_forward_router.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp,
                                                  ctypes.c_size_t, vp, vp, vp,
                                                  ctypes.POINTER(moe_ffn_opts), vp]
+            L.moe_ffn_forward_mxfp8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp,
+                                                ctypes.c_size_t, vp, vp, ctypes.POINTER(moe_ffn_opts), vp]
             for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
-                      L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc, L.moe_ffn_forward_router):
+                      L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc, L.moe_ffn_forward_router,
+                      L.moe_ffn_forward_mxfp8):
                 f.restype = i32
             if hasattr(L, "moe_ffn_debug_fused_timeline"):   # instrumented build only
                 L.moe_ffn_debug_fused_timeline.argtypes = [vp, i32]
@@ -287,6 +290,45 @@ def moe_ffn_forward_router(x, w_router, router_bias, w_gate_up, w_down, k: int, 
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(logits),
         _ptr(topk_idx), _ptr(topk_w), ctypes.byref(opts) if opts is not None else None,
         _stream(stream)), "moe_ffn_forward_router")
+    return out
+
+
+def mx_scale_bytes(K: int) -> int:
+    """Bytes per row of an MXFP8 scale array for rows of K elements
+    (MOE_FFN_MX_SCALE_BYTES)."""
+    return (K // 32 + 15) // 16 * 16
+
+
+def moe_ffn_forward_mxfp8(x, logits, w_gate_up_q, w_gate_up_s, w_down_q, w_down_s, k: int, out=None,
+                          workspace=None, topk_idx=None, topk_w=None, opts: moe_ffn_opts | None = None,
+                          stream=None):
+    """The layer with MXFP8 expert weights (one to four tokens): x bf16 [T,H],
+    logits f32 [T,E], E4M3 codes uint8 w_gate_up_q [E,2I,H] / w_down_q
+    [E,H,I], E8M0 scales uint8 w_gate_up_s [E,2I,mx_scale_bytes(H)] /
+    w_down_s [E,H,mx_scale_bytes(I)].  Returns out f32 [T,H]."""
+    T, H = x.shape
+    E = logits.shape[1]
+    I = w_down_q.shape[2]
+    if tuple(w_gate_up_q.shape) != (E, 2 * I, H) or tuple(w_down_q.shape) != (E, H, I) \
+            or tuple(w_gate_up_s.shape) != (E, 2 * I, mx_scale_bytes(H)) \
+            or tuple(w_down_s.shape) != (E, H, mx_scale_bytes(I)):
+        raise ValueError("shape mismatch")
+    for t, d, n in ((x, torch.bfloat16, "x"), (logits, torch.float32, "logits"),
+                    (w_gate_up_q, torch.uint8, "w_gate_up_q"), (w_gate_up_s, torch.uint8, "w_gate_up_s"),
+                    (w_down_q, torch.uint8, "w_down_q"), (w_down_s, torch.uint8, "w_down_s")):
+        _dev(t, d, n)
+    for t, d, n in ((topk_idx, torch.int32, "topk_idx"), (topk_w, torch.float32, "topk_w")):
+        if t is not None:
+            _dev(t, d, n)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = new_workspace(T, H, I, E, k, device=x.device)
+    _check(lib().moe_ffn_forward_mxfp8(
+        _ptr(x), _ptr(logits), _ptr(w_gate_up_q), _ptr(w_gate_up_s), _ptr(w_down_q), _ptr(w_down_s),
+        T, H, I, E, k, _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(topk_idx), _ptr(topk_w), ctypes.byref(opts) if opts is not None else None,
+        _stream(stream)), "moe_ffn_forward_mxfp8")
     return out
 
 

@@ -2,6 +2,7 @@
 
     python -m mixture_experts_ffn_gate_gb300.timeline [--workload NAME] [--T T]
                                                       [--steps K] [--reps N]
+                                                      [--router | --mxfp8]
 
 Builds the library with -DMOE_FUSED_TIMELINE (a separate build; the product
 build carries no stamps), runs K calls of a decode workload back to back as
@@ -39,6 +40,8 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=5)
     p.add_argument("--router", action="store_true",
                    help="pass router weights instead of logits (moe_ffn_forward_router)")
+    p.add_argument("--mxfp8", action="store_true",
+                   help="MXFP8 expert weights (moe_ffn_forward_mxfp8)")
     args = p.parse_args(argv)
 
     from . import _build
@@ -55,7 +58,8 @@ def main(argv=None):
     R = max(2, -(-3 * (129 << 20) // touched))
     R = min(R, max(1, int((72 << 30) // wl.weight_bytes())))
     dev = torch.device("cuda")
-    layers = [synth.make_weights(wl, device=dev, layer=r) for r in range(R)]
+    make = synth.make_weights_mxfp8 if args.mxfp8 else synth.make_weights
+    layers = [make(wl, device=dev, layer=r) for r in range(R)]
     bias = synth.make_bias(wl)
     batches = [synth.make_tokens(wl, T, call=i, device=dev, bias=bias) for i in range(K + 5)]
     routers = [synth.make_router(wl, device=dev, layer=r) for r in range(R)] if args.router else None
@@ -65,8 +69,11 @@ def main(argv=None):
 
     def call(j, s):
         x, L = batches[j % len(batches)]
-        g, d = layers[j % R]
         o = m.moe_ffn_opts()
+        if args.mxfp8:
+            m.moe_ffn_forward_mxfp8(x, L, *layers[j % R], wl.k, out=out, workspace=ws, opts=o, stream=s)
+            return o
+        g, d = layers[j % R]
         if routers is not None:
             m.moe_ffn_forward_router(x, routers[j % R], rbias, g, d, wl.k, out=out, workspace=ws, opts=o,
                                      stream=s)
@@ -116,7 +123,8 @@ def main(argv=None):
         rows.append(row)
     best = min(rows, key=lambda r: r["us_per_call_instrumented"])
     best["us_per_call_instrumented_median"] = statistics.median(r["us_per_call_instrumented"] for r in rows)
-    print(json.dumps({"workload": args.workload, "T": T, "router": args.router, "steps": K, "layers": R,
+    print(json.dumps({"workload": args.workload, "T": T, "router": args.router, "mxfp8": args.mxfp8,
+                      "steps": K, "layers": R,
                       **best}))
 
 

@@ -188,3 +188,23 @@ def test_router_entry_argument_checks(L, case, want):
 def test_router_workspace_bytes(L):
     assert L.moe_ffn_router_workspace_bytes(4, 256, 128, 8, 2) > L.moe_ffn_workspace_bytes(4, 256, 128, 8, 2)
     assert L.moe_ffn_router_workspace_bytes(4, 256, 128, 8, 9) == 0
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(x=None), 1), (dict(gs=None), 1), (dict(ds=FAKE + 8), 1), (dict(gq=FAKE + 1), 1),
+    (dict(logits=None), 1), (dict(workspace=FAKE + 16), 1), (dict(ws_bytes=1024), 5), (dict(k=9), 1),
+    (dict(H=200), 2), (dict(T=0), 0), (dict(T=0, x=None), 0),
+])
+def test_mxfp8_entry_argument_checks(L, case, want):
+    a = dict(x=FAKE, logits=FAKE, gq=FAKE, gs=FAKE, dq=FAKE, ds=FAKE, T=4, H=256, I=128, E=8, k=2, out=FAKE,
+             workspace=FAKE, ws_bytes=1 << 40)
+    a.update(case)
+    st = L.moe_ffn_forward_mxfp8(a["x"], a["logits"], a["gq"], a["gs"], a["dq"], a["ds"], a["T"], a["H"], a["I"],
+                                 a["E"], a["k"], a["out"], a["workspace"], a["ws_bytes"], None, None, None, None)
+    assert st == want
+
+
+def test_mx_scale_row_bytes_agree():
+    from mixture_experts_ffn_gate_gb300 import moe_ffn, synth
+    for K in (32, 64, 96, 512, 768, 1536, 2048, 6144, 7168):
+        assert moe_ffn.mx_scale_bytes(K) == synth.mx_scale_row_bytes(K) == -(-(K // 32) // 16) * 16
