@@ -542,7 +542,8 @@ class Measure:
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": stored_traffic(dom, wl.name, T),
+                    "traffic": stored_traffic(dom, wl.name + ("+mxfp8" if self.mx else "+router" if self.routers
+                                                              is not None else ""), T),
                     "peak_source": f"{peaks['source']} HBM copy (burst)",
                     "algorithmic_bytes_per_launch": dom_bytes,
                     "kernel_time": ("timed region / K (one kernel per step)" if one_kernel
