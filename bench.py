@@ -33,9 +33,10 @@ call's HBM fraction, the dominant kernel's roofline and the TFLOP/s against
 dense BF16 peak and against min(peak, HBM peak x flop/byte).  Two of the
 rows ("entry": moe_ffn_forward_router) run the 2048-hidden decode layer at
 T=1 and 2 with the router projection inside the call (router weights and
-bias passed instead of logits); four ("entry": moe_ffn_forward_mxfp8) run
-the 2048-hidden layer at T=1/2/4 and the 7168-hidden one at T=1 with MXFP8
-expert weights (their bytes counted at 1 + 1/32 per weight).
+bias passed instead of logits); six ("entry": moe_ffn_forward_mxfp8) run
+the 2048-hidden layer at T=1/2/4, the 4096-hidden one at T=1 and the
+7168-hidden one at T=1/8 with MXFP8 expert weights (their bytes counted at
+1 + 1/32 per weight; T > 4 takes the general decode kernels).
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -356,7 +357,8 @@ SUPPLEMENTARY = [
     ("decode_h2048_i768_e128_k8", (2,)),
     ("decode_h2048_i768_e128_k8+router", (1, 2)),
     ("decode_h2048_i768_e128_k8+mxfp8", (1, 2, 4)),
-    ("decode_h7168_i2048_e384_k8_bias+mxfp8", (1,)),
+    ("decode_h4096_i1536_e128_k8_bias+mxfp8", (1,)),
+    ("decode_h7168_i2048_e384_k8_bias+mxfp8", (1, 8)),
     ("decode_h4096_i1536_e128_k8_bias", (1, 4, 16, 64)),
     ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),

@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,6 +57,32 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float f[8])
     f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
     f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
     f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+// MXFP8 weights (the OCP MX specification's MXFP8: E4M3 codes, one E8M0
+// scale per 32 elements along the reduction axis).
+// 2^(s - 127) as a float: the biased exponent itself for s >= 1, the
+// subnormal 2^-127 for s = 0 (s = 255, NaN in the format, is not an input).
+__device__ __forceinline__ float e8m0_scale(uint32_t s)
+{
+    return __uint_as_float(s ? s << 23 : 0x00400000u);
+}
+
+// 16 E4M3 codes (byte j = element j) to their values in FP32, exactly
+// (E4M3 -> F16 -> F32: every E4M3 value is an F16 number).
+__device__ __forceinline__ void unpack16_e4m3(const uint4 &v, float (&f)[16])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const __half2_raw r =
+                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> (16 * hf)), __NV_E4M3);
+            const float2 f2 = __half22float2(__half2(r));
+            f[4 * q + 2 * hf] = f2.x;
+            f[4 * q + 2 * hf + 1] = f2.y;
+        }
 }
 
 // Warp sum with a fixed butterfly: every lane ends with the same bits, and

@@ -19,6 +19,12 @@
 // Every output's arithmetic (lane split, chunk order, butterfly, slot order)
 // is independent of the launch shape, so the bits do not change with the
 // warps-per-block knobs.
+//
+// MX instantiations take MXFP8 weights (E4M3 codes, one E8M0 scale per 32
+// elements along the reduction axis): a lane reads 16 codes per step,
+// converts them to FP32 exactly, forms the partial sum with the FP32
+// activations and adds it times the block's power-of-two scale, as the fused
+// kernel's MX instantiation does.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -27,16 +33,24 @@ namespace moe {
 constexpr int GU_UNR = 4;  // 256-element chunks in flight per lane
 constexpr int DOWN_HW = 4; // output dims per block in down
 constexpr int DOWN_UNR = 2;
+constexpr int MX_UNR = 2;   // 512-element steps in flight per lane (MXFP8 rows)
+
+// MXFP8 weights of a call: codes gq [E][2I][H], dq [E][H][I]; scales gs
+// [E][2I][hs], ds [E][H][is] (hs, is: scale bytes per row).
+struct DecodeMx {
+    const uint8_t *gq, *gs, *dq, *ds;
+    int hs, is;
+};
 
 // GU_TB: assignments (tokens of one expert) per pass; at most T.
-template <int GU_TB>
+template <int GU_TB, bool MX>
 __global__ void __launch_bounds__(512) decode_gate_up_kernel(const uint16_t *__restrict__ x,
                                                               const uint16_t *__restrict__ wgu,
                                                               const int32_t *__restrict__ uexp,
                                                               const int32_t *__restrict__ ucount,
                                                               const int32_t *__restrict__ offs,
                                                               const int32_t *__restrict__ perm, int H, int I,
-                                                              int k, float *__restrict__ act)
+                                                              int k, float *__restrict__ act, DecodeMx mx)
 {
     const int s = blockIdx.y;
     if (s >= *ucount) return;
@@ -61,6 +75,50 @@ __global__ void __launch_bounds__(512) decode_gate_up_kernel(const uint16_t *__r
 #pragma unroll
         for (int b = 0; b < GU_TB; ++b) g[b] = u[b] = 0.0f;
 
+        if constexpr (MX) {
+            const int64_t r0 = (int64_t)e * 2 * I + i;  // gate row; up row r0 + I
+            const uint8_t *gq = mx.gq + r0 * H, *uq = gq + (int64_t)I * H;
+            const uint8_t *gs = mx.gs + r0 * mx.hs, *us = gs + (int64_t)I * mx.hs;
+            for (int h = lane * 16; h < H; h += 512 * MX_UNR) {
+                uint4 gw[MX_UNR], uw[MX_UNR];
+                float sg[MX_UNR], su[MX_UNR];
+#pragma unroll
+                for (int q = 0; q < MX_UNR; ++q) {
+                    const int hq = h + q * 512;
+                    if (hq < H) {
+                        gw[q] = ld_stream16(gq + hq);
+                        uw[q] = ld_stream16(uq + hq);
+                        sg[q] = e8m0_scale(__ldg(gs + (hq >> 5)));
+                        su[q] = e8m0_scale(__ldg(us + (hq >> 5)));
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < MX_UNR; ++q) {
+                    const int hq = h + q * 512;
+                    if (hq < H) {
+                        float gf[16], uf[16];
+                        unpack16_e4m3(gw[q], gf);
+                        unpack16_e4m3(uw[q], uf);
+#pragma unroll
+                        for (int b = 0; b < GU_TB; ++b) {
+                            if (b < nb) {
+                                float xf[16];
+                                unpack8(ld_nc16(xr[b] + hq), xf);
+                                unpack8(ld_nc16(xr[b] + hq + 8), xf + 8);
+                                float pg = 0.0f, pu = 0.0f;
+#pragma unroll
+                                for (int c = 0; c < 16; ++c) {
+                                    pg = fmaf(gf[c], xf[c], pg);
+                                    pu = fmaf(uf[c], xf[c], pu);
+                                }
+                                g[b] = fmaf(pg, sg[q], g[b]);
+                                u[b] = fmaf(pu, su[q], u[b]);
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
         for (int h = lane * 8; h < H; h += 256 * GU_UNR) {
             uint4 gw[GU_UNR], uw[GU_UNR];
 #pragma unroll
@@ -93,6 +151,7 @@ __global__ void __launch_bounds__(512) decode_gate_up_kernel(const uint16_t *__r
                 }
             }
         }
+        }
 #pragma unroll
         for (int b = 0; b < GU_TB; ++b) {
             if (b < nb) {
@@ -119,7 +178,7 @@ __device__ __forceinline__ int lower_bound_token(const int32_t *perm, int lo, in
 // Block (blockIdx.x = group of DOWN_HW output dims, blockIdx.y = tile of
 // tok_tile tokens).  part[hw][(t - t0)*k + j] holds W_down[e_j, h0+hw, :] .
 // act[t*k+j, :] for the tile's tokens.  DOWN_TB: assignments per pass.
-template <int DOWN_TB>
+template <int DOWN_TB, bool MX>
 __global__ void __launch_bounds__(512) decode_down_kernel(const float *__restrict__ act,
                                                            const uint16_t *__restrict__ wd,
                                                            const float *__restrict__ wts,
@@ -127,7 +186,7 @@ __global__ void __launch_bounds__(512) decode_down_kernel(const float *__restric
                                                            const int32_t *__restrict__ ucount,
                                                            const int32_t *__restrict__ offs,
                                                            const int32_t *__restrict__ perm, int T, int H, int I,
-                                                           int k, int tok_tile, float *__restrict__ out)
+                                                           int k, int tok_tile, float *__restrict__ out, DecodeMx mx)
 {
     extern __shared__ float part[];  // [DOWN_HW][tok_tile * k]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
@@ -157,6 +216,55 @@ __global__ void __launch_bounds__(512) decode_down_kernel(const float *__restric
 #pragma unroll
                 for (int b = 0; b < DOWN_TB; ++b) acc[r][b] = 0.0f;
 
+            if constexpr (MX) {
+                const int64_t r0 = (int64_t)e * H + h0;
+                const uint8_t *wq = mx.dq + r0 * I, *ws = mx.ds + r0 * mx.is;
+                for (int c = lane * 16; c < I; c += 512 * MX_UNR) {
+                    uint4 wv[MX_UNR][DOWN_HW];
+                    float sc[MX_UNR][DOWN_HW];
+#pragma unroll
+                    for (int q = 0; q < MX_UNR; ++q) {
+                        const int cq = c + q * 512;
+                        if (cq < I) {
+#pragma unroll
+                            for (int r = 0; r < DOWN_HW; ++r) {
+                                wv[q][r] = ld_stream16(wq + (int64_t)r * I + cq);
+                                sc[q][r] = e8m0_scale(__ldg(ws + (int64_t)r * mx.is + (cq >> 5)));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < MX_UNR; ++q) {
+                        const int cq = c + q * 512;
+                        if (cq < I) {
+#pragma unroll
+                            for (int b = 0; b < DOWN_TB; ++b) {
+                                if (b < nb) {
+                                    const float *ar = act + (int64_t)arow[b] * I + cq;
+                                    float af[16];
+#pragma unroll
+                                    for (int v = 0; v < 4; ++v) {
+                                        const float4 a4 = ld_nc_f4(ar + 4 * v);
+                                        af[4 * v] = a4.x;
+                                        af[4 * v + 1] = a4.y;
+                                        af[4 * v + 2] = a4.z;
+                                        af[4 * v + 3] = a4.w;
+                                    }
+#pragma unroll
+                                    for (int r = 0; r < DOWN_HW; ++r) {
+                                        float wf[16];
+                                        unpack16_e4m3(wv[q][r], wf);
+                                        float p = 0.0f;
+#pragma unroll
+                                        for (int cc = 0; cc < 16; ++cc) p = fmaf(wf[cc], af[cc], p);
+                                        acc[r][b] = fmaf(p, sc[q][r], acc[r][b]);
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+            } else {
             for (int c = lane * 8; c < I; c += 256 * DOWN_UNR) {
                 uint4 wv[DOWN_UNR][DOWN_HW];
 #pragma unroll
@@ -189,6 +297,7 @@ __global__ void __launch_bounds__(512) decode_down_kernel(const float *__restric
                     }
                 }
             }
+            }
 #pragma unroll
             for (int b = 0; b < DOWN_TB; ++b) {
                 if (b < nb) {
@@ -215,20 +324,31 @@ __global__ void __launch_bounds__(512) decode_down_kernel(const float *__restric
 
 cudaError_t launch_decode_gate_up(const void *x, const void *wgu, const int32_t *uexp, const int32_t *ucount,
                                   const int32_t *offs, const int32_t *perm, int T, int H, int I, int E, int k,
-                                  int warps, float *act, cudaStream_t s)
+                                  int warps, float *act, const FusedMx *mxw, cudaStream_t s)
 {
     const int u_max = (int)((int64_t)T * k < E ? (int64_t)T * k : E);
     dim3 grid((unsigned)ceil_div(I, warps), (unsigned)u_max);
-    auto kern = T == 1 ? decode_gate_up_kernel<1> : T <= 2 ? decode_gate_up_kernel<2>
-              : T <= 4 ? decode_gate_up_kernel<4> : decode_gate_up_kernel<8>;
+    DecodeMx mx{};
+    if (mxw)
+        mx = DecodeMx{(const uint8_t *)mxw->gq, (const uint8_t *)mxw->gs, (const uint8_t *)mxw->dq,
+                      (const uint8_t *)mxw->ds, mx_scale_bytes(H), mx_scale_bytes(I)};
+    auto kern = mxw ? (T == 1   ? decode_gate_up_kernel<1, true>
+                       : T <= 2 ? decode_gate_up_kernel<2, true>
+                       : T <= 4 ? decode_gate_up_kernel<4, true>
+                                : decode_gate_up_kernel<8, true>)
+                    : (T == 1   ? decode_gate_up_kernel<1, false>
+                       : T <= 2 ? decode_gate_up_kernel<2, false>
+                       : T <= 4 ? decode_gate_up_kernel<4, false>
+                                : decode_gate_up_kernel<8, false>);
     kern<<<grid, warps * 32, 0, s>>>((const uint16_t *)x, (const uint16_t *)wgu, uexp, ucount, offs, perm, H, I, k,
-                                     act);
+                                     act, mx);
     return cudaPeekAtLastError();
 }
 
 cudaError_t decode_init_device()
 {
-    for (auto kern : {decode_down_kernel<1>, decode_down_kernel<2>, decode_down_kernel<4>}) {
+    for (auto kern : {decode_down_kernel<1, false>, decode_down_kernel<2, false>, decode_down_kernel<4, false>,
+                      decode_down_kernel<1, true>, decode_down_kernel<2, true>, decode_down_kernel<4, true>}) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
         if (e != cudaSuccess) return e;
     }
@@ -244,14 +364,21 @@ int decode_down_tok_tile(int T, int k)
 
 cudaError_t launch_decode_down(const float *act, const void *wd, const float *w, const int32_t *uexp,
                                const int32_t *ucount, const int32_t *offs, const int32_t *perm, int T, int H,
-                               int I, int k, int warps, float *out, cudaStream_t s)
+                               int I, int k, int warps, float *out, const FusedMx *mxw, cudaStream_t s)
 {
     const int tt = decode_down_tok_tile(T, k);
     dim3 grid((unsigned)(H / DOWN_HW), (unsigned)ceil_div(T, tt));
     const size_t smem = (size_t)DOWN_HW * tt * k * sizeof(float);
-    auto kern = T == 1 ? decode_down_kernel<1> : T <= 2 ? decode_down_kernel<2> : decode_down_kernel<4>;
+    DecodeMx mx{};
+    if (mxw)
+        mx = DecodeMx{(const uint8_t *)mxw->gq, (const uint8_t *)mxw->gs, (const uint8_t *)mxw->dq,
+                      (const uint8_t *)mxw->ds, mx_scale_bytes(H), mx_scale_bytes(I)};
+    auto kern = mxw ? (T == 1 ? decode_down_kernel<1, true> : T <= 2 ? decode_down_kernel<2, true>
+                                                                     : decode_down_kernel<4, true>)
+                    : (T == 1 ? decode_down_kernel<1, false> : T <= 2 ? decode_down_kernel<2, false>
+                                                                      : decode_down_kernel<4, false>);
     kern<<<grid, warps * 32, smem, s>>>(act, (const uint16_t *)wd, w, uexp, ucount, offs, perm, T, H, I, k, tt,
-                                        out);
+                                        out, mx);
     return cudaPeekAtLastError();
 }
 

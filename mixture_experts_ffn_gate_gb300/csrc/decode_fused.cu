@@ -80,8 +80,6 @@
 #include <random>
 #include <type_traits>
 
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -157,6 +155,10 @@ constexpr int kSizeWord = kDecodeFusedSizeWord;
 constexpr int kGoWord = kMaxGridCtas + 16;
 static_assert(kGoWord < kDecodeFusedFlagWords, "flags array too small");
 constexpr unsigned long long kCheckKey = 0x6d6f652d7461672dull;  // xor the flags address
+
+// the kernel's mode bits: the test hook that skips the last CTA's arrival
+// at the grid barrier, and the L2 prefetch of the inputs
+constexpr int kSkipArrival = 1, kPrefetchInputs = 2;
 
 enum : uint32_t {
     FAULT_LOGITS = 8u,
@@ -374,29 +376,6 @@ struct MxArgs {
     int hs, is;              // scale bytes per row (K / 32 padded to 16)
 };
 
-// 2^(s - 127) as a float: the biased exponent itself for s >= 1, the
-// subnormal 2^-127 for s = 0 (s = 255, NaN in the format, is not an input).
-__device__ __forceinline__ float e8m0_scale(uint32_t s)
-{
-    return __uint_as_float(s ? s << 23 : 0x00400000u);
-}
-
-// 16 E4M3 codes (byte j = element j) to their values in FP32, exactly.
-__device__ __forceinline__ void unpack16_e4m3(const uint4 &v, float (&f)[16])
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const __half2_raw r =
-                __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[q] >> (16 * hf)), __NV_E4M3);
-            const float2 f2 = __half22float2(__half2(r));
-            f[4 * q + 2 * hf] = f2.x;
-            f[4 * q + 2 * hf + 1] = f2.y;
-        }
-}
-
 // gate_up_pair with MXFP8 rows: codes grow/urow, scale rows gsc/usc.
 template <int NB>
 __device__ __forceinline__ void gate_up_pair_mx(const uint8_t *grow, const uint8_t *urow, const uint8_t *gsc,
@@ -552,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         unsigned long long tag_cap, unsigned long long *__restrict__ flags,
                         unsigned long long epoch_salt, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
                         float *__restrict__ out, int32_t *__restrict__ exchange_out, uint64_t wait_ns,
-                        int skip_arrival, RouterArgs ra, MxArgs mx)
+                        int mode, RouterArgs ra, MxArgs mx)
 {
     static_assert(!(ROUTER && MX), "the router projection is built for BF16 weights only");
     extern __shared__ __align__(128) uint8_t sm[];
@@ -585,6 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of these exits), and nothing written by the previous launch -- the
     // caller's inputs included -- is read before it has completed.
     ptx::griddep_launch_dependents();
+    // The tokens' logits and x rows, which every CTA reads first, fetched
+    // into L2 while the previous launch drains (whole 16-byte pieces only)
+    if ((mode & kPrefetchInputs) && threadIdx.x == 0 && blockIdx.x < 2) {
+        const uint32_t n = blockIdx.x == 0 ? (ROUTER ? 0u : (uint32_t)(T * E * 4) & ~15u) : (uint32_t)(T * H * 2);
+        if (n) ptx::bulk_prefetch_l2(blockIdx.x == 0 ? (const void *)logits : (const void *)x, n);
+    }
     ptx::griddep_wait();
     if (threadIdx.x == 0) MOE_TL(1);
     if (threadIdx.x == 0) {
@@ -736,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t e32 = (uint32_t)(epoch_salt + 2 * calls);
     const bool tag_region = act_in_smem && act_t;  // this call may use, or prepare, the tag region
     const unsigned long long check_key = kCheckKey ^ (unsigned long long)flags;
+    const bool skip_arrival = (mode & kSkipArrival) != 0;
     const bool tagged = tag_region && !skip_arrival && s_flags[1] == check_key &&
                         s_flags[2] >= (unsigned long long)(T * k) * I;
     uint32_t *arrive = reinterpret_cast<uint32_t *>(flags);
@@ -1260,7 +1246,8 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
                                 unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
                                 float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
-                                const FusedRouter *router, const FusedMx *mxw, cudaStream_t s)
+                                const FusedRouter *router, const FusedMx *mxw, bool prefetch_inputs,
+                                cudaStream_t s)
 {
     if (router && mxw) return cudaErrorInvalidValue;  // no such instantiation
     const Plan p = plan_for(T, H, I, k, n_sm, mxw != nullptr);
@@ -1298,7 +1285,7 @@ cudaError_t launch_decode_fused(const void *x, const float *logits, const void *
     return cudaLaunchKernelEx(&cfg, kern, (const uint16_t *)x, logits, (const uint16_t *)wgu, (const uint16_t *)wd, T,
                               H, I, E, k, p.slots, p.slot_bytes, p.rpc, p.rps, p.nh_max, p.act_in_smem, act, act_tag,
                               tag_cap, flags, epoch_salt(), idx_out, w_out, out, exchange_out, (uint64_t)wait_ns,
-                              skip_arrival, ra, ma);
+                              (skip_arrival ? kSkipArrival : 0) | (prefetch_inputs ? kPrefetchInputs : 0), ra, ma);
 }
 
 cudaError_t read_decode_fused_fault_word(uint32_t *flags, bool clear)

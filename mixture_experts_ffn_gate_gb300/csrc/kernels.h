@@ -9,6 +9,16 @@ namespace moe {
 // Grouped path: at most this many assignments (token rows) per GEMM N-chunk.
 constexpr int kGemmChunkMax = 64;
 
+// MXFP8 expert weights of a call -- E4M3 codes gq [E, 2I, H] and dq [E, H,
+// I], E8M0 scales gs [E, 2I, mx_scale_bytes(H)] and ds [E, H,
+// mx_scale_bytes(I)] -- for the decode kernels (the weight pointers are then
+// not read).
+struct FusedMx {
+    const void *gq, *gs, *dq, *ds;
+};
+// Bytes per scale row for rows of K elements: K / 32 scales padded to 16.
+constexpr int mx_scale_bytes(int K) { return (K / 32 + 15) / 16 * 16; }
+
 // routing.cu
 cudaError_t routing_init_device();
 // tag_size (nullable): the fused decode kernel's size word in a workspace
@@ -35,10 +45,10 @@ cudaError_t decode_init_device();
 int decode_down_tok_tile(int T, int k);
 cudaError_t launch_decode_gate_up(const void *x, const void *wgu, const int32_t *uexp, const int32_t *ucount,
                                   const int32_t *offs, const int32_t *perm, int T, int H, int I, int E, int k,
-                                  int warps, float *act, cudaStream_t s);
+                                  int warps, float *act, const FusedMx *mxw, cudaStream_t s);
 cudaError_t launch_decode_down(const float *act, const void *wd, const float *w, const int32_t *uexp,
                                const int32_t *ucount, const int32_t *offs, const int32_t *perm, int T, int H,
-                               int I, int k, int warps, float *out, cudaStream_t s);
+                               int I, int k, int warps, float *out, const FusedMx *mxw, cudaStream_t s);
 
 // decode_fused.cu: a decode step of up to four tokens in one cooperative
 // kernel.  act: [T*k][I] FP32 scratch; flags: kDecodeFusedFlagWords 64-bit
@@ -76,20 +86,15 @@ struct FusedRouter {
     unsigned long long *ltag;
     float *logits_out;
 };
-// mxw (nullable): MXFP8 expert weights -- E4M3 codes gq [E, 2I, H] and dq
-// [E, H, I], E8M0 scales gs [E, 2I, mx_scale_bytes(H)] and ds [E, H,
-// mx_scale_bytes(I)] -- instead of wgu/wd (then not read); not together
-// with router.
-struct FusedMx {
-    const void *gq, *gs, *dq, *ds;
-};
-// Bytes per scale row for rows of K elements: K / 32 scales padded to 16.
-constexpr int mx_scale_bytes(int K) { return (K / 32 + 15) / 16 * 16; }
+// mxw (nullable): MXFP8 expert weights (FusedMx) instead of wgu/wd (then
+// not read); not together with router.  prefetch_inputs: fetch x and the
+// logits into L2 while the previous launch drains (device memory only).
 cudaError_t launch_decode_fused(const void *x, const float *logits, const void *wgu, const void *wd, int T, int H,
                                 int I, int E, int k, int n_sm, float *act, unsigned long long *act_tag,
                                 unsigned long long tag_cap, unsigned long long *flags, int32_t *idx_out, float *w_out,
                                 float *out, int32_t *exchange_out, unsigned long long wait_ns, int skip_arrival,
-                                const FusedRouter *router, const FusedMx *mxw, cudaStream_t s);
+                                const FusedRouter *router, const FusedMx *mxw, bool prefetch_inputs,
+                                cudaStream_t s);
 constexpr unsigned long long kDecodeFusedWaitNs = 2000000000ull;  // default bound of its waits
 
 // moe_ffn_api.cu: an identifier of the calling thread's current CUDA

@@ -16,6 +16,9 @@ using moe::round_up;
 // (H7168 I2048 E384 k8: 748 vs 979 us at T=8; 417 vs 697 us at H4096, T=16).
 constexpr int kDefaultDecodeMaxTokens = 4;
 constexpr int kDefaultWarps = 8;
+// MXFP8 weights take the decode kernels only (no tensor-core form): calls of
+// up to this many tokens
+constexpr int kMxMaxTokens = 64;
 constexpr int kMaxDevices = 64;
 
 struct Shape {
@@ -199,11 +202,12 @@ struct Stages {
 // wr (nullable): the call passes the router weights [E, H] (and rbias [E],
 // nullable) instead of logits; the logits are computed here (and copied to
 // logits_out, nullable).  mx (nullable): MXFP8 expert weights instead of
-// wgu/wd; such calls take the fused decode kernel or nothing.
+// wgu/wd; such calls take the decode kernels only.  host_inputs: x and the
+// logits are page-locked host memory read in place (not prefetched to L2).
 int run_forward(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s, float *out,
                 char *ws, const Layout &L, bool keep_state, int32_t *idx_out, float *w_out, moe_ffn_opts *opts,
                 cudaStream_t stream, const void *wr = nullptr, const float *rbias = nullptr,
-                float *logits_out = nullptr, const moe::FusedMx *mx = nullptr)
+                float *logits_out = nullptr, const moe::FusedMx *mx = nullptr, bool host_inputs = false)
 {
     DeviceInfo *dev = nullptr;
     int st = device_setup(&dev);
@@ -233,8 +237,7 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (mx && (path != MOE_PATH_DECODE || !moe::decode_fused_supported(T, H, I, E, k, dev->n_sm, true)))
-        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (mx && (path != MOE_PATH_DECODE || T > kMxMaxTokens)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (path == MOE_PATH_DECODE && (wr ? moe::decode_fused_router_supported(T, H, I, E, k, dev->n_sm)
                                        : moe::decode_fused_supported(T, H, I, E, k, dev->n_sm, mx != nullptr))) {
         // a few tokens: one cooperative kernel that routes them, streams both
@@ -249,7 +252,7 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
             x, logits, wgu, wd, T, H, I, E, k, dev->n_sm, (float *)(ws + L.act),
             keep_state ? (unsigned long long *)(ws + L.act_tag) : nullptr, L.tag_cap,
             (unsigned long long *)(ws + L.flags), idx_out, w_out, out, opts ? opts->exchange_out : nullptr, wait_ns,
-            opts ? opts->test_skip_arrival : 0, wr ? &fr : nullptr, mx, stream)));
+            opts ? opts->test_skip_arrival : 0, wr ? &fr : nullptr, mx, !host_inputs, stream)));
         if (opts) {
             opts->n_stages = stg.n;
             opts->path_taken = path;
@@ -269,9 +272,9 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
         MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
                                           nullptr, nullptr, stream)));
         MOE_TRY(stg.done(moe::launch_decode_gate_up(x, wgu, uexp, ucount, offs, perm, T, H, I, E, k, gu_warps,
-                                                    act, stream)));
+                                                    act, mx, stream)));
         MOE_TRY(stg.done(moe::launch_decode_down(act, wd, w, uexp, ucount, offs, perm, T, H, I, k, dn_warps, out,
-                                                 stream)));
+                                                 mx, stream)));
     } else {
         void *xs = ws + L.xs;
         void *act_hi = ws + L.act_hi;
@@ -531,7 +534,8 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host, const voi
         const void *xd = mapped_host(x_host), *ld = mapped_host(logits_host), *od = mapped_host(out_host);
         if (xd && ld && od && aligned16(xd) && aligned16(ld) && aligned16(od)) {
             return run_forward(xd, (const float *)ld, w_gate_up_bf16, w_down_bf16, s, (float *)od, p,
-                               make_layout(s), true, nullptr, nullptr, opts, stream);
+                               make_layout(s), true, nullptr, nullptr, opts, stream, nullptr, nullptr, nullptr,
+                               nullptr, true);
         }
     }
     // the device workspace first, so the fused decode kernel's state sits at

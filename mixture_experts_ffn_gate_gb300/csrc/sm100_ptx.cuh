@@ -116,6 +116,14 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (a hint: L2 is the point of
+// coherence, so lines fetched before another kernel writes them are updated
+// by those writes).  p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // GPU-scope release store / acquire load of a 64-bit flag (grid barriers).
 __device__ __forceinline__ void st_release_gpu(unsigned long long *p, unsigned long long v)
 {

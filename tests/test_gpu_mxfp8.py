@@ -1,5 +1,6 @@
-"""The layer with MXFP8 expert weights (moe_ffn_forward_mxfp8, the fused
-decode kernel's MX instantiation) against the oracle on the exactly
+"""The layer with MXFP8 expert weights (moe_ffn_forward_mxfp8: the fused
+decode kernel's MX instantiation for T <= 4, the general decode kernels'
+for larger T) against the oracle on the exactly
 dequantised weights: routing indices bit-exact, routing weights and outputs
 within the parity tolerance (tests/gpu_util.py), at small ragged shapes, at
 the decode workloads' full sizes, with signed zeros, subnormal codes and
@@ -38,7 +39,7 @@ def _run(x, L, gq, gs, dq, ds, k, workspace=None, opts=None):
     o = opts or m.moe_ffn_opts()
     out = m.moe_ffn_forward_mxfp8(x, L, gq, gs, dq, ds, k, topk_idx=idx, topk_w=w, opts=o, workspace=workspace)
     torch.cuda.synchronize()
-    assert o.path_taken == m.MOE_PATH_DECODE_FUSED
+    assert o.path_taken == (m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_DECODE)
     return out.cpu(), idx.cpu(), w.cpu()
 
 
@@ -56,9 +57,11 @@ def _oracle(x, L, gq, gs, dq, ds, k):
 
 # (T, H, I, E, k, bias variance): ragged lane coverage (H or I not a
 # multiple of 512), scale rows with padding (I = 192: 6 scales in 16 bytes),
-# many experts with k = 32, one to four tokens
+# many experts with k = 32, one to four tokens (fused kernel) and 5 to 64
+# (general decode kernels, incl. several token passes per expert)
 SMALL = [(1, 256, 128, 8, 2, 0.0), (2, 576, 192, 16, 4, 0.5), (3, 1024, 320, 32, 8, 1.0),
-         (4, 512, 192, 12, 3, 0.5), (1, 64, 64, 1024, 32, 1.0), (4, 2048, 768, 128, 8, 0.0)]
+         (4, 512, 192, 12, 3, 0.5), (1, 64, 64, 1024, 32, 1.0), (4, 2048, 768, 128, 8, 0.0),
+         (5, 576, 192, 16, 4, 0.5), (13, 1024, 320, 8, 3, 1.0), (64, 512, 256, 12, 2, 4.0)]
 
 
 @pytest.mark.parametrize("T,H,I,E,k,bv", SMALL)
@@ -70,7 +73,8 @@ def test_mxfp8_parity_small(T, H, I, E, k, bv):
 
 
 @pytest.mark.parametrize("name,T", [("decode_h2048_i768_e128_k8", 1), ("decode_h2048_i768_e128_k8", 2),
-                                    ("decode_h4096_i1536_e128_k8_bias", 4), ("decode_h7168_i2048_e384_k8_bias", 1)])
+                                    ("decode_h4096_i1536_e128_k8_bias", 4), ("decode_h7168_i2048_e384_k8_bias", 1),
+                                    ("decode_h4096_i1536_e128_k8_bias", 16), ("decode_h7168_i2048_e384_k8_bias", 8)])
 def test_mxfp8_parity_full_size(name, T):
     wl = synth.WORKLOADS[name]
     x, L, gq, gs, dq, ds = _layer(wl, T, call=7)
@@ -152,10 +156,12 @@ def test_mxfp8_argument_checks():
     assert call(gs_=p(gs) + 1) == m.MOE_ERR_INVALID_ARG           # misaligned scales
     assert call(gs_=None) == m.MOE_ERR_INVALID_ARG
     assert call(n_=1024) == m.MOE_ERR_WORKSPACE_TOO_SMALL
-    x8 = torch.cat([x] * 4)
-    L8 = torch.cat([L] * 4)
-    assert lib.moe_ffn_forward_mxfp8(p(x8), p(L8), p(gq), p(gs), p(dq), p(ds), 5, H, I, E, k, p(out), p(ws), nbytes,
-                                     None, None, None, None) == m.MOE_ERR_UNSUPPORTED_SHAPE   # T > 4
+    xb = torch.cat([x] * 33)
+    Lb = torch.cat([L] * 33)
+    wsb = m.new_workspace(65, H, I, E, k)
+    outb = torch.empty((66, H), dtype=torch.float32, device="cuda")
+    assert lib.moe_ffn_forward_mxfp8(p(xb), p(Lb), p(gq), p(gs), p(dq), p(ds), 65, H, I, E, k, p(outb), p(wsb),
+                                     wsb.numel(), None, None, None, None) == m.MOE_ERR_UNSUPPORTED_SHAPE   # T > 64
     o = m.moe_ffn_opts()
     o.path = m.MOE_PATH_GROUPED
     assert call(o=m.ctypes.byref(o)) == m.MOE_ERR_UNSUPPORTED_SHAPE
