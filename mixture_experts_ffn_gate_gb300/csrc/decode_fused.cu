@@ -434,43 +434,51 @@ __device__ __forceinline__ void gate_up_pair_mx(const uint8_t *grow, const uint8
     }
 }
 
-// down_rows with MXFP8 rows: codes rowp[r], scale rows scp[r].
-template <int NB>
+// down_rows with MXFP8 rows: codes rowp[r], scale rows scp[r].  A lane
+// takes LE = 16 consecutive elements per step, or 8 when I is not a
+// multiple of 512 (then 16 would leave lanes idle in the last step: I = 768
+// is one and a half steps of 16, three of 8).
+template <int NB, int LE>
 __device__ __forceinline__ void down_rows_mx(const uint8_t *const *rowp, const uint8_t *const *scp,
                                              const float *const *arow, int I, int lane, int nu, const int *asg,
                                              float *part, int A)
 {
+    static_assert(LE == 8 || LE == 16, "lane elements");
     constexpr int RB = rows_for(NB);
     constexpr int N = pow2_ceil(RB * NB);  // row r, assignment b in slot r * NB + b
     float acc[N];
 #pragma unroll
     for (int q = 0; q < N; ++q) acc[q] = 0.0f;
-    for (int i = lane * 16; i < I; i += 512) {
-        // elements i .. i + 15 of the two-plane act rows: groups i / 8 and
-        // i / 8 + 1, each 4 values in plane 0 and 4 in plane 1
-        float af[NB][16];
+    for (int i = lane * LE; i < I; i += 32 * LE) {
+        // elements i .. i + LE - 1 of the two-plane act rows: LE / 8 groups
+        // of 8 (group u: 4 values at 4u in plane 0, 4 at 4u in plane 1)
+        float af[NB][LE];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            const float *p0 = arow[b] + i / 2, *p1 = arow[b] + I / 2 + i / 2;
-            const float4 v0 = *reinterpret_cast<const float4 *>(p0);
-            const float4 v1 = *reinterpret_cast<const float4 *>(p1);
-            const float4 v2 = *reinterpret_cast<const float4 *>(p0 + 4);
-            const float4 v3 = *reinterpret_cast<const float4 *>(p1 + 4);
-            af[b][0] = v0.x; af[b][1] = v0.y; af[b][2] = v0.z; af[b][3] = v0.w;
-            af[b][4] = v1.x; af[b][5] = v1.y; af[b][6] = v1.z; af[b][7] = v1.w;
-            af[b][8] = v2.x; af[b][9] = v2.y; af[b][10] = v2.z; af[b][11] = v2.w;
-            af[b][12] = v3.x; af[b][13] = v3.y; af[b][14] = v3.z; af[b][15] = v3.w;
+#pragma unroll
+            for (int g = 0; g < LE / 8; ++g) {
+                const float *p0 = arow[b] + i / 2 + 4 * g, *p1 = p0 + I / 2;
+                const float4 v0 = *reinterpret_cast<const float4 *>(p0);
+                const float4 v1 = *reinterpret_cast<const float4 *>(p1);
+                af[b][8 * g + 0] = v0.x; af[b][8 * g + 1] = v0.y; af[b][8 * g + 2] = v0.z; af[b][8 * g + 3] = v0.w;
+                af[b][8 * g + 4] = v1.x; af[b][8 * g + 5] = v1.y; af[b][8 * g + 6] = v1.z; af[b][8 * g + 7] = v1.w;
+            }
         }
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             float wf[16];
-            unpack16_e4m3(lds16(rowp[r] + i), wf);
+            if constexpr (LE == 16) {
+                unpack16_e4m3(lds16(rowp[r] + i), wf);
+            } else {
+                const uint2 w2 = *reinterpret_cast<const uint2 *>(rowp[r] + i);
+                unpack16_e4m3(make_uint4(w2.x, w2.y, 0u, 0u), wf);  // the first 8 values
+            }
             const float sc = e8m0_scale(scp[r][i >> 5]);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 float p = 0.0f;
 #pragma unroll
-                for (int q = 0; q < 16; ++q) p = fmaf(wf[q], af[b][q], p);
+                for (int q = 0; q < LE; ++q) p = fmaf(wf[q], af[b][q], p);
                 acc[r * NB + b] = fmaf(p, sc, acc[r * NB + b]);
             }
         }
@@ -479,6 +487,22 @@ __device__ __forceinline__ void down_rows_mx(const uint8_t *const *rowp, const u
     const float t = warp_sum_split(acc, lane);
     const int slot = lane / W, r = slot / NB, b = slot - r * NB;
     if (lane % W == 0 && slot < RB * NB && r < nu) part[r * A + asg[b]] = t;
+}
+
+// down_rows_mx for a row group serving na (1 <= na <= NT) assignments.
+template <int NT, int LE>
+__device__ __forceinline__ void down_rows_mx_na(int na, const uint8_t *const *rowp, const uint8_t *const *scp,
+                                                const float *const *arow, int I, int lane, int nu, const int *asg,
+                                                float *part, int A)
+{
+    if (na == 1) down_rows_mx<1, LE>(rowp, scp, arow, I, lane, nu, asg, part, A);
+    if constexpr (NT >= 2) {
+        if (na == 2) down_rows_mx<2, LE>(rowp, scp, arow, I, lane, nu, asg, part, A);
+    }
+    if constexpr (NT >= 4) {
+        if (na == 3) down_rows_mx<3, LE>(rowp, scp, arow, I, lane, nu, asg, part, A);
+        if (na == 4) down_rows_mx<4, LE>(rowp, scp, arow, I, lane, nu, asg, part, A);
+    }
 }
 
 // The router projection's inputs for the ROUTER instantiation: W_r [E][H]
@@ -1085,13 +1109,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         rowp[r] = chunk + rw * I;
                                         scp[r] = chunk + (size_t)rps * I + rw * mx.is;
                                     }
-                                    if (na == 1) down_rows_mx<1>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
-                                    if constexpr (NT >= 2) {
-                                        if (na == 2) down_rows_mx<2>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
-                                    }
-                                    if constexpr (NT >= 4) {
-                                        if (na == 3) down_rows_mx<3>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
-                                        if (na == 4) down_rows_mx<4>(rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    // 8-element lane steps unless I is a multiple of 512
+                                    if (I % 512) {
+                                        down_rows_mx_na<NT, 8>(na, rowp, scp, arow, I, lane, nu, s_asg + a0, pu, A);
+                                    } else {
+                                        down_rows_mx_na<NT, 16>(na, rowp, scp, arow, I, lane, nu, s_asg + a0, pu,
+                                                                A);
                                     }
                                 } else {
 #pragma unroll
