@@ -113,6 +113,19 @@ def test_ties_and_signed_zero_through_the_fused_kernel(T):
     _fused_and_general_agree(x, L.cuda(), wgu, wd, k)
 
 
+@pytest.mark.parametrize("T,E,k", [(1, 300, 8), (3, 1024, 8), (4, 1024, 7), (2, 130, 1)])
+def test_fused_routing_ties_many_experts(T, E, k):
+    """The fused kernel's routing (k <= 8: each lane's keys through the
+    sorting network, 8 at a time, then merged) on ties and signed zeros, with
+    E up to 1024 and ragged: the same bits as the router kernel of the
+    general decode path, and the oracle's indices."""
+    H, I = 256, 128
+    wl = gu.custom(T, H, I, E, k, name="fused_routing_ties")
+    x, _, wgu, wd = gu.make_layer(wl, T)
+    L = _tie_logits(T, E, seed=40 + T + E)
+    _fused_and_general_agree(x, L.cuda(), wgu, wd, k)
+
+
 @pytest.mark.parametrize("T,k", [(4, 9), (4, 16), (1, 32), (2, 32)])
 def test_ties_in_the_rescan_branch(T, k):
     """k > 8 selects by rescanning the lane's keys below the last winner
