@@ -226,8 +226,8 @@ def kernel_bytes(kernel, wl, T, U, k, bpe=2.0):
         return U * 2 * I * H * 2 + T * H * 2 + T * k * I * 4
     if kernel == "decode_down":
         return U * H * I * 2 + T * k * I * 4 + T * H * 4 + T * k * 4
-    if kernel == "gemm_gate_up":
-        return U * 2 * I * H * 2 + T * k * H * 2 + 2 * T * k * I * 2
+    if kernel == "gemm_gate_up":  # x rows read by the sorted order (re-reads of a row come from L2)
+        return U * 2 * I * H * 2 + T * H * 2 + 2 * T * k * I * 2
     if kernel == "gemm_down":
         return U * H * I * 2 + 2 * T * k * I * 2 + T * k * H * 4
     return None

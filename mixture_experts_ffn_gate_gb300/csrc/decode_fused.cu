@@ -71,7 +71,7 @@
 //     to cover them, and every call on the workspace lowers the size word
 //     to its tag_cap, the words of the region before the call's first other
 //     region, because a call with a smaller k*I places its routing, act or
-//     gathered rows inside the region of a larger one (this kernel does so
+//     z rows inside the region of a larger one (this kernel does so
 //     in CTA 0 once every CTA has read the flags; the other paths' router
 //     kernel before anything else).  So memory that held other data never
 //     stands in for an act value, whatever shapes share the workspace; only

@@ -13,7 +13,10 @@
 // a skewed or tiny expert load never pads the weight tile.  A work item is
 // one chunk against MT weight tiles of one expert (gate_up 4, down 3), which
 // share the chunk's token tile:
-//   gate_up: D[128 x N] = W_gu[e][rows] . xs[chunk]^T, K = H.  The 128 rows of
+//   gate_up: D[128 x N] = W_gu[e][rows] . x[tokens of the chunk]^T, K = H.
+//            The chunk's token rows are read from x by the sorted order (row
+//            p is token perm[p] / k), so no gathered copy of x is built.
+//            The 128 rows of
 //            a tile are 4 groups of (16 gate rows i.., 16 up rows I+i..), so
 //            each epilogue warp holds gate and up of the same 16 neurons in
 //            its lanes 0-15 / 16-31 and pairs them with one shuffle.  The
@@ -34,7 +37,11 @@
 //
 // One persistent CTA per SM: warp 0 issues TMA loads into a ring of smem
 // stages, warp 1 issues tcgen05.mma into one of two TMEM accumulators,
-// warps 2-5 drain the other accumulator (tcgen05.ld) and store.  Every
+// warps 2-5 drain the other accumulator (tcgen05.ld) and store.  gate_up
+// has three more warps, one per ring stage, that copy the chunk's x rows
+// into their stage (16-byte cp.async copies placed at the 128-byte-swizzled
+// offsets the MMA's B descriptor expects), wait for them, fence the proxies
+// and give the stage's full barrier its second arrival.  Every
 // mbarrier wait is bounded: on time-out the CTA raises a bit in the device
 // fault word, lets its copies and MMAs in flight finish (again bounded),
 // frees its TMEM and returns.
@@ -65,7 +72,8 @@ constexpr int BK = 64;                   // K elements per stage: one 128-byte s
 constexpr int NMAX = kGemmChunkMax;      // tokens per chunk (MMA N <= NMAX)
 constexpr int ACC_COLS = 64;             // TMEM columns per accumulator (>= NMAX)
 constexpr int SMALL_ROWS = 16;           // B box for chunks of at most 16 rows
-constexpr int kThreads = 192;
+constexpr int kThreads = 192;           // down: producer, MMA issuer, 4 epilogue warps
+constexpr int kThreadsGateUp = 288;     // gate_up: + one x-row loader warp per ring stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain after an abort
 
@@ -108,6 +116,9 @@ struct GemmArgs {
     int tiles;            // weight tiles per expert (the last group may have fewer)
     int a_bytes;          // bytes of one weight box (MT tiles, fewer if the tensor is smaller)
     void *out0, *out1;    // act_hi, act_lo | z
+    const uint16_t *x;    // gate_up: the tokens [T, H] (BF16 bits) and the
+    const int32_t *perm;  // sorted order (assignment t*k+j at row p)
+    int k;
 };
 
 struct Item {
@@ -132,7 +143,7 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs &a)
 __device__ __forceinline__ int pad16(int n) { return (n + 15) & ~15; }
 
 template <bool GATE_UP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0s,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1s,
                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
@@ -141,8 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      first: H, 16 rows, gate|up, row group, expert) whose {64,16,2,4,1}
     //      box is one 128-row tile of 4 x (16 gate rows, 16 up rows);
     //      down -- 3-D [E][H][I], box 64 x 128 x 1 (one tile).
-    // tmB0/tmB1: the chunk's token rows (x, or act_hi/act_lo), box 64 x NMAX;
+    // tmB0/tmB1 (down): the chunk's act_hi/act_lo rows, box 64 x NMAX;
     // tmB0s/tmB1s: the same with a 16-row box, for chunks of <= 16 rows.
+    // gate_up leaves the B maps unread.
     using C = Cfg<GATE_UP>;
     constexpr int MT = C::MT;
     extern __shared__ uint8_t smem_raw[];
@@ -160,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            ptx::mbar_init(full + s, 1);
+            // gate_up: the weight box's expect-tx arrival and the x rows' arrival
+            ptx::mbar_init(full + s, GATE_UP ? 2 : 1);
             ptx::mbar_init(empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -171,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::prefetch_tensormap(&tmA);
-        ptx::prefetch_tensormap(&tmB0);
-        ptx::prefetch_tensormap(&tmB0s);
         if (!GATE_UP) {
+            ptx::prefetch_tensormap(&tmB0);
+            ptx::prefetch_tensormap(&tmB0s);
             ptx::prefetch_tensormap(&tmB1);
             ptx::prefetch_tensormap(&tmB1s);
         }
@@ -202,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item it = nxt;
                 if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);  // loads overlap this item
                 const bool small = it.n <= SMALL_ROWS;
-                const uint32_t bytes = args.a_bytes + (small ? SMALL_ROWS : NMAX) * BK * 2 * (GATE_UP ? 1 : 2);
+                // gate_up: the weight box only (the x rows come from the loader warps)
+                const uint32_t bytes = args.a_bytes + (GATE_UP ? 0 : (small ? SMALL_ROWS : NMAX) * BK * 2 * 2);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!ptx::mbar_wait_bounded(empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
                         if (!*abort_flag) raise_fault(FAULT_GEMM_PRODUCER);
@@ -222,13 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int t = 0; t < MT; ++t)
                             ptx::tma_load_3d(a + t * C::A_TILE, &tmA, k0, (it.m * MT + t) * BM, it.e, full + stage);
                     }
-                    uint8_t *b = sB + stage * C::B_BYTES;
-                    ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
-                    // down: the lo rows right after the hi rows (a whole
-                    // number of 1024-byte swizzle groups), one B tile
-                    if (!GATE_UP)
+                    // down: the hi rows, then the lo rows right after them (a
+                    // whole number of 1024-byte swizzle groups), one B tile
+                    if (!GATE_UP) {
+                        uint8_t *b = sB + stage * C::B_BYTES;
+                        ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
                         ptx::tma_load_2d(b + (small ? SMALL_ROWS : NMAX) * BK * 2, small ? &tmB1s : &tmB1, k0, it.p0,
                                          full + stage);
+                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1;
@@ -296,6 +311,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(drain);
             ptx::mbar_wait_bounded(drain, 0, abort_flag, kDrainLimitNs);
         }
+    } else if (GATE_UP && warp >= 6) {
+        // ------------------------------------- x-row loaders (gate_up only)
+        // Warp 6 + sl fills ring stage sl: the CTA's K steps n = sl, sl +
+        // STAGES, ... over its items in the producer's order (item i = block
+        // + j * grid, K steps in order; stage n % STAGES, phase (n / STAGES)
+        // & 1).  Lane l copies rows l and l + 32 of the chunk, 128 bytes per
+        // row, piece q of row r at (q ^ (r & 7)) * 16; rows past the chunk
+        // are not loaded (the MMA's columns for them are never stored).
+        const int sl = warp - 6;
+        uint32_t swz[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) swz[q] = (uint32_t)((q ^ (lane & 7)) << 4);
+        uint8_t *b = sB + sl * C::B_BYTES;
+        int n = 0;  // this CTA's K steps before the current item
+        for (int i = blockIdx.x; i < total; i += gridDim.x, n += KB) {
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;  // warp-uniform
+            // this item's K steps that fall on stage sl
+            int kb = (sl - n % C::STAGES + C::STAGES) % C::STAGES;
+            if (kb >= KB) continue;
+            const Item it = decode_item(i, args);
+            const uint16_t *row0 = nullptr, *row1 = nullptr;
+            if (lane < it.n) row0 = args.x + (int64_t)(__ldg(args.perm + it.p0 + lane) / args.k) * args.H;
+            if (lane + 32 < it.n) row1 = args.x + (int64_t)(__ldg(args.perm + it.p0 + lane + 32) / args.k) * args.H;
+            bool ok = true;
+            for (; kb < KB; kb += C::STAGES) {
+                const uint32_t phase = (uint32_t)((n + kb) / C::STAGES) & 1u;
+                int got = 1;
+                if (lane == 0) got = ptx::mbar_wait_bounded(empty + sl, phase ^ 1, abort_flag, kWaitLimitNs);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    if (lane == 0) {
+                        if (!*abort_flag) raise_fault(FAULT_GEMM_PRODUCER);
+                        *abort_flag = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+                const int k0 = kb * BK;
+                if (row0) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) ptx::cp_async16(b + lane * 128 + swz[q], row0 + k0 + 8 * q);
+                }
+                if (row1) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) ptx::cp_async16(b + (lane + 32) * 128 + swz[q], row1 + k0 + 8 * q);
+                }
+                ptx::cp_async_commit();
+                ptx::cp_async_wait_all();
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(full + sl);
+            }
+            if (!ok) break;
+        }
+        ptx::cp_async_wait_all();
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -468,22 +537,21 @@ bool gemm_supported(int H, int I, int E)
            encoder() != nullptr;
 }
 
-cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chunks, const int32_t *nchunks,
-                                const int32_t *offs, int n_assign, int H, int I, int E, void *act_hi, void *act_lo,
-                                int ctas, cudaStream_t s)
+cudaError_t launch_gemm_gate_up(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E,
+                                void *act_hi, void *act_lo, int ctas, cudaStream_t s)
 {
-    CUtensorMap tA, tBs, tB;
+    CUtensorMap tA;
     constexpr int MT = Cfg<true>::MT;
     // groups of 16 neurons per box: MT tiles of 4, but never more than the tensor has
     const uint32_t groups = (uint32_t)(4 * MT < I / 16 ? 4 * MT : I / 16);
     cudaError_t e = make_gate_up_map(&tA, wgu, E, I, H, groups);
-    if (e == cudaSuccess) e = make_map(&tBs, xs, n_assign, H, SMALL_ROWS);
-    if (e == cudaSuccess) e = make_map(&tB, xs, n_assign, H, NMAX);
     if (e != cudaSuccess) return e;
     GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK * 2, act_hi,
-               act_lo};
-    grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<true>::SMEM, s>>>(
-        tA, tBs, tB, tBs, tB, a);
+               act_lo, (const uint16_t *)x, perm, k};
+    // the token rows come from x through the loader warps: the B maps are not read
+    grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreadsGateUp, Cfg<true>::SMEM, s>>>(
+        tA, tA, tA, tA, tA, a);
     return cudaPeekAtLastError();
 }
 
@@ -500,7 +568,8 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
     if (e == cudaSuccess) e = make_map(&tB1, act_lo, n_assign, I, NMAX);
     if (e != cudaSuccess) return e;
     const int tiles = (H + BM - 1) / BM;
-    GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, MT * BM * BK * 2, z, nullptr};
+    GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, MT * BM * BK * 2, z, nullptr, nullptr,
+               nullptr, 0};
     grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(
         tA, tB0s, tB0, tB1s, tB1, a);
     return cudaPeekAtLastError();

@@ -35,8 +35,6 @@ size_t sort_smem_bytes(int E);
 cudaError_t launch_sort(const int32_t *idx, int n_assign, int E, int chunk_max, int32_t *offs, int32_t *perm,
                         int32_t *pos, int32_t *uexp, int32_t *ucount, int4 *chunks, int32_t *nchunks,
                         cudaStream_t s);
-cudaError_t launch_gather(const void *x, const int32_t *perm, int k, int H, int n_rows, void *xs, int n_sm,
-                          cudaStream_t s);
 cudaError_t launch_combine(const float *z, const float *w, const int32_t *pos, int T, int H, int k, float *out,
                            int n_sm, cudaStream_t s);
 
@@ -105,9 +103,11 @@ unsigned long long current_context_id();
 // grouped_gemm.cu
 cudaError_t gemm_init_device();
 bool gemm_supported(int H, int I, int E);
-cudaError_t launch_gemm_gate_up(const void *xs, const void *wgu, const int4 *chunks, const int32_t *nchunks,
-                                const int32_t *offs, int n_assign, int H, int I, int E, void *act_hi, void *act_lo,
-                                int ctas, cudaStream_t s);
+// gate_up reads the chunk's token rows from x [T, H] by perm (row p of the
+// sorted order is token perm[p] / k)
+cudaError_t launch_gemm_gate_up(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E,
+                                void *act_hi, void *act_lo, int ctas, cudaStream_t s);
 cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void *wd, const int4 *chunks,
                              const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, float *z,
                              int ctas, cudaStream_t s);

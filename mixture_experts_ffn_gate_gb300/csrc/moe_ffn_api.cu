@@ -37,7 +37,7 @@ struct Layout {
     size_t flags, act_tag, idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, common_end;
     unsigned long long tag_cap;          // 64-bit words from act_tag to the next region
     size_t act;                          // decode: act f32 [T*k, I]
-    size_t xs, act_hi, act_lo, z;        // grouped
+    size_t act_hi, act_lo, z;            // grouped
     size_t decode_total, grouped_total, total;
     // calls that pass the router weights: the logits [T, E] f32 (paths other
     // than the fused decode kernel) and the fused kernel's tagged logit words
@@ -76,7 +76,6 @@ Layout make_layout(const Shape &s)
     L.decode_total = o;
     // grouped path
     o = L.common_end;
-    L.xs = take(n * (size_t)s.H * 2);
     L.act_hi = take(n * (size_t)s.I * 2);
     L.act_lo = take(n * (size_t)s.I * 2);
     L.z = take(n * (size_t)s.H * 4);
@@ -161,7 +160,7 @@ int device_setup(DeviceInfo **info)
 
 const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
 const char *kDecodeFusedStages[] = {"decode_fused"};
-const char *kGroupedStages[] = {"router", "sort", "gather", "gemm_gate_up", "gemm_down", "combine"};
+const char *kGroupedStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "combine"};
 
 // Records stage events around the launches of one call.  While the stream is
 // being captured into a CUDA graph the records become external event-record
@@ -276,15 +275,13 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
         MOE_TRY(stg.done(moe::launch_decode_down(act, wd, w, uexp, ucount, offs, perm, T, H, I, k, dn_warps, out,
                                                  mx, stream)));
     } else {
-        void *xs = ws + L.xs;
         void *act_hi = ws + L.act_hi;
         void *act_lo = ws + L.act_lo;
         auto *z = (float *)(ws + L.z);
         MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
                                           chunks, nchunks, stream)));
-        MOE_TRY(stg.done(moe::launch_gather(x, perm, k, H, n_assign, xs, dev->n_sm, stream)));
-        MOE_TRY(stg.done(moe::launch_gemm_gate_up(xs, wgu, chunks, nchunks, offs, n_assign, H, I, E, act_hi,
-                                                  act_lo, gemm_ctas, stream)));
+        MOE_TRY(stg.done(moe::launch_gemm_gate_up(x, perm, k, wgu, chunks, nchunks, offs, n_assign, H, I, E,
+                                                  act_hi, act_lo, gemm_ctas, stream)));
         MOE_TRY(stg.done(moe::launch_gemm_down(act_hi, act_lo, wd, chunks, nchunks, offs, n_assign, H, I, E, z,
                                                gemm_ctas, stream)));
         MOE_TRY(stg.done(moe::launch_combine(z, w, pos, T, H, k, out, dev->n_sm, stream)));

@@ -1,6 +1,6 @@
-// routing.cu -- router (top-k + softmax), deterministic counting sort of the
-// token->expert assignments, the row gather for the grouped path and the
-// fixed-order combine.
+// routing.cu -- router (top-k + softmax), the router projection for callers
+// that pass the router weights, deterministic counting sort of the
+// token->expert assignments and the fixed-order combine.
 //
 // Determinism: none of these kernels uses a floating-point atomic.  The sort
 // uses integer shared-memory atomics only to count, and places every
@@ -23,7 +23,7 @@ constexpr int kRouterWarps = 8;
 //
 // On a workspace that keeps the fused decode kernel's state, block 0 also
 // lowers that kernel's size word to tag_cap: this call's other regions
-// (routing, act, gathered rows ...) start tag_cap words into the tag region,
+// (routing, act, the grouped path's act and z rows ...) start tag_cap words into the tag region,
 // and a later fused call must not take what they leave there for tags.
 __global__ void __launch_bounds__(32 * kRouterWarps) router_kernel(const float *__restrict__ logits, int T, int E,
                                                                    int k, int32_t *__restrict__ idx,
@@ -180,19 +180,6 @@ __global__ void __launch_bounds__(SORT_THREADS) sort_kernel(const int32_t *__res
     }
 }
 
-// ---------------------------------------------------------------- gather
-// xs[p, :] = x[perm[p] / k, :]  (rows of H bf16, 16-byte vectors)
-__global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm, int k,
-                                   int vec_per_row, int n_rows, uint4 *__restrict__ xs)
-{
-    const int64_t total = (int64_t)n_rows * vec_per_row;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t p = i / vec_per_row, v = i - p * vec_per_row;
-        const int t = perm[p] / k;
-        xs[i] = ld_nc16(x + (int64_t)t * vec_per_row + v);
-    }
-}
-
 // ---------------------------------------------------------------- combine
 // out[t, h] = sum_{j ascending} w[t,j] * z[pos[t*k+j], h]   (FP32, fixed order)
 __global__ void combine_kernel(const float *__restrict__ z, const float *__restrict__ w,
@@ -248,17 +235,6 @@ cudaError_t launch_sort(const int32_t *idx, int n_assign, int E, int chunk_max, 
     const size_t smem = sort_smem_bytes(E);
     sort_kernel<<<1, SORT_THREADS, smem, s>>>(idx, n_assign, E, chunk_max, offs, perm, pos, uexp, ucount, chunks,
                                               nchunks);
-    return cudaPeekAtLastError();
-}
-
-cudaError_t launch_gather(const void *x, const int32_t *perm, int k, int H, int n_rows, void *xs, int n_sm,
-                          cudaStream_t s)
-{
-    const int vec = H / 8;
-    const int64_t total = (int64_t)n_rows * vec;
-    const int64_t blocks = ceil_div(total, 256);
-    const int grid = (int)(blocks < (int64_t)n_sm * 8 ? blocks : (int64_t)n_sm * 8);
-    gather_rows_kernel<<<grid, 256, 0, s>>>((const uint4 *)x, perm, k, vec, n_rows, (uint4 *)xs);
     return cudaPeekAtLastError();
 }
 

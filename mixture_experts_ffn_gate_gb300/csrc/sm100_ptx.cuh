@@ -124,6 +124,26 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// 16-byte copy global -> shared by the issuing thread (cp.async, through L2
+// only).  These are generic-proxy writes: before tcgen05.mma may read them
+// the thread waits for its copies (cp_async_wait_all) and fences the proxies
+// (fence_proxy_async_smem), then signals the MMA issuer.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy accesses (TMA, tcgen05.mma) that synchronise with it.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // GPU-scope release store / acquire load of a 64-bit flag (grid barriers).
 __device__ __forceinline__ void st_release_gpu(unsigned long long *p, unsigned long long v)
 {

@@ -65,7 +65,8 @@ def test_stage_names(L):
     assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE, i) for i in range(5)] == \
         ["router", "sort", "decode_gate_up", "decode_down", None]
     assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE_FUSED, i) for i in range(2)] == ["decode_fused", None]
-    assert m.moe_ffn_stage_name(m.MOE_PATH_GROUPED, 3) == "gemm_gate_up"
+    assert [m.moe_ffn_stage_name(m.MOE_PATH_GROUPED, i) for i in range(6)] == \
+        ["router", "sort", "gemm_gate_up", "gemm_down", "combine", None]
     assert m.moe_ffn_stage_name(m.MOE_PATH_AUTO, 0) is None
     assert m.moe_ffn_stage_name(m.MOE_PATH_DECODE, -1) is None
 

@@ -233,7 +233,7 @@ def test_auto_path_choice():
         o.decode_max_tokens = thr
         m.moe_ffn_forward_ex(x, L, wgu, wd, k, opts=o)
         assert o.path_taken == want, (thr, o.path_taken)
-        assert o.n_stages == (4 if want == m.MOE_PATH_DECODE else 6)
+        assert o.n_stages == (4 if want == m.MOE_PATH_DECODE else 5)
 
 
 @pytest.mark.parametrize("T", [1, 6, 200])
@@ -260,7 +260,7 @@ def test_plain_forward_and_host_entry_match_ex(T):
         assert torch.equal(oh, ref.cpu()), pinned
 
 
-@pytest.mark.parametrize("T,path,stages", [(3, "decode", 1), (8, "decode", 4), (8, "grouped", 6)])
+@pytest.mark.parametrize("T,path,stages", [(3, "decode", 1), (8, "decode", 4), (8, "grouped", 5)])
 def test_stage_events_time_each_kernel(T, path, stages):
     H, I, E, k = 256, 128, 8, 2
     wl = gu.custom(T, H, I, E, k, name="events")
