@@ -192,3 +192,11 @@ def forward_mxfp8(x, logits, wgu_q, wgu_s, wd_q, wd_s, k, **kw):
     Returns (out, idx, w)."""
     from .mxfp8 import dequantize_bf16
     return forward(x, logits, dequantize_bf16(wgu_q, wgu_s), dequantize_bf16(wd_q, wd_s), k, **kw)
+
+
+def backward(x, logits, wgu, wd, dout, k, **kw):
+    """The layer's gradients for the upstream gradient ``dout`` (float32
+    [T, H]) in FP64; see moe_backward.py.  Returns a dict with dx, dlogits,
+    dwgu, dwd (and the routing idx, w and dL/dw)."""
+    from .moe_backward import backward as f
+    return f(x, logits, wgu, wd, dout, k, route, **kw)
