@@ -82,13 +82,14 @@ enum {
     MOE_PATH_AUTO = 0,    /* decode for T <= decode_max_tokens, else grouped */
     MOE_PATH_DECODE = 1,  /* warp per output scalar, weights streamed once   */
     MOE_PATH_GROUPED = 2, /* counting sort + tcgen05 grouped GEMMs + combine */
-    MOE_PATH_DECODE_FUSED = 3 /* reported only (path_taken): the decode path
-                                 for T <= 4 as one kernel that routes the
-                                 tokens itself; same results as
-                                 MOE_PATH_DECODE */
+    MOE_PATH_DECODE_FUSED = 3, /* reported only (path_taken): the decode path
+                                  for T <= 4 as one kernel that routes the
+                                  tokens itself; same results as
+                                  MOE_PATH_DECODE */
+    MOE_PATH_BACKWARD = 4 /* reported only: moe_ffn_backward's kernels */
 };
 
-#define MOE_MAX_STAGES 8
+#define MOE_MAX_STAGES 12
 
 /*
  * Optional knobs and outputs of moe_ffn_forward_ex.  Zero-initialise and set
@@ -297,6 +298,47 @@ int moe_ffn_forward_noalloc(const void *x_bf16, const float *router_logits_f32,
                             int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
                             float *out_f32, cudaStream_t stream);
 
+/*
+ * The backward pass of the layer (the Mixture-of-Kittens article,
+ * asapai.co.kr, section 2.37배는 어떤 기준선과 비교한 숫자인가, measures the
+ * layer's forward and backward passes in training; the gradients below are
+ * the chain rule of the forward definition at the top of this file).  For
+ * the upstream gradient dout_f32 [T,H] = dL/dout, with the routing of the
+ * forward pass recomputed from the logits (same selection and weights):
+ *   q = W_down[e]^T dout[t],  dw_j = a . q,  da = w_j q,
+ *   dg = da u s (1 + g (1 - s)),  du = da g s      (s = sigmoid(g));
+ *   dx_f32 [T,H]          = sum_j W_gate[e]^T dg + W_up[e]^T du
+ *   dlogits_f32 [T,E]     = w_j (dw_j - sum_m w_m dw_m) at the selected
+ *                           experts s_j, 0 elsewhere (the selection is
+ *                           piecewise constant in the logits)
+ *   dw_gate_up_f32 [E,2I,H] = sum over e's assignments of [dg ; du] x[t]^T
+ *   dw_down_f32 [E,H,I]   = sum over e's assignments of (w_j dout[t]) a^T
+ * All four outputs are fully overwritten (experts no token selects get
+ * zeros) and must not alias each other or an input.  Arithmetic: BF16
+ * inputs, FP32 accumulation, FP32 intermediates; tensor-core products take
+ * FP32 operands as BF16 hi + lo pairs.  Deterministic (no floating-point
+ * atomics): the same inputs give the same output bits on every run.
+ * Same shape limits and pointer rules as the forward pass; the call runs
+ * the grouped tensor-core kernels for every T (opts->path AUTO or GROUPED,
+ * else MOE_ERR_UNSUPPORTED_SHAPE).  workspace: device, 256-byte aligned, at
+ * least moe_ffn_backward_workspace_bytes; NULL makes the call allocate one
+ * stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`).  The
+ * workspace may be one that forward calls also use: the backward call
+ * keeps the fused decode kernel's state words valid (it marks the state's
+ * tag region as spent).  T == 0 zeroes the two weight gradients
+ * (cudaMemsetAsync) and returns.  opts (nullable): gemm_ctas and
+ * stage_events as for the forward pass; path_taken = MOE_PATH_BACKWARD.
+ */
+size_t moe_ffn_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E,
+                                        int64_t k);
+int moe_ffn_backward(const void *x_bf16, const float *router_logits_f32,
+                     const void *w_gate_up_bf16, const void *w_down_bf16,
+                     const float *dout_f32, int64_t T, int64_t H, int64_t I,
+                     int64_t E, int64_t k, float *dx_f32, float *dlogits_f32,
+                     float *dw_gate_up_f32, float *dw_down_f32, void *workspace,
+                     size_t workspace_bytes, moe_ffn_opts *opts,
+                     cudaStream_t stream);
+
 /* Static text for a status code. */
 const char *moe_ffn_status_string(int status);
 
@@ -305,7 +347,9 @@ const char *moe_ffn_stage_name(int path, int stage);
 
 /*
  * Device fault word: bit flags that kernels set when a bounded device-side
- * wait gives up (instead of hanging).  Reads the current device's word
+ * wait gives up (instead of hanging): bits 0-7 the grouped GEMMs, 8-15 the
+ * fused decode kernel, 16-23 the backward pass's weight-gradient GEMMs.
+ * Reads the current device's word
  * synchronously into *flags and, if clear != 0, resets it.  Returns MOE_OK,
  * or MOE_ERR_CUDA if the read fails.  A non-zero word means some call since
  * the last clear returned garbage in out_f32.

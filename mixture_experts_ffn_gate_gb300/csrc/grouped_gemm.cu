@@ -79,8 +79,23 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain after an abo
 
 static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulator");
 
-template <bool GATE_UP>
+// What a kernel instance computes (the forward pass's two GEMMs, and the
+// backward pass's recomputation of gate/up and its two GEMMs against the
+// weights read along their other axis).
+enum : int {
+    kDown = 0,       // z = W_down . [act_hi ; act_lo]
+    kGateUp = 1,     // act = silu(W_gate x) * (W_up x) as a BF16 hi/lo pair
+    kGateUpRaw = 2,  // g = W_gate x and u = W_up x in FP32
+    kBwdQ = 3,       // q = W_down^T . [dout_hi ; dout_lo], then the SwiGLU backward
+    kBwdDx = 4,      // z = W_gate_up^T . [dgu_hi ; dgu_lo]
+};
+
+template <int KIND>
 struct Cfg {
+    static constexpr bool GATE_UP = KIND == kGateUp || KIND == kGateUpRaw;
+    // the weight tile is read along its rows' index (MN-major): the
+    // backward's contractions over H (W_down) and over 2I (W_gate_up)
+    static constexpr bool A_MN = KIND == kBwdQ || KIND == kBwdDx;
     static constexpr int MT = GATE_UP ? 4 : 3;  // weight tiles per item (they share one token tile)
     // accumulator columns per weight tile: the chunk's tokens (gate_up), or
     // its hi rows then its lo rows (down); gate_up double-buffers them so the
@@ -106,6 +121,17 @@ struct Cfg {
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
 };
 
+// Inputs and outputs of the backward pass's q GEMM epilogue (kBwdQ), all
+// indexed by the (padded) sorted row r: g, u [rows][I] FP32 and the routing
+// weight w_s [rows] in; dgu_hi/lo [rows][2I] (dg | du), wa_hi/lo [rows][I]
+// (w * act) as BF16 pairs and dwp [rows][I/32] (partial sums of act . q
+// over 32 neurons) out.
+struct BwdQArgs {
+    const float *g, *u, *w_s;
+    __nv_bfloat16 *dgu_hi, *dgu_lo, *wa_hi, *wa_lo;
+    float *dwp;
+};
+
 struct GemmArgs {
     const int4 *chunks;   // {expert, first sorted row, rows, first chunk of expert}
     const int32_t *nchunks;
@@ -119,6 +145,7 @@ struct GemmArgs {
     const uint16_t *x;    // gate_up: the tokens [T, H] (BF16 bits) and the
     const int32_t *perm;  // sorted order (assignment t*k+j at row p)
     int k;
+    BwdQArgs q;           // kBwdQ only
 };
 
 struct Item {
@@ -142,8 +169,78 @@ __device__ __forceinline__ Item decode_item(int i, const GemmArgs &a)
 
 __device__ __forceinline__ int pad16(int n) { return (n + 15) & ~15; }
 
-template <bool GATE_UP>
-__global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
+__device__ __forceinline__ void store_pair(__nv_bfloat16 *hi, __nv_bfloat16 *lo, int64_t at, float v)
+{
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[at] = h;
+    lo[at] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+// After this, lane l holds the sum over the warp's 32 lanes of v[l] (a
+// 32 x 32 transpose-and-add in 31 shuffles, in a fixed order): each round
+// a lane keeps one half of its remaining columns and adds its partner's
+// copy of that half.
+__device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < s; ++i) {
+            const float send = upper ? v[i] : v[i + s];
+            const float keep = upper ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+        }
+    }
+    return v[0];
+}
+
+// The backward pass's SwiGLU step for 32 columns (sorted rows it.p0 + c0 +
+// j) of neuron i, whose q = W_down[e]^T dout_t values are r[j]:
+//   s = sigmoid(g), a = g s u, da = w q,
+//   dg = da u s (1 + g (1 - s)), du = da g s,
+// stored as BF16 pairs (dgu rows: dg at i, du at I + i; wa = w a), zeros in
+// the expert's pad rows; and act . q summed over the warp's 32 neurons
+// into dwp[row][grp].
+__device__ __forceinline__ void bwd_q_columns(const uint32_t (&r)[32], int ncols, int p0, int n, int c0, int i,
+                                              int grp, const GemmArgs &args, int lane)
+{
+    const int I = args.I;
+    const int npad = pad16(n);
+    const BwdQArgs &b = args.q;
+    float prod[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int col = c0 + j;
+        prod[j] = 0.0f;
+        if (j < ncols && col < npad) {
+            const int64_t row = p0 + col;
+            float dg = 0.0f, du = 0.0f, wa = 0.0f;
+            if (col < n) {
+                const float qv = __uint_as_float(r[j]);
+                const float g = __ldg(b.g + row * I + i);
+                const float u = __ldg(b.u + row * I + i);
+                const float w = __ldg(b.w_s + row);
+                const float sg = 1.0f / (1.0f + expf(-g));
+                const float silu = g * sg;
+                const float a = silu * u;
+                const float da = w * qv;
+                dg = da * u * (sg * (1.0f + g * (1.0f - sg)));
+                du = da * silu;
+                wa = w * a;
+                prod[j] = a * qv;
+            }
+            store_pair(b.dgu_hi, b.dgu_lo, row * 2 * I + i, dg);
+            store_pair(b.dgu_hi, b.dgu_lo, row * 2 * I + I + i, du);
+            store_pair(b.wa_hi, b.wa_lo, row * I + i, wa);
+        }
+    }
+    const float sum = warp_column_sums(prod, lane);
+    if (lane < ncols && c0 + lane < n) b.dwp[(int64_t)(p0 + c0 + lane) * (I / 32) + grp] = sum;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(Cfg<KIND>::GATE_UP ? kThreadsGateUp : kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0s,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1s,
                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
@@ -151,11 +248,17 @@ __global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
     // tmA: gate_up -- 5-D view of W_gu [E][2][I/16][16][H] (dims innermost
     //      first: H, 16 rows, gate|up, row group, expert) whose {64,16,2,4,1}
     //      box is one 128-row tile of 4 x (16 gate rows, 16 up rows);
-    //      down -- 3-D [E][H][I], box 64 x 128 x 1 (one tile).
-    // tmB0/tmB1 (down): the chunk's act_hi/act_lo rows, box 64 x NMAX;
-    // tmB0s/tmB1s: the same with a 16-row box, for chunks of <= 16 rows.
-    // gate_up leaves the B maps unread.
-    using C = Cfg<GATE_UP>;
+    //      down -- 3-D [E][H][I], box 64 x 128 x 1 (one tile);
+    //      q -- 3-D [E][H][I] with I innermost, box 64 (I) x 64 (H) x 1:
+    //      two boxes (neurons i0.., i0+64..) per tile and K step;
+    //      dx -- 3-D [E][2I][H] with H innermost, box 64 (H) x 64 (2I) x 1,
+    //      two boxes (dims h0.., h0+64..) per tile and K step.
+    // tmB0/tmB1 (down, q, dx): the chunk's hi/lo rows (act, dout or dgu),
+    // box 64 x NMAX; tmB0s/tmB1s: the same with a 16-row box, for chunks of
+    // <= 16 rows.  gate_up leaves the B maps unread.
+    using C = Cfg<KIND>;
+    constexpr bool GATE_UP = C::GATE_UP;
+    constexpr bool A_MN = C::A_MN;
     constexpr int MT = C::MT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -231,6 +334,13 @@ __global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
                     // rows past the expert's end read 0 and are never stored
                     if (GATE_UP) {
                         ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4 * MT, it.e, full + stage);
+                    } else if (A_MN) {
+#pragma unroll
+                        for (int t = 0; t < MT; ++t) {
+                            const int mn0 = (it.m * MT + t) * BM;
+                            ptx::tma_load_3d(a + t * C::A_TILE, &tmA, mn0, k0, it.e, full + stage);
+                            ptx::tma_load_3d(a + t * C::A_TILE + C::A_TILE / 2, &tmA, mn0 + 64, k0, it.e, full + stage);
+                        }
                     } else {
 #pragma unroll
                         for (int t = 0; t < MT; ++t)
@@ -268,7 +378,8 @@ __global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
                 if (i + (int)gridDim.x < total) nxt = decode_item(i + gridDim.x, args);
                 // down: N spans the hi box and the lo rows that matter
                 const int box = it.n <= SMALL_ROWS ? SMALL_ROWS : NMAX;
-                const uint32_t idesc = ptx::idesc_bf16_f32(BM, GATE_UP ? pad16(it.n) : box + pad16(it.n));
+                const uint32_t idesc =
+                    ptx::idesc_bf16_f32_mn(BM, GATE_UP ? pad16(it.n) : box + pad16(it.n), A_MN, false);
                 const int acc = C::ACC_BUFS == 2 ? (li & 1) : 0;
                 const uint32_t aph = C::ACC_BUFS == 2 ? (li >> 1) & 1 : li & 1;
                 if (!ptx::mbar_wait_bounded(tempty + acc, aph ^ 1, abort_flag, kWaitLimitNs)) {
@@ -294,7 +405,11 @@ __global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
                         const uint64_t bd = ptx::sw128_desc(b_addr + k * 32);
 #pragma unroll
                         for (int t = 0; t < MT; ++t) {
-                            const uint64_t ad = ptx::sw128_desc(a_addr + t * C::A_TILE + k * 32);
+                            // K-major: the K step is 32 bytes along the row;
+                            // MN-major: 16 K rows of 128 bytes, the tile's
+                            // second 64-wide MN block a box (8 KB) on
+                            const uint64_t ad = A_MN ? ptx::sw128_desc_mn(a_addr + t * C::A_TILE + k * 2048, C::A_TILE / 2)
+                                                     : ptx::sw128_desc(a_addr + t * C::A_TILE + k * 32);
                             ptx::mma_bf16(d + t * C::TILE_COLS, ad, bd, idesc, (kb | k) != 0);
                         }
                     }
@@ -383,6 +498,8 @@ __global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
             ptx::tc_fence_after();
             for (int t = 0; t < MT && it.m * MT + t < args.tiles; ++t) {
             const int tile = it.m * MT + t;
+            // q: a warp whose 32 neurons lie past I has nothing to do
+            if (KIND == kBwdQ && tile * BM + 32 * q >= args.I) continue;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (acc * MT + t) * C::TILE_COLS;
             for (int c0 = 0; c0 < it.n; c0 += 32) {
                 uint32_t r[32];
@@ -406,7 +523,16 @@ __global__ void __launch_bounds__(GATE_UP ? kThreadsGateUp : kThreads, 1)
                 } else {
                     ptx::tmem_wait_ld();
                 }
-                if (GATE_UP) {
+                if constexpr (KIND == kGateUpRaw) {
+                    const int neuron = tile * 64 + 16 * q + (lane & 15);
+                    float *dst = reinterpret_cast<float *>(lane < 16 ? args.out0 : args.out1);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < it.n) dst[(int64_t)(it.p0 + c0 + j) * args.I + neuron] = __uint_as_float(r[j]);
+                } else if constexpr (KIND == kBwdQ) {
+                    bwd_q_columns(r, it.n > SMALL_ROWS ? 32 : SMALL_ROWS, it.p0, it.n, c0, tile * BM + 32 * q + lane,
+                                  tile * 4 + q, args, lane);
+                } else if constexpr (KIND == kGateUp) {
                     const int neuron = tile * 64 + 16 * q + (lane & 15);
                     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(lane < 16 ? args.out0 : args.out1);
 #pragma unroll
@@ -521,13 +647,21 @@ int grid_for(int ctas, int n_assign, int m_tiles, int E)
 
 }  // namespace
 
+template <int KIND>
+cudaError_t set_smem()
+{
+    return cudaFuncSetAttribute(grouped_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<KIND>::SMEM);
+}
+
 cudaError_t gemm_init_device()
 {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<true>::SMEM);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(grouped_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<false>::SMEM);
+    cudaError_t e = set_smem<kGateUp>();
+    if (e == cudaSuccess) e = set_smem<kDown>();
+    if (e == cudaSuccess) e = set_smem<kGateUpRaw>();
+    if (e == cudaSuccess) e = set_smem<kBwdQ>();
+    if (e == cudaSuccess) e = set_smem<kBwdDx>();
+    return e;
 }
 
 bool gemm_supported(int H, int I, int E)
@@ -537,22 +671,106 @@ bool gemm_supported(int H, int I, int E)
            encoder() != nullptr;
 }
 
-cudaError_t launch_gemm_gate_up(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
-                                const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E,
-                                void *act_hi, void *act_lo, int ctas, cudaStream_t s)
+namespace {
+
+template <int KIND>
+cudaError_t gate_up_like(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                         const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, void *out0,
+                         void *out1, int ctas, cudaStream_t s)
 {
     CUtensorMap tA;
-    constexpr int MT = Cfg<true>::MT;
+    constexpr int MT = Cfg<KIND>::MT;
     // groups of 16 neurons per box: MT tiles of 4, but never more than the tensor has
     const uint32_t groups = (uint32_t)(4 * MT < I / 16 ? 4 * MT : I / 16);
     cudaError_t e = make_gate_up_map(&tA, wgu, E, I, H, groups);
     if (e != cudaSuccess) return e;
-    GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK * 2, act_hi,
-               act_lo, (const uint16_t *)x, perm, k};
+    GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK * 2, out0,
+               out1, (const uint16_t *)x, perm, k};
     // the token rows come from x through the loader warps: the B maps are not read
-    grouped_gemm_kernel<true><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreadsGateUp, Cfg<true>::SMEM, s>>>(
+    grouped_gemm_kernel<KIND><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreadsGateUp, Cfg<KIND>::SMEM, s>>>(
         tA, tA, tA, tA, tA, a);
     return cudaPeekAtLastError();
+}
+
+// The B maps of a hi/lo operand pair [rows][cols]: NMAX- and 16-row boxes.
+cudaError_t make_pair_maps(CUtensorMap (&m)[4], const void *hi, const void *lo, uint64_t rows, uint64_t cols)
+{
+    cudaError_t e = make_map(&m[0], hi, rows, cols, SMALL_ROWS);
+    if (e == cudaSuccess) e = make_map(&m[1], hi, rows, cols, NMAX);
+    if (e == cudaSuccess) e = make_map(&m[2], lo, rows, cols, SMALL_ROWS);
+    if (e == cudaSuccess) e = make_map(&m[3], lo, rows, cols, NMAX);
+    return e;
+}
+
+// A 3-D BF16 map [d2][d1][d0] (d0 innermost) with a 64 x 64 x 1 box: 64
+// elements of d0 (128 bytes, 128-byte swizzle) by 64 of d1.
+cudaError_t make_mn_map(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const cuuint32_t box[3] = {64, BK, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// q and dx: M (the weight side) of size m_size in tiles of 128, K = k_size.
+template <int KIND>
+cudaError_t launch_mn(const CUtensorMap &tA, const CUtensorMap (&tB)[4], const int4 *chunks, const int32_t *nchunks,
+                      const int32_t *offs, int n_rows, int H, int I, int E, int m_size, int k_size, void *out0,
+                      const BwdQArgs &q, int ctas, cudaStream_t s)
+{
+    constexpr int MT = Cfg<KIND>::MT;
+    const int tiles = (m_size + BM - 1) / BM;
+    GemmArgs a{chunks, nchunks, offs, H, I, k_size, (tiles + MT - 1) / MT, tiles, MT * BM * BK * 2, out0, nullptr,
+               nullptr, nullptr, 0, q};
+    grouped_gemm_kernel<KIND><<<grid_for(ctas, n_rows, a.m_tiles, E), kThreads, Cfg<KIND>::SMEM, s>>>(
+        tA, tB[0], tB[1], tB[2], tB[3], a);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_gate_up(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E,
+                                void *act_hi, void *act_lo, int ctas, cudaStream_t s)
+{
+    return gate_up_like<kGateUp>(x, perm, k, wgu, chunks, nchunks, offs, n_assign, H, I, E, act_hi, act_lo, ctas, s);
+}
+
+cudaError_t launch_gemm_gate_up_raw(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                    const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
+                                    float *g, float *u, int ctas, cudaStream_t s)
+{
+    return gate_up_like<kGateUpRaw>(x, perm, k, wgu, chunks, nchunks, offs, n_rows, H, I, E, g, u, ctas, s);
+}
+
+cudaError_t launch_bwd_q(const void *ds_hi, const void *ds_lo, const void *wd, const int4 *chunks,
+                         const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
+                         const BwdQOut &o, int ctas, cudaStream_t s)
+{
+    CUtensorMap tA, tB[4];
+    cudaError_t e = make_mn_map(&tA, wd, I, H, E);
+    if (e == cudaSuccess) e = make_pair_maps(tB, ds_hi, ds_lo, n_rows, H);
+    if (e != cudaSuccess) return e;
+    const BwdQArgs q{o.g, o.u, o.w_s, (__nv_bfloat16 *)o.dgu_hi, (__nv_bfloat16 *)o.dgu_lo,
+                     (__nv_bfloat16 *)o.wa_hi, (__nv_bfloat16 *)o.wa_lo, o.dwp};
+    return launch_mn<kBwdQ>(tA, tB, chunks, nchunks, offs, n_rows, H, I, E, I, H, nullptr, q, ctas, s);
+}
+
+cudaError_t launch_bwd_dx(const void *dgu_hi, const void *dgu_lo, const void *wgu, const int4 *chunks,
+                          const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E, float *z,
+                          int ctas, cudaStream_t s)
+{
+    CUtensorMap tA, tB[4];
+    cudaError_t e = make_mn_map(&tA, wgu, H, 2 * (uint64_t)I, E);
+    if (e == cudaSuccess) e = make_pair_maps(tB, dgu_hi, dgu_lo, n_rows, 2 * (uint64_t)I);
+    if (e != cudaSuccess) return e;
+    return launch_mn<kBwdDx>(tA, tB, chunks, nchunks, offs, n_rows, H, I, E, H, 2 * I, z, BwdQArgs{}, ctas, s);
 }
 
 cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void *wd, const int4 *chunks,
@@ -560,7 +778,7 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
                              int ctas, cudaStream_t s)
 {
     CUtensorMap tA, tB0s, tB0, tB1s, tB1;
-    constexpr int MT = Cfg<false>::MT;
+    constexpr int MT = Cfg<kDown>::MT;
     cudaError_t e = make_down_map(&tA, wd, E, H, I);
     if (e == cudaSuccess) e = make_map(&tB0s, act_hi, n_assign, I, SMALL_ROWS);
     if (e == cudaSuccess) e = make_map(&tB0, act_hi, n_assign, I, NMAX);
@@ -570,7 +788,7 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
     const int tiles = (H + BM - 1) / BM;
     GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, MT * BM * BK * 2, z, nullptr, nullptr,
                nullptr, 0};
-    grouped_gemm_kernel<false><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<false>::SMEM, s>>>(
+    grouped_gemm_kernel<kDown><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreads, Cfg<kDown>::SMEM, s>>>(
         tA, tB0s, tB0, tB1s, tB1, a);
     return cudaPeekAtLastError();
 }

@@ -32,9 +32,12 @@ cudaError_t launch_router(const float *logits, int T, int E, int k, int32_t *idx
 cudaError_t launch_router_gemv(const void *x, const void *wr, const float *bias, int T, int H, int E, float *logits,
                                float *logits_copy, cudaStream_t s);
 size_t sort_smem_bytes(int E);
+// pad > 1: every expert's segment rounded up to a multiple of pad rows (pad
+// rows' perm = -1); counts (nullable): assignments per expert
 cudaError_t launch_sort(const int32_t *idx, int n_assign, int E, int chunk_max, int32_t *offs, int32_t *perm,
                         int32_t *pos, int32_t *uexp, int32_t *ucount, int4 *chunks, int32_t *nchunks,
-                        cudaStream_t s);
+                        cudaStream_t s, int pad = 1, int32_t *counts = nullptr);
+// w (nullable): without it the rows are summed unweighted
 cudaError_t launch_combine(const float *z, const float *w, const int32_t *pos, int T, int H, int k, float *out,
                            int n_sm, cudaStream_t s);
 
@@ -112,5 +115,47 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
                              const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, float *z,
                              int ctas, cudaStream_t s);
 cudaError_t read_fault_word(uint32_t *flags, bool clear);
+
+// Backward pass.  Rows r index the padded sorted order (launch_sort with
+// pad 16: each expert's segment rounded up to 16 rows, pad rows zero).
+// gate_up_raw: g = W_gate x, u = W_up x [rows][I] FP32.
+cudaError_t launch_gemm_gate_up_raw(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                    const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
+                                    float *g, float *u, int ctas, cudaStream_t s);
+// q = W_down^T dout (dout as ds_hi + ds_lo [rows][H]) and the SwiGLU
+// backward: in g, u, w_s; out dgu_hi/lo [rows][2I], wa_hi/lo [rows][I]
+// (BF16 pairs) and dwp [rows][I/32] (partial sums of act . q)
+struct BwdQOut {
+    const float *g, *u, *w_s;
+    void *dgu_hi, *dgu_lo, *wa_hi, *wa_lo;
+    float *dwp;
+};
+cudaError_t launch_bwd_q(const void *ds_hi, const void *ds_lo, const void *wd, const int4 *chunks,
+                         const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
+                         const BwdQOut &o, int ctas, cudaStream_t s);
+// z [rows][H] = W_gate_up^T (dgu_hi + dgu_lo)
+cudaError_t launch_bwd_dx(const void *dgu_hi, const void *dgu_lo, const void *wgu, const int4 *chunks,
+                          const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E, float *z,
+                          int ctas, cudaStream_t s);
+
+// grouped_bwd.cu
+cudaError_t bwd_init_device();
+cudaError_t read_bwd_fault_word(uint32_t *flags, bool clear);
+// per padded row: xs = x[token] (BF16), ds_hi/lo = dout[token] split, w_s =
+// routing weight; zeros in pad rows
+cudaError_t launch_bwd_prep(const void *x, const float *dout, const float *w, const int32_t *perm,
+                            const int32_t *offs, int n_rows_max, int E, int H, int k, void *xs, void *ds_hi,
+                            void *ds_lo, float *w_s, int n_sm, cudaStream_t s);
+// dW_down [E][H][I] = sum_r ds[r] (x) wa[r] over each expert's rows
+cudaError_t launch_wgrad_down(const void *ds_hi, const void *ds_lo, const void *wa_hi, const void *wa_lo,
+                              const int32_t *offs, const int32_t *counts, int n_rows, int H, int I, int E,
+                              float *dwd, int ctas, cudaStream_t s);
+// dW_gate_up [E][2I][H] = sum_r dgu[r] (x) xs[r]
+cudaError_t launch_wgrad_gate_up(const void *dgu_hi, const void *dgu_lo, const void *xs, const int32_t *offs,
+                                 const int32_t *counts, int n_rows, int H, int I, int E, float *dwgu, int ctas,
+                                 cudaStream_t s);
+// dlogits [T][E] from dwp (I/32 partial sums per row), pos, idx, w
+cudaError_t launch_dlogits(const float *dwp, const int32_t *pos, const int32_t *idx, const float *w, int T, int E,
+                           int k, int I, float *dlogits, cudaStream_t s);
 
 }  // namespace moe

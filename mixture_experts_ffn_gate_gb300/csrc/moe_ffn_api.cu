@@ -150,6 +150,7 @@ int device_setup(DeviceInfo **info)
         if (moe::decode_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::decode_fused_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         if (moe::gemm_init_device() != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::bwd_init_device() != cudaSuccess) return MOE_ERR_CUDA;
         // the attribute calls above created the context if there was none
         d.ctx = moe::current_context_id();
         d.ready = true;
@@ -161,6 +162,9 @@ int device_setup(DeviceInfo **info)
 const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
 const char *kDecodeFusedStages[] = {"decode_fused"};
 const char *kGroupedStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "combine"};
+const char *kBackwardStages[] = {"router",  "sort",    "prep",      "gemm_gate_up", "gemm_q",
+                                 "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
+static_assert(sizeof kBackwardStages / sizeof *kBackwardStages <= MOE_MAX_STAGES, "stage events");
 
 // Records stage events around the launches of one call.  While the stream is
 // being captured into a CUDA graph the records become external event-record
@@ -289,6 +293,111 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
     if (opts) {
         opts->n_stages = stg.n;
         opts->path_taken = path;
+    }
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- backward
+// Workspace of moe_ffn_backward, 256-byte aligned regions.  The fused decode
+// kernel's flags come first, where every forward layout has them, so a
+// workspace shared with forward calls keeps their state consistent: this
+// call's router lowers the state's size word to 0 (no tag region), and the
+// next fused call re-prepares it.  Rows r index the padded sorted order:
+// each expert's segment rounded up to 16 rows, at most 15 pad rows for each
+// of the min(E, T*k) touched experts.
+struct BwdLayout {
+    size_t flags, idx, w, offs, perm, pos, uexp, ucount, chunks, nchunks, counts;
+    size_t xs, ds_hi, ds_lo, w_s, g, u, dgu_hi, dgu_lo, wa_hi, wa_lo, dwp, z, total;
+    int64_t rows;
+};
+
+BwdLayout make_bwd_layout(const Shape &s)
+{
+    BwdLayout L{};
+    const int64_t n = s.T * s.k;
+    L.rows = n + 15 * (s.E < n ? s.E : n);
+    const size_t R = (size_t)L.rows;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    L.flags = take((size_t)moe::kDecodeFusedFlagWords * 8);
+    L.idx = take((size_t)n * 4);
+    L.w = take((size_t)n * 4);
+    L.offs = take((size_t)(s.E + 1) * 4);
+    L.perm = take(R * 4);
+    L.pos = take((size_t)n * 4);
+    L.uexp = take((size_t)s.E * 4);
+    L.ucount = take(4);
+    L.chunks = take((size_t)(s.E + ceil_div(L.rows, (int64_t)moe::kGemmChunkMax) + 1) * 16);
+    L.nchunks = take(4);
+    L.counts = take((size_t)s.E * 4);
+    L.xs = take(R * (size_t)s.H * 2);
+    L.ds_hi = take(R * (size_t)s.H * 2);
+    L.ds_lo = take(R * (size_t)s.H * 2);
+    L.w_s = take(R * 4);
+    L.g = take(R * (size_t)s.I * 4);
+    L.u = take(R * (size_t)s.I * 4);
+    L.dgu_hi = take(R * (size_t)s.I * 4);
+    L.dgu_lo = take(R * (size_t)s.I * 4);
+    L.wa_hi = take(R * (size_t)s.I * 2);
+    L.wa_lo = take(R * (size_t)s.I * 2);
+    L.dwp = take(R * (size_t)(s.I / 32) * 4);
+    L.z = take(R * (size_t)s.H * 4);
+    L.total = o;
+    return L;
+}
+
+int run_backward(const void *x, const float *logits, const void *wgu, const void *wd, const float *dout,
+                 const Shape &s, float *dx, float *dlogits, float *dwgu, float *dwd, char *ws, const BwdLayout &L,
+                 moe_ffn_opts *opts, cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    int st = device_setup(&dev);
+    if (st != MOE_OK) return st;
+    const int T = (int)s.T, H = (int)s.H, I = (int)s.I, E = (int)s.E, k = (int)s.k;
+    const int rows = (int)L.rows;
+    const int ctas = (opts && opts->gemm_ctas) ? opts->gemm_ctas : dev->n_sm;
+    auto *idx = (int32_t *)(ws + L.idx);
+    auto *w = (float *)(ws + L.w);
+    auto *offs = (int32_t *)(ws + L.offs);
+    auto *perm = (int32_t *)(ws + L.perm);
+    auto *pos = (int32_t *)(ws + L.pos);
+    auto *chunks = (int4 *)(ws + L.chunks);
+    auto *nchunks = (int32_t *)(ws + L.nchunks);
+    auto *counts = (int32_t *)(ws + L.counts);
+    auto *g = (float *)(ws + L.g);
+    auto *u = (float *)(ws + L.u);
+    auto *w_s = (float *)(ws + L.w_s);
+    auto *dwp = (float *)(ws + L.dwp);
+    auto *z = (float *)(ws + L.z);
+    auto *tag_size = (unsigned long long *)(ws + L.flags) + moe::kDecodeFusedSizeWord;
+
+    Stages stg{opts ? opts->stage_events : nullptr, stream};
+    MOE_TRY(stg.begin());
+    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, nullptr, nullptr, tag_size, 0, stream)));
+    MOE_TRY(stg.done(moe::launch_sort(idx, T * k, E, moe::kGemmChunkMax, offs, perm, pos, (int32_t *)(ws + L.uexp),
+                                      (int32_t *)(ws + L.ucount), chunks, nchunks, stream, 16, counts)));
+    MOE_TRY(stg.done(moe::launch_bwd_prep(x, dout, w, perm, offs, rows, E, H, k, ws + L.xs, ws + L.ds_hi,
+                                          ws + L.ds_lo, w_s, dev->n_sm, stream)));
+    MOE_TRY(stg.done(moe::launch_gemm_gate_up_raw(x, perm, k, wgu, chunks, nchunks, offs, rows, H, I, E, g, u, ctas,
+                                                  stream)));
+    const moe::BwdQOut qo{g, u, w_s, ws + L.dgu_hi, ws + L.dgu_lo, ws + L.wa_hi, ws + L.wa_lo, dwp};
+    MOE_TRY(stg.done(moe::launch_bwd_q(ws + L.ds_hi, ws + L.ds_lo, wd, chunks, nchunks, offs, rows, H, I, E, qo, ctas,
+                                       stream)));
+    MOE_TRY(stg.done(moe::launch_bwd_dx(ws + L.dgu_hi, ws + L.dgu_lo, wgu, chunks, nchunks, offs, rows, H, I, E, z,
+                                        ctas, stream)));
+    MOE_TRY(stg.done(moe::launch_combine(z, nullptr, pos, T, H, k, dx, dev->n_sm, stream)));
+    MOE_TRY(stg.done(moe::launch_wgrad_down(ws + L.ds_hi, ws + L.ds_lo, ws + L.wa_hi, ws + L.wa_lo, offs, counts,
+                                            rows, H, I, E, dwd, ctas, stream)));
+    MOE_TRY(stg.done(moe::launch_wgrad_gate_up(ws + L.dgu_hi, ws + L.dgu_lo, ws + L.xs, offs, counts, rows, H, I, E,
+                                               dwgu, ctas, stream)));
+    MOE_TRY(stg.done(moe::launch_dlogits(dwp, pos, idx, w, T, E, k, I, dlogits, stream)));
+    if (opts) {
+        opts->n_stages = stg.n;
+        opts->path_taken = MOE_PATH_BACKWARD;
     }
     return MOE_OK;
 }
@@ -551,6 +660,65 @@ int moe_ffn_forward_host(const void *x_host, const float *logits_host, const voi
     return MOE_OK;
 }
 
+size_t moe_ffn_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k)
+{
+    Shape s{T, H, I, E, k};
+    if (check_shape(s) != MOE_OK) return 0;
+    return make_bwd_layout(s).total;
+}
+
+int moe_ffn_backward(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+                     const void *w_down_bf16, const float *dout_f32, int64_t T, int64_t H, int64_t I, int64_t E,
+                     int64_t k, float *dx_f32, float *dlogits_f32, float *dw_gate_up_f32, float *dw_down_f32,
+                     void *workspace, size_t workspace_bytes, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    int st = check_shape(s);
+    if (st != MOE_OK) return st;
+    st = check_opts(opts);
+    if (st != MOE_OK) return st;
+    if (opts) {
+        opts->n_stages = 0;
+        opts->path_taken = 0;
+        if (opts->path != MOE_PATH_AUTO && opts->path != MOE_PATH_GROUPED) return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (!w_gate_up_bf16 || !w_down_bf16 || !dw_gate_up_f32 || !dw_down_f32) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w_gate_up_bf16) || !aligned16(w_down_bf16) || !aligned16(dw_gate_up_f32) ||
+        !aligned16(dw_down_f32))
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!x_bf16 || !router_logits_f32 || !dout_f32 || !dx_f32 || !dlogits_f32) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(x_bf16) || !aligned16(router_logits_f32) || !aligned16(dout_f32) || !aligned16(dx_f32) ||
+            !aligned16(dlogits_f32))
+            return MOE_ERR_INVALID_ARG;
+    }
+    const BwdLayout L = make_bwd_layout(s);
+    if (L.rows > INT32_MAX / 2 || E * 2 * I * H >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (workspace && ((uintptr_t)workspace & 255)) return MOE_ERR_INVALID_ARG;
+    if (workspace && T > 0 && workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    // the first check that asks the CUDA runtime (the TMA encoder)
+    if (!moe::gemm_supported((int)H, (int)I, (int)E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) {
+        // no tokens: both weight gradients are zero
+        if (cudaMemsetAsync(dw_gate_up_f32, 0, (size_t)(E * 2 * I * H) * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(dw_down_f32, 0, (size_t)(E * H * I) * 4, stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (workspace)
+        return run_backward(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, dout_f32, s, dx_f32, dlogits_f32,
+                            dw_gate_up_f32, dw_down_f32, (char *)workspace, L, opts, stream);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, L.total, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_NO_MEMORY;
+    }
+    st = run_backward(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, dout_f32, s, dx_f32, dlogits_f32,
+                      dw_gate_up_f32, dw_down_f32, (char *)ws, L, opts, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && st == MOE_OK) st = MOE_ERR_CUDA;
+    return st;
+}
+
 const char *moe_ffn_status_string(int status)
 {
     switch (status) {
@@ -574,16 +742,20 @@ const char *moe_ffn_stage_name(int path, int stage)
         return kDecodeFusedStages[stage];
     if (path == MOE_PATH_GROUPED && stage < (int)(sizeof kGroupedStages / sizeof *kGroupedStages))
         return kGroupedStages[stage];
+    if (path == MOE_PATH_BACKWARD && stage < (int)(sizeof kBackwardStages / sizeof *kBackwardStages))
+        return kBackwardStages[stage];
     return nullptr;
 }
 
 int moe_ffn_device_faults(uint32_t *flags, int clear)
 {
     if (!flags) return MOE_ERR_INVALID_ARG;
-    uint32_t gemm = 0, decode = 0;
+    uint32_t gemm = 0, decode = 0, wgrad = 0;
     if (moe::read_fault_word(&gemm, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
     if (moe::read_decode_fused_fault_word(&decode, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
-    *flags = gemm | (decode << 8);  // bits 0-7: grouped GEMMs, 8-15: fused decode
+    if (moe::read_bwd_fault_word(&wgrad, clear != 0) != cudaSuccess) return MOE_ERR_CUDA;
+    // bits 0-7: grouped GEMMs, 8-15: fused decode, 16-23: weight-gradient GEMMs
+    *flags = gemm | (decode << 8) | (wgrad << 16);
     return MOE_OK;
 }
 

@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(32 * kRouterWarps) router_gemv_kernel(const ui
 // range in order and places assignment a at
 //   offs[e] + (assignments of e in earlier warps) + (earlier ones in this warp),
 // i.e. the assignments of each expert end up in ascending a = token order.
+// With pad > 1 every expert's segment is rounded up to a multiple of pad
+// rows (offs are the padded offsets, the pad rows' perm is -1) and counts[e]
+// (nullable) gets the expert's number of assignments.
 constexpr int SORT_THREADS = 1024;
 constexpr int SORT_WARPS = SORT_THREADS / 32;
 
@@ -113,7 +116,8 @@ __global__ void __launch_bounds__(SORT_THREADS) sort_kernel(const int32_t *__res
                                                            int chunk_max, int32_t *__restrict__ offs,
                                                            int32_t *__restrict__ perm, int32_t *__restrict__ pos,
                                                            int32_t *__restrict__ uexp, int32_t *__restrict__ ucount,
-                                                           int4 *__restrict__ chunks, int32_t *__restrict__ nchunks)
+                                                           int4 *__restrict__ chunks, int32_t *__restrict__ nchunks,
+                                                           int pad, int32_t *__restrict__ counts)
 {
     extern __shared__ int hist[];  // [SORT_WARPS][E]
     __shared__ int scratch[SORT_WARPS + 1];
@@ -131,10 +135,13 @@ __global__ void __launch_bounds__(SORT_THREADS) sort_kernel(const int32_t *__res
     if (e < E)
         for (int q = 0; q < SORT_WARPS; ++q) cnt += hist[q * E + e];
     int total;
-    const int off = block_exclusive_scan(e < E ? cnt : 0, scratch, &total);
+    const int padded = (cnt + pad - 1) / pad * pad;
+    const int off = block_exclusive_scan(e < E ? padded : 0, scratch, &total);
     if (e < E) {
         offs[e] = off;
-        if (e == E - 1) offs[E] = off + cnt;
+        if (e == E - 1) offs[E] = off + padded;
+        if (counts) counts[e] = cnt;
+        for (int p = off + cnt; p < off + padded; ++p) perm[p] = -1;
         int run = off;
         for (int q = 0; q < SORT_WARPS; ++q) {
             const int h = hist[q * E + e];
@@ -181,7 +188,8 @@ __global__ void __launch_bounds__(SORT_THREADS) sort_kernel(const int32_t *__res
 }
 
 // ---------------------------------------------------------------- combine
-// out[t, h] = sum_{j ascending} w[t,j] * z[pos[t*k+j], h]   (FP32, fixed order)
+// out[t, h] = sum_{j ascending} w[t,j] * z[pos[t*k+j], h]   (FP32, fixed order);
+// with w null the rows are summed unweighted (the backward pass's dx)
 __global__ void combine_kernel(const float *__restrict__ z, const float *__restrict__ w,
                                const int32_t *__restrict__ pos, int T, int H, int k, float *__restrict__ out)
 {
@@ -191,7 +199,7 @@ __global__ void combine_kernel(const float *__restrict__ z, const float *__restr
         const int t = (int)(i / hv), c = (int)(i - (int64_t)t * hv);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int j = 0; j < k; ++j) {
-            const float wj = __ldg(w + (int64_t)t * k + j);
+            const float wj = w ? __ldg(w + (int64_t)t * k + j) : 1.0f;
             const float4 v = ld_nc_f4(z + (int64_t)__ldg(pos + (int64_t)t * k + j) * H + 4 * c);
             acc.x = fmaf(wj, v.x, acc.x);
             acc.y = fmaf(wj, v.y, acc.y);
@@ -230,11 +238,11 @@ cudaError_t routing_init_device()
 
 cudaError_t launch_sort(const int32_t *idx, int n_assign, int E, int chunk_max, int32_t *offs, int32_t *perm,
                         int32_t *pos, int32_t *uexp, int32_t *ucount, int4 *chunks, int32_t *nchunks,
-                        cudaStream_t s)
+                        cudaStream_t s, int pad, int32_t *counts)
 {
     const size_t smem = sort_smem_bytes(E);
     sort_kernel<<<1, SORT_THREADS, smem, s>>>(idx, n_assign, E, chunk_max, offs, perm, pos, uexp, ucount, chunks,
-                                              nchunks);
+                                              nchunks, pad, counts);
     return cudaPeekAtLastError();
 }
 

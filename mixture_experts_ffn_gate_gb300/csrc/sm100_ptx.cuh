@@ -283,6 +283,23 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
+// The same for an MN-major operand tile (the M or N index contiguous): the
+// tile is a sequence of 64-element-wide MN blocks, each a stack of K rows of
+// 128 B (one row per K index, 128-byte swizzled in groups of 8 rows); the
+// leading byte offset is the distance between MN blocks, the stride byte
+// offset the distance between 8-row K groups (1024 B).  A K step of 16
+// starts 2048 B further on.
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t saddr, uint32_t mn_block_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((mn_block_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: D = F32, A = B = BF16, both K-major,
 // dense, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
@@ -292,6 +309,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
            | (1u << 10)         // B format BF16
            | ((N >> 3) << 17)   // N / 8
            | ((M >> 4) << 24);  // M / 16
+}
+
+// The same with A and/or B MN-major (the transpose bits 15 and 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(uint32_t M, uint32_t N, bool a_mn, bool b_mn)
+{
+    return idesc_bf16_f32(M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

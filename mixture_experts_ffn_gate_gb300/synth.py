@@ -14,6 +14,8 @@ with ``Tensor.to(torch.bfloat16)``):
 * ``w_down``      [E, H, I]   ~ N(0, 1/I) (fan-in I)            -> BF16
 * ``w_router``    [E, H]      ~ N(0, 1/H) (fan-in H)            -> BF16
   (calls that pass the router weights; their logits are x . W_r^T + bias)
+* ``dout``        [T, H]      ~ N(0, 1)                            (FP32)
+  (the upstream gradient of the backward pass)
 
 ``N(0, v)`` names the variance, so std = sqrt(v).  Each expert's weights come
 from a generator seeded with ``seed_for(workload, tensor, expert)``; token
@@ -189,6 +191,12 @@ def make_tokens(wl: Workload, T: int, call: int = 0, device="cpu", *, H=None,
         bias = make_bias(wl, E)
     logits += bias.to("cpu")[None, :]
     return x.to(torch.bfloat16).to(device), logits.to(device)
+
+
+def make_dout(wl: Workload, T: int, call: int = 0, device="cpu", *, H=None):
+    """The upstream gradient dL/dout [T,H] FP32 ~ N(0, 1) for call n."""
+    H = H or wl.H
+    return _randn((T, H), 1.0, "cpu", seed_for(wl.name, H, "dout", T, call)).to(device)
 
 
 def bf16_bits(t: torch.Tensor):

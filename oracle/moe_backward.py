@@ -49,6 +49,32 @@ def sigmoid(v: np.ndarray) -> np.ndarray:
     return 1.0 / (1.0 + np.exp(-v))
 
 
+def expert_backward(xe, de, we, wgu_e, wd_e):
+    """One expert's part of the backward pass, for the n assignments routed
+    to it: xe [n, H] and de [n, H] the tokens' x and dout rows (float64),
+    we [n] their routing weights, wgu_e uint16 [2I, H] and wd_e uint16
+    [H, I] its BF16 weights.  Returns (dx rows [n, H] -- this expert's
+    contribution to each token's dx --, dw [n] = dL/dw, dW_gate_up [2I, H],
+    dW_down [H, I]), all float64."""
+    I = wgu_e.shape[0] // 2
+    Wg = bf16_to_f64(wgu_e[:I])                 # [I, H]
+    Wu = bf16_to_f64(wgu_e[I:])
+    Wd = bf16_to_f64(wd_e)                      # [H, I]
+    g = xe @ Wg.T
+    u = xe @ Wu.T
+    s = sigmoid(g)
+    a = g * s * u
+    q = de @ Wd                                 # rows: W_down^T dout_t
+    dw = np.sum(a * q, axis=1)
+    da = we[:, None] * q
+    dg = da * u * s * (1.0 + g * (1.0 - s))
+    du = da * g * s
+    dx_rows = dg @ Wg + du @ Wu
+    dwd = (we[:, None] * de).T @ a
+    dwgu = np.concatenate([dg.T @ xe, du.T @ xe])
+    return dx_rows, dw, dwgu, dwd
+
+
 def backward(x, logits, wgu, wd, dout, k, route, *, expert_map=None):
     """The layer's gradients in FP64.
 
@@ -84,24 +110,9 @@ def backward(x, logits, wgu, wd, dout, k, route, *, expert_map=None):
         if b < 0:
             raise ValueError(f"expert {e} is selected but has no weights")
         tok, slot = np.nonzero(idx == e)          # ascending token order
-        we = w[tok, slot]
-        Wg = bf16_to_f64(wgu[b, :I])               # [I, H]
-        Wu = bf16_to_f64(wgu[b, I:])
-        Wd = bf16_to_f64(wd[b])                    # [H, I]
-        Xe, De = xf[tok], douf[tok]                # [n, H]
-        g = Xe @ Wg.T
-        u = Xe @ Wu.T
-        s = sigmoid(g)
-        a = g * s * u
-        q = De @ Wd                                # rows: W_down^T dout_t
-        dw[tok, slot] = np.sum(a * q, axis=1)
-        da = we[:, None] * q
-        dg = da * u * s * (1.0 + g * (1.0 - s))
-        du = da * g * s
-        dx[tok] += dg @ Wg + du @ Wu               # a token picks e at most once
-        dwd[b] = (we[:, None] * De).T @ a
-        dwgu[b, :I] = dg.T @ Xe
-        dwgu[b, I:] = du.T @ Xe
+        dx_rows, dw_e, dwgu[b], dwd[b] = expert_backward(xf[tok], douf[tok], w[tok, slot], wgu[b], wd[b])
+        dx[tok] += dx_rows                        # a token picks e at most once
+        dw[tok, slot] = dw_e
 
     dlogits = np.zeros((T, E))
     S = np.sum(w * dw, axis=1)

@@ -67,6 +67,9 @@ def test_stage_names(L):
     assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE_FUSED, i) for i in range(2)] == ["decode_fused", None]
     assert [m.moe_ffn_stage_name(m.MOE_PATH_GROUPED, i) for i in range(6)] == \
         ["router", "sort", "gemm_gate_up", "gemm_down", "combine", None]
+    assert [m.moe_ffn_stage_name(m.MOE_PATH_BACKWARD, i) for i in range(11)] == \
+        ["router", "sort", "prep", "gemm_gate_up", "gemm_q", "gemm_dx", "combine", "wgrad_down",
+         "wgrad_gate_up", "dlogits", None]
     assert m.moe_ffn_stage_name(m.MOE_PATH_AUTO, 0) is None
     assert m.moe_ffn_stage_name(m.MOE_PATH_DECODE, -1) is None
 
@@ -209,3 +212,40 @@ def test_mx_scale_row_bytes_agree():
     from mixture_experts_ffn_gate_gb300 import moe_ffn, synth
     for K in (32, 64, 96, 512, 768, 1536, 2048, 6144, 7168):
         assert moe_ffn.mx_scale_bytes(K) == synth.mx_scale_row_bytes(K) == -(-(K // 32) // 16) * 16
+
+
+def test_backward_workspace_bytes(L):
+    ws = L.moe_ffn_backward_workspace_bytes
+    assert ws(4, 256, 128, 8, 2) > 0
+    assert ws(4, 256, 128, 8, 9) == 0        # k > E
+    assert ws(4, 250, 128, 8, 2) == 0        # H % 64
+    assert ws(2048, 6144, 2048, 256, 8) > ws(64, 6144, 2048, 256, 8)
+    # the padded rows: T*k assignments plus at most 15 pad rows per touched expert
+    n = 2048 * 8
+    rows = n + 15 * 256
+    assert ws(2048, 6144, 2048, 256, 8) >= rows * (6144 * 2 * 3 + 6144 * 4 + 2048 * 4 * 4)
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(T=-1), 1), (dict(k=9), 1), (dict(H=200), 2), (dict(E=1025, k=2), 2),
+    (dict(x=None), 1), (dict(logits=None), 1), (dict(wgu=None), 1), (dict(wd=None), 1),
+    (dict(dout=None), 1), (dict(dx=None), 1), (dict(dlogits=None), 1), (dict(dwgu=None), 1),
+    (dict(dwd=None), 1), (dict(dout=FAKE + 4), 1), (dict(dwd=FAKE + 8), 1),
+    (dict(workspace=FAKE + 16), 1), (dict(ws_bytes=1024), 5), (dict(T=0, dwgu=None), 1),
+])
+def test_backward_entry_argument_checks(L, case, want):
+    a = dict(x=FAKE, logits=FAKE, wgu=FAKE, wd=FAKE, dout=FAKE, T=4, H=256, I=128, E=8, k=2, dx=FAKE,
+             dlogits=FAKE, dwgu=FAKE, dwd=FAKE, workspace=FAKE, ws_bytes=1 << 40)
+    a.update(case)
+    st = L.moe_ffn_backward(a["x"], a["logits"], a["wgu"], a["wd"], a["dout"], a["T"], a["H"], a["I"], a["E"],
+                            a["k"], a["dx"], a["dlogits"], a["dwgu"], a["dwd"], a["workspace"], a["ws_bytes"],
+                            None, None)
+    assert st == want
+
+
+def test_backward_rejects_decode_path(L):
+    from mixture_experts_ffn_gate_gb300 import moe_ffn as m
+    o = m.moe_ffn_opts()
+    o.path = m.MOE_PATH_DECODE
+    assert L.moe_ffn_backward(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE,
+                              1 << 40, ctypes.byref(o), None) == m.MOE_ERR_UNSUPPORTED_SHAPE

@@ -23,6 +23,20 @@ def test_backward_pin(pin):
     pin(oracle.backward)
 
 
+def test_backward_is_the_sum_of_expert_parts():
+    # the per-expert step on one expert's rows gives that expert's gradients
+    rng = np.random.default_rng(31)
+    x, L, wgu, wd = backward_pins.rand_layer(rng, 6, 32, 16, 5)
+    dout = backward_pins.rand_dout(rng, 6, 32)
+    full = oracle.backward(x, L, wgu, wd, dout, 2)
+    xf, df = bwd_mod.bf16_to_f64(x), dout.astype(np.float64)
+    for e in np.unique(full["idx"]):
+        tok, slot = np.nonzero(full["idx"] == e)
+        _, dw, dwgu, dwd = bwd_mod.expert_backward(xf[tok], df[tok], full["w"][tok, slot], wgu[e], wd[e])
+        assert np.array_equal(dwgu, full["dwgu"][e]) and np.array_equal(dwd, full["dwd"][e])
+        assert np.array_equal(dw, full["dw"][tok, slot])
+
+
 def test_backward_expert_map_matches_full():
     # only the selected experts' blocks passed: the same gradients for them
     rng = np.random.default_rng(30)
@@ -42,14 +56,15 @@ def test_backward_expert_map_matches_full():
 MUTANTS = {
     "silu_derivative_term_dropped": ("dg = da * u * s * (1.0 + g * (1.0 - s))", "dg = da * u * s"),
     "du_without_gate": ("du = da * g * s", "du = da * s"),
-    "dx_up_term_dropped": ("dx[tok] += dg @ Wg + du @ Wu", "dx[tok] += dg @ Wg"),
-    "dwd_weight_dropped": ("dwd[b] = (we[:, None] * De).T @ a", "dwd[b] = De.T @ a"),
+    "dx_up_term_dropped": ("dx_rows = dg @ Wg + du @ Wu", "dx_rows = dg @ Wg"),
+    "dwd_weight_dropped": ("dwd = (we[:, None] * de).T @ a", "dwd = de.T @ a"),
     "dlogits_sign": ("w * (dw - S[:, None])", "w * (S[:, None] - dw)"),
     "dlogits_centering_dropped": ("w * (dw - S[:, None])", "w * dw"),
-    "q_reversed": ("q = De @ Wd ", "q = (De @ Wd)[:, ::-1] "),
-    "dwgu_gate_up_swapped": ("dwgu[b, :I] = dg.T @ Xe", "dwgu[b, :I] = du.T @ Xe"),
+    "q_reversed": ("q = de @ Wd ", "q = (de @ Wd)[:, ::-1] "),
+    "dwgu_gate_up_swapped": ("np.concatenate([dg.T @ xe, du.T @ xe])", "np.concatenate([du.T @ xe, dg.T @ xe])"),
     "da_weight_dropped": ("da = we[:, None] * q", "da = q"),
-    "gate_up_swapped": ("g = Xe @ Wg.T\n        u = Xe @ Wu.T", "g = Xe @ Wu.T\n        u = Xe @ Wg.T"),
+    "gate_up_swapped": ("g = xe @ Wg.T\n    u = xe @ Wu.T", "g = xe @ Wu.T\n    u = xe @ Wg.T"),
+    "dw_not_reduced_over_neurons": ("dw = np.sum(a * q, axis=1)", "dw = a[:, 0] * q[:, 0]"),
 }
 
 
