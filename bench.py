@@ -36,7 +36,10 @@ T=1 and 2 with the router projection inside the call (router weights and
 bias passed instead of logits); six ("entry": moe_ffn_forward_mxfp8) run
 the 2048-hidden layer at T=1/2/4, the 4096-hidden one at T=1 and the
 7168-hidden one at T=1/8 with MXFP8 expert weights (their bytes counted at
-1 + 1/32 per weight; T > 4 takes the general decode kernels).
+1 + 1/32 per weight; T > 4 takes the general decode kernels).  One row
+("entry": moe_ffn_backward) runs the backward pass of the T=2048
+training-size layer (dout ~ N(0,1) FP32 per call; all four gradients written
+every call), with its own byte model (backward_bytes) and 16 H I T k flops.
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -70,6 +73,10 @@ KERNEL_SOURCES = {
     "decode_down": ["decode.cu"],
     "gemm_gate_up": ["grouped_gemm.cu"],
     "gemm_down": ["grouped_gemm.cu"],
+    "gemm_q": ["grouped_gemm.cu"],
+    "gemm_dx": ["grouped_gemm.cu"],
+    "wgrad_down": ["grouped_bwd.cu"],
+    "wgrad_gate_up": ["grouped_bwd.cu"],
 }
 
 
@@ -95,6 +102,9 @@ def parse():
                    help="launch every step from Python instead of replaying a CUDA graph of the steps")
     p.add_argument("--cold-steps", type=int, default=200,
                    help="single calls timed after an L2 flush each (secondary figure)")
+    p.add_argument("--backward", action="store_true",
+                   help="time the backward pass (moe_ffn_backward) as the step instead of the forward pass "
+                        "(no e2e or CPU-baseline figures; e.g. with --E for a profiling-size variant)")
     p.add_argument("--no-supplementary", action="store_true",
                    help="omit the other configurations' rows (measured after the headline line)")
     p.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
@@ -233,6 +243,34 @@ def kernel_bytes(kernel, wl, T, U, k, bpe=2.0):
     return None
 
 
+def backward_bytes(wl, T, U):
+    """Per-call algorithmic HBM bytes of the backward pass: the touched
+    experts' W_gate_up read twice (the recomputation of gate/up, and dx) and
+    W_down once; both weight gradients written once in FP32 (every expert,
+    untouched ones as zeros); x, logits and dout read; dx and dlogits
+    written."""
+    H, I, E = wl.H, wl.I, wl.E
+    return (U * (2 * 2 * I * H * 2 + H * I * 2) + E * 3 * H * I * 4
+            + T * H * 2 + T * E * 4 + T * H * 4 + T * H * 4 + T * E * 4)
+
+
+def backward_kernel_bytes(kernel, wl, T, U, k):
+    """Algorithmic bytes of one launch of a backward-pass kernel (n = T k
+    assignment rows; intermediates FP32 or BF16 hi/lo pairs)."""
+    H, I, E = wl.H, wl.I, wl.E
+    n = T * k
+    return {
+        "prep": T * H * 2 + T * H * 4 + n * H * 2 + 2 * n * H * 2 + n * 4,
+        "gemm_gate_up": U * 2 * I * H * 2 + T * H * 2 + 2 * n * I * 4,
+        "gemm_q": U * H * I * 2 + 2 * n * H * 2 + 2 * n * I * 4 + 2 * n * 2 * I * 2 + 2 * n * I * 2
+        + n * (I // 32) * 4 + n * 4,
+        "gemm_dx": U * 2 * I * H * 2 + 2 * n * 2 * I * 2 + n * H * 4,
+        "combine": n * H * 4 + T * H * 4,
+        "wgrad_down": E * H * I * 4 + 2 * n * H * 2 + 2 * n * I * 2,
+        "wgrad_gate_up": E * 2 * I * H * 4 + 2 * n * 2 * I * 2 + n * H * 2,
+    }.get(kernel)
+
+
 def reference_arm(args, wl, T):
     """The FP64 oracle on the host cores, on a bounded sample of the workload."""
     import numpy as np
@@ -362,6 +400,7 @@ SUPPLEMENTARY = [
     ("decode_h4096_i1536_e128_k8_bias", (1, 4, 16, 64)),
     ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),
+    ("fwd_t2048_h6144_i2048_e256_k8_bias+backward", (2048,)),
 ]
 
 
@@ -380,7 +419,8 @@ class Measure:
     launches); stages() replays them with the library's stage events between
     kernels; summary() gives the figures of one line."""
 
-    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager, routers=None, mx=False):
+    def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager, routers=None, mx=False,
+                 backward=False):
         import torch
         from mixture_experts_ffn_gate_gb300 import moe_ffn as m
         from mixture_experts_ffn_gate_gb300 import synth
@@ -396,13 +436,24 @@ class Measure:
         # and the calls go through moe_ffn_forward_mxfp8
         self.mx = mx
         self.bpe = BPE["mxfp8" if mx else "bf16"]
-        batch_bytes = T * (wl.H * 2 + wl.E * 4)
+        # backward: the steps are moe_ffn_backward calls, each with its own
+        # upstream gradient, writing all four gradients
+        self.backward = backward
+        batch_bytes = T * (wl.H * 2 + wl.E * 4 + (wl.H * 4 if backward else 0))
         self.NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
         calls = rank_calls(rank, W, K)   # rank r processes its own calls of the token stream
         self.batches = [synth.make_tokens(wl, T, call=calls[i], device=dev, bias=bias)
                         for i in range(self.NB)]
-        self.ws = (m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev) if routers is None
-                   else m.new_router_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev))
+        if backward:
+            self.douts = [synth.make_dout(wl, T, call=calls[i], device=dev) for i in range(self.NB)]
+            self.ws = m.new_backward_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
+            self.grads = (torch.empty((T, wl.H), dtype=torch.float32, device=dev),
+                          torch.empty((T, wl.E), dtype=torch.float32, device=dev),
+                          torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.float32, device=dev),
+                          torch.empty((wl.E, wl.H, wl.I), dtype=torch.float32, device=dev))
+        else:
+            self.ws = (m.new_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev) if routers is None
+                       else m.new_router_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev))
         self.out = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
         self.stream = torch.cuda.current_stream()
         probe = self.new_opts()
@@ -414,6 +465,10 @@ class Measure:
         U_of = {}
         for j in range(W, W + K):
             if j % self.NB not in U_of:
+                if backward:   # the selection by torch.topk (ties aside, the same experts)
+                    U_of[j % self.NB] = int(torch.unique(torch.topk(self.batches[j % self.NB][1], wl.k).indices)
+                                            .numel())
+                    continue
                 self.call(j, self.stream, None, idx_buf)
                 U_of[j % self.NB] = int(torch.unique(idx_buf).numel())
         self.U = [U_of[j % self.NB] for j in range(W, W + K)]
@@ -430,6 +485,11 @@ class Measure:
     def call(self, j, stream, opts=None, idx=None):
         x, L = self.batches[j % self.NB]
         opts = opts if opts is not None else self.new_opts()
+        if self.backward:
+            lw_gu, lw_d = self.layers[j % self.R]
+            self.m.moe_ffn_backward(x, L, lw_gu, lw_d, self.douts[j % self.NB], self.wl.k, *self.grads,
+                                    workspace=self.ws, opts=opts, stream=stream)
+            return
         if self.mx:
             self.m.moe_ffn_forward_mxfp8(x, L, *self.layers[j % self.R], self.wl.k, out=self.out, workspace=self.ws,
                                          topk_idx=idx, opts=opts, stream=stream)
@@ -524,6 +584,8 @@ class Measure:
         """Throughput, the whole call's HBM fraction, the dominant kernel's
         roofline and the tensor figures of one workload line."""
         wl, T, K = self.wl, self.T, self.K
+        if self.backward:
+            return self.summary_backward(total_ms, kern_avg, peaks, world)
         call_bytes = sum(algorithmic_bytes(wl, T, u, self.bpe) for u in self.U) / K
         # calls with the router projection inside also read W_r (E*H BF16)
         router_bytes = wl.E * wl.H * 2 if self.routers is not None else 0
@@ -570,6 +632,50 @@ class Measure:
         }
 
 
+    def summary_backward(self, total_ms, kern_avg, peaks, world):
+        """The figures of a backward-pass line (byte model backward_bytes,
+        flops 16 H I T k: gate/up recomputed, q, dx and both weight
+        gradients)."""
+        wl, T, K = self.wl, self.T, self.K
+        call_bytes = sum(backward_bytes(wl, T, u) for u in self.U) / K
+        flops = 16.0 * wl.H * wl.I * T * wl.k
+        ms_call = total_ms / K
+        dom = max(kern_avg, key=kern_avg.get)
+        dom_bytes = sum(backward_kernel_bytes(dom, wl, T, u, wl.k) for u in self.U) / K
+        achieved = dom_bytes / (kern_avg[dom] / 1e3) / 1e9
+        per_kernel = {}
+        for n, v in kern_avg.items():
+            b = backward_kernel_bytes(n, wl, T, sum(self.U) / K, wl.k)
+            per_kernel[n] = {"us": round(1e3 * v, 3)}
+            if b:
+                per_kernel[n]["gbs"] = round(b / (v / 1e3) / 1e9, 1)
+                per_kernel[n]["frac_of_hbm_peak"] = round(b / (v / 1e3) / 1e9 / peaks["hbm_gbs"], 3)
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": stored_traffic(dom, wl.name + "+backward", T),
+                    "peak_source": f"{peaks['source']} HBM copy (burst)",
+                    "algorithmic_bytes_per_launch": dom_bytes,
+                    "kernel_time": "stage events between kernels, CUDA-graph replay",
+                    "kernels": per_kernel}
+        gbs = call_bytes / (ms_call / 1e3) / 1e9
+        tflops = flops / (ms_call / 1e3) / 1e12
+        intensity = flops / call_bytes
+        attainable = min(peaks["bf16_tflops"], peaks["hbm_gbs"] * 1e9 * intensity / 1e12)
+        return {
+            "value": whole_job_tokens_per_s(T, K, world, total_ms),
+            "ms_per_step": ms_call,
+            "path": "backward",
+            "roofline": roofline,
+            "call_hbm": {"achieved_gbs": gbs, "frac_of_measured": gbs / peaks["hbm_gbs"],
+                         "frac_of_8tbs_spec": gbs / 8000.0, "bytes_per_call": call_bytes,
+                         "unique_experts_mean": sum(self.U) / K},
+            "tensor": {"tflops": tflops, "frac_of_dense_bf16_peak": tflops / peaks["bf16_tflops"],
+                       "flop_per_byte": intensity, "attainable_tflops": attainable,
+                       "frac_of_attainable": tflops / attainable,
+                       "attainable": "min(dense BF16 peak, measured HBM copy peak x flop/byte)"},
+        }
+
+
 def supplementary_rows(args, dev, peaks, skip):
     """The other configurations, one short timed run each (W warm-up and K
     timed steps as for the headline line); weights are shared by the T of a
@@ -592,7 +698,8 @@ def supplementary_rows(args, dev, peaks, skip):
         bias = synth.make_bias(wl)
         for T in Ts:
             run = Measure(wl, T, dev, args.steps, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
-                args.path], layers, bias, 0, args.eager, routers=routers, mx=how == "mxfp8")
+                args.path] if how != "backward" else 0, layers, bias, 0, args.eager, routers=routers,
+                mx=how == "mxfp8", backward=how == "backward")
             with ClockSampler(dev.index or 0) as clocks:
                 total_ms, _ = run.timed(1)
                 kern = run.stages()
@@ -600,6 +707,10 @@ def supplementary_rows(args, dev, peaks, skip):
             if how == "router":
                 row["entry"] = ("moe_ffn_forward_router: router weights W_r [E,H] ~ N(0,1/H) and the "
                                 "workload's bias passed instead of logits; the projection runs inside the call")
+            if how == "backward":
+                row["entry"] = ("moe_ffn_backward: dx, dlogits, dW_gate_up and dW_down (FP32) for dout ~ N(0,1) "
+                                "FP32; gate/up recomputed from x inside the call")
+                row["dtype"] = "bf16 inputs, f32 arithmetic and gradients"
             if how == "mxfp8":
                 row["entry"] = ("moe_ffn_forward_mxfp8: the same seeded weights quantised to MXFP8 (E4M3 "
                                 "codes, one E8M0 scale per 32 elements along K); bytes per weight 1 + 1/32")
@@ -647,7 +758,7 @@ def main():
     K, W = args.steps, max(3, args.warmup)
     bias = synth.make_bias(wl)
     mx = args.weights == "mxfp8"
-    if mx:   # the MXFP8 entry has no host-buffer form; the oracle baseline is the BF16 one
+    if mx or args.backward:   # no host-buffer form; the oracle baseline is the BF16 forward
         args.no_e2e = args.skip_baseline = True
     R, touched = layer_count(wl, T, args.layers, BPE[args.weights])
     make = synth.make_weights_mxfp8 if mx else synth.make_weights
@@ -655,7 +766,8 @@ def main():
     wgu, wd = (None, None) if mx else layers[0]
     path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
                  "grouped": m.MOE_PATH_GROUPED}[args.path]
-    run = Measure(wl, T, dev, K, W, path_code, layers, bias, rank, args.eager, mx=mx)
+    run = Measure(wl, T, dev, K, W, path_code if not args.backward else 0, layers, bias, rank, args.eager, mx=mx,
+                  backward=args.backward)
     stream = run.stream
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sum = torch.empty((), dtype=torch.float32, device=dev)

@@ -25,9 +25,9 @@
 //       dW_gate_up: A = dgu_hi/lo [rows][2I], B = x_s [rows][H]
 //                   (hi.x + lo.x; x is exact in BF16)
 //     One item is one 128 x 256 output tile of one expert; K is the
-//     expert's rows in steps of 64 (the MMA's K steps of 16 stop at the
+//     expert's rows in steps of 32 (the MMA's K steps of 16 stop at the
 //     16-row padding, whose rows are zero).  Both operands are MN-major:
-//     TMA boxes of 64 elements (128 bytes, 128-byte swizzle) by 64 rows.
+//     TMA boxes of 64 elements (128 bytes, 128-byte swizzle) by 32 rows.
 //     Experts without rows get zero tiles.  Each output element is one MMA
 //     chain in a fixed order, so the gradients are bit-identical from run
 //     to run whatever the grid.
@@ -37,7 +37,11 @@
 // One persistent CTA per SM runs wgrad: warp 0 issues the TMA loads into
 // a ring of stages, warp 1 the MMAs into one of two 256-column TMEM
 // accumulators, warps 2-9 drain the other one (two warps per TMEM lane
-// quarter, 128 columns each) straight to global memory.  Every mbarrier
+// quarter, 128 columns each).  The gradients are written by TMA tensor
+// stores: each epilogue warp places a 32-row x 32-column FP32 block in one
+// of its two 128-byte-swizzled staging buffers and hands it to the TMA
+// engine, so every row leaves as one 128-byte line (a warp's own stores,
+// one row per lane, would split into 32 partial sectors).  Every mbarrier
 // wait is bounded; on time-out the CTA raises a bit in the device fault
 // word, drains what it has in flight (bounded) and frees its TMEM.
 #include <cuda.h>
@@ -65,9 +69,11 @@ namespace {
 
 constexpr int WBM = 128;               // output rows per tile (MMA M)
 constexpr int WNB = 256;               // output columns per tile (MMA N)
-constexpr int WK = 64;                 // rows per K step (TMA box height)
-constexpr int BOX = 64 * WK * 2;       // one 64-element x 64-row BF16 box: 8 KB
+constexpr int WK = 32;                 // rows per K step (TMA box height)
+constexpr int BOX = 64 * WK * 2;       // one 64-element x 32-row BF16 box: 4 KB
 constexpr int kWThreads = 320;         // producer, MMA issuer, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int OUT_BLOCK = 32 * 32 * 4;  // one staged 32 x 32 FP32 output block: 4 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint64_t kDrainNs = 200000000ull;
 
@@ -81,16 +87,17 @@ struct WCfg {
     static constexpr int A_BYTES = 2 * A_HALF;
     static constexpr int B_BYTES = (B_PAIR ? 2 : 1) * B_HALF;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = B_PAIR ? 2 : 3;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+    static constexpr int STAGES = B_PAIR ? 3 : 4;
+    static constexpr int STAGING = kEpiWarps * 2 * OUT_BLOCK;   // two blocks per epilogue warp
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STAGING + 256;
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 struct WArgs {
     const int32_t *offs;    // [E+1] padded segment starts
     const int32_t *counts;  // [E] rows per expert
-    int M, N, E;            // output [E][M][N]
+    int M, N, E;            // output [E][M][N] (written through the output tensor map)
     int m_tiles, n_tiles;
-    float *out;
 };
 
 __device__ __forceinline__ void raise(uint32_t bit) { atomicOr(&g_bwd_fault_word, bit); }
@@ -98,12 +105,15 @@ __device__ __forceinline__ void raise(uint32_t bit) { atomicOr(&g_bwd_fault_word
 template <int KIND>
 __global__ void __launch_bounds__(kWThreads, 1)
     wgrad_kernel(const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmAl,
-                 const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl, const WArgs args)
+                 const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmBl,
+                 const __grid_constant__ CUtensorMap tmOut, const WArgs args)
 {
+    // tmOut: the gradient [E][M][N] FP32, box 32 x 32 x 1, 128-byte swizzle
     using C = WCfg<KIND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
+    uint8_t *staging = smem + C::STAGES * C::STAGE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(staging + C::STAGING);
     uint64_t *empty = full + C::STAGES;
     uint64_t *tfull = empty + C::STAGES;
     uint64_t *tempty = tfull + 2;
@@ -128,6 +138,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
         ptx::prefetch_tensormap(&tmAl);
         ptx::prefetch_tensormap(&tmBh);
         if (C::B_PAIR) ptx::prefetch_tensormap(&tmBl);
+        ptx::prefetch_tensormap(&tmOut);
     }
     if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, 2 * WNB);
@@ -225,7 +236,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t a_addr = ptx::smem_u32(smem + stage * C::STAGE_BYTES);
                     const uint32_t b_addr = a_addr + C::A_BYTES;
-                    const int nk = min(WK, padded - kr) / 16;
+                    const int nk = min(WK, padded - kr) / 16;   // 1 or 2
                     for (int k = 0; k < nk; ++k) {
                         const uint64_t ah = ptx::sw128_desc_mn(a_addr + k * 2048, BOX);
                         const uint64_t al = ptx::sw128_desc_mn(a_addr + C::A_HALF + k * 2048, BOX);
@@ -251,20 +262,43 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
-        // warps 2..9: TMEM lane quarter warp % 4, columns half * 128 ...
+        // warps 2..9: TMEM lane quarter warp % 4 (output rows m0 + 32 q ..),
+        // columns half * 128 ... in four 32-column blocks.  Lane l holds row
+        // l of a block; its 16-byte piece j goes to (j ^ (l % 8)) * 16 of the
+        // row's 128 bytes in the staging buffer (the tensor map's swizzle).
         const int q = warp & 3, half = (warp - 2) >> 2;
+        uint8_t *stg = staging + (warp - 2) * 2 * OUT_BLOCK;
+        int buf = 0;
+        auto put_block = [&](const uint32_t (&r)[32], int e, int row0, int col0) {
+            uint8_t *b = stg + buf * OUT_BLOCK + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(b + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // rows past M and columns past N are not written by the store
+                ptx::tma_store_3d(&tmOut, stg + buf * OUT_BLOCK, col0, row0, e);
+                ptx::bulk_commit_group();
+                ptx::bulk_wait_group_read<1>();   // the other buffer is free again
+            }
+            __syncwarp();
+            buf ^= 1;
+        };
         int li = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
             int e, m0, n0, rows, r0;
             decode(i, e, m0, n0, rows, r0);
-            const int m = m0 + 32 * q + lane;
-            float *orow = args.out + ((int64_t)e * args.M + m) * args.N;
+            const int row0 = m0 + 32 * q;
+            const bool rows_in = row0 < args.M;   // M is a multiple of 32: a block is all in or all out
             if (rows == 0) {
                 // nothing selected this expert: its gradient is zero
-                if (m < args.M) {
-                    for (int c = half * (WNB / 2); c < (half + 1) * (WNB / 2) && n0 + c < args.N; c += 4)
-                        *reinterpret_cast<float4 *>(orow + n0 + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                uint32_t z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0u;
+                for (int c0 = half * (WNB / 2); c0 < (half + 1) * (WNB / 2); c0 += 32)
+                    if (rows_in && n0 + c0 < args.N) put_block(z, e, row0, n0 + c0);
                 continue;
             }
             const int acc = li & 1;
@@ -282,18 +316,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 ptx::tmem_ld32(tbase + c0, r);
                 ptx::tmem_wait_ld();
                 // N is a multiple of 64, so a 32-column block is all in or all out
-                if (m < args.M && n0 + c0 < args.N) {
-                    float4 *dst = reinterpret_cast<float4 *>(orow + n0 + c0);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-                }
+                if (rows_in && n0 + c0 < args.N) put_block(r, e, row0, n0 + c0);
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty + acc);
         }
+        if (lane == 0) ptx::bulk_wait_all();   // the last stores have left shared memory and landed
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -407,20 +437,37 @@ cudaError_t make_rows_map(CUtensorMap *map, const void *base, uint64_t rows, uin
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// the gradient [E][M][N] FP32, box 32 columns (128 bytes, 128-byte swizzle)
+// x 32 rows x 1 expert
+cudaError_t make_out_map(CUtensorMap *map, float *base, uint64_t E, uint64_t M, uint64_t N)
+{
+    EncodeTiledFn enc = wencoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {N, M, E};
+    const cuuint64_t strides[2] = {N * 4, N * M * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int KIND>
 cudaError_t launch_wgrad(const void *ah, const void *al, const void *bh, const void *bl, const int32_t *offs,
                          const int32_t *counts, int n_rows, int M, int N, int E, float *out, int ctas, cudaStream_t s)
 {
-    CUtensorMap tAh, tAl, tBh, tBl;
+    CUtensorMap tAh, tAl, tBh, tBl, tOut;
     cudaError_t e = make_rows_map(&tAh, ah, n_rows, M);
     if (e == cudaSuccess) e = make_rows_map(&tAl, al, n_rows, M);
     if (e == cudaSuccess) e = make_rows_map(&tBh, bh, n_rows, N);
     if (e == cudaSuccess) e = make_rows_map(&tBl, bl ? bl : bh, n_rows, N);
+    if (e == cudaSuccess) e = make_out_map(&tOut, out, E, M, N);
     if (e != cudaSuccess) return e;
-    const WArgs a{offs, counts, M, N, E, (M + WBM - 1) / WBM, (N + WNB - 1) / WNB, out};
+    const WArgs a{offs, counts, M, N, E, (M + WBM - 1) / WBM, (N + WNB - 1) / WNB};
     const int64_t items = (int64_t)E * a.m_tiles * a.n_tiles;
     const int grid = (int)(items < ctas ? items : ctas);
-    wgrad_kernel<KIND><<<grid, kWThreads, WCfg<KIND>::SMEM, s>>>(tAh, tAl, tBh, tBl, a);
+    wgrad_kernel<KIND><<<grid, kWThreads, WCfg<KIND>::SMEM, s>>>(tAh, tAl, tBh, tBl, tOut, a);
     return cudaPeekAtLastError();
 }
 

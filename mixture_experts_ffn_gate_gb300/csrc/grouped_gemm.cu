@@ -96,6 +96,11 @@ struct Cfg {
     // the weight tile is read along its rows' index (MN-major): the
     // backward's contractions over H (W_down) and over 2I (W_gate_up)
     static constexpr bool A_MN = KIND == kBwdQ || KIND == kBwdDx;
+    // epilogue warps: q's SwiGLU backward reads and writes several arrays
+    // per element, so two warps share each TMEM lane quarter (one 32-column
+    // block each) to drain its single accumulator set sooner
+    static constexpr int EPI_WARPS = KIND == kBwdQ ? 8 : 4;
+    static constexpr int THREADS = GATE_UP ? kThreadsGateUp : 32 * (2 + EPI_WARPS);
     static constexpr int MT = GATE_UP ? 4 : 3;  // weight tiles per item (they share one token tile)
     // accumulator columns per weight tile: the chunk's tokens (gate_up), or
     // its hi rows then its lo rows (down); gate_up double-buffers them so the
@@ -240,7 +245,7 @@ __device__ __forceinline__ void bwd_q_columns(const uint32_t (&r)[32], int ncols
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(Cfg<KIND>::GATE_UP ? kThreadsGateUp : kThreads, 1)
+__global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0s,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1s,
                         const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::GATE_UP ? kThreadsGateUp : kThreads
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull + b, 1);
-            ptx::mbar_init(tempty + b, 4);
+            ptx::mbar_init(tempty + b, C::EPI_WARPS);
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -483,6 +488,9 @@ __global__ void __launch_bounds__(Cfg<KIND>::GATE_UP ? kThreadsGateUp : kThreads
     } else {
         // ---------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // q: warps 2-5 take the chunk's 32-column blocks 0, 2, ..., warps 6-9 blocks 1, 3, ...
+        const int c_first = C::EPI_WARPS == 8 ? 32 * ((warp - 2) >> 2) : 0;
+        constexpr int c_step = C::EPI_WARPS == 8 ? 64 : 32;
         int li = 0;
         Item nxt = blockIdx.x < total ? decode_item(blockIdx.x, args) : Item{};
         for (int i = blockIdx.x; i < total; i += gridDim.x, ++li) {
@@ -501,7 +509,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::GATE_UP ? kThreadsGateUp : kThreads
             // q: a warp whose 32 neurons lie past I has nothing to do
             if (KIND == kBwdQ && tile * BM + 32 * q >= args.I) continue;
             const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (acc * MT + t) * C::TILE_COLS;
-            for (int c0 = 0; c0 < it.n; c0 += 32) {
+            for (int c0 = c_first; c0 < it.n; c0 += c_step) {
                 uint32_t r[32];
                 ptx::tmem_ld32(tbase + c0, r);
                 if (!GATE_UP) {
@@ -728,7 +736,7 @@ cudaError_t launch_mn(const CUtensorMap &tA, const CUtensorMap (&tB)[4], const i
     const int tiles = (m_size + BM - 1) / BM;
     GemmArgs a{chunks, nchunks, offs, H, I, k_size, (tiles + MT - 1) / MT, tiles, MT * BM * BK * 2, out0, nullptr,
                nullptr, nullptr, 0, q};
-    grouped_gemm_kernel<KIND><<<grid_for(ctas, n_rows, a.m_tiles, E), kThreads, Cfg<KIND>::SMEM, s>>>(
+    grouped_gemm_kernel<KIND><<<grid_for(ctas, n_rows, a.m_tiles, E), Cfg<KIND>::THREADS, Cfg<KIND>::SMEM, s>>>(
         tA, tB[0], tB[1], tB[2], tB[3], a);
     return cudaPeekAtLastError();
 }
