@@ -215,29 +215,44 @@ __device__ __forceinline__ void bwd_q_columns(const uint32_t (&r)[32], int ncols
     const BwdQArgs &b = args.q;
     float prod[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int col = c0 + j;
-        prod[j] = 0.0f;
-        if (j < ncols && col < npad) {
-            const int64_t row = p0 + col;
-            float dg = 0.0f, du = 0.0f, wa = 0.0f;
-            if (col < n) {
-                const float qv = __uint_as_float(r[j]);
-                const float g = __ldg(b.g + row * I + i);
-                const float u = __ldg(b.u + row * I + i);
-                const float w = __ldg(b.w_s + row);
-                const float sg = 1.0f / (1.0f + expf(-g));
-                const float silu = g * sg;
-                const float a = silu * u;
-                const float da = w * qv;
-                dg = da * u * (sg * (1.0f + g * (1.0f - sg)));
-                du = da * silu;
-                wa = w * a;
-                prod[j] = a * qv;
+    for (int h = 0; h < 2; ++h) {
+        // each half's loads first (predicated), so that they are in flight
+        // together: the stores below could alias them as far as the
+        // compiler knows, and would otherwise hold each column's loads back
+        float gv[16], uv[16], wv[16];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int j = 16 * h + jj;
+            const bool live = j < ncols && c0 + j < n;
+            const int64_t row = p0 + c0 + j;
+            gv[jj] = live ? __ldg(b.g + row * I + i) : 0.0f;
+            uv[jj] = live ? __ldg(b.u + row * I + i) : 0.0f;
+            wv[jj] = live ? __ldg(b.w_s + row) : 0.0f;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const int j = 16 * h + jj;
+            const int col = c0 + j;
+            prod[j] = 0.0f;
+            if (j < ncols && col < npad) {
+                const int64_t row = p0 + col;
+                float dg = 0.0f, du = 0.0f, wa = 0.0f;
+                if (col < n) {
+                    const float qv = __uint_as_float(r[j]);
+                    const float g = gv[jj], u = uv[jj], w = wv[jj];
+                    const float sg = 1.0f / (1.0f + expf(-g));
+                    const float silu = g * sg;
+                    const float a = silu * u;
+                    const float da = w * qv;
+                    dg = da * u * (sg * (1.0f + g * (1.0f - sg)));
+                    du = da * silu;
+                    wa = w * a;
+                    prod[j] = a * qv;
+                }
+                store_pair(b.dgu_hi, b.dgu_lo, row * 2 * I + i, dg);
+                store_pair(b.dgu_hi, b.dgu_lo, row * 2 * I + I + i, du);
+                store_pair(b.wa_hi, b.wa_lo, row * I + i, wa);
             }
-            store_pair(b.dgu_hi, b.dgu_lo, row * 2 * I + i, dg);
-            store_pair(b.dgu_hi, b.dgu_lo, row * 2 * I + I + i, du);
-            store_pair(b.wa_hi, b.wa_lo, row * I + i, wa);
         }
     }
     const float sum = warp_column_sums(prod, lane);
