@@ -101,13 +101,16 @@ struct Cfg {
     // block each) to drain its single accumulator set sooner
     static constexpr int EPI_WARPS = KIND == kBwdQ ? 8 : 4;
     static constexpr int THREADS = GATE_UP ? kThreadsGateUp : 32 * (2 + EPI_WARPS);
-    static constexpr int MT = GATE_UP ? 4 : 3;  // weight tiles per item (they share one token tile)
+    // weight tiles per item (they share one token tile); q takes two, so
+    // that its accumulators fit twice (its long epilogue then overlaps the
+    // next item's MMAs) and I's 128-row tiles split evenly
+    static constexpr int MT = GATE_UP ? 4 : KIND == kBwdQ ? 2 : 3;
     // accumulator columns per weight tile: the chunk's tokens (gate_up), or
-    // its hi rows then its lo rows (down); gate_up double-buffers them so the
-    // epilogue of one item overlaps the MMAs of the next, down (three tiles
-    // of 128 columns) has room for one set
+    // its hi rows then its lo rows (down, q, dx); gate_up and q double-buffer
+    // them so the epilogue of one item overlaps the MMAs of the next, down
+    // and dx (three tiles of 128 columns) have room for one set
     static constexpr int TILE_COLS = GATE_UP ? ACC_COLS : 2 * ACC_COLS;
-    static constexpr int ACC_BUFS = GATE_UP ? 2 : 1;
+    static constexpr int ACC_BUFS = GATE_UP || KIND == kBwdQ ? 2 : 1;
     static constexpr int TMEM_COLS = ACC_BUFS * MT * TILE_COLS;
     // tcgen05.alloc takes a power of two of at least 32 columns
     static constexpr int TMEM_ALLOC = TMEM_COLS <= 32    ? 32
@@ -116,7 +119,7 @@ struct Cfg {
                                       : TMEM_COLS <= 256 ? 256
                                                          : 512;
     static_assert(TMEM_COLS <= 512, "accumulators exceed TMEM");
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = KIND == kBwdQ ? 4 : 3;
     static constexpr int A_TILE = BM * BK * 2;                            // 16 KB per weight tile
     static constexpr int A_BYTES = MT * A_TILE;
     static constexpr int B_TILE = NMAX * BK * 2;                          // 8 KB per operand
