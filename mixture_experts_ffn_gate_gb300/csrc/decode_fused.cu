@@ -160,6 +160,12 @@ constexpr unsigned long long kCheckKey = 0x6d6f652d7461672dull;  // xor the flag
 // at the grid barrier, and the L2 prefetch of the inputs
 constexpr int kSkipArrival = 1, kPrefetchInputs = 2;
 
+// Named barriers of the one-token start (id 1 is the consumers' own):
+// warp 0 publishes the ring's barriers and the flag words to the consumers
+// (kBarPublish), the routing warp hands the touched experts to warp 0
+// (kBarRouted), the consumers meet once the routing is in (kBarConsumers).
+constexpr int kBarPublish = 2, kBarRouted = 3, kBarConsumers = 4;
+
 enum : uint32_t {
     FAULT_LOGITS = 8u,
     FAULT_PRODUCER = 16u,
@@ -619,6 +625,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // One token (and logits passed in): its k experts are distinct, so the
+    // routing warp lays out the touched list itself and the producer starts
+    // its copies as soon as that warp is done, without waiting for the
+    // block; the consumers meet on their own barriers.
+    constexpr bool kFastStart = NT == 1 && !ROUTER;
+    if constexpr (kFastStart) {
+        if (warp == 0) {
+            __syncwarp();
+            ptx::named_arrive(kBarPublish, kThreads);
+        }
+    }
 
     if constexpr (ROUTER) {
         // x of all tokens into shared memory for phase A, while the
@@ -683,7 +700,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_sel[t * k + lane] = e;
             s_w[t * k + lane] = wt;
         }
+        if constexpr (kFastStart) {
+            if (lane < k) {
+                if (blockIdx.x == 0) {
+                    if (idx_out) idx_out[lane] = e;
+                    if (w_out) w_out[lane] = wt;
+                }
+                s_uexp[lane] = e;
+                s_ubeg[lane] = lane;
+                s_asg[lane] = lane;
+                s_xoff[lane] = 0;
+                s_rlog[lane] = (int8_t)(rows_for(1) == 4 ? 2 : rows_for(1) == 2 ? 1 : 0);
+            }
+            if (lane == 0) {
+                s_U = k;
+                s_ubeg[k] = k;
+            }
+            __syncwarp();
+            ptx::named_arrive(kBarRouted, 64);
+        }
     }
+    if constexpr (kFastStart) {
+        if (warp == 0) {
+            ptx::named_sync(kBarRouted, 64);
+        } else {
+            ptx::named_sync(kBarPublish, kThreads);
+            ptx::named_sync(kBarConsumers, kThreads - 32);
+        }
+    } else {
     __syncthreads();
     if (threadIdx.x < A) {
         const int a = threadIdx.x;
@@ -732,13 +776,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (T > 1) __syncthreads();
-    const int U = s_U;
-    if (threadIdx.x < U) {
+    if (threadIdx.x < s_U) {
         const int na = s_ubeg[threadIdx.x + 1] - s_ubeg[threadIdx.x];
         s_rlog[threadIdx.x] = (int8_t)(rows_for(na) == 4 ? 2 : rows_for(na) == 2 ? 1 : 0);
     }
     if (threadIdx.x < A) s_xoff[threadIdx.x] = s_asg[threadIdx.x] / k * H;
     __syncthreads();
+    }
+    const int U = s_U;
     if (threadIdx.x == 0) MOE_TL(2);
 
     const unsigned long long calls = s_flags[0];

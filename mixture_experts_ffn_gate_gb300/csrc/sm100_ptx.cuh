@@ -247,6 +247,14 @@ __device__ __forceinline__ void named_sync(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrival at a named barrier without waiting for it: the barrier completes
+// when `threads` threads have arrived or synced; this thread's earlier
+// shared-memory writes are visible to the threads that sync on it.
+__device__ __forceinline__ void named_arrive(int id, int threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // Named barrier that also ORs a predicate over the participating threads:
 // every thread gets the same answer, so all of them can leave together.
 __device__ __forceinline__ bool named_sync_or(int id, int threads, bool pred)
