@@ -33,10 +33,10 @@ call's HBM fraction, the dominant kernel's roofline and the TFLOP/s against
 dense BF16 peak and against min(peak, HBM peak x flop/byte).  Two of the
 rows ("entry": moe_ffn_forward_router) run the 2048-hidden decode layer at
 T=1 and 2 with the router projection inside the call (router weights and
-bias passed instead of logits); six ("entry": moe_ffn_forward_mxfp8) run
-the 2048-hidden layer at T=1/2/4, the 4096-hidden one at T=1 and the
-7168-hidden one at T=1/8 with MXFP8 expert weights (their bytes counted at
-1 + 1/32 per weight; T > 4 takes the general decode kernels).  One row
+bias passed instead of logits); nine ("entry": moe_ffn_forward_mxfp8) run
+the 2048-hidden layer at T=1/2/4, the 4096-hidden one at T=1/16/64 and the
+7168-hidden one at T=1/8/32 with MXFP8 expert weights (their bytes counted
+at 1 + 1/32 per weight; T > 4 takes the grouped tensor-core path).  One row
 ("entry": moe_ffn_backward) runs the backward pass of the T=2048
 training-size layer (dout ~ N(0,1) FP32 per call; all four gradients written
 every call), with its own byte model (backward_bytes) and 16 H I T k flops.
@@ -237,9 +237,9 @@ def kernel_bytes(kernel, wl, T, U, k, bpe=2.0):
     if kernel == "decode_down":
         return U * H * I * 2 + T * k * I * 4 + T * H * 4 + T * k * 4
     if kernel == "gemm_gate_up":  # x rows read by the sorted order (re-reads of a row come from L2)
-        return U * 2 * I * H * 2 + T * H * 2 + 2 * T * k * I * 2
+        return U * 2 * I * H * bpe + T * H * 2 + 2 * T * k * I * 2
     if kernel == "gemm_down":
-        return U * H * I * 2 + 2 * T * k * I * 2 + T * k * H * 4
+        return U * H * I * bpe + 2 * T * k * I * 2 + T * k * H * 4
     return None
 
 
@@ -395,8 +395,8 @@ SUPPLEMENTARY = [
     ("decode_h2048_i768_e128_k8", (2,)),
     ("decode_h2048_i768_e128_k8+router", (1, 2)),
     ("decode_h2048_i768_e128_k8+mxfp8", (1, 2, 4)),
-    ("decode_h4096_i1536_e128_k8_bias+mxfp8", (1,)),
-    ("decode_h7168_i2048_e384_k8_bias+mxfp8", (1, 8)),
+    ("decode_h4096_i1536_e128_k8_bias+mxfp8", (1, 16, 64)),
+    ("decode_h7168_i2048_e384_k8_bias+mxfp8", (1, 8, 32)),
     ("decode_h4096_i1536_e128_k8_bias", (1, 4, 16, 64)),
     ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),

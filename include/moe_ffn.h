@@ -215,8 +215,7 @@ int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16,
                            moe_ffn_opts *opts, cudaStream_t stream);
 
 /*
- * The layer with MXFP8 expert weights, for decode steps of up to 64
- * tokens.  The Mixture-of-Kittens article ("커서가 MoE 학습 메가커널 믹스처 오브
+ * The layer with MXFP8 expert weights.  The Mixture-of-Kittens article ("커서가 MoE 학습 메가커널 믹스처 오브
  * 키튼스를 아파치 2.0으로 공개했다", section 2.37배는 어떤 기준선과 비교한
  * 숫자인가) measures the layer with MXFP8 operands; the format is the OCP
  * Microscaling (MX) specification's MXFP8 with E4M3 elements, applied here
@@ -231,11 +230,16 @@ int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16,
  * and sums are formed in FP32 as in the BF16 path; the results are within
  * the same tolerance of the FP64 layer on the dequantised weights.
  * All device pointers 16-byte aligned; the workspace is moe_ffn_forward_ex's
- * (at least moe_ffn_workspace_bytes, same state rules).  Only the decode
- * path is built for this format: the fused decode kernel for T <= 4 where it
- * fits, the general decode kernels otherwise (path_taken tells which).
- * T > 64 and opts->path other than AUTO or DECODE return
- * MOE_ERR_UNSUPPORTED_SHAPE, with nothing launched.
+ * (at least moe_ffn_workspace_bytes, same state rules).  Paths (path_taken
+ * tells which): AUTO takes the fused decode kernel for T <= 4 where it fits,
+ * the general decode kernels up to T = 16 (opts->decode_max_tokens moves
+ * this bound) and the grouped tensor-core GEMMs beyond, which load the E4M3
+ * code tiles and convert
+ * them to exact BF16 tiles (each weight a BF16 number whenever its value is
+ * in BF16's range) in shared memory before their BF16 MMAs.  opts->path
+ * DECODE forces the decode kernels, which take at most 64 tokens (larger T
+ * returns MOE_ERR_UNSUPPORTED_SHAPE, with nothing launched); GROUPED forces
+ * the grouped path.
  */
 #define MOE_FFN_MX_SCALE_BYTES(K) ((((K) / 32) + 15) / 16 * 16)
 int moe_ffn_forward_mxfp8(const void *x_bf16, const float *router_logits_f32,

@@ -14,6 +14,7 @@ enum : uint32_t {
     FAULT_GEMM_PRODUCER = 1u << 0,
     FAULT_GEMM_MMA = 1u << 1,
     FAULT_GEMM_EPILOGUE = 1u << 2,
+    FAULT_GEMM_CONVERT = 1u << 3,  // the MXFP8 code converters
 };
 
 // 16-byte streaming load that bypasses L1 allocation: expert weights are
@@ -66,6 +67,35 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float f[8])
 __device__ __forceinline__ float e8m0_scale(uint32_t s)
 {
     return __uint_as_float(s ? s << 23 : 0x00400000u);
+}
+
+// The factors of e4m3x2_to_bf16x2_scaled for the E8M0 scale s: the pair's
+// values times 2^-112 are multiplied by f.x then f.y, together 2^(s - 15):
+// 2^(s - 15) and 1 when that is a BF16 number (s <= 142), else 2^112 and
+// 2^(s - 127).  Both are powers of two, so the multiplies are exact whenever
+// the result is a BF16 number.
+__device__ __forceinline__ uint2 mx_bf16_factors(uint32_t s)
+{
+    const float a = __uint_as_float((s <= 142u ? s + 112u : 239u) << 23);
+    const float b = __uint_as_float((s <= 142u ? 127u : s) << 23);
+    const __nv_bfloat162 fa = __float2bfloat162_rn(a), fb = __float2bfloat162_rn(b);
+    return make_uint2(*reinterpret_cast<const uint32_t *>(&fa), *reinterpret_cast<const uint32_t *>(&fb));
+}
+
+// Two E4M3 codes (low byte first) times 2^(s - 127) as a BF16 pair, given
+// f = mx_bf16_factors(s); exact whenever the products are BF16 numbers.  The
+// F16 pair of the codes (exact) with its signs cleared and shifted right by
+// 3, the signs put back, is the BF16 pair of the values times 2^-112 (E4M3
+// values are F16 normals or zero with at most 3 mantissa bits: the exponent
+// field moves into BF16's, the mantissa's top 7 bits into BF16's).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two_codes, uint2 f)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+    const uint32_t x = (uint32_t)h.x | ((uint32_t)h.y << 16);
+    const uint32_t t = ((x & 0x7fff7fffu) >> 3) | (x & 0x80008000u);
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+    b = __hmul2(__hmul2(b, *reinterpret_cast<const __nv_bfloat162 *>(&f.x)), *reinterpret_cast<const __nv_bfloat162 *>(&f.y));
+    return *reinterpret_cast<const uint32_t *>(&b);
 }
 
 // 16 E4M3 codes (byte j = element j) to their values in FP32, exactly

@@ -75,6 +75,7 @@ constexpr int SMALL_ROWS = 16;           // B box for chunks of at most 16 rows
 constexpr int kThreads = 192;           // down: producer, MMA issuer, 4 epilogue warps
 constexpr int kThreadsGateUp = 288;     // gate_up: + one x-row loader warp per ring stage
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr int kPrefetchSteps = 6;                 // MX: code boxes fetched into L2 this far ahead
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s to drain after an abort
 
 static_assert(NMAX <= ACC_COLS && NMAX % 16 == 0, "chunk must fit one accumulator");
@@ -88,11 +89,17 @@ enum : int {
     kGateUpRaw = 2,  // g = W_gate x and u = W_up x in FP32
     kBwdQ = 3,       // q = W_down^T . [dout_hi ; dout_lo], then the SwiGLU backward
     kBwdDx = 4,      // z = W_gate_up^T . [dgu_hi ; dgu_lo]
+    kGateUpMx = 5,   // kGateUp with MXFP8 weights
+    kDownMx = 6,     // kDown with MXFP8 weights
 };
 
 template <int KIND>
 struct Cfg {
-    static constexpr bool GATE_UP = KIND == kGateUp || KIND == kGateUpRaw;
+    // MXFP8 weights: the producer loads E4M3 code tiles, converter warps
+    // write them as exact BF16 (each 32-element block times its E8M0
+    // scale) into the tile the MMA reads
+    static constexpr bool MX = KIND == kGateUpMx || KIND == kDownMx;
+    static constexpr bool GATE_UP = KIND == kGateUp || KIND == kGateUpRaw || KIND == kGateUpMx;
     // the weight tile is read along its rows' index (MN-major): the
     // backward's contractions over H (W_down) and over 2I (W_gate_up)
     static constexpr bool A_MN = KIND == kBwdQ || KIND == kBwdDx;
@@ -100,17 +107,20 @@ struct Cfg {
     // per element, so two warps share each TMEM lane quarter (one 32-column
     // block each) to drain its single accumulator set sooner
     static constexpr int EPI_WARPS = KIND == kBwdQ ? 8 : 4;
-    static constexpr int THREADS = GATE_UP ? kThreadsGateUp : 32 * (2 + EPI_WARPS);
+    static constexpr int CONV_WARPS = MX ? 8 : 0;
+    static constexpr int FIRST_CONV = 2 + EPI_WARPS + (GATE_UP ? 3 : 0);  // after the x-row loaders
+    static constexpr int THREADS = 32 * (FIRST_CONV + CONV_WARPS);
     // weight tiles per item (they share one token tile); q takes two, so
     // that its accumulators fit twice (its long epilogue then overlaps the
     // next item's MMAs) and I's 128-row tiles split evenly
-    static constexpr int MT = GATE_UP ? 4 : KIND == kBwdQ ? 2 : 3;
+    // (MX: two, so that the code tiles fit beside three stages)
+    static constexpr int MT = MX ? 2 : GATE_UP ? 4 : KIND == kBwdQ ? 2 : 3;
     // accumulator columns per weight tile: the chunk's tokens (gate_up), or
     // its hi rows then its lo rows (down, q, dx); gate_up and q double-buffer
     // them so the epilogue of one item overlaps the MMAs of the next, down
     // and dx (three tiles of 128 columns) have room for one set
     static constexpr int TILE_COLS = GATE_UP ? ACC_COLS : 2 * ACC_COLS;
-    static constexpr int ACC_BUFS = GATE_UP || KIND == kBwdQ ? 2 : 1;
+    static constexpr int ACC_BUFS = GATE_UP || KIND == kBwdQ || MX ? 2 : 1;
     static constexpr int TMEM_COLS = ACC_BUFS * MT * TILE_COLS;
     // tcgen05.alloc takes a power of two of at least 32 columns
     static constexpr int TMEM_ALLOC = TMEM_COLS <= 32    ? 32
@@ -124,9 +134,13 @@ struct Cfg {
     static constexpr int A_BYTES = MT * A_TILE;
     static constexpr int B_TILE = NMAX * BK * 2;                          // 8 KB per operand
     static constexpr int B_BYTES = B_TILE * (GATE_UP ? 1 : 2);            // x | act_hi + act_lo
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int CODE_TILE = BM * BK;                             // 8 KB of E4M3 codes per tile
+    static constexpr int CODE_BYTES = MX ? MT * CODE_TILE : 0;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + CODE_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static_assert(THREADS == (GATE_UP && !MX ? kThreadsGateUp : THREADS), "gate_up keeps 288 threads");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
 // Inputs and outputs of the backward pass's q GEMM epilogue (kBwdQ), all
@@ -154,6 +168,8 @@ struct GemmArgs {
     const int32_t *perm;  // sorted order (assignment t*k+j at row p)
     int k;
     BwdQArgs q;           // kBwdQ only
+    const uint8_t *scales;  // MX: the E8M0 scales [E][rows][scale_row] of the weight
+    int scale_row;          // bytes per scale row (K / 32 padded to 16)
 };
 
 struct Item {
@@ -279,17 +295,22 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     // tmB0/tmB1 (down, q, dx): the chunk's hi/lo rows (act, dout or dgu),
     // box 64 x NMAX; tmB0s/tmB1s: the same with a 16-row box, for chunks of
     // <= 16 rows.  gate_up leaves the B maps unread.
+    // MX (gate_up, down): tmA is the same view of the E4M3 codes (uint8,
+    // no swizzle: 64-byte rows), its box a tile's codes.
     using C = Cfg<KIND>;
     constexpr bool GATE_UP = C::GATE_UP;
     constexpr bool A_MN = C::A_MN;
+    constexpr bool MX = C::MX;
     constexpr int MT = C::MT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + C::STAGES * C::A_BYTES;
+    uint8_t *sCode = sB + C::STAGES * C::B_BYTES;  // MX only
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::STAGE_BYTES);
     uint64_t *empty = full + C::STAGES;
-    uint64_t *tfull = empty + C::STAGES;
+    uint64_t *cfull = empty + C::STAGES;           // MX: a stage's codes (and down's B rows) landed
+    uint64_t *tfull = cfull + C::STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -298,9 +319,11 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            // gate_up: the weight box's expect-tx arrival and the x rows' arrival
-            ptx::mbar_init(full + s, GATE_UP ? 2 : 1);
+            // gate_up: the weight box's expect-tx arrival and the x rows'
+            // arrival; MX: the converter warps' arrivals (and gate_up's x rows)
+            ptx::mbar_init(full + s, MX ? C::CONV_WARPS + (GATE_UP ? 1 : 0) : GATE_UP ? 2 : 1);
             ptx::mbar_init(empty + s, 1);
+            ptx::mbar_init(cfull + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(tfull + b, 1);
@@ -343,20 +366,45 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 const bool small = it.n <= SMALL_ROWS;
                 // gate_up: the weight box only (the x rows come from the loader warps)
                 const uint32_t bytes = args.a_bytes + (GATE_UP ? 0 : (small ? SMALL_ROWS : NMAX) * BK * 2 * 2);
+                uint64_t *const land = MX ? cfull : full;  // where the TMA copies complete
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!ptx::mbar_wait_bounded(empty + stage, phase ^ 1, abort_flag, kWaitLimitNs)) {
                         if (!*abort_flag) raise_fault(FAULT_GEMM_PRODUCER);
                         *abort_flag = 1;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(full + stage, bytes);
+                    ptx::mbar_arrive_expect_tx(land + stage, bytes);
                     ++armed[stage];
                     const int k0 = kb * BK;
-                    uint8_t *a = sA + stage * C::A_BYTES;
+                    if constexpr (MX) {
+                        // the code box kPrefetchSteps K steps on (this item's,
+                        // or the next one's) into L2: a stage holds few code
+                        // bytes, so its copies must not wait on DRAM
+                        int pk = kb + kPrefetchSteps;
+                        const Item *pi = &it;
+                        if (pk >= KB) {
+                            pk -= KB;
+                            pi = (i + (int)gridDim.x < total && pk < KB) ? &nxt : nullptr;
+                        }
+                        if (pi) {
+                            if (GATE_UP) {
+                                ptx::tma_prefetch_5d(&tmA, pk * BK, 0, 0, pi->m * 4 * MT, pi->e);
+                            } else {
+#pragma unroll
+                                for (int t = 0; t < MT; ++t)
+                                    ptx::tma_prefetch_3d(&tmA, pk * BK, (pi->m * MT + t) * BM, pi->e);
+                            }
+                        }
+                    }
+                    uint8_t *a = MX ? sCode + stage * C::CODE_BYTES : sA + stage * C::A_BYTES;
                     // MT tiles: one box (gate_up) or one box per tile (down);
                     // rows past the expert's end read 0 and are never stored
                     if (GATE_UP) {
-                        ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4 * MT, it.e, full + stage);
+                        ptx::tma_load_5d(a, &tmA, k0, 0, 0, it.m * 4 * MT, it.e, land + stage);
+                    } else if (MX) {
+#pragma unroll
+                        for (int t = 0; t < MT; ++t)
+                            ptx::tma_load_3d(a + t * C::CODE_TILE, &tmA, k0, (it.m * MT + t) * BM, it.e, land + stage);
                     } else if (A_MN) {
 #pragma unroll
                         for (int t = 0; t < MT; ++t) {
@@ -373,9 +421,9 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                     // whole number of 1024-byte swizzle groups), one B tile
                     if (!GATE_UP) {
                         uint8_t *b = sB + stage * C::B_BYTES;
-                        ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, full + stage);
+                        ptx::tma_load_2d(b, small ? &tmB0s : &tmB0, k0, it.p0, land + stage);
                         ptx::tma_load_2d(b + (small ? SMALL_ROWS : NMAX) * BK * 2, small ? &tmB1s : &tmB1, k0, it.p0,
-                                         full + stage);
+                                         land + stage);
                     }
                     if (++stage == C::STAGES) {
                         stage = 0;
@@ -387,7 +435,8 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
             // armed phase of each stage completes after all earlier ones)
             const volatile int keep_waiting = 0;
             for (int s = 0; s < C::STAGES; ++s)
-                if (armed[s]) ptx::mbar_wait_bounded(full + s, (armed[s] - 1) & 1, &keep_waiting, kDrainLimitNs);
+                if (armed[s])
+                    ptx::mbar_wait_bounded((MX ? cfull : full) + s, (armed[s] - 1) & 1, &keep_waiting, kDrainLimitNs);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------- MMA issuer
@@ -448,6 +497,82 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
             // every MMA this thread issued has completed once drain fires
             ptx::mma_commit(drain);
             ptx::mbar_wait_bounded(drain, 0, abort_flag, kDrainLimitNs);
+        }
+    } else if (MX && warp >= C::FIRST_CONV) {
+        // ------------------------------------ E4M3 -> BF16 converters (MX)
+        // Per K step the stage holds MT tiles x 128 rows x 64 codes: 4
+        // pieces of 16 codes per row, NP pieces per converter thread.  Piece
+        // p = ct + NC j is chunk c = p & 3 of row r = (p >> 2) & 127 of tile
+        // t = p >> 9; its 16 values, each code's value times the E8M0 scale
+        // of its 32-element block (exact: the weights are BF16 numbers), go
+        // to the row's 128-byte-swizzled 16-byte chunks 2c and 2c + 1.
+        constexpr int NC = 32 * C::CONV_WARPS, NP = MT * BM * 4 / (NC > 0 ? NC : 1);
+        static_assert(!MX || NP * NC == MT * BM * 4, "whole pieces per converter thread");
+        const int ct = threadIdx.x - 32 * C::FIRST_CONV;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+            const Item it = decode_item(i, args);
+            const uint8_t *srow[NP];  // each piece's scale row (null: a row past the weight's end)
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int p = ct + NC * j, r = (p >> 2) & 127, t = p >> 9;
+                int64_t grow;
+                bool in;
+                if constexpr (GATE_UP) {  // 4 groups x (16 gate rows, 16 up rows) of 16 neurons
+                    const int neuron = ((it.m * MT + t) * 4 + (r >> 5)) * 16 + (r & 15);
+                    in = neuron < args.I;
+                    grow = ((int64_t)it.e * 2 + ((r >> 4) & 1)) * args.I + neuron;
+                } else {
+                    const int h = (it.m * MT + t) * BM + r;
+                    in = h < args.H;
+                    grow = (int64_t)it.e * args.H + h;
+                }
+                srow[j] = in ? args.scales + grow * args.scale_row : nullptr;
+            }
+            for (int kb = 0; kb < KB; ++kb) {
+                uint32_t sc[NP];  // the scales do not depend on the codes: read them before the wait
+#pragma unroll
+                for (int j = 0; j < NP; ++j)
+                    sc[j] = srow[j] ? __ldg(srow[j] + kb * 2 + (((ct + NC * j) & 3) >> 1)) : 127u;
+                int got = 1;
+                if (lane == 0) got = ptx::mbar_wait_bounded(cfull + stage, phase, abort_flag, kWaitLimitNs);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    if (lane == 0) {
+                        if (!*abort_flag) raise_fault(FAULT_GEMM_CONVERT);
+                        *abort_flag = 1;
+                    }
+                    ok = false;
+                    break;
+                }
+                const uint8_t *code = sCode + stage * C::CODE_BYTES;
+                uint8_t *a = sA + stage * C::A_BYTES;
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const int p = ct + NC * j, c = p & 3, r = (p >> 2) & 127, t = p >> 9;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(code + t * C::CODE_TILE + r * BK + c * 16);
+                    const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
+                    const uint2 f = mx_bf16_factors(sc[j]);
+                    uint32_t w[8];
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        w[2 * q2] = e4m3x2_to_bf16x2_scaled(cw[q2], f);
+                        w[2 * q2 + 1] = e4m3x2_to_bf16x2_scaled(cw[q2] >> 16, f);
+                    }
+                    uint8_t *row = a + t * C::A_TILE + r * 128;
+                    *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) =
+                        make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                ptx::fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(full + stage);
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
         }
     } else if (GATE_UP && warp >= 6) {
         // ------------------------------------- x-row loaders (gate_up only)
@@ -558,7 +683,7 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 } else if constexpr (KIND == kBwdQ) {
                     bwd_q_columns(r, it.n > SMALL_ROWS ? 32 : SMALL_ROWS, it.p0, it.n, c0, tile * BM + 32 * q + lane,
                                   tile * 4 + q, args, lane);
-                } else if constexpr (KIND == kGateUp) {
+                } else if constexpr (KIND == kGateUp || KIND == kGateUpMx) {
                     const int neuron = tile * 64 + 16 * q + (lane & 15);
                     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(lane < 16 ? args.out0 : args.out1);
 #pragma unroll
@@ -664,6 +789,37 @@ cudaError_t make_gate_up_map(CUtensorMap *map, const void *base, int E, int I, i
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The same two weight views over MXFP8 codes (uint8 [E, 2I, H] and
+// [E, H, I]): 64 codes (64 bytes) per box row, no swizzle.
+cudaError_t make_gate_up_code_map(CUtensorMap *map, const void *base, int E, int I, int H, uint32_t groups)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t row = (cuuint64_t)H;
+    const cuuint64_t dims[5] = {(cuuint64_t)H, 16, 2, (cuuint64_t)I / 16, (cuuint64_t)E};
+    const cuuint64_t strides[4] = {row, row * I, row * 16, row * 2 * I};
+    const cuuint32_t box[5] = {BK, 16, 2, groups, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_down_code_map(CUtensorMap *map, const void *base, int E, int H, int I)
+{
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
+    const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)I * H};
+    const cuuint32_t box[3] = {BK, BM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int grid_for(int ctas, int n_assign, int m_tiles, int E)
 {
     // an upper bound on the number of items: chunks <= E + n_assign / NMAX
@@ -687,6 +843,8 @@ cudaError_t gemm_init_device()
     if (e == cudaSuccess) e = set_smem<kGateUpRaw>();
     if (e == cudaSuccess) e = set_smem<kBwdQ>();
     if (e == cudaSuccess) e = set_smem<kBwdDx>();
+    if (e == cudaSuccess) e = set_smem<kGateUpMx>();
+    if (e == cudaSuccess) e = set_smem<kDownMx>();
     return e;
 }
 
@@ -713,7 +871,7 @@ cudaError_t gate_up_like(const void *x, const int32_t *perm, int k, const void *
     GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK * 2, out0,
                out1, (const uint16_t *)x, perm, k};
     // the token rows come from x through the loader warps: the B maps are not read
-    grouped_gemm_kernel<KIND><<<grid_for(ctas, n_assign, a.m_tiles, E), kThreadsGateUp, Cfg<KIND>::SMEM, s>>>(
+    grouped_gemm_kernel<KIND><<<grid_for(ctas, n_assign, a.m_tiles, E), Cfg<KIND>::THREADS, Cfg<KIND>::SMEM, s>>>(
         tA, tA, tA, tA, tA, a);
     return cudaPeekAtLastError();
 }
@@ -766,6 +924,39 @@ cudaError_t launch_gemm_gate_up(const void *x, const int32_t *perm, int k, const
                                 void *act_hi, void *act_lo, int ctas, cudaStream_t s)
 {
     return gate_up_like<kGateUp>(x, perm, k, wgu, chunks, nchunks, offs, n_assign, H, I, E, act_hi, act_lo, ctas, s);
+}
+
+cudaError_t launch_gemm_gate_up_mx(const void *x, const int32_t *perm, int k, const void *gq, const void *gs,
+                                   const int4 *chunks, const int32_t *nchunks, const int32_t *offs, int n_assign, int H,
+                                   int I, int E, void *act_hi, void *act_lo, int ctas, cudaStream_t s)
+{
+    CUtensorMap tA;
+    constexpr int MT = Cfg<kGateUpMx>::MT;
+    const uint32_t groups = (uint32_t)(4 * MT < I / 16 ? 4 * MT : I / 16);
+    cudaError_t e = make_gate_up_code_map(&tA, gq, E, I, H, groups);
+    if (e != cudaSuccess) return e;
+    GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK, act_hi, act_lo,
+               (const uint16_t *)x, perm, k, BwdQArgs{}, (const uint8_t *)gs, mx_scale_bytes(H)};
+    grouped_gemm_kernel<kGateUpMx><<<grid_for(ctas, n_assign, a.m_tiles, E), Cfg<kGateUpMx>::THREADS,
+                                     Cfg<kGateUpMx>::SMEM, s>>>(tA, tA, tA, tA, tA, a);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_gemm_down_mx(const void *act_hi, const void *act_lo, const void *dq, const void *ds,
+                                const int4 *chunks, const int32_t *nchunks, const int32_t *offs, int n_assign, int H,
+                                int I, int E, float *z, int ctas, cudaStream_t s)
+{
+    CUtensorMap tA, tB[4];
+    constexpr int MT = Cfg<kDownMx>::MT;
+    cudaError_t e = make_down_code_map(&tA, dq, E, H, I);
+    if (e == cudaSuccess) e = make_pair_maps(tB, act_hi, act_lo, n_assign, I);
+    if (e != cudaSuccess) return e;
+    const int tiles = (H + BM - 1) / BM;
+    GemmArgs a{chunks, nchunks, offs, H, I, I, (tiles + MT - 1) / MT, tiles, MT * Cfg<kDownMx>::CODE_TILE, z, nullptr,
+               nullptr, nullptr, 0, BwdQArgs{}, (const uint8_t *)ds, mx_scale_bytes(I)};
+    grouped_gemm_kernel<kDownMx><<<grid_for(ctas, n_assign, a.m_tiles, E), Cfg<kDownMx>::THREADS,
+                                   Cfg<kDownMx>::SMEM, s>>>(tA, tB[0], tB[1], tB[2], tB[3], a);
+    return cudaPeekAtLastError();
 }
 
 cudaError_t launch_gemm_gate_up_raw(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,

@@ -115,6 +115,15 @@ cudaError_t launch_gemm_down(const void *act_hi, const void *act_lo, const void 
                              const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, float *z,
                              int ctas, cudaStream_t s);
 cudaError_t read_fault_word(uint32_t *flags, bool clear);
+// The same two GEMMs with MXFP8 weights: E4M3 codes gq [E, 2I, H] / dq
+// [E, H, I] and E8M0 scales gs [E, 2I, mx_scale_bytes(H)] / ds [E, H,
+// mx_scale_bytes(I)], converted to exact BF16 tiles inside the kernel.
+cudaError_t launch_gemm_gate_up_mx(const void *x, const int32_t *perm, int k, const void *gq, const void *gs,
+                                   const int4 *chunks, const int32_t *nchunks, const int32_t *offs, int n_assign, int H,
+                                   int I, int E, void *act_hi, void *act_lo, int ctas, cudaStream_t s);
+cudaError_t launch_gemm_down_mx(const void *act_hi, const void *act_lo, const void *dq, const void *ds,
+                                const int4 *chunks, const int32_t *nchunks, const int32_t *offs, int n_assign, int H,
+                                int I, int E, float *z, int ctas, cudaStream_t s);
 
 // Backward pass.  Rows r index the padded sorted order (launch_sort with
 // pad 16: each expert's segment rounded up to 16 rows, pad rows zero).

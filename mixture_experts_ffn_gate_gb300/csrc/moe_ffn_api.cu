@@ -16,9 +16,14 @@ using moe::round_up;
 // (H7168 I2048 E384 k8: 748 vs 979 us at T=8; 417 vs 697 us at H4096, T=16).
 constexpr int kDefaultDecodeMaxTokens = 4;
 constexpr int kDefaultWarps = 8;
-// MXFP8 weights take the decode kernels only (no tensor-core form): calls of
-// up to this many tokens
+// MXFP8 weights on the general decode kernels (CUDA cores): calls of up to
+// kMxMaxTokens tokens when the caller forces the decode path.  AUTO takes
+// them up to kMxDecodeTokens and the tensor-core grouped path beyond, whose
+// in-kernel code conversion is bound by the SMs' integer pipe (measured on
+// GB300: 4096-hidden layer T = 16 518 vs 526 us, T = 64 1641 vs 789 us;
+// 7168-hidden T = 8 742 vs 1045 us)
 constexpr int kMxMaxTokens = 64;
+constexpr int kMxDecodeTokens = 16;
 constexpr int kMaxDevices = 64;
 
 struct Shape {
@@ -220,8 +225,10 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
     const int n_assign = T * k;
     int path = opts ? opts->path : MOE_PATH_AUTO;
     if (path == MOE_PATH_AUTO) {
-        const int dmax = (opts && opts->decode_max_tokens) ? opts->decode_max_tokens : kDefaultDecodeMaxTokens;
-        path = (T <= dmax || !moe::gemm_supported(H, I, E)) ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
+        const int dlim = (opts && opts->decode_max_tokens) ? opts->decode_max_tokens
+                         : mx                                ? kMxDecodeTokens
+                                                             : kDefaultDecodeMaxTokens;
+        path = (T <= dlim || !moe::gemm_supported(H, I, E)) ? MOE_PATH_DECODE : MOE_PATH_GROUPED;
     }
     if (path == MOE_PATH_GROUPED && !moe::gemm_supported(H, I, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
     const int gu_warps = (opts && opts->gate_up_warps) ? opts->gate_up_warps : kDefaultWarps;
@@ -240,7 +247,7 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (mx && (path != MOE_PATH_DECODE || T > kMxMaxTokens)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (mx && path == MOE_PATH_DECODE && T > kMxMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (path == MOE_PATH_DECODE && (wr ? moe::decode_fused_router_supported(T, H, I, E, k, dev->n_sm)
                                        : moe::decode_fused_supported(T, H, I, E, k, dev->n_sm, mx != nullptr))) {
         // a few tokens: one cooperative kernel that routes them, streams both
@@ -284,10 +291,17 @@ int run_forward(const void *x, const float *logits, const void *wgu, const void 
         auto *z = (float *)(ws + L.z);
         MOE_TRY(stg.done(moe::launch_sort(idx, n_assign, E, moe::kGemmChunkMax, offs, perm, pos, uexp, ucount,
                                           chunks, nchunks, stream)));
-        MOE_TRY(stg.done(moe::launch_gemm_gate_up(x, perm, k, wgu, chunks, nchunks, offs, n_assign, H, I, E,
-                                                  act_hi, act_lo, gemm_ctas, stream)));
-        MOE_TRY(stg.done(moe::launch_gemm_down(act_hi, act_lo, wd, chunks, nchunks, offs, n_assign, H, I, E, z,
-                                               gemm_ctas, stream)));
+        if (mx) {
+            MOE_TRY(stg.done(moe::launch_gemm_gate_up_mx(x, perm, k, mx->gq, mx->gs, chunks, nchunks, offs, n_assign,
+                                                         H, I, E, act_hi, act_lo, gemm_ctas, stream)));
+            MOE_TRY(stg.done(moe::launch_gemm_down_mx(act_hi, act_lo, mx->dq, mx->ds, chunks, nchunks, offs,
+                                                      n_assign, H, I, E, z, gemm_ctas, stream)));
+        } else {
+            MOE_TRY(stg.done(moe::launch_gemm_gate_up(x, perm, k, wgu, chunks, nchunks, offs, n_assign, H, I, E,
+                                                      act_hi, act_lo, gemm_ctas, stream)));
+            MOE_TRY(stg.done(moe::launch_gemm_down(act_hi, act_lo, wd, chunks, nchunks, offs, n_assign, H, I, E, z,
+                                                   gemm_ctas, stream)));
+        }
         MOE_TRY(stg.done(moe::launch_combine(z, w, pos, T, H, k, out, dev->n_sm, stream)));
     }
     if (opts) {
@@ -550,20 +564,12 @@ int moe_ffn_forward_mxfp8(const void *x_bf16, const float *router_logits_f32, co
         return MOE_ERR_INVALID_ARG;
     if ((topk_idx_out && !aligned16(topk_idx_out)) || (topk_w_out && !aligned16(topk_w_out)))
         return MOE_ERR_INVALID_ARG;
-    if (opts && opts->path != MOE_PATH_AUTO && opts->path != MOE_PATH_DECODE) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!workspace || ((uintptr_t)workspace & 255)) return MOE_ERR_INVALID_ARG;
     const Layout L = make_layout(s);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    moe_ffn_opts o = opts ? *opts : moe_ffn_opts{};
-    o.path = MOE_PATH_DECODE;
     const moe::FusedMx mx{w_gate_up_e4m3, w_gate_up_scale, w_down_e4m3, w_down_scale};
-    st = run_forward(x_bf16, router_logits_f32, nullptr, nullptr, s, out_f32, (char *)workspace, L, true, topk_idx_out,
-                     topk_w_out, &o, stream, nullptr, nullptr, nullptr, &mx);
-    if (opts) {
-        opts->n_stages = o.n_stages;
-        opts->path_taken = o.path_taken;
-    }
-    return st;
+    return run_forward(x_bf16, router_logits_f32, nullptr, nullptr, s, out_f32, (char *)workspace, L, true,
+                       topk_idx_out, topk_w_out, opts, stream, nullptr, nullptr, nullptr, &mx);
 }
 
 int moe_ffn_forward(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,

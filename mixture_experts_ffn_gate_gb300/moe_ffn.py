@@ -308,7 +308,9 @@ def mx_scale_bytes(K: int) -> int:
 def moe_ffn_forward_mxfp8(x, logits, w_gate_up_q, w_gate_up_s, w_down_q, w_down_s, k: int, out=None,
                           workspace=None, topk_idx=None, topk_w=None, opts: moe_ffn_opts | None = None,
                           stream=None):
-    """The layer with MXFP8 expert weights (one to four tokens): x bf16 [T,H],
+    """The layer with MXFP8 expert weights (fused decode kernel up to four
+    tokens, tensor-core grouped path beyond; MOE_PATH_DECODE forces the
+    general decode kernels, up to 64 tokens): x bf16 [T,H],
     logits f32 [T,E], E4M3 codes uint8 w_gate_up_q [E,2I,H] / w_down_q
     [E,H,I], E8M0 scales uint8 w_gate_up_s [E,2I,mx_scale_bytes(H)] /
     w_down_s [E,H,mx_scale_bytes(I)].  Returns out f32 [T,H]."""

@@ -1,11 +1,13 @@
 """The layer with MXFP8 expert weights (moe_ffn_forward_mxfp8: the fused
-decode kernel's MX instantiation for T <= 4, the general decode kernels'
-for larger T) against the oracle on the exactly
-dequantised weights: routing indices bit-exact, routing weights and outputs
-within the parity tolerance (tests/gpu_util.py), at small ragged shapes, at
-the decode workloads' full sizes, with signed zeros, subnormal codes and
-spread scales, across calls on one workspace (both act exchanges) and in
-CUDA-graph replays; plus the argument checks."""
+decode kernel's MX instantiation for T <= 4, the general decode kernels' MX
+instantiations up to 16 tokens (and up to 64 when MOE_PATH_DECODE is
+forced), the tensor-core grouped GEMMs' MX kinds beyond) against the oracle on the exactly dequantised
+weights: routing indices bit-exact, routing weights and outputs within the
+parity tolerance (tests/gpu_util.py), at small ragged shapes, at the decode
+workloads' full sizes, with signed zeros, subnormal codes and spread scales,
+across calls on one workspace (both act exchanges) and in CUDA-graph replays,
+bit-identical across runs and grid widths on the grouped path; plus the
+argument checks."""
 import numpy as np
 import pytest
 import torch
@@ -32,14 +34,20 @@ def _layer(wl, T, call=0):
     return x.cuda(), L.cuda(), gq, gs, dq, ds
 
 
-def _run(x, L, gq, gs, dq, ds, k, workspace=None, opts=None):
+def _run(x, L, gq, gs, dq, ds, k, workspace=None, opts=None, path=None):
     T = x.shape[0]
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, k), dtype=torch.float32, device="cuda")
     o = opts or m.moe_ffn_opts()
+    if path is not None:
+        o.path = path
     out = m.moe_ffn_forward_mxfp8(x, L, gq, gs, dq, ds, k, topk_idx=idx, topk_w=w, opts=o, workspace=workspace)
     torch.cuda.synchronize()
-    assert o.path_taken == (m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_DECODE)
+    if path == m.MOE_PATH_DECODE:
+        assert o.path_taken in (m.MOE_PATH_DECODE_FUSED, m.MOE_PATH_DECODE)
+    else:
+        want = m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_DECODE if T <= 16 else m.MOE_PATH_GROUPED
+        assert o.path_taken == (m.MOE_PATH_GROUPED if path == m.MOE_PATH_GROUPED else want)
     return out.cpu(), idx.cpu(), w.cpu()
 
 
@@ -57,11 +65,13 @@ def _oracle(x, L, gq, gs, dq, ds, k):
 
 # (T, H, I, E, k, bias variance): ragged lane coverage (H or I not a
 # multiple of 512), scale rows with padding (I = 192: 6 scales in 16 bytes),
-# many experts with k = 32, one to four tokens (fused kernel) and 5 to 64
-# (general decode kernels, incl. several token passes per expert)
+# many experts with k = 32, one to four tokens (fused kernel) and more
+# (grouped path: ragged 128-row tiles with H = 576 or I = 192 / 320, experts
+# with several 64-row chunks, a skewed load, one expert)
 SMALL = [(1, 256, 128, 8, 2, 0.0), (2, 576, 192, 16, 4, 0.5), (3, 1024, 320, 32, 8, 1.0),
          (4, 512, 192, 12, 3, 0.5), (1, 64, 64, 1024, 32, 1.0), (4, 2048, 768, 128, 8, 0.0),
-         (5, 576, 192, 16, 4, 0.5), (13, 1024, 320, 8, 3, 1.0), (64, 512, 256, 12, 2, 4.0)]
+         (5, 576, 192, 16, 4, 0.5), (13, 1024, 320, 8, 3, 1.0), (64, 512, 256, 12, 2, 4.0),
+         (300, 256, 128, 4, 2, 0.0), (97, 640, 320, 24, 5, 2.0), (40, 128, 64, 1, 1, 0.0)]
 
 
 @pytest.mark.parametrize("T,H,I,E,k,bv", SMALL)
@@ -72,9 +82,30 @@ def test_mxfp8_parity_small(T, H, I, E, k, bv):
     gu.assert_accepted(out, idx, w, *_oracle(x, L, gq, gs, dq, ds, k), what=f"mxfp8 {T, H, I, E, k}")
 
 
+@pytest.mark.parametrize("T,H,I,E,k,bv", [(5, 576, 192, 16, 4, 0.5), (13, 1024, 320, 8, 3, 1.0),
+                                          (64, 512, 256, 12, 2, 4.0)])
+def test_mxfp8_parity_general_decode(T, H, I, E, k, bv):
+    """The general decode kernels' MX instantiations (MOE_PATH_DECODE)."""
+    wl = gu.custom(T, H, I, E, k, bv, name="mx_small")
+    x, L, gq, gs, dq, ds = _layer(wl, T)
+    out, idx, w = _run(x, L, gq, gs, dq, ds, k, path=m.MOE_PATH_DECODE)
+    gu.assert_accepted(out, idx, w, *_oracle(x, L, gq, gs, dq, ds, k), what=f"mxfp8 decode {T, H, I, E, k}")
+
+
+def test_mxfp8_grouped_bit_identical_across_runs_and_widths():
+    wl = gu.custom(200, 512, 256, 16, 4, 1.0, name="mx_det")
+    x, L, gq, gs, dq, ds = _layer(wl, 200)
+    ref = _run(x, L, gq, gs, dq, ds, 4)[0]
+    for ctas in (0, 37, 1):
+        o = m.moe_ffn_opts()
+        o.gemm_ctas = ctas
+        assert torch.equal(_run(x, L, gq, gs, dq, ds, 4, opts=o)[0], ref), ctas
+
+
 @pytest.mark.parametrize("name,T", [("decode_h2048_i768_e128_k8", 1), ("decode_h2048_i768_e128_k8", 2),
                                     ("decode_h4096_i1536_e128_k8_bias", 4), ("decode_h7168_i2048_e384_k8_bias", 1),
-                                    ("decode_h4096_i1536_e128_k8_bias", 16), ("decode_h7168_i2048_e384_k8_bias", 8)])
+                                    ("decode_h4096_i1536_e128_k8_bias", 16), ("decode_h7168_i2048_e384_k8_bias", 8),
+                                    ("decode_h4096_i1536_e128_k8_bias", 64), ("decode_h7168_i2048_e384_k8_bias", 32)])
 def test_mxfp8_parity_full_size(name, T):
     wl = synth.WORKLOADS[name]
     x, L, gq, gs, dq, ds = _layer(wl, T, call=7)
@@ -160,10 +191,19 @@ def test_mxfp8_argument_checks():
     Lb = torch.cat([L] * 33)
     wsb = m.new_workspace(65, H, I, E, k)
     outb = torch.empty((66, H), dtype=torch.float32, device="cuda")
+    o = m.moe_ffn_opts()
+    o.path = m.MOE_PATH_DECODE   # the general decode kernels take at most 64 tokens
     assert lib.moe_ffn_forward_mxfp8(p(xb), p(Lb), p(gq), p(gs), p(dq), p(ds), 65, H, I, E, k, p(outb), p(wsb),
-                                     wsb.numel(), None, None, None, None) == m.MOE_ERR_UNSUPPORTED_SHAPE   # T > 64
+                                     wsb.numel(), None, None, m.ctypes.byref(o), None) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    o = m.moe_ffn_opts()         # the grouped path takes them
+    assert lib.moe_ffn_forward_mxfp8(p(xb), p(Lb), p(gq), p(gs), p(dq), p(ds), 65, H, I, E, k, p(outb), p(wsb),
+                                     wsb.numel(), None, None, m.ctypes.byref(o), None) == m.MOE_OK
+    torch.cuda.synchronize()
+    assert o.path_taken == m.MOE_PATH_GROUPED
     o = m.moe_ffn_opts()
     o.path = m.MOE_PATH_GROUPED
-    assert call(o=m.ctypes.byref(o)) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert call(o=m.ctypes.byref(o)) == m.MOE_OK
+    torch.cuda.synchronize()
+    assert o.path_taken == m.MOE_PATH_GROUPED
     assert lib.moe_ffn_forward_mxfp8(p(x), p(L), p(gq), p(gs), p(dq), p(ds), 0, H, I, E, k, p(out), p(ws), nbytes,
                                      None, None, None, None) == m.MOE_OK                        # T = 0
