@@ -69,33 +69,43 @@ __device__ __forceinline__ float e8m0_scale(uint32_t s)
     return __uint_as_float(s ? s << 23 : 0x00400000u);
 }
 
-// The factors of e4m3x2_to_bf16x2_scaled for the E8M0 scale s: the pair's
-// values times 2^-112 are multiplied by f.x then f.y, together 2^(s - 15):
-// 2^(s - 15) and 1 when that is a BF16 number (s <= 142), else 2^112 and
-// 2^(s - 127).  Both are powers of two, so the multiplies are exact whenever
-// the result is a BF16 number.
+// The factors of e4m3x4_to_bf16x2_scaled for the E8M0 scale s, each a BF16
+// power of two repeated in both halves: the values times 2^-112 are
+// multiplied by 2^(min(s, 127) - 15) and then by 2^(max(s, 127) - 127),
+// together 2^(s - 15), each factor a BF16 number for every s.  Powers of two,
+// so the multiplies are exact whenever the result is a BF16 number.
 __device__ __forceinline__ uint2 mx_bf16_factors(uint32_t s)
 {
-    const float a = __uint_as_float((s <= 142u ? s + 112u : 239u) << 23);
-    const float b = __uint_as_float((s <= 142u ? 127u : s) << 23);
-    const __nv_bfloat162 fa = __float2bfloat162_rn(a), fb = __float2bfloat162_rn(b);
-    return make_uint2(*reinterpret_cast<const uint32_t *>(&fa), *reinterpret_cast<const uint32_t *>(&fb));
+    const uint32_t a = (min(s, 127u) + 112u) << 7, b = max(s, 127u) << 7;
+    return make_uint2(a * 0x00010001u, b * 0x00010001u);
 }
 
-// Two E4M3 codes (low byte first) times 2^(s - 127) as a BF16 pair, given
-// f = mx_bf16_factors(s); exact whenever the products are BF16 numbers.  The
-// F16 pair of the codes (exact) with its signs cleared and shifted right by
-// 3, the signs put back, is the BF16 pair of the values times 2^-112 (E4M3
-// values are F16 normals or zero with at most 3 mantissa bits: the exponent
-// field moves into BF16's, the mantissa's top 7 bits into BF16's).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two_codes, uint2 f)
+// Four E4M3 codes (byte j = element j) times 2^(s - 127) as two BF16 pairs
+// (elements 0-1, then 2-3), given f = mx_bf16_factors(s); exact whenever the
+// products are BF16 numbers.  The F16 pair of two codes (exact) with its
+// signs cleared and shifted right by 3, the signs put back, is the BF16 pair
+// of the values times 2^-112 (E4M3 values are F16 normals or zero with at
+// most 3 mantissa bits: the exponent field moves into BF16's, the
+// mantissa's top 7 bits into BF16's); the two multiplies by f finish it.
+__device__ __forceinline__ void e4m3x4_to_bf16x2_scaled(uint32_t four_codes, uint2 f, uint32_t &lo, uint32_t &hi)
 {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
-    const uint32_t x = (uint32_t)h.x | ((uint32_t)h.y << 16);
-    const uint32_t t = ((x & 0x7fff7fffu) >> 3) | (x & 0x80008000u);
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&t);
-    b = __hmul2(__hmul2(b, *reinterpret_cast<const __nv_bfloat162 *>(&f.x)), *reinterpret_cast<const __nv_bfloat162 *>(&f.y));
-    return *reinterpret_cast<const uint32_t *>(&b);
+    uint32_t a, b;
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(a), "=r"(b)
+        : "r"(four_codes));
+    a = ((a & 0x7fff7fffu) >> 3) | (a & 0x80008000u);
+    b = ((b & 0x7fff7fffu) >> 3) | (b & 0x80008000u);
+    asm("mul.rn.bf16x2 %0, %0, %2;\n\t"
+        "mul.rn.bf16x2 %0, %0, %3;\n\t"
+        "mul.rn.bf16x2 %1, %1, %2;\n\t"
+        "mul.rn.bf16x2 %1, %1, %3;"
+        : "+r"(a), "+r"(b)
+        : "r"(f.x), "r"(f.y));
+    lo = a;
+    hi = b;
 }
 
 // 16 E4M3 codes (byte j = element j) to their values in FP32, exactly

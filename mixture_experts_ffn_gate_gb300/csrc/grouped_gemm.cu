@@ -509,6 +509,15 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
         constexpr int NC = 32 * C::CONV_WARPS, NP = MT * BM * 4 / (NC > 0 ? NC : 1);
         static_assert(!MX || NP * NC == MT * BM * 4, "whole pieces per converter thread");
         const int ct = threadIdx.x - 32 * C::FIRST_CONV;
+        // each piece's offsets in a stage's code buffer and BF16 tile
+        uint32_t src_off[NP], dst_off0[NP], dst_off1[NP];
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+            const int p = ct + NC * j, c = p & 3, r = (p >> 2) & 127, t = p >> 9;
+            src_off[j] = t * C::CODE_TILE + r * BK + c * 16;
+            dst_off0[j] = t * C::A_TILE + r * 128 + (((2 * c) ^ (r & 7)) << 4);
+            dst_off1[j] = t * C::A_TILE + r * 128 + (((2 * c + 1) ^ (r & 7)) << 4);
+        }
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -550,20 +559,14 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 uint8_t *a = sA + stage * C::A_BYTES;
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
-                    const int p = ct + NC * j, c = p & 3, r = (p >> 2) & 127, t = p >> 9;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(code + t * C::CODE_TILE + r * BK + c * 16);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(code + src_off[j]);
                     const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
                     const uint2 f = mx_bf16_factors(sc[j]);
                     uint32_t w[8];
 #pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        w[2 * q2] = e4m3x2_to_bf16x2_scaled(cw[q2], f);
-                        w[2 * q2 + 1] = e4m3x2_to_bf16x2_scaled(cw[q2] >> 16, f);
-                    }
-                    uint8_t *row = a + t * C::A_TILE + r * 128;
-                    *reinterpret_cast<uint4 *>(row + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ (r & 7)) << 4)) =
-                        make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int q2 = 0; q2 < 4; ++q2) e4m3x4_to_bf16x2_scaled(cw[q2], f, w[2 * q2], w[2 * q2 + 1]);
+                    *reinterpret_cast<uint4 *>(a + dst_off0[j]) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(a + dst_off1[j]) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
                 ptx::fence_proxy_async_smem();  // the MMA (async proxy) reads what these stores wrote
                 __syncwarp();
