@@ -232,7 +232,7 @@ int moe_ffn_forward_router(const void *x_bf16, const void *w_router_bf16,
  * All device pointers 16-byte aligned; the workspace is moe_ffn_forward_ex's
  * (at least moe_ffn_workspace_bytes, same state rules).  Paths (path_taken
  * tells which): AUTO takes the fused decode kernel for T <= 4 where it fits,
- * the general decode kernels up to T = 16 (opts->decode_max_tokens moves
+ * the general decode kernels up to T = 8 (opts->decode_max_tokens moves
  * this bound) and the grouped tensor-core GEMMs beyond, which load the E4M3
  * code tiles and convert
  * them to exact BF16 tiles (each weight a BF16 number whenever its value is

@@ -18,12 +18,12 @@ constexpr int kDefaultDecodeMaxTokens = 4;
 constexpr int kDefaultWarps = 8;
 // MXFP8 weights on the general decode kernels (CUDA cores): calls of up to
 // kMxMaxTokens tokens when the caller forces the decode path.  AUTO takes
-// them up to kMxDecodeTokens and the tensor-core grouped path beyond, whose
-// in-kernel code conversion is bound by the SMs' integer pipe (measured on
-// GB300: 4096-hidden layer T = 16 518 vs 526 us, T = 64 1641 vs 789 us;
-// 7168-hidden T = 8 742 vs 1045 us)
+// them up to kMxDecodeTokens and the tensor-core grouped path beyond
+// (measured on GB300: 2048-hidden layer T = 8 119 vs 134 us, 7168-hidden
+// T = 8 735 vs 802 us; 4096-hidden T = 16 521 vs 408 us, T = 32 921 vs
+// 508 us)
 constexpr int kMxMaxTokens = 64;
-constexpr int kMxDecodeTokens = 16;
+constexpr int kMxDecodeTokens = 8;
 constexpr int kMaxDevices = 64;
 
 struct Shape {

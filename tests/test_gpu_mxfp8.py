@@ -1,6 +1,6 @@
 """The layer with MXFP8 expert weights (moe_ffn_forward_mxfp8: the fused
 decode kernel's MX instantiation for T <= 4, the general decode kernels' MX
-instantiations up to 16 tokens (and up to 64 when MOE_PATH_DECODE is
+instantiations up to 8 tokens (and up to 64 when MOE_PATH_DECODE is
 forced), the tensor-core grouped GEMMs' MX kinds beyond) against the oracle on the exactly dequantised
 weights: routing indices bit-exact, routing weights and outputs within the
 parity tolerance (tests/gpu_util.py), at small ragged shapes, at the decode
@@ -46,7 +46,7 @@ def _run(x, L, gq, gs, dq, ds, k, workspace=None, opts=None, path=None):
     if path == m.MOE_PATH_DECODE:
         assert o.path_taken in (m.MOE_PATH_DECODE_FUSED, m.MOE_PATH_DECODE)
     else:
-        want = m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_DECODE if T <= 16 else m.MOE_PATH_GROUPED
+        want = m.MOE_PATH_DECODE_FUSED if T <= 4 else m.MOE_PATH_DECODE if T <= 8 else m.MOE_PATH_GROUPED
         assert o.path_taken == (m.MOE_PATH_GROUPED if path == m.MOE_PATH_GROUPED else want)
     return out.cpu(), idx.cpu(), w.cpu()
 
