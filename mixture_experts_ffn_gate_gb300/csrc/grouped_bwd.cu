@@ -38,10 +38,10 @@
 // a ring of stages, warp 1 the MMAs into one of two 256-column TMEM
 // accumulators, warps 2-9 drain the other one (two warps per TMEM lane
 // quarter, 128 columns each).  The gradients are written by TMA tensor
-// stores: each epilogue warp places a 32-row x 32-column FP32 block in one
-// of its two 128-byte-swizzled staging buffers and hands it to the TMA
-// engine, so every row leaves as one 128-byte line (a warp's own stores,
-// one row per lane, would split into 32 partial sectors).  Every mbarrier
+// stores: each epilogue warp places a 32-row x 32-column FP32 block in its
+// 128-byte-swizzled staging buffer and hands it to the TMA engine, so every
+// row leaves as one 128-byte line (a warp's own stores, one row per lane,
+// would split into 32 partial sectors).  Every mbarrier
 // wait is bounded; on time-out the CTA raises a bit in the device fault
 // word, drains what it has in flight (bounded) and frees its TMEM.
 #include <cuda.h>
@@ -87,8 +87,11 @@ struct WCfg {
     static constexpr int A_BYTES = 2 * A_HALF;
     static constexpr int B_BYTES = (B_PAIR ? 2 : 1) * B_HALF;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = B_PAIR ? 3 : 4;
-    static constexpr int STAGING = kEpiWarps * 2 * OUT_BLOCK;   // two blocks per epilogue warp
+    static constexpr int STAGES = B_PAIR ? 4 : 5;
+    // one staged block per epilogue warp: the shared memory serves the
+    // operand stages better (measured: two blocks per warp and one stage
+    // fewer, 2.62 / 5.00 ms at T = 2048; one block, 2.53 / 4.92 ms)
+    static constexpr int STAGING = kEpiWarps * OUT_BLOCK;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STAGING + 256;
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -267,10 +270,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
         // l of a block; its 16-byte piece j goes to (j ^ (l % 8)) * 16 of the
         // row's 128 bytes in the staging buffer (the tensor map's swizzle).
         const int q = warp & 3, half = (warp - 2) >> 2;
-        uint8_t *stg = staging + (warp - 2) * 2 * OUT_BLOCK;
-        int buf = 0;
+        uint8_t *stg = staging + (warp - 2) * OUT_BLOCK;
         auto put_block = [&](const uint32_t (&r)[32], int e, int row0, int col0) {
-            uint8_t *b = stg + buf * OUT_BLOCK + lane * 128;
+            uint8_t *b = stg + lane * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 *reinterpret_cast<uint4 *>(b + ((j ^ (lane & 7)) << 4)) =
@@ -279,12 +281,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 // rows past M and columns past N are not written by the store
-                ptx::tma_store_3d(&tmOut, stg + buf * OUT_BLOCK, col0, row0, e);
+                ptx::tma_store_3d(&tmOut, stg, col0, row0, e);
                 ptx::bulk_commit_group();
-                ptx::bulk_wait_group_read<1>();   // the other buffer is free again
+                ptx::bulk_wait_group_read<0>();   // the buffer is free again once the store has read it
             }
             __syncwarp();
-            buf ^= 1;
         };
         int li = 0;
         for (int i = blockIdx.x; i < total; i += gridDim.x) {
