@@ -59,19 +59,36 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// The same test with a suspend-time hint: a thread whose phase is not yet
+// complete sleeps until it completes or about kSuspendNs pass, instead of
+// returning at once (a spinning warp takes issue slots from the warps that
+// share its SM sub-partition).
+constexpr uint32_t kSuspendNs = 100000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, for at most
-// limit_ns.  Returns false on time-out or when *abort becomes non-zero.
+// limit_ns (checked each time the thread wakes).  Returns false on time-out
+// or when *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, const volatile int *abort,
                                                   uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t spin = 0;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 63) == 63) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
