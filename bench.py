@@ -697,13 +697,16 @@ def supplementary_rows(args, dev, peaks, skip):
         routers = [synth.make_router(wl, device=dev, layer=r) for r in range(R)] if how == "router" else None
         bias = synth.make_bias(wl)
         for T in Ts:
-            run = Measure(wl, T, dev, args.steps, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
+            # the training-size rows take ms per call: at most 100 timed steps
+            # each, so that the default run (2000 steps) stays within minutes
+            K = min(args.steps, 100) if T >= 2048 else args.steps
+            run = Measure(wl, T, dev, K, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
                 args.path] if how != "backward" else 0, layers, bias, 0, args.eager, routers=routers,
                 mx=how == "mxfp8", backward=how == "backward")
             with ClockSampler(dev.index or 0) as clocks:
                 total_ms, _ = run.timed(1)
                 kern = run.stages()
-            row = {"workload": name, "T": T, "layers": R, "warmup": run.warm_steps}
+            row = {"workload": name, "T": T, "layers": R, "steps": K, "warmup": run.warm_steps}
             if how == "router":
                 row["entry"] = ("moe_ffn_forward_router: router weights W_r [E,H] ~ N(0,1/H) and the "
                                 "workload's bias passed instead of logits; the projection runs inside the call")
