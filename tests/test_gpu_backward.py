@@ -75,6 +75,7 @@ SMALL = [
     (9, 128, 128, 1, 1, 0.0),      # one expert
     (50, 384, 256, 16, 8, 1.0),
     (17, 192, 320, 64, 32, 0.5),   # k = 32, many experts
+    (64, 64, 64, 1024, 4, 1.0),    # 1024 experts: mostly one row each, 15 pad rows each, ~800 untouched
 ]
 
 

@@ -113,8 +113,13 @@ def test_mxfp8_parity_full_size(name, T):
     gu.assert_accepted(out, idx, w, *_oracle(x, L, gq, gs, dq, ds, wl.k), what=f"mxfp8 {name} T={T}")
 
 
-def test_mxfp8_signed_zeros_subnormal_codes_and_spread_scales():
-    T, H, I, E, k = 3, 512, 256, 16, 4
+@pytest.mark.parametrize("T,spread", [(3, 12), (40, 12), (40, 40)])
+def test_mxfp8_signed_zeros_subnormal_codes_and_spread_scales(T, spread):
+    """+-0 and subnormal codes, scales moved by up to +-spread: T = 3 takes
+    the fused kernel, T = 40 the grouped path, whose conversion multiplies by
+    2^(min(s, 127) - 15) and 2^(max(s, 127) - 127) (the spread of 40 takes
+    scales past 142, where 2^(s - 15) itself is no BF16 number)."""
+    H, I, E, k = 512, 256, 16, 4
     wl = gu.custom(T, H, I, E, k, 0.5, name="mx_edges")
     x, L, gq, gs, dq, ds = _layer(wl, T)
     g = torch.Generator(device="cpu").manual_seed(11)
@@ -126,10 +131,12 @@ def test_mxfp8_signed_zeros_subnormal_codes_and_spread_scales():
         codes = torch.where(r % 4 == 0, sub, codes)
         q.copy_(codes.to(torch.uint8).cuda())
     for s in (gs, ds):
-        r = torch.randint(-12, 13, s.shape, generator=g, dtype=torch.int32)
+        r = torch.randint(-spread, spread + 1, s.shape, generator=g, dtype=torch.int32)
         s.copy_((s.cpu().to(torch.int32) + r).clamp(1, 254).to(torch.uint8).cuda())
+    if spread > 30:
+        assert int(gs.max()) > 142 or int(ds.max()) > 142
     out, idx, w = _run(x, L, gq, gs, dq, ds, k)
-    gu.assert_accepted(out, idx, w, *_oracle(x, L, gq, gs, dq, ds, k), what="mxfp8 edge codes")
+    gu.assert_accepted(out, idx, w, *_oracle(x, L, gq, gs, dq, ds, k), what=f"mxfp8 edge codes T={T} spread={spread}")
 
 
 def test_mxfp8_workspace_reuse_exchanges_and_graph_replay():
