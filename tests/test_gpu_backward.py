@@ -6,8 +6,10 @@ forward output: ||g - g_ref||_2 / ||g_ref||_2 <= 1e-4 and max |g - g_ref| <=
 1e-3 * rms(g_ref); an all-zero reference must be matched exactly (untouched
 experts, one selected expert's logit gradient).  Shapes span ragged tiles
 (I or H not a multiple of 128 or 256), experts with several 64-row chunks,
-one expert, k = 32, skewed routing, and the training-size layer (sampled
-tokens and experts, the oracle fed only what they need).  Plus: bit-identical
+one expert, k = 32, skewed routing, tied and signed-zero logits, and the
+training-size layer (sampled tokens and experts, the oracle fed only what
+they need).  Plus: exact linearity in dout (2 dout gives twice every
+gradient bit for bit, dout = 0 gives zeros), bit-identical
 results across runs and launch widths, T = 0, a CUDA graph replay, a
 workspace shared with the fused decode kernel's forward calls, and the
 stage events."""
@@ -101,6 +103,41 @@ def test_backward_parity_mid_size():
     ref = _oracle(x, L, wgu, wd, dout, 4)
     for n in NAMES:
         _accept(got[n], ref[n], f"{n} mid")
+
+
+def test_backward_is_exactly_linear_in_dout():
+    """Every gradient is linear in dout, and every step of the path (the
+    hi/lo splits, the MMAs' products and FP32 sums, the SwiGLU chain rule,
+    the logit gradient) commutes with a power-of-two scale: 2 dout must give
+    twice each gradient bit for bit, and dout = 0 exactly zero gradients."""
+    wl = gu.custom(70, 320, 192, 12, 3, 1.0, name="bwd_linear")
+    x, L, wgu, wd, dout = _layer(wl, 70, call=4)
+    a = _gpu(x, L, wgu, wd, dout, 3)
+    b = _gpu(x, L, wgu, wd, 2.0 * dout, 3)
+    for n in NAMES:
+        assert torch.equal(b[n], 2.0 * a[n]), n
+    z = _gpu(x, L, wgu, wd, torch.zeros_like(dout), 3)
+    for n in NAMES:
+        assert torch.count_nonzero(z[n]) == 0, n
+
+
+def test_backward_ties_and_signed_zero():
+    """Logits drawn from {-1, -0.0, +0.0, 1}: the selection follows the
+    lower-index rule on ties (-0.0 == +0.0), and the logit gradient lands on
+    the experts the oracle selects."""
+    T, H, I, E, k = 48, 256, 128, 16, 5
+    wl = gu.custom(T, H, I, E, k, name="bwd_ties")
+    x, _, wgu, wd, dout = _layer(wl, T, call=6)
+    g = torch.Generator().manual_seed(11)
+    vals = torch.tensor([-1.0, -0.0, 0.0, 1.0])
+    L = vals[torch.randint(0, 4, (T, E), generator=g)].contiguous().cuda()
+    got = _gpu(x, L, wgu, wd, dout, k)
+    ref = _oracle(x, L, wgu, wd, dout, k)
+    for n in NAMES:
+        _accept(got[n], ref[n], f"{n} ties")
+    mask = np.zeros((T, E), bool)
+    mask[np.arange(T)[:, None], ref["idx"]] = True
+    assert torch.count_nonzero(got["dlogits"].cpu()[torch.as_tensor(~mask)]) == 0
 
 
 def test_backward_bit_identical_across_runs_and_widths():
