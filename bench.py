@@ -40,6 +40,9 @@ at 1 + 1/32 per weight; T > 4 takes the grouped tensor-core path).  One row
 ("entry": moe_ffn_backward) runs the backward pass of the T=2048
 training-size layer (dout ~ N(0,1) FP32 per call; all four gradients written
 every call), with its own byte model (backward_bytes) and 16 H I T k flops.
+One row ("entry": moe_ffn_forward_train + moe_ffn_backward_train) runs a
+training step of that layer: the forward pass keeping g, u and the routing,
+then the backward pass from them (byte model train_bytes, 18 H I T k flops).
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -105,6 +108,9 @@ def parse():
     p.add_argument("--backward", action="store_true",
                    help="time the backward pass (moe_ffn_backward) as the step instead of the forward pass "
                         "(no e2e or CPU-baseline figures; e.g. with --E for a profiling-size variant)")
+    p.add_argument("--train", action="store_true",
+                   help="time a training step (moe_ffn_forward_train, then moe_ffn_backward_train) as the step "
+                        "(no e2e or CPU-baseline figures)")
     p.add_argument("--no-supplementary", action="store_true",
                    help="omit the other configurations' rows (measured after the headline line)")
     p.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
@@ -271,6 +277,25 @@ def backward_kernel_bytes(kernel, wl, T, U, k):
     }.get(kernel)
 
 
+def train_bytes(wl, T, U):
+    """Per-step algorithmic HBM bytes of the training pair: the forward
+    call's (algorithmic_bytes) plus g and u written for the backward, plus
+    the backward call's (backward_bytes) without the recomputation's read of
+    W_gate_up, which the pair does not repeat."""
+    return (algorithmic_bytes(wl, T, U) + 2 * T * wl.k * wl.I * 4 + backward_bytes(wl, T, U)
+            - U * 2 * wl.I * wl.H * 2)
+
+
+def train_kernel_bytes(kernel, wl, T, U, k):
+    """Algorithmic bytes of one launch of a kernel of the training pair
+    (stage names "fwd:..." and "bwd:...")."""
+    side, _, name = kernel.partition(":")
+    if side == "fwd":
+        b = kernel_bytes(name, wl, T, U, k)
+        return b + 2 * T * k * wl.I * 4 if name == "gemm_gate_up" else b
+    return backward_kernel_bytes(name, wl, T, U, k)
+
+
 def reference_arm(args, wl, T):
     """The FP64 oracle on the host cores, on a bounded sample of the workload."""
     import numpy as np
@@ -401,6 +426,7 @@ SUPPLEMENTARY = [
     ("decode_h7168_i2048_e384_k8_bias", (1, 8, 32)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias", (2048,)),
     ("fwd_t2048_h6144_i2048_e256_k8_bias+backward", (2048,)),
+    ("fwd_t2048_h6144_i2048_e256_k8_bias+train", (2048,)),
 ]
 
 
@@ -420,7 +446,7 @@ class Measure:
     kernels; summary() gives the figures of one line."""
 
     def __init__(self, wl, T, dev, K, W, path_code, layers, bias, rank, eager, routers=None, mx=False,
-                 backward=False):
+                 backward=False, train=False):
         import torch
         from mixture_experts_ffn_gate_gb300 import moe_ffn as m
         from mixture_experts_ffn_gate_gb300 import synth
@@ -439,14 +465,18 @@ class Measure:
         # backward: the steps are moe_ffn_backward calls, each with its own
         # upstream gradient, writing all four gradients
         self.backward = backward
-        batch_bytes = T * (wl.H * 2 + wl.E * 4 + (wl.H * 4 if backward else 0))
+        # train: a step is moe_ffn_forward_train and then moe_ffn_backward_train
+        # on one state buffer (a training step of the layer)
+        self.train = train
+        batch_bytes = T * (wl.H * 2 + wl.E * 4 + (wl.H * 4 if backward or train else 0))
         self.NB = max(1, min(W + K, 256, int(BATCH_MEM_CAP // max(batch_bytes, 1))))
         calls = rank_calls(rank, W, K)   # rank r processes its own calls of the token stream
         self.batches = [synth.make_tokens(wl, T, call=calls[i], device=dev, bias=bias)
                         for i in range(self.NB)]
-        if backward:
+        if backward or train:
             self.douts = [synth.make_dout(wl, T, call=calls[i], device=dev) for i in range(self.NB)]
-            self.ws = m.new_backward_workspace(T, wl.H, wl.I, wl.E, wl.k, device=dev)
+            self.ws = (m.new_train_state if train else m.new_backward_workspace)(T, wl.H, wl.I, wl.E, wl.k,
+                                                                                  device=dev)
             self.grads = (torch.empty((T, wl.H), dtype=torch.float32, device=dev),
                           torch.empty((T, wl.E), dtype=torch.float32, device=dev),
                           torch.empty((wl.E, 2 * wl.I, wl.H), dtype=torch.float32, device=dev),
@@ -460,12 +490,17 @@ class Measure:
         self.call(0, self.stream, probe)
         self.path, self.n_stages = probe.path_taken, probe.n_stages
         self.stage_names = [m.moe_ffn_stage_name(self.path, s) for s in range(self.n_stages)]
+        if train:   # the forward call's stages, then the backward call's
+            fwd = [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_FORWARD, s) for s in range(self.TRAIN_FWD_STAGES)]
+            bwd = [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_BACKWARD, s) for s in range(self.n_stages)]
+            self.path = "train"
+            self.stage_names = ["fwd:" + n for n in fwd] + ["bwd:" + n for n in bwd]
         # unique experts touched per step (routing of each batch, untimed)
         idx_buf = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
         U_of = {}
         for j in range(W, W + K):
             if j % self.NB not in U_of:
-                if backward:   # the selection by torch.topk (ties aside, the same experts)
+                if backward or train:   # the selection by torch.topk (ties aside, the same experts)
                     U_of[j % self.NB] = int(torch.unique(torch.topk(self.batches[j % self.NB][1], wl.k).indices)
                                             .numel())
                     continue
@@ -477,6 +512,8 @@ class Measure:
             self.g_warm = self.capture(range(W))
             self.g_main = self.capture(range(W, W + K))
 
+    TRAIN_FWD_STAGES = 5   # moe_ffn_forward_train's kernels
+
     def new_opts(self):
         o = self.m.moe_ffn_opts()
         o.path = self.path_code
@@ -485,6 +522,21 @@ class Measure:
     def call(self, j, stream, opts=None, idx=None):
         x, L = self.batches[j % self.NB]
         opts = opts if opts is not None else self.new_opts()
+        if self.train:
+            # the backward call records its stage events after the forward
+            # call's (event TRAIN_FWD_STAGES is its start); opts reports the
+            # backward call's path and stages
+            lw_gu, lw_d = self.layers[j % self.R]
+            of = self.new_opts()
+            if opts.stage_events:
+                of.stage_events = opts.stage_events
+                opts.stage_events = opts.stage_events + self.TRAIN_FWD_STAGES * self.m.ctypes.sizeof(
+                    self.m.ctypes.c_void_p)
+            self.m.moe_ffn_forward_train(x, L, lw_gu, lw_d, self.wl.k, self.ws, out=self.out, opts=of,
+                                         stream=stream)
+            self.m.moe_ffn_backward_train(x, lw_gu, lw_d, self.douts[j % self.NB], self.wl.k, self.ws,
+                                          *self.grads, opts=opts, stream=stream)
+            return
         if self.backward:
             lw_gu, lw_d = self.layers[j % self.R]
             self.m.moe_ffn_backward(x, L, lw_gu, lw_d, self.douts[j % self.NB], self.wl.k, *self.grads,
@@ -586,6 +638,8 @@ class Measure:
         wl, T, K = self.wl, self.T, self.K
         if self.backward:
             return self.summary_backward(total_ms, kern_avg, peaks, world)
+        if self.train:
+            return self.summary_backward(total_ms, kern_avg, peaks, world, train=True)
         call_bytes = sum(algorithmic_bytes(wl, T, u, self.bpe) for u in self.U) / K
         # calls with the router projection inside also read W_r (E*H BF16)
         router_bytes = wl.E * wl.H * 2 if self.routers is not None else 0
@@ -632,27 +686,29 @@ class Measure:
         }
 
 
-    def summary_backward(self, total_ms, kern_avg, peaks, world):
+    def summary_backward(self, total_ms, kern_avg, peaks, world, train=False):
         """The figures of a backward-pass line (byte model backward_bytes,
         flops 16 H I T k: gate/up recomputed, q, dx and both weight
-        gradients)."""
+        gradients), or with train of a training-step line (train_bytes,
+        flops 18 H I T k: the forward's 6 and the backward's 12)."""
         wl, T, K = self.wl, self.T, self.K
-        call_bytes = sum(backward_bytes(wl, T, u) for u in self.U) / K
-        flops = 16.0 * wl.H * wl.I * T * wl.k
+        step_bytes, kbytes = (train_bytes, train_kernel_bytes) if train else (backward_bytes, backward_kernel_bytes)
+        call_bytes = sum(step_bytes(wl, T, u) for u in self.U) / K
+        flops = (18.0 if train else 16.0) * wl.H * wl.I * T * wl.k
         ms_call = total_ms / K
         dom = max(kern_avg, key=kern_avg.get)
-        dom_bytes = sum(backward_kernel_bytes(dom, wl, T, u, wl.k) for u in self.U) / K
+        dom_bytes = sum(kbytes(dom, wl, T, u, wl.k) for u in self.U) / K
         achieved = dom_bytes / (kern_avg[dom] / 1e3) / 1e9
         per_kernel = {}
         for n, v in kern_avg.items():
-            b = backward_kernel_bytes(n, wl, T, sum(self.U) / K, wl.k)
+            b = kbytes(n, wl, T, sum(self.U) / K, wl.k)
             per_kernel[n] = {"us": round(1e3 * v, 3)}
             if b:
                 per_kernel[n]["gbs"] = round(b / (v / 1e3) / 1e9, 1)
                 per_kernel[n]["frac_of_hbm_peak"] = round(b / (v / 1e3) / 1e9 / peaks["hbm_gbs"], 3)
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": stored_traffic(dom, wl.name + "+backward", T),
+                    "traffic": stored_traffic(dom.partition(":")[2] or dom, wl.name + "+backward", T),
                     "peak_source": f"{peaks['source']} HBM copy (burst)",
                     "algorithmic_bytes_per_launch": dom_bytes,
                     "kernel_time": "stage events between kernels, CUDA-graph replay",
@@ -664,7 +720,7 @@ class Measure:
         return {
             "value": whole_job_tokens_per_s(T, K, world, total_ms),
             "ms_per_step": ms_call,
-            "path": "backward",
+            "path": "train" if train else "backward",
             "roofline": roofline,
             "call_hbm": {"achieved_gbs": gbs, "frac_of_measured": gbs / peaks["hbm_gbs"],
                          "frac_of_8tbs_spec": gbs / 8000.0, "bytes_per_call": call_bytes,
@@ -701,8 +757,8 @@ def supplementary_rows(args, dev, peaks, skip):
             # each, so that the default run (2000 steps) stays within minutes
             K = min(args.steps, 100) if T >= 2048 else args.steps
             run = Measure(wl, T, dev, K, max(3, args.warmup), {"auto": 0, "decode": 1, "grouped": 2}[
-                args.path] if how != "backward" else 0, layers, bias, 0, args.eager, routers=routers,
-                mx=how == "mxfp8", backward=how == "backward")
+                args.path] if how not in ("backward", "train") else 0, layers, bias, 0, args.eager,
+                routers=routers, mx=how == "mxfp8", backward=how == "backward", train=how == "train")
             with ClockSampler(dev.index or 0) as clocks:
                 total_ms, _ = run.timed(1)
                 kern = run.stages()
@@ -713,6 +769,11 @@ def supplementary_rows(args, dev, peaks, skip):
             if how == "backward":
                 row["entry"] = ("moe_ffn_backward: dx, dlogits, dW_gate_up and dW_down (FP32) for dout ~ N(0,1) "
                                 "FP32; gate/up recomputed from x inside the call")
+                row["dtype"] = "bf16 inputs, f32 arithmetic and gradients"
+            if how == "train":
+                row["entry"] = ("moe_ffn_forward_train then moe_ffn_backward_train: a training step (output and "
+                                "all four gradients for dout ~ N(0,1) FP32); the forward keeps g, u and the "
+                                "routing in a state buffer, so the backward neither routes nor recomputes gate/up")
                 row["dtype"] = "bf16 inputs, f32 arithmetic and gradients"
             if how == "mxfp8":
                 row["entry"] = ("moe_ffn_forward_mxfp8: the same seeded weights quantised to MXFP8 (E4M3 "
@@ -761,7 +822,7 @@ def main():
     K, W = args.steps, max(3, args.warmup)
     bias = synth.make_bias(wl)
     mx = args.weights == "mxfp8"
-    if mx or args.backward:   # no host-buffer form; the oracle baseline is the BF16 forward
+    if mx or args.backward or args.train:   # no host-buffer form; the oracle baseline is the BF16 forward
         args.no_e2e = args.skip_baseline = True
     R, touched = layer_count(wl, T, args.layers, BPE[args.weights])
     make = synth.make_weights_mxfp8 if mx else synth.make_weights
@@ -769,8 +830,8 @@ def main():
     wgu, wd = (None, None) if mx else layers[0]
     path_code = {"auto": m.MOE_PATH_AUTO, "decode": m.MOE_PATH_DECODE,
                  "grouped": m.MOE_PATH_GROUPED}[args.path]
-    run = Measure(wl, T, dev, K, W, path_code if not args.backward else 0, layers, bias, rank, args.eager, mx=mx,
-                  backward=args.backward)
+    run = Measure(wl, T, dev, K, W, path_code if not (args.backward or args.train) else 0, layers, bias, rank,
+                  args.eager, mx=mx, backward=args.backward, train=args.train)
     stream = run.stream
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sum = torch.empty((), dtype=torch.float32, device=dev)

@@ -91,6 +91,7 @@ enum : int {
     kBwdDx = 4,      // z = W_gate_up^T . [dgu_hi ; dgu_lo]
     kGateUpMx = 5,   // kGateUp with MXFP8 weights
     kDownMx = 6,     // kDown with MXFP8 weights
+    kGateUpSave = 7, // kGateUp that also keeps g and u in FP32 (the training forward)
 };
 
 template <int KIND>
@@ -99,7 +100,7 @@ struct Cfg {
     // write them as exact BF16 (each 32-element block times its E8M0
     // scale) into the tile the MMA reads
     static constexpr bool MX = KIND == kGateUpMx || KIND == kDownMx;
-    static constexpr bool GATE_UP = KIND == kGateUp || KIND == kGateUpRaw || KIND == kGateUpMx;
+    static constexpr bool GATE_UP = KIND == kGateUp || KIND == kGateUpRaw || KIND == kGateUpMx || KIND == kGateUpSave;
     // the weight tile is read along its rows' index (MN-major): the
     // backward's contractions over H (W_down) and over 2I (W_gate_up)
     static constexpr bool A_MN = KIND == kBwdQ || KIND == kBwdDx;
@@ -170,6 +171,7 @@ struct GemmArgs {
     BwdQArgs q;           // kBwdQ only
     const uint8_t *scales;  // MX: the E8M0 scales [E][rows][scale_row] of the weight
     int scale_row;          // bytes per scale row (K / 32 padded to 16)
+    float *g_keep, *u_keep; // kGateUpSave: g and u [rows][I] FP32 besides act
 };
 
 struct Item {
@@ -686,9 +688,10 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 } else if constexpr (KIND == kBwdQ) {
                     bwd_q_columns(r, it.n > SMALL_ROWS ? 32 : SMALL_ROWS, it.p0, it.n, c0, tile * BM + 32 * q + lane,
                                   tile * 4 + q, args, lane);
-                } else if constexpr (KIND == kGateUp || KIND == kGateUpMx) {
+                } else if constexpr (KIND == kGateUp || KIND == kGateUpMx || KIND == kGateUpSave) {
                     const int neuron = tile * 64 + 16 * q + (lane & 15);
                     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(lane < 16 ? args.out0 : args.out1);
+                    float *keep = lane < 16 ? args.g_keep : args.u_keep;   // kGateUpSave: g (lanes 0-15), u
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const float v = __uint_as_float(r[j]);
@@ -696,8 +699,11 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                         const float a = lane < 16 ? swiglu(v, o) : swiglu(o, v);
                         const __nv_bfloat16 hi = __float2bfloat16_rn(a);
                         const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
-                        if (c0 + j < it.n)
-                            dst[(int64_t)(it.p0 + c0 + j) * args.I + neuron] = lane < 16 ? hi : lo;
+                        if (c0 + j < it.n) {
+                            const int64_t at = (int64_t)(it.p0 + c0 + j) * args.I + neuron;
+                            dst[at] = lane < 16 ? hi : lo;
+                            if constexpr (KIND == kGateUpSave) keep[at] = v;
+                        }
                     }
                 } else {
                     const int h = tile * BM + 32 * q + lane;
@@ -848,6 +854,7 @@ cudaError_t gemm_init_device()
     if (e == cudaSuccess) e = set_smem<kBwdDx>();
     if (e == cudaSuccess) e = set_smem<kGateUpMx>();
     if (e == cudaSuccess) e = set_smem<kDownMx>();
+    if (e == cudaSuccess) e = set_smem<kGateUpSave>();
     return e;
 }
 
@@ -863,7 +870,7 @@ namespace {
 template <int KIND>
 cudaError_t gate_up_like(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
                          const int32_t *nchunks, const int32_t *offs, int n_assign, int H, int I, int E, void *out0,
-                         void *out1, int ctas, cudaStream_t s)
+                         void *out1, int ctas, cudaStream_t s, float *g_keep = nullptr, float *u_keep = nullptr)
 {
     CUtensorMap tA;
     constexpr int MT = Cfg<KIND>::MT;
@@ -873,6 +880,8 @@ cudaError_t gate_up_like(const void *x, const int32_t *perm, int k, const void *
     if (e != cudaSuccess) return e;
     GemmArgs a{chunks, nchunks, offs, H, I, H, (I / 64 + MT - 1) / MT, I / 64, (int)groups * 32 * BK * 2, out0,
                out1, (const uint16_t *)x, perm, k};
+    a.g_keep = g_keep;
+    a.u_keep = u_keep;
     // the token rows come from x through the loader warps: the B maps are not read
     grouped_gemm_kernel<KIND><<<grid_for(ctas, n_assign, a.m_tiles, E), Cfg<KIND>::THREADS, Cfg<KIND>::SMEM, s>>>(
         tA, tA, tA, tA, tA, a);
@@ -967,6 +976,14 @@ cudaError_t launch_gemm_gate_up_raw(const void *x, const int32_t *perm, int k, c
                                     float *g, float *u, int ctas, cudaStream_t s)
 {
     return gate_up_like<kGateUpRaw>(x, perm, k, wgu, chunks, nchunks, offs, n_rows, H, I, E, g, u, ctas, s);
+}
+
+cudaError_t launch_gemm_gate_up_keep(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                     const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
+                                     void *act_hi, void *act_lo, float *g, float *u, int ctas, cudaStream_t s)
+{
+    return gate_up_like<kGateUpSave>(x, perm, k, wgu, chunks, nchunks, offs, n_rows, H, I, E, act_hi, act_lo, ctas, s,
+                                     g, u);
 }
 
 cudaError_t launch_bwd_q(const void *ds_hi, const void *ds_lo, const void *wd, const int4 *chunks,

@@ -131,6 +131,11 @@ cudaError_t launch_gemm_down_mx(const void *act_hi, const void *act_lo, const vo
 cudaError_t launch_gemm_gate_up_raw(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
                                     const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
                                     float *g, float *u, int ctas, cudaStream_t s);
+// The forward gate_up GEMM (act as a BF16 hi/lo pair) that also keeps g and
+// u [n_rows][I] in FP32 for a later backward pass (the training forward).
+cudaError_t launch_gemm_gate_up_keep(const void *x, const int32_t *perm, int k, const void *wgu, const int4 *chunks,
+                                     const int32_t *nchunks, const int32_t *offs, int n_rows, int H, int I, int E,
+                                     void *act_hi, void *act_lo, float *g, float *u, int ctas, cudaStream_t s);
 // q = W_down^T dout (dout as ds_hi + ds_lo [rows][H]) and the SwiGLU
 // backward: in g, u, w_s; out dgu_hi/lo [rows][2I], wa_hi/lo [rows][I]
 // (BF16 pairs) and dwp [rows][I/32] (partial sums of act . q)

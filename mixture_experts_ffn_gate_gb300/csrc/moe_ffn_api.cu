@@ -170,6 +170,8 @@ const char *kGroupedStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "
 const char *kBackwardStages[] = {"router",  "sort",    "prep",      "gemm_gate_up", "gemm_q",
                                  "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
 static_assert(sizeof kBackwardStages / sizeof *kBackwardStages <= MOE_MAX_STAGES, "stage events");
+const char *kTrainForwardStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "combine"};
+const char *kTrainBackwardStages[] = {"prep", "gemm_q", "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
 
 // Records stage events around the launches of one call.  While the stream is
 // being captured into a CUDA graph the records become external event-record
@@ -364,9 +366,11 @@ BwdLayout make_bwd_layout(const Shape &s)
     return L;
 }
 
+// recompute: route, sort and recompute g and u (moe_ffn_backward); else
+// they are in the workspace from moe_ffn_forward_train (moe_ffn_backward_train)
 int run_backward(const void *x, const float *logits, const void *wgu, const void *wd, const float *dout,
                  const Shape &s, float *dx, float *dlogits, float *dwgu, float *dwd, char *ws, const BwdLayout &L,
-                 moe_ffn_opts *opts, cudaStream_t stream)
+                 moe_ffn_opts *opts, cudaStream_t stream, bool recompute = true)
 {
     DeviceInfo *dev = nullptr;
     int st = device_setup(&dev);
@@ -391,13 +395,17 @@ int run_backward(const void *x, const float *logits, const void *wgu, const void
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, nullptr, nullptr, tag_size, 0, stream)));
-    MOE_TRY(stg.done(moe::launch_sort(idx, T * k, E, moe::kGemmChunkMax, offs, perm, pos, (int32_t *)(ws + L.uexp),
-                                      (int32_t *)(ws + L.ucount), chunks, nchunks, stream, 16, counts)));
+    if (recompute) {
+        MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, nullptr, nullptr, tag_size, 0, stream)));
+        MOE_TRY(stg.done(moe::launch_sort(idx, T * k, E, moe::kGemmChunkMax, offs, perm, pos,
+                                          (int32_t *)(ws + L.uexp), (int32_t *)(ws + L.ucount), chunks, nchunks,
+                                          stream, 16, counts)));
+    }
     MOE_TRY(stg.done(moe::launch_bwd_prep(x, dout, w, perm, offs, rows, E, H, k, ws + L.xs, ws + L.ds_hi,
                                           ws + L.ds_lo, w_s, dev->n_sm, stream)));
-    MOE_TRY(stg.done(moe::launch_gemm_gate_up_raw(x, perm, k, wgu, chunks, nchunks, offs, rows, H, I, E, g, u, ctas,
-                                                  stream)));
+    if (recompute)
+        MOE_TRY(stg.done(moe::launch_gemm_gate_up_raw(x, perm, k, wgu, chunks, nchunks, offs, rows, H, I, E, g, u,
+                                                      ctas, stream)));
     const moe::BwdQOut qo{g, u, w_s, ws + L.dgu_hi, ws + L.dgu_lo, ws + L.wa_hi, ws + L.wa_lo, dwp};
     MOE_TRY(stg.done(moe::launch_bwd_q(ws + L.ds_hi, ws + L.ds_lo, wd, chunks, nchunks, offs, rows, H, I, E, qo, ctas,
                                        stream)));
@@ -411,7 +419,51 @@ int run_backward(const void *x, const float *logits, const void *wgu, const void
     MOE_TRY(stg.done(moe::launch_dlogits(dwp, pos, idx, w, T, E, k, I, dlogits, stream)));
     if (opts) {
         opts->n_stages = stg.n;
-        opts->path_taken = MOE_PATH_BACKWARD;
+        opts->path_taken = recompute ? MOE_PATH_BACKWARD : MOE_PATH_TRAIN_BACKWARD;
+    }
+    return MOE_OK;
+}
+
+// The forward pass on the backward's workspace layout (the padded sorted
+// order), keeping what the backward needs: the routing (idx, w), the sorted
+// order (perm, pos, offs, chunks, counts) and g, u in FP32.  act's hi/lo pair
+// lives in the w*act regions, which the backward overwrites; the down GEMM's
+// rows in z.  The kernels and their per-element order are the grouped
+// forward's, so out has the same bits as a grouped moe_ffn_forward_ex call.
+int run_forward_train(const void *x, const float *logits, const void *wgu, const void *wd, const Shape &s,
+                      float *out, char *ws, const BwdLayout &L, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    DeviceInfo *dev = nullptr;
+    int st = device_setup(&dev);
+    if (st != MOE_OK) return st;
+    const int T = (int)s.T, H = (int)s.H, I = (int)s.I, E = (int)s.E, k = (int)s.k;
+    const int rows = (int)L.rows;
+    const int ctas = (opts && opts->gemm_ctas) ? opts->gemm_ctas : dev->n_sm;
+    auto *idx = (int32_t *)(ws + L.idx);
+    auto *w = (float *)(ws + L.w);
+    auto *offs = (int32_t *)(ws + L.offs);
+    auto *perm = (int32_t *)(ws + L.perm);
+    auto *pos = (int32_t *)(ws + L.pos);
+    auto *chunks = (int4 *)(ws + L.chunks);
+    auto *nchunks = (int32_t *)(ws + L.nchunks);
+    auto *counts = (int32_t *)(ws + L.counts);
+    auto *z = (float *)(ws + L.z);
+    auto *tag_size = (unsigned long long *)(ws + L.flags) + moe::kDecodeFusedSizeWord;
+
+    Stages stg{opts ? opts->stage_events : nullptr, stream};
+    MOE_TRY(stg.begin());
+    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, nullptr, nullptr, tag_size, 0, stream)));
+    MOE_TRY(stg.done(moe::launch_sort(idx, T * k, E, moe::kGemmChunkMax, offs, perm, pos, (int32_t *)(ws + L.uexp),
+                                      (int32_t *)(ws + L.ucount), chunks, nchunks, stream, 16, counts)));
+    MOE_TRY(stg.done(moe::launch_gemm_gate_up_keep(x, perm, k, wgu, chunks, nchunks, offs, rows, H, I, E,
+                                                   ws + L.wa_hi, ws + L.wa_lo, (float *)(ws + L.g),
+                                                   (float *)(ws + L.u), ctas, stream)));
+    MOE_TRY(stg.done(moe::launch_gemm_down(ws + L.wa_hi, ws + L.wa_lo, wd, chunks, nchunks, offs, rows, H, I, E, z,
+                                           ctas, stream)));
+    MOE_TRY(stg.done(moe::launch_combine(z, w, pos, T, H, k, out, dev->n_sm, stream)));
+    if (opts) {
+        opts->n_stages = stg.n;
+        opts->path_taken = MOE_PATH_TRAIN_FORWARD;
     }
     return MOE_OK;
 }
@@ -725,6 +777,84 @@ int moe_ffn_backward(const void *x_bf16, const float *router_logits_f32, const v
     return st;
 }
 
+size_t moe_ffn_train_state_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k)
+{
+    return moe_ffn_backward_workspace_bytes(T, H, I, E, k);
+}
+
+namespace {
+
+// The checks the training pair shares with moe_ffn_backward: shape, options,
+// weights, the state buffer and its size.  None asks the CUDA runtime.
+int check_train_call(const Shape &s, moe_ffn_opts *opts, const void *wgu, const void *wd, const void *state,
+                     size_t state_bytes, BwdLayout *L)
+{
+    int st = check_shape(s);
+    if (st != MOE_OK) return st;
+    st = check_opts(opts);
+    if (st != MOE_OK) return st;
+    if (opts) {
+        opts->n_stages = 0;
+        opts->path_taken = 0;
+        if (opts->path != MOE_PATH_AUTO && opts->path != MOE_PATH_GROUPED) return MOE_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (!wgu || !wd || !state) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(wgu) || !aligned16(wd) || ((uintptr_t)state & 255)) return MOE_ERR_INVALID_ARG;
+    *L = make_bwd_layout(s);
+    if (L->rows > INT32_MAX / 2 || s.E * 2 * s.I * s.H >= ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (s.T > 0 && state_bytes < L->total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+}  // namespace
+
+int moe_ffn_forward_train(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+                          const void *w_down_bf16, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                          float *out_f32, void *state, size_t state_bytes, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    BwdLayout L;
+    int st = check_train_call(s, opts, w_gate_up_bf16, w_down_bf16, state, state_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (T > 0) {
+        if (!x_bf16 || !router_logits_f32 || !out_f32) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(x_bf16) || !aligned16(router_logits_f32) || !aligned16(out_f32)) return MOE_ERR_INVALID_ARG;
+    }
+    // the first check that asks the CUDA runtime (the TMA encoder)
+    if (!moe::gemm_supported((int)H, (int)I, (int)E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    return run_forward_train(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, s, out_f32, (char *)state, L,
+                             opts, stream);
+}
+
+int moe_ffn_backward_train(const void *x_bf16, const void *w_gate_up_bf16, const void *w_down_bf16,
+                           const float *dout_f32, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                           float *dx_f32, float *dlogits_f32, float *dw_gate_up_f32, float *dw_down_f32, void *state,
+                           size_t state_bytes, moe_ffn_opts *opts, cudaStream_t stream)
+{
+    Shape s{T, H, I, E, k};
+    BwdLayout L;
+    int st = check_train_call(s, opts, w_gate_up_bf16, w_down_bf16, state, state_bytes, &L);
+    if (st != MOE_OK) return st;
+    if (!dw_gate_up_f32 || !dw_down_f32 || !aligned16(dw_gate_up_f32) || !aligned16(dw_down_f32))
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!x_bf16 || !dout_f32 || !dx_f32 || !dlogits_f32) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(x_bf16) || !aligned16(dout_f32) || !aligned16(dx_f32) || !aligned16(dlogits_f32))
+            return MOE_ERR_INVALID_ARG;
+    }
+    // the first check that asks the CUDA runtime (the TMA encoder)
+    if (!moe::gemm_supported((int)H, (int)I, (int)E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) {
+        if (cudaMemsetAsync(dw_gate_up_f32, 0, (size_t)(E * 2 * I * H) * 4, stream) != cudaSuccess ||
+            cudaMemsetAsync(dw_down_f32, 0, (size_t)(E * H * I) * 4, stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    return run_backward(x_bf16, nullptr, w_gate_up_bf16, w_down_bf16, dout_f32, s, dx_f32, dlogits_f32,
+                        dw_gate_up_f32, dw_down_f32, (char *)state, L, opts, stream, false);
+}
+
 const char *moe_ffn_status_string(int status)
 {
     switch (status) {
@@ -750,6 +880,10 @@ const char *moe_ffn_stage_name(int path, int stage)
         return kGroupedStages[stage];
     if (path == MOE_PATH_BACKWARD && stage < (int)(sizeof kBackwardStages / sizeof *kBackwardStages))
         return kBackwardStages[stage];
+    if (path == MOE_PATH_TRAIN_FORWARD && stage < (int)(sizeof kTrainForwardStages / sizeof *kTrainForwardStages))
+        return kTrainForwardStages[stage];
+    if (path == MOE_PATH_TRAIN_BACKWARD && stage < (int)(sizeof kTrainBackwardStages / sizeof *kTrainBackwardStages))
+        return kTrainBackwardStages[stage];
     return nullptr;
 }
 

@@ -28,13 +28,16 @@ MOE_PATH_DECODE = 1
 MOE_PATH_GROUPED = 2
 MOE_PATH_DECODE_FUSED = 3  # reported only: the decode path for T <= 4 as one kernel
 MOE_PATH_BACKWARD = 4      # reported only: moe_ffn_backward's kernels
+MOE_PATH_TRAIN_FORWARD = 5   # reported only: moe_ffn_forward_train
+MOE_PATH_TRAIN_BACKWARD = 6  # reported only: moe_ffn_backward_train
 MOE_MAX_STAGES = 12
 
 EXPORTED = ["moe_ffn_forward", "moe_ffn_workspace_bytes", "moe_ffn_forward_ex",
             "moe_ffn_host_workspace_bytes", "moe_ffn_forward_host", "moe_ffn_status_string",
             "moe_ffn_stage_name", "moe_ffn_device_faults", "moe_ffn_forward_noalloc",
             "moe_ffn_router_workspace_bytes", "moe_ffn_forward_router", "moe_ffn_forward_mxfp8",
-            "moe_ffn_backward_workspace_bytes", "moe_ffn_backward"]
+            "moe_ffn_backward_workspace_bytes", "moe_ffn_backward", "moe_ffn_train_state_bytes",
+            "moe_ffn_forward_train", "moe_ffn_backward_train"]
 
 # Size of the library's fixed scratch array used by moe_ffn_forward_noalloc.
 MOE_FFN_NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -112,9 +115,16 @@ def lib():
             L.moe_ffn_backward_workspace_bytes.restype = ctypes.c_size_t
             L.moe_ffn_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
                                            ctypes.c_size_t, ctypes.POINTER(moe_ffn_opts), vp]
+            L.moe_ffn_train_state_bytes.argtypes = [i64] * 5
+            L.moe_ffn_train_state_bytes.restype = ctypes.c_size_t
+            L.moe_ffn_forward_train.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, ctypes.c_size_t,
+                                                ctypes.POINTER(moe_ffn_opts), vp]
+            L.moe_ffn_backward_train.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+                                                 ctypes.c_size_t, ctypes.POINTER(moe_ffn_opts), vp]
             for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
                       L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc, L.moe_ffn_forward_router,
-                      L.moe_ffn_forward_mxfp8, L.moe_ffn_backward):
+                      L.moe_ffn_forward_mxfp8, L.moe_ffn_backward, L.moe_ffn_forward_train,
+                      L.moe_ffn_backward_train):
                 f.restype = i32
             if hasattr(L, "moe_ffn_debug_fused_timeline"):   # instrumented build only
                 L.moe_ffn_debug_fused_timeline.argtypes = [vp, i32]
@@ -404,6 +414,78 @@ def moe_ffn_backward(x, logits, w_gate_up, w_down, dout, k: int, dx=None, dlogit
         _ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down), _ptr(dout), T, H, I, E, k, _ptr(dx),
         _ptr(dlogits), _ptr(dw_gate_up), _ptr(dw_down), _ptr(workspace), nbytes,
         ctypes.byref(opts) if opts is not None else None, _stream(stream)), "moe_ffn_backward")
+    return dx, dlogits, dw_gate_up, dw_down
+
+
+def moe_ffn_train_state_bytes(T, H, I, E, k) -> int:
+    return int(lib().moe_ffn_train_state_bytes(T, H, I, E, k))
+
+
+def new_train_state(T, H, I, E, k, device="cuda"):
+    """A state buffer for the training pair (moe_ffn_forward_train, then
+    moe_ffn_backward_train)."""
+    n = moe_ffn_train_state_bytes(T, H, I, E, k)
+    if n == 0:
+        raise MoeFfnError(MOE_ERR_UNSUPPORTED_SHAPE, "state size")
+    st = torch.empty(n, dtype=torch.uint8, device=device)
+    st[:MOE_FFN_WORKSPACE_STATE_BYTES].zero_()
+    return st
+
+
+def moe_ffn_forward_train(x, logits, w_gate_up, w_down, k: int, state, out=None,
+                          opts: moe_ffn_opts | None = None, stream=None):
+    """The layer's output f32 [T,H], keeping in ``state`` (from
+    new_train_state) what moe_ffn_backward_train needs."""
+    T, H, I, E = _shape(x, logits, w_gate_up, w_down)
+    for t, d, n in ((x, torch.bfloat16, "x"), (logits, torch.float32, "logits"),
+                    (w_gate_up, torch.bfloat16, "w_gate_up"), (w_down, torch.bfloat16, "w_down"),
+                    (state, torch.uint8, "state")):
+        _dev(t, d, n)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    _dev(out, torch.float32, "out")
+    if tuple(out.shape) != (T, H):
+        raise ValueError(f"out must be [{T}, {H}], got {tuple(out.shape)}")
+    _check(lib().moe_ffn_forward_train(
+        _ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down), T, H, I, E, k, _ptr(out), _ptr(state),
+        state.numel(), ctypes.byref(opts) if opts is not None else None, _stream(stream)), "moe_ffn_forward_train")
+    return out
+
+
+def moe_ffn_backward_train(x, w_gate_up, w_down, dout, k: int, state, dx=None, dlogits=None, dw_gate_up=None,
+                           dw_down=None, opts: moe_ffn_opts | None = None, stream=None):
+    """The layer's gradients for dout f32 [T,H] from the state a
+    moe_ffn_forward_train call on the same x and weights left: returns (dx,
+    dlogits, dw_gate_up, dw_down) as moe_ffn_backward does."""
+    T, H = x.shape
+    E, I = w_gate_up.shape[0], w_down.shape[2]
+    if tuple(w_gate_up.shape) != (E, 2 * I, H) or tuple(w_down.shape) != (E, H, I):
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)} w_gate_up {tuple(w_gate_up.shape)} "
+                         f"w_down {tuple(w_down.shape)}")
+    for t, d, n in ((x, torch.bfloat16, "x"), (w_gate_up, torch.bfloat16, "w_gate_up"),
+                    (w_down, torch.bfloat16, "w_down"), (dout, torch.float32, "dout"),
+                    (state, torch.uint8, "state")):
+        _dev(t, d, n)
+    if tuple(dout.shape) != (T, H):
+        raise ValueError(f"dout must be [{T}, {H}], got {tuple(dout.shape)}")
+    dev = x.device
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if dlogits is None:
+        dlogits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if dw_gate_up is None:
+        dw_gate_up = torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev)
+    if dw_down is None:
+        dw_down = torch.empty((E, H, I), dtype=torch.float32, device=dev)
+    for t, shape, n in ((dx, (T, H), "dx"), (dlogits, (T, E), "dlogits"), (dw_gate_up, (E, 2 * I, H), "dw_gate_up"),
+                        (dw_down, (E, H, I), "dw_down")):
+        _dev(t, torch.float32, n)
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{n} must be {list(shape)}, got {tuple(t.shape)}")
+    _check(lib().moe_ffn_backward_train(
+        _ptr(x), _ptr(w_gate_up), _ptr(w_down), _ptr(dout), T, H, I, E, k, _ptr(dx), _ptr(dlogits),
+        _ptr(dw_gate_up), _ptr(dw_down), _ptr(state), state.numel(),
+        ctypes.byref(opts) if opts is not None else None, _stream(stream)), "moe_ffn_backward_train")
     return dx, dlogits, dw_gate_up, dw_down
 
 
