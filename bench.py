@@ -41,8 +41,8 @@ at 1 + 1/32 per weight; T > 4 takes the grouped tensor-core path).  One row
 training-size layer (dout ~ N(0,1) FP32 per call; all four gradients written
 every call), with its own byte model (backward_bytes) and 16 H I T k flops.
 One row ("entry": moe_ffn_forward_train + moe_ffn_backward_train) runs a
-training step of that layer: the forward pass keeping g, u and the routing,
-then the backward pass from them (byte model train_bytes, 18 H I T k flops).
+training step of that layer: the forward pass keeping g and u, then the
+backward pass reading them (byte model train_bytes, 18 H I T k flops).
 
 --impl reference times the FP64 CPU oracle on this machine's host cores on a
 bounded sample of the same workload (it is the slow baseline, not a target).
@@ -534,7 +534,7 @@ class Measure:
                     self.m.ctypes.c_void_p)
             self.m.moe_ffn_forward_train(x, L, lw_gu, lw_d, self.wl.k, self.ws, out=self.out, opts=of,
                                          stream=stream)
-            self.m.moe_ffn_backward_train(x, lw_gu, lw_d, self.douts[j % self.NB], self.wl.k, self.ws,
+            self.m.moe_ffn_backward_train(x, L, lw_gu, lw_d, self.douts[j % self.NB], self.wl.k, self.ws,
                                           *self.grads, opts=opts, stream=stream)
             return
         if self.backward:
@@ -611,8 +611,10 @@ class Measure:
         events (captured as event-record nodes when graphs are used)."""
         torch, m = self.torch, self.m
         K, W = self.K, self.W
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_MAX_STAGES + 1)]
-               for _ in range(K)]
+        # a training step is two calls: the backward call's events follow
+        # the forward call's TRAIN_FWD_STAGES
+        n_ev = m.MOE_MAX_STAGES + 1 + (self.TRAIN_FWD_STAGES if self.train else 0)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
         arrs = []
         for j in range(K):
             for e in evs[j]:
@@ -772,8 +774,8 @@ def supplementary_rows(args, dev, peaks, skip):
                 row["dtype"] = "bf16 inputs, f32 arithmetic and gradients"
             if how == "train":
                 row["entry"] = ("moe_ffn_forward_train then moe_ffn_backward_train: a training step (output and "
-                                "all four gradients for dout ~ N(0,1) FP32); the forward keeps g, u and the "
-                                "routing in a state buffer, so the backward neither routes nor recomputes gate/up")
+                                "all four gradients for dout ~ N(0,1) FP32); the forward keeps g and u in a state "
+                                "buffer, so the backward does not recompute gate/up")
                 row["dtype"] = "bf16 inputs, f32 arithmetic and gradients"
             if how == "mxfp8":
                 row["entry"] = ("moe_ffn_forward_mxfp8: the same seeded weights quantised to MXFP8 (E4M3 "

@@ -347,28 +347,28 @@ int moe_ffn_backward(const void *x_bf16, const float *router_logits_f32,
 
 /*
  * The training pair: a forward pass that keeps, in a caller-owned state
- * buffer, what the backward pass needs, and the backward pass that starts
- * from it instead of routing again and recomputing the gate/up projections
- * (which re-reads every touched expert's W_gate_up).  The layer and the
- * gradients are those of moe_ffn_forward and moe_ffn_backward (same
- * sources, same definitions), with the same bits:
+ * buffer, the gate/up projections the backward pass needs, and the backward
+ * pass that reads them instead of recomputing them (which re-reads every
+ * touched expert's W_gate_up).  The layer and the gradients are those of
+ * moe_ffn_forward and moe_ffn_backward (same definitions), with the same
+ * bits:
  *   - moe_ffn_forward_train's out equals moe_ffn_forward_ex's on the
  *     grouped path (opts->path = MOE_PATH_GROUPED) bit for bit;
  *   - moe_ffn_backward_train's four gradients equal moe_ffn_backward's on
  *     the same inputs bit for bit.
  * state: device, 256-byte aligned, at least moe_ffn_train_state_bytes
- * (= moe_ffn_backward_workspace_bytes) for the call's T, H, I, E, k; it
- * holds the routing (top-k indices and weights), the sorted order of the
- * assignments (each expert's segment rounded up to 16 rows) and g = W_gate
- * x, u = W_up x in FP32 per assignment, plus scratch space for both calls.
- * Call order on the stream: moe_ffn_forward_train, then
- * moe_ffn_backward_train with the same x, weights and shape, and nothing
- * else writing to the state in between (a plain forward or backward call
- * given the state as its workspace overwrites it).  The backward call
- * leaves the kept part intact, so it may run again on the same state (for
- * another dout).  The library does not check that the state came from a
- * matching forward call: a mismatched one gives wrong gradients, not a
- * fault (every index it reads is bounded by the call's own shape).
+ * (= moe_ffn_backward_workspace_bytes) for the call's T, H, I, E, k; the
+ * forward call leaves in it g = W_gate x and u = W_up x in FP32 for every
+ * assignment, in the order of the assignments sorted by expert (each
+ * expert's segment rounded up to 16 rows); the rest is scratch space of
+ * either call.  Call order on the stream: moe_ffn_forward_train, then
+ * moe_ffn_backward_train with the same x, logits, weights and shape, and
+ * nothing else writing to the state in between (a plain forward or
+ * backward call given the state as its workspace overwrites it).  The
+ * backward call routes and sorts the logits again (two small kernels) and
+ * reads only g and u from the state, never writing them, so it may run
+ * again on one state (for another dout), and a state from another call
+ * gives wrong gradients but no access outside the call's own buffers.
  * Both run the grouped tensor-core kernels for every T (opts->path AUTO or
  * GROUPED, else MOE_ERR_UNSUPPORTED_SHAPE); same shape limits, pointer
  * rules and statuses as moe_ffn_backward; opts (nullable): gemm_ctas and
@@ -383,12 +383,12 @@ int moe_ffn_forward_train(const void *x_bf16, const float *router_logits_f32,
                           int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
                           float *out_f32, void *state, size_t state_bytes,
                           moe_ffn_opts *opts, cudaStream_t stream);
-int moe_ffn_backward_train(const void *x_bf16, const void *w_gate_up_bf16,
-                           const void *w_down_bf16, const float *dout_f32,
-                           int64_t T, int64_t H, int64_t I, int64_t E,
-                           int64_t k, float *dx_f32, float *dlogits_f32,
-                           float *dw_gate_up_f32, float *dw_down_f32,
-                           void *state, size_t state_bytes, moe_ffn_opts *opts,
+int moe_ffn_backward_train(const void *x_bf16, const float *router_logits_f32,
+                           const void *w_gate_up_bf16, const void *w_down_bf16,
+                           const float *dout_f32, int64_t T, int64_t H, int64_t I,
+                           int64_t E, int64_t k, float *dx_f32, float *dlogits_f32,
+                           float *dw_gate_up_f32, float *dw_down_f32, void *state,
+                           size_t state_bytes, moe_ffn_opts *opts,
                            cudaStream_t stream);
 
 /* Static text for a status code. */

@@ -171,7 +171,8 @@ const char *kBackwardStages[] = {"router",  "sort",    "prep",      "gemm_gate_u
                                  "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
 static_assert(sizeof kBackwardStages / sizeof *kBackwardStages <= MOE_MAX_STAGES, "stage events");
 const char *kTrainForwardStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "combine"};
-const char *kTrainBackwardStages[] = {"prep", "gemm_q", "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
+const char *kTrainBackwardStages[] = {"router", "sort",          "prep",   "gemm_q", "gemm_dx",
+                                      "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
 
 // Records stage events around the launches of one call.  While the stream is
 // being captured into a CUDA graph the records become external event-record
@@ -366,8 +367,10 @@ BwdLayout make_bwd_layout(const Shape &s)
     return L;
 }
 
-// recompute: route, sort and recompute g and u (moe_ffn_backward); else
-// they are in the workspace from moe_ffn_forward_train (moe_ffn_backward_train)
+// recompute: g and u recomputed from x (moe_ffn_backward); else they are in
+// the workspace from moe_ffn_forward_train (moe_ffn_backward_train).  Both
+// route and sort: everything that indexes memory is this call's own, so a
+// state from another call can give wrong values but no stray access.
 int run_backward(const void *x, const float *logits, const void *wgu, const void *wd, const float *dout,
                  const Shape &s, float *dx, float *dlogits, float *dwgu, float *dwd, char *ws, const BwdLayout &L,
                  moe_ffn_opts *opts, cudaStream_t stream, bool recompute = true)
@@ -395,12 +398,9 @@ int run_backward(const void *x, const float *logits, const void *wgu, const void
 
     Stages stg{opts ? opts->stage_events : nullptr, stream};
     MOE_TRY(stg.begin());
-    if (recompute) {
-        MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, nullptr, nullptr, tag_size, 0, stream)));
-        MOE_TRY(stg.done(moe::launch_sort(idx, T * k, E, moe::kGemmChunkMax, offs, perm, pos,
-                                          (int32_t *)(ws + L.uexp), (int32_t *)(ws + L.ucount), chunks, nchunks,
-                                          stream, 16, counts)));
-    }
+    MOE_TRY(stg.done(moe::launch_router(logits, T, E, k, idx, w, nullptr, nullptr, tag_size, 0, stream)));
+    MOE_TRY(stg.done(moe::launch_sort(idx, T * k, E, moe::kGemmChunkMax, offs, perm, pos, (int32_t *)(ws + L.uexp),
+                                      (int32_t *)(ws + L.ucount), chunks, nchunks, stream, 16, counts)));
     MOE_TRY(stg.done(moe::launch_bwd_prep(x, dout, w, perm, offs, rows, E, H, k, ws + L.xs, ws + L.ds_hi,
                                           ws + L.ds_lo, w_s, dev->n_sm, stream)));
     if (recompute)
@@ -425,8 +425,8 @@ int run_backward(const void *x, const float *logits, const void *wgu, const void
 }
 
 // The forward pass on the backward's workspace layout (the padded sorted
-// order), keeping what the backward needs: the routing (idx, w), the sorted
-// order (perm, pos, offs, chunks, counts) and g, u in FP32.  act's hi/lo pair
+// order), keeping g and u in FP32 for the backward call, which routes and
+// sorts the same logits again and finds them in the same rows.  act's hi/lo pair
 // lives in the w*act regions, which the backward overwrites; the down GEMM's
 // rows in z.  The kernels and their per-element order are the grouped
 // forward's, so out has the same bits as a grouped moe_ffn_forward_ex call.
@@ -827,8 +827,9 @@ int moe_ffn_forward_train(const void *x_bf16, const float *router_logits_f32, co
                              opts, stream);
 }
 
-int moe_ffn_backward_train(const void *x_bf16, const void *w_gate_up_bf16, const void *w_down_bf16,
-                           const float *dout_f32, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+int moe_ffn_backward_train(const void *x_bf16, const float *router_logits_f32, const void *w_gate_up_bf16,
+                           const void *w_down_bf16, const float *dout_f32, int64_t T, int64_t H, int64_t I,
+                           int64_t E, int64_t k,
                            float *dx_f32, float *dlogits_f32, float *dw_gate_up_f32, float *dw_down_f32, void *state,
                            size_t state_bytes, moe_ffn_opts *opts, cudaStream_t stream)
 {
@@ -839,8 +840,9 @@ int moe_ffn_backward_train(const void *x_bf16, const void *w_gate_up_bf16, const
     if (!dw_gate_up_f32 || !dw_down_f32 || !aligned16(dw_gate_up_f32) || !aligned16(dw_down_f32))
         return MOE_ERR_INVALID_ARG;
     if (T > 0) {
-        if (!x_bf16 || !dout_f32 || !dx_f32 || !dlogits_f32) return MOE_ERR_INVALID_ARG;
-        if (!aligned16(x_bf16) || !aligned16(dout_f32) || !aligned16(dx_f32) || !aligned16(dlogits_f32))
+        if (!x_bf16 || !router_logits_f32 || !dout_f32 || !dx_f32 || !dlogits_f32) return MOE_ERR_INVALID_ARG;
+        if (!aligned16(x_bf16) || !aligned16(router_logits_f32) || !aligned16(dout_f32) || !aligned16(dx_f32) ||
+            !aligned16(dlogits_f32))
             return MOE_ERR_INVALID_ARG;
     }
     // the first check that asks the CUDA runtime (the TMA encoder)
@@ -851,7 +853,7 @@ int moe_ffn_backward_train(const void *x_bf16, const void *w_gate_up_bf16, const
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
-    return run_backward(x_bf16, nullptr, w_gate_up_bf16, w_down_bf16, dout_f32, s, dx_f32, dlogits_f32,
+    return run_backward(x_bf16, router_logits_f32, w_gate_up_bf16, w_down_bf16, dout_f32, s, dx_f32, dlogits_f32,
                         dw_gate_up_f32, dw_down_f32, (char *)state, L, opts, stream, false);
 }
 

@@ -119,7 +119,7 @@ def lib():
             L.moe_ffn_train_state_bytes.restype = ctypes.c_size_t
             L.moe_ffn_forward_train.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, ctypes.c_size_t,
                                                 ctypes.POINTER(moe_ffn_opts), vp]
-            L.moe_ffn_backward_train.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
+            L.moe_ffn_backward_train.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp,
                                                  ctypes.c_size_t, ctypes.POINTER(moe_ffn_opts), vp]
             for f in (L.moe_ffn_forward, L.moe_ffn_forward_ex, L.moe_ffn_forward_host,
                       L.moe_ffn_device_faults, L.moe_ffn_forward_noalloc, L.moe_ffn_forward_router,
@@ -452,19 +452,16 @@ def moe_ffn_forward_train(x, logits, w_gate_up, w_down, k: int, state, out=None,
     return out
 
 
-def moe_ffn_backward_train(x, w_gate_up, w_down, dout, k: int, state, dx=None, dlogits=None, dw_gate_up=None,
-                           dw_down=None, opts: moe_ffn_opts | None = None, stream=None):
-    """The layer's gradients for dout f32 [T,H] from the state a
-    moe_ffn_forward_train call on the same x and weights left: returns (dx,
-    dlogits, dw_gate_up, dw_down) as moe_ffn_backward does."""
-    T, H = x.shape
-    E, I = w_gate_up.shape[0], w_down.shape[2]
-    if tuple(w_gate_up.shape) != (E, 2 * I, H) or tuple(w_down.shape) != (E, H, I):
-        raise ValueError(f"shape mismatch: x {tuple(x.shape)} w_gate_up {tuple(w_gate_up.shape)} "
-                         f"w_down {tuple(w_down.shape)}")
-    for t, d, n in ((x, torch.bfloat16, "x"), (w_gate_up, torch.bfloat16, "w_gate_up"),
-                    (w_down, torch.bfloat16, "w_down"), (dout, torch.float32, "dout"),
-                    (state, torch.uint8, "state")):
+def moe_ffn_backward_train(x, logits, w_gate_up, w_down, dout, k: int, state, dx=None, dlogits=None,
+                           dw_gate_up=None, dw_down=None, opts: moe_ffn_opts | None = None, stream=None):
+    """The layer's gradients for dout f32 [T,H], reading g and u from the
+    state a moe_ffn_forward_train call on the same x, logits and weights
+    left: returns (dx, dlogits, dw_gate_up, dw_down) as moe_ffn_backward
+    does."""
+    T, H, I, E = _shape(x, logits, w_gate_up, w_down)
+    for t, d, n in ((x, torch.bfloat16, "x"), (logits, torch.float32, "logits"),
+                    (w_gate_up, torch.bfloat16, "w_gate_up"), (w_down, torch.bfloat16, "w_down"),
+                    (dout, torch.float32, "dout"), (state, torch.uint8, "state")):
         _dev(t, d, n)
     if tuple(dout.shape) != (T, H):
         raise ValueError(f"dout must be [{T}, {H}], got {tuple(dout.shape)}")
@@ -483,7 +480,7 @@ def moe_ffn_backward_train(x, w_gate_up, w_down, dout, k: int, state, dx=None, d
         if tuple(t.shape) != shape:
             raise ValueError(f"{n} must be {list(shape)}, got {tuple(t.shape)}")
     _check(lib().moe_ffn_backward_train(
-        _ptr(x), _ptr(w_gate_up), _ptr(w_down), _ptr(dout), T, H, I, E, k, _ptr(dx), _ptr(dlogits),
+        _ptr(x), _ptr(logits), _ptr(w_gate_up), _ptr(w_down), _ptr(dout), T, H, I, E, k, _ptr(dx), _ptr(dlogits),
         _ptr(dw_gate_up), _ptr(dw_down), _ptr(state), state.numel(),
         ctypes.byref(opts) if opts is not None else None, _stream(stream)), "moe_ffn_backward_train")
     return dx, dlogits, dw_gate_up, dw_down

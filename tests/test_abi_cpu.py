@@ -72,8 +72,8 @@ def test_stage_names(L):
          "wgrad_gate_up", "dlogits", None]
     assert [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_FORWARD, i) for i in range(6)] == \
         ["router", "sort", "gemm_gate_up", "gemm_down", "combine", None]
-    assert [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_BACKWARD, i) for i in range(8)] == \
-        ["prep", "gemm_q", "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits", None]
+    assert [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_BACKWARD, i) for i in range(10)] == \
+        ["router", "sort", "prep", "gemm_q", "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits", None]
     assert m.moe_ffn_stage_name(m.MOE_PATH_AUTO, 0) is None
     assert m.moe_ffn_stage_name(m.MOE_PATH_DECODE, -1) is None
 
@@ -276,16 +276,17 @@ def test_forward_train_argument_checks(L, case, want):
 
 
 @pytest.mark.parametrize("case,want", [
-    (dict(T=-1), 1), (dict(k=9), 1), (dict(H=200), 2), (dict(x=None), 1), (dict(wgu=None), 1),
-    (dict(wd=None), 1), (dict(dout=None), 1), (dict(dx=None), 1), (dict(dlogits=None), 1), (dict(dwgu=None), 1),
+    (dict(T=-1), 1), (dict(k=9), 1), (dict(H=200), 2), (dict(x=None), 1), (dict(logits=None), 1),
+    (dict(wgu=None), 1), (dict(wd=None), 1), (dict(dout=None), 1), (dict(dx=None), 1), (dict(dlogits=None), 1), (dict(dwgu=None), 1),
     (dict(dwd=None), 1), (dict(dwd=FAKE + 8), 1), (dict(state=None), 1), (dict(state=FAKE + 16), 1),
     (dict(state_bytes=1024), 5), (dict(T=0, dwgu=None), 1),
 ])
 def test_backward_train_argument_checks(L, case, want):
-    a = dict(x=FAKE, wgu=FAKE, wd=FAKE, dout=FAKE, T=4, H=256, I=128, E=8, k=2, dx=FAKE, dlogits=FAKE, dwgu=FAKE,
-             dwd=FAKE, state=FAKE, state_bytes=1 << 40)
+    a = dict(x=FAKE, logits=FAKE, wgu=FAKE, wd=FAKE, dout=FAKE, T=4, H=256, I=128, E=8, k=2, dx=FAKE, dlogits=FAKE,
+             dwgu=FAKE, dwd=FAKE, state=FAKE, state_bytes=1 << 40)
     a.update(case)
-    st = L.moe_ffn_backward_train(a["x"], a["wgu"], a["wd"], a["dout"], a["T"], a["H"], a["I"], a["E"], a["k"],
+    st = L.moe_ffn_backward_train(a["x"], a["logits"], a["wgu"], a["wd"], a["dout"], a["T"], a["H"], a["I"],
+                                  a["E"], a["k"],
                                   a["dx"], a["dlogits"], a["dwgu"], a["dwd"], a["state"], a["state_bytes"], None,
                                   None)
     assert st == want
@@ -297,5 +298,5 @@ def test_train_pair_rejects_decode_path(L):
     o.path = m.MOE_PATH_DECODE
     assert L.moe_ffn_forward_train(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 8, 2, FAKE, FAKE, 1 << 40,
                                    ctypes.byref(o), None) == m.MOE_ERR_UNSUPPORTED_SHAPE
-    assert L.moe_ffn_backward_train(FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE,
+    assert L.moe_ffn_backward_train(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 256, 128, 8, 2, FAKE, FAKE, FAKE, FAKE, FAKE,
                                     1 << 40, ctypes.byref(o), None) == m.MOE_ERR_UNSUPPORTED_SHAPE

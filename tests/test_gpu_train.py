@@ -4,9 +4,9 @@ forward path; the gradients against the FP64 backward oracle and, bit for
 bit, against moe_ffn_backward, which routes and recomputes gate/up itself.
 The pair runs the same kernels in the same per-element order as those
 entries, so any difference in a bit is a bug in what the state keeps.
-Also: a second backward call on one state (another dout), T = 0, a CUDA
-graph of the whole training step, the stage names, and the training-size
-layer."""
+Also: a second backward call on one state (another dout), a state no
+forward call filled, T = 0, a CUDA graph of the whole training step, and
+the training-size layer."""
 import numpy as np
 import pytest
 import torch
@@ -52,11 +52,11 @@ def _pair(x, L, wgu, wd, dout, k, state=None, **opt_fields):
         for f, v in opt_fields.items():
             setattr(o, f, v)
     out = m.moe_ffn_forward_train(x, L, wgu, wd, k, state, opts=of)
-    grads = m.moe_ffn_backward_train(x, wgu, wd, dout, k, state, opts=ob)
+    grads = m.moe_ffn_backward_train(x, L, wgu, wd, dout, k, state, opts=ob)
     torch.cuda.synchronize()
     if T:
         assert of.path_taken == m.MOE_PATH_TRAIN_FORWARD and of.n_stages == 5
-        assert ob.path_taken == m.MOE_PATH_TRAIN_BACKWARD and ob.n_stages == 7
+        assert ob.path_taken == m.MOE_PATH_TRAIN_BACKWARD and ob.n_stages == 9
     return out, dict(zip(NAMES, grads)), state
 
 
@@ -102,12 +102,31 @@ def test_backward_train_runs_again_on_one_state():
     x, L, wgu, wd, dout = _layer(wl, 50, call=2)
     _, first, state = _pair(x, L, wgu, wd, dout, 8)
     dout2 = synth.make_dout(wl, 50, call=7, device="cuda")
-    again = m.moe_ffn_backward_train(x, wgu, wd, dout2, 8, state)
+    again = m.moe_ffn_backward_train(x, L, wgu, wd, dout2, 8, state)
     ref2 = m.moe_ffn_backward(x, L, wgu, wd, dout2, 8)
     torch.cuda.synchronize()
     for n, a, b in zip(NAMES, again, ref2):
         assert torch.equal(a, b), n
     assert not torch.equal(again[0], first["dx"])
+
+
+def test_backward_train_on_a_foreign_state_stays_in_bounds():
+    """The backward call routes and sorts the logits itself and takes only
+    the values g and u from the state: a state that no matching forward
+    call filled (here every byte 0xFF, NaN as FP32) gives wrong gradients
+    but no fault, and the same buffer then serves a proper pair."""
+    wl = gu.custom(60, 256, 128, 16, 4, 1.0, name="train_foreign")
+    x, L, wgu, wd, dout = _layer(wl, 60, call=5)
+    state = m.new_train_state(60, 256, 128, 16, 4)
+    state.fill_(255)
+    bad = m.moe_ffn_backward_train(x, L, wgu, wd, dout, 4, state)
+    torch.cuda.synchronize()
+    assert torch.isnan(bad[0]).any()
+    _, got, _ = _pair(x, L, wgu, wd, dout, 4, state=state)
+    ref = m.moe_ffn_backward(x, L, wgu, wd, dout, 4)
+    torch.cuda.synchronize()
+    for n, b in zip(NAMES, ref):
+        assert torch.equal(got[n], b), n
 
 
 def test_train_pair_widths_and_no_tokens():
@@ -125,7 +144,8 @@ def test_train_pair_widths_and_no_tokens():
     out0 = m.moe_ffn_forward_train(x0, L[:0].contiguous(), wgu, wd, 4, state)
     dwgu = torch.full_like(a["dwgu"], float("nan"))
     dwd = torch.full_like(a["dwd"], float("nan"))
-    m.moe_ffn_backward_train(x0, wgu, wd, dout[:0].contiguous(), 4, state, dw_gate_up=dwgu, dw_down=dwd)
+    m.moe_ffn_backward_train(x0, L[:0].contiguous(), wgu, wd, dout[:0].contiguous(), 4, state, dw_gate_up=dwgu,
+                             dw_down=dwd)
     torch.cuda.synchronize()
     assert out0.shape == (0, 512)
     assert torch.count_nonzero(dwgu) == 0 and torch.count_nonzero(dwd) == 0
@@ -144,7 +164,7 @@ def test_train_step_as_one_graph():
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s), torch.cuda.graph(graph, stream=s, capture_error_mode="thread_local"):
         m.moe_ffn_forward_train(x, L, wgu, wd, 2, state, out=out, stream=s)
-        m.moe_ffn_backward_train(x, wgu, wd, dout, 2, state, *grads, stream=s)
+        m.moe_ffn_backward_train(x, L, wgu, wd, dout, 2, state, *grads, stream=s)
     for _ in range(2):
         out.fill_(float("nan"))
         for g in grads:
