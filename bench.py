@@ -272,8 +272,9 @@ def backward_kernel_bytes(kernel, wl, T, U, k):
         + n * (I // 32) * 4 + n * 4,
         "gemm_dx": U * 2 * I * H * 2 + 2 * n * 2 * I * 2 + n * H * 4,
         "combine": n * H * 4 + T * H * 4,
-        "wgrad_down": E * H * I * 4 + 2 * n * H * 2 + 2 * n * I * 2,
-        "wgrad_gate_up": E * 2 * I * H * 4 + 2 * n * 2 * I * 2 + n * H * 2,
+        "zero_grads": (E - U) * 3 * H * I * 4,
+        "wgrad_down": U * H * I * 4 + 2 * n * H * 2 + 2 * n * I * 2,
+        "wgrad_gate_up": U * 2 * I * H * 4 + 2 * n * 2 * I * 2 + n * H * 2,
     }.get(kernel)
 
 

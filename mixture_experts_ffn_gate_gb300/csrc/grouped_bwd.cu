@@ -28,9 +28,13 @@
 //     expert's rows in steps of 32 (the MMA's K steps of 16 stop at the
 //     16-row padding, whose rows are zero).  Both operands are MN-major:
 //     TMA boxes of 64 elements (128 bytes, 128-byte swizzle) by 32 rows.
-//     Experts without rows get zero tiles.  Each output element is one MMA
+//     Experts without rows are skipped: zero_untouched_kernel has written
+//     their zeros with plain 16-byte stores.  Each output element is one MMA
 //     chain in a fixed order, so the gradients are bit-identical from run
 //     to run whatever the grid.
+//   zero_untouched_kernel -- the gradients of the experts no row selects,
+//     written as zeros by a plain write stream before the weight-gradient
+//     kernels run (they skip those experts).
 //   dlogits_kernel   -- one warp per token: dw_j from the q epilogue's
 //     partial sums (fixed order), then the softmax gradient.
 //
@@ -293,15 +297,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             decode(i, e, m0, n0, rows, r0);
             const int row0 = m0 + 32 * q;
             const bool rows_in = row0 < args.M;   // M is a multiple of 32: a block is all in or all out
-            if (rows == 0) {
-                // nothing selected this expert: its gradient is zero
-                uint32_t z[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) z[j] = 0u;
-                for (int c0 = half * (WNB / 2); c0 < (half + 1) * (WNB / 2); c0 += 32)
-                    if (rows_in && n0 + c0 < args.N) put_block(z, e, row0, n0 + c0);
-                continue;
-            }
+            if (rows == 0) continue;   // nothing selected this expert: zero_untouched_kernel wrote its zeros
             const int acc = li & 1;
             const uint32_t aph = (li >> 1) & 1;
             ++li;
@@ -368,6 +364,35 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *__restric
             reinterpret_cast<uint4 *>(ds_hi + (int64_t)r * H)[c] = *reinterpret_cast<const uint4 *>(hi);
             reinterpret_cast<uint4 *>(ds_lo + (int64_t)r * H)[c] = *reinterpret_cast<const uint4 *>(lo);
         }
+    }
+}
+
+// ---------------------------------------------------------------- zeros
+// The weight gradients of the experts no row selects are zero: every block
+// walks the experts in order and, for each one with counts[e] == 0, writes
+// its share of dW_gate_up[e] and dW_down[e] with 16-byte stores (four
+// whole 128-byte lines per warp instruction, a plain write stream).
+__global__ void __launch_bounds__(256) zero_untouched_kernel(const int32_t *__restrict__ counts, int E,
+                                                             float4 *__restrict__ dwgu, int64_t gu4,
+                                                             float4 *__restrict__ dwd, int64_t d4)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto fill = [&](float4 *p, int64_t n) {
+        int64_t i = first;
+        for (; i + 3 * stride < n; i += 4 * stride) {   // four independent stores per step
+            p[i] = z;
+            p[i + stride] = z;
+            p[i + 2 * stride] = z;
+            p[i + 3 * stride] = z;
+        }
+        for (; i < n; i += stride) p[i] = z;
+    };
+    for (int e = 0; e < E; ++e) {
+        if (__ldg(counts + e) != 0) continue;
+        fill(dwgu + (int64_t)e * gu4, gu4);
+        fill(dwd + (int64_t)e * d4, d4);
     }
 }
 
@@ -503,6 +528,16 @@ cudaError_t launch_wgrad_gate_up(const void *dgu_hi, const void *dgu_lo, const v
                                  cudaStream_t s)
 {
     return launch_wgrad<kDwGateUp>(dgu_hi, dgu_lo, xs, nullptr, offs, counts, n_rows, 2 * I, H, E, dwgu, ctas, s);
+}
+
+cudaError_t launch_zero_untouched(const int32_t *counts, int E, int H, int I, float *dwgu, float *dwd, int n_sm,
+                                  cudaStream_t s)
+{
+    // 2I*H and H*I are multiples of 4 (H and I are multiples of 64)
+    zero_untouched_kernel<<<8 * n_sm, 256, 0, s>>>(counts, E, reinterpret_cast<float4 *>(dwgu),
+                                                   (int64_t)2 * I * H / 4, reinterpret_cast<float4 *>(dwd),
+                                                   (int64_t)H * I / 4);
+    return cudaPeekAtLastError();
 }
 
 cudaError_t launch_dlogits(const float *dwp, const int32_t *pos, const int32_t *idx, const float *w, int T, int E,

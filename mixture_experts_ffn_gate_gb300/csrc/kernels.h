@@ -169,6 +169,10 @@ cudaError_t launch_wgrad_gate_up(const void *dgu_hi, const void *dgu_lo, const v
                                  const int32_t *counts, int n_rows, int H, int I, int E, float *dwgu, int ctas,
                                  cudaStream_t s);
 // dlogits [T][E] from dwp (I/32 partial sums per row), pos, idx, w
+// Zeroes dW_gate_up[e] and dW_down[e] of every expert with counts[e] == 0
+// (the weight-gradient kernels skip those experts).
+cudaError_t launch_zero_untouched(const int32_t *counts, int E, int H, int I, float *dwgu, float *dwd, int n_sm,
+                                  cudaStream_t s);
 cudaError_t launch_dlogits(const float *dwp, const int32_t *pos, const int32_t *idx, const float *w, int T, int E,
                            int k, int I, float *dlogits, cudaStream_t s);
 

@@ -167,12 +167,12 @@ int device_setup(DeviceInfo **info)
 const char *kDecodeStages[] = {"router", "sort", "decode_gate_up", "decode_down"};
 const char *kDecodeFusedStages[] = {"decode_fused"};
 const char *kGroupedStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "combine"};
-const char *kBackwardStages[] = {"router",  "sort",    "prep",      "gemm_gate_up", "gemm_q",
-                                 "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
+const char *kBackwardStages[] = {"router",  "sort",       "prep",       "gemm_gate_up",  "gemm_q", "gemm_dx",
+                                 "combine", "zero_grads", "wgrad_down", "wgrad_gate_up", "dlogits"};
 static_assert(sizeof kBackwardStages / sizeof *kBackwardStages <= MOE_MAX_STAGES, "stage events");
 const char *kTrainForwardStages[] = {"router", "sort", "gemm_gate_up", "gemm_down", "combine"};
-const char *kTrainBackwardStages[] = {"router", "sort",          "prep",   "gemm_q", "gemm_dx",
-                                      "combine", "wgrad_down", "wgrad_gate_up", "dlogits"};
+const char *kTrainBackwardStages[] = {"router",     "sort",       "prep",          "gemm_q",  "gemm_dx", "combine",
+                                      "zero_grads", "wgrad_down", "wgrad_gate_up", "dlogits"};
 
 // Records stage events around the launches of one call.  While the stream is
 // being captured into a CUDA graph the records become external event-record
@@ -412,6 +412,7 @@ int run_backward(const void *x, const float *logits, const void *wgu, const void
     MOE_TRY(stg.done(moe::launch_bwd_dx(ws + L.dgu_hi, ws + L.dgu_lo, wgu, chunks, nchunks, offs, rows, H, I, E, z,
                                         ctas, stream)));
     MOE_TRY(stg.done(moe::launch_combine(z, nullptr, pos, T, H, k, dx, dev->n_sm, stream)));
+    MOE_TRY(stg.done(moe::launch_zero_untouched(counts, E, H, I, dwgu, dwd, dev->n_sm, stream)));
     MOE_TRY(stg.done(moe::launch_wgrad_down(ws + L.ds_hi, ws + L.ds_lo, ws + L.wa_hi, ws + L.wa_lo, offs, counts,
                                             rows, H, I, E, dwd, ctas, stream)));
     MOE_TRY(stg.done(moe::launch_wgrad_gate_up(ws + L.dgu_hi, ws + L.dgu_lo, ws + L.xs, offs, counts, rows, H, I, E,

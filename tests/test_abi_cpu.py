@@ -67,13 +67,14 @@ def test_stage_names(L):
     assert [m.moe_ffn_stage_name(m.MOE_PATH_DECODE_FUSED, i) for i in range(2)] == ["decode_fused", None]
     assert [m.moe_ffn_stage_name(m.MOE_PATH_GROUPED, i) for i in range(6)] == \
         ["router", "sort", "gemm_gate_up", "gemm_down", "combine", None]
-    assert [m.moe_ffn_stage_name(m.MOE_PATH_BACKWARD, i) for i in range(11)] == \
-        ["router", "sort", "prep", "gemm_gate_up", "gemm_q", "gemm_dx", "combine", "wgrad_down",
+    assert [m.moe_ffn_stage_name(m.MOE_PATH_BACKWARD, i) for i in range(12)] == \
+        ["router", "sort", "prep", "gemm_gate_up", "gemm_q", "gemm_dx", "combine", "zero_grads", "wgrad_down",
          "wgrad_gate_up", "dlogits", None]
     assert [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_FORWARD, i) for i in range(6)] == \
         ["router", "sort", "gemm_gate_up", "gemm_down", "combine", None]
-    assert [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_BACKWARD, i) for i in range(10)] == \
-        ["router", "sort", "prep", "gemm_q", "gemm_dx", "combine", "wgrad_down", "wgrad_gate_up", "dlogits", None]
+    assert [m.moe_ffn_stage_name(m.MOE_PATH_TRAIN_BACKWARD, i) for i in range(11)] == \
+        ["router", "sort", "prep", "gemm_q", "gemm_dx", "combine", "zero_grads", "wgrad_down", "wgrad_gate_up",
+         "dlogits", None]
     assert m.moe_ffn_stage_name(m.MOE_PATH_AUTO, 0) is None
     assert m.moe_ffn_stage_name(m.MOE_PATH_DECODE, -1) is None
 

@@ -48,7 +48,7 @@ def _gpu(x, L, wgu, wd, dout, k, **opt_fields):
     got = m.moe_ffn_backward(x, L, wgu, wd, dout, k, opts=o)
     torch.cuda.synchronize()
     if x.shape[0]:
-        assert o.path_taken == m.MOE_PATH_BACKWARD and o.n_stages == 10
+        assert o.path_taken == m.MOE_PATH_BACKWARD and o.n_stages == 11
     return dict(zip(NAMES, got))
 
 
@@ -227,7 +227,7 @@ def test_backward_stage_events():
     o.stage_events = m.ctypes.cast(arr, m.ctypes.c_void_p)
     m.moe_ffn_backward(x, L, wgu, wd, dout, 2, opts=o)
     torch.cuda.synchronize()
-    assert o.n_stages == 10
+    assert o.n_stages == 11
     names = [m.moe_ffn_stage_name(m.MOE_PATH_BACKWARD, i) for i in range(o.n_stages)]
     assert names[0] == "router" and names[-1] == "dlogits"
     for i in range(o.n_stages):

@@ -56,7 +56,7 @@ def _pair(x, L, wgu, wd, dout, k, state=None, **opt_fields):
     torch.cuda.synchronize()
     if T:
         assert of.path_taken == m.MOE_PATH_TRAIN_FORWARD and of.n_stages == 5
-        assert ob.path_taken == m.MOE_PATH_TRAIN_BACKWARD and ob.n_stages == 9
+        assert ob.path_taken == m.MOE_PATH_TRAIN_BACKWARD and ob.n_stages == 10
     return out, dict(zip(NAMES, grads)), state
 
 
