@@ -1,6 +1,6 @@
 /*
- * moe_ffn.h -- C ABI of libmoeffn.so: the forward pass of a routed
- * Mixture-of-Experts SwiGLU FFN layer on one GB300 GPU (sm_103a).
+ * moe_ffn.h -- C ABI of libmoeffn.so: the forward and backward passes of a
+ * routed Mixture-of-Experts SwiGLU FFN layer on one GB300 GPU (sm_103a).
  *
  * The layer, per token t with activation x[t] (H values) and router logits
  * l[t] (E values):
@@ -37,8 +37,9 @@
  *     reaches the point of the call.  The library keeps no pointer after a
  *     call returns; the caller keeps every buffer alive until the stream's
  *     work is done.
- *   - moe_ffn_forward_ex and moe_ffn_forward_noalloc may be captured into a
- *     CUDA graph (make one uncaptured call first: it sets up the device);
+ *   - moe_ffn_forward_ex, moe_ffn_forward_noalloc, moe_ffn_backward (with a
+ *     caller workspace) and the training pair may be captured into a CUDA
+ *     graph (make one uncaptured call first: it sets up the device);
  *     replays recompute from the captured buffers' current contents.
  *   - Launch failures are returned as MOE_ERR_CUDA (cudaPeekAtLastError);
  *     faults during execution surface at the caller's next synchronisation.
