@@ -563,10 +563,10 @@ __global__ void __launch_bounds__(Cfg<KIND>::THREADS, 1)
                 for (int j = 0; j < NP; ++j) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(code + src_off[j]);
                     const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
-                    const uint2 f = mx_bf16_factors(sc[j]);
+                    const float f = mx_f32_scale(sc[j]);
                     uint32_t w[8];
 #pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) e4m3x4_to_bf16x2_scaled(cw[q2], f, w[2 * q2], w[2 * q2 + 1]);
+                    for (int q2 = 0; q2 < 4; ++q2) e4m3x4_to_bf16x2_f32(cw[q2], f, w[2 * q2], w[2 * q2 + 1]);
                     *reinterpret_cast<uint4 *>(a + dst_off0[j]) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4 *>(a + dst_off1[j]) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
