@@ -190,6 +190,8 @@ __global__ void __launch_bounds__(SORT_THREADS) sort_kernel(const int32_t *__res
 // ---------------------------------------------------------------- combine
 // out[t, h] = sum_{j ascending} w[t,j] * z[pos[t*k+j], h]   (FP32, fixed order);
 // with w null the rows are summed unweighted (the backward pass's dx)
+constexpr int kCombineBatch = 8;   // slots whose rows one thread loads together
+
 __global__ void combine_kernel(const float *__restrict__ z, const float *__restrict__ w,
                                const int32_t *__restrict__ pos, int T, int H, int k, float *__restrict__ out)
 {
@@ -198,13 +200,25 @@ __global__ void combine_kernel(const float *__restrict__ z, const float *__restr
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / hv), c = (int)(i - (int64_t)t * hv);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const float wj = w ? __ldg(w + (int64_t)t * k + j) : 1.0f;
-            const float4 v = ld_nc_f4(z + (int64_t)__ldg(pos + (int64_t)t * k + j) * H + 4 * c);
+        auto add = [&](float wj, const float4 &v) {
             acc.x = fmaf(wj, v.x, acc.x);
             acc.y = fmaf(wj, v.y, acc.y);
             acc.z = fmaf(wj, v.z, acc.z);
             acc.w = fmaf(wj, v.w, acc.w);
+        };
+        if (k <= kCombineBatch) {
+            // every slot's row load in flight at once; the sum keeps slot order
+            float4 v[kCombineBatch];
+#pragma unroll
+            for (int j = 0; j < kCombineBatch; ++j)
+                if (j < k) v[j] = ld_nc_f4(z + (int64_t)__ldg(pos + (int64_t)t * k + j) * H + 4 * c);
+#pragma unroll
+            for (int j = 0; j < kCombineBatch; ++j)
+                if (j < k) add(w ? __ldg(w + (int64_t)t * k + j) : 1.0f, v[j]);
+        } else {
+            for (int j = 0; j < k; ++j)
+                add(w ? __ldg(w + (int64_t)t * k + j) : 1.0f,
+                    ld_nc_f4(z + (int64_t)__ldg(pos + (int64_t)t * k + j) * H + 4 * c));
         }
         reinterpret_cast<float4 *>(out)[i] = acc;
     }
