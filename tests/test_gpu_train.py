@@ -67,7 +67,8 @@ SHAPES = [
     (200, 128, 64, 4, 3, 0.0),     # several 64-row chunks per expert
     (64, 256, 128, 32, 1, 4.0),    # k = 1, skewed routing, untouched experts
     (17, 192, 320, 64, 32, 0.5),   # k = 32
-    (64, 64, 64, 1024, 4, 1.0),    # 1024 experts
+    (64, 64, 64, 1024, 4, 1.0),    # 1024 experts, most of them untouched
+    (9, 128, 128, 1, 1, 0.0),      # one expert
 ]
 
 
